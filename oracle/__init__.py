@@ -1,0 +1,18 @@
+"""CPU oracle for tile-pipelined AllGather+GEMM and GEMM+ReduceScatter.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` use it. It shares no code with the CUDA library (no kernels, headers,
+helpers, tables or constants); both sides take their inputs from ``workloads.py``, which holds
+none of the method's arithmetic.
+
+The oracle computes what the overlapped kernels must produce, written as the plain definition in
+fp64 (see ``reference.py``). Every function there is pinned by ``tests/test_oracle.py`` against
+brute force in exact rational arithmetic, closed forms, the identity-matrix special cases, a
+hand-worked fixture and library routines (torch's bf16 and e4m3 casts).
+"""
+from .reference import (  # noqa: F401
+    decode_bf16, decode_e4m3, round_bf16_rne, round_fp32_rne,
+    ag_gemm, ag_gemm_rows, gemm_rs, gemm_rs_rows, round_out,
+    ag_chunk_release_order, ag_tile_schedule, rs_item_schedule, expected_flags,
+)

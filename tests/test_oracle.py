@@ -1,0 +1,409 @@
+"""Pins for the CPU oracle (CPU only; no GPU, no CUDA library).
+
+Each pin checks the oracle against something other than itself: brute force in exact rational
+arithmetic on tiny inputs, hand-worked fixtures (tests/golden/hand_examples.json), closed forms,
+the identity-matrix special cases, invariants (rank permutation, linearity) and library routines
+(torch's bf16 and float8_e4m3fn casts). The mutation tests at the end plant plausible mistakes in
+copies of the oracle's functions and check that some pin fails for each.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import reference as R
+import workloads
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ------------------------------------------------------------------ brute force (exact rationals)
+
+def bf16_bits_to_fraction(b: int) -> Fraction:
+    """bf16 bit pattern -> exact rational, from the bit fields (independent of the oracle)."""
+    s = -1 if (b >> 15) & 1 else 1
+    e = (b >> 7) & 0xFF
+    m = b & 0x7F
+    assert e != 0xFF, "no inf/nan in these tests"
+    if e == 0:
+        return s * Fraction(m, 128) * Fraction(2) ** -126
+    return s * (1 + Fraction(m, 128)) * Fraction(2) ** (e - 127)
+
+
+def brute_gemm(A, B):
+    M, K = len(A), len(A[0])
+    N = len(B[0])
+    return [[sum((A[i][k] * B[k][n] for k in range(K)), Fraction(0)) for n in range(N)]
+            for i in range(M)]
+
+
+def rand_bf16_bits(rng, shape, integer):
+    if integer:
+        x = rng.integers(-4, 5, size=shape).astype(np.float32)
+    else:
+        x = rng.standard_normal(size=shape).astype(np.float32)
+    return workloads.to_bf16_bits(x)
+
+
+def check_ag_brute(ag_gemm, W, M_local, K, N, integer, seed):
+    rng = np.random.default_rng(seed)
+    shards = [rand_bf16_bits(rng, (M_local, K), integer) for _ in range(W)]
+    b = rand_bf16_bits(rng, (K, N), integer)
+    Gq = [[bf16_bits_to_fraction(int(v)) for v in row] for s in shards for row in s]
+    Bq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in b]
+    exact = brute_gemm(Gq, Bq)
+    got = ag_gemm(shards, b, "bf16")
+    assert got.shape == (W * M_local, N)
+    for i in range(W * M_local):
+        for n in range(N):
+            if integer:
+                assert got[i, n] == exact[i][n]
+            else:
+                bound = sum(abs(Gq[i][k] * Bq[k][n]) for k in range(K)) * Fraction(K, 2 ** 52)
+                assert abs(Fraction(got[i, n]) - exact[i][n]) <= bound
+
+
+def check_rs_brute(gemm_rs, W, M, K, N, integer, seed):
+    rng = np.random.default_rng(seed)
+    A = [rand_bf16_bits(rng, (M, K), integer) for _ in range(W)]
+    B = [rand_bf16_bits(rng, (K, N), integer) for _ in range(W)]
+    exact = [[Fraction(0)] * N for _ in range(M)]
+    mag = [[Fraction(0)] * N for _ in range(M)]
+    for r in range(W):
+        Aq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in A[r]]
+        Bq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in B[r]]
+        P = brute_gemm(Aq, Bq)
+        for i in range(M):
+            for n in range(N):
+                exact[i][n] += P[i][n]
+                mag[i][n] += sum(abs(Aq[i][k] * Bq[k][n]) for k in range(K))
+    shards = gemm_rs(A, B, "bf16")
+    assert len(shards) == W
+    h = M // W
+    for j in range(W):
+        assert shards[j].shape == (h, N)
+        for i in range(h):
+            for n in range(N):
+                e = exact[j * h + i][n]
+                if integer:
+                    assert shards[j][i, n] == e
+                else:
+                    assert abs(Fraction(shards[j][i, n]) - e) <= mag[j * h + i][n] * Fraction(W * K + W, 2 ** 52)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+@pytest.mark.parametrize("M_local", [1, 2, 5])
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_brute_force(W, M_local, integer):
+    check_ag_brute(R.ag_gemm, W, M_local, K=7 + W, N=3 + 2 * M_local, integer=integer,
+                   seed=1000 * W + 10 * M_local + integer)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_brute_force(W, integer):
+    check_rs_brute(R.gemm_rs, W, M=2 * W, K=5 + W, N=6, integer=integer, seed=77 + W + integer)
+
+
+# ------------------------------------------------------------------ hand-worked fixtures
+
+def _bf16(a):
+    return workloads.to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def check_golden_ag(ag_gemm, golden):
+    for ex in golden["ag_gemm"]:
+        shards = [_bf16(s) for s in ex["shards"]]
+        got = ag_gemm(shards, _bf16(ex["B"]), "bf16")
+        assert np.array_equal(got, np.asarray(ex["C"], dtype=np.float64))
+    ex = golden["ag_gemm_e4m3"]
+    shards = [np.asarray(s, dtype=np.uint8) for s in ex["shards"]]
+    got = ag_gemm(shards, np.asarray(ex["B"], dtype=np.uint8), "e4m3", ex["scale_a"], ex["scale_b"])
+    assert np.array_equal(got, np.asarray(ex["C"], dtype=np.float64))
+
+
+def check_golden_rs(gemm_rs, golden):
+    for ex in golden["gemm_rs"]:
+        A = [_bf16(a) for a in ex["A"]]
+        B = [_bf16(b) for b in ex["B"]]
+        got = gemm_rs(A, B, "bf16")
+        for j, want in enumerate(ex["out"]):
+            assert np.array_equal(got[j], np.asarray(want, dtype=np.float64))
+
+
+def test_golden_ag(golden):
+    check_golden_ag(R.ag_gemm, golden)
+
+
+def test_golden_rs(golden):
+    check_golden_rs(R.gemm_rs, golden)
+
+
+def test_golden_e4m3_codes(golden):
+    ex = golden["e4m3_codes"]
+    for code, val in ex.items():
+        if code.startswith("_") or code == "nan":
+            continue
+        got = R.decode_e4m3(np.array([int(code)], dtype=np.uint8))[0]
+        assert got == val and np.signbit(got) == np.signbit(val)
+    for code in ex["nan"]:
+        assert np.isnan(R.decode_e4m3(np.array([code], dtype=np.uint8))[0])
+
+
+def test_golden_bf16_rne(golden):
+    for expr, bits in golden["bf16_rne"]["cases"]:
+        x = float(eval(expr))   # the fixture's own arithmetic on exact powers of two
+        assert int(R.round_bf16_rne(np.array([x]))[0]) == bits, expr
+
+
+# ------------------------------------------------------------------ number formats vs library
+
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = R.decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_decode_matches_torch():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = R.decode_bf16(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_bf16_rne_matches_torch_on_fp32_inputs():
+    # For inputs that are already binary32 values there is no double rounding, so torch's
+    # fp32 -> bf16 cast (round to nearest even) is an independent reference.
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.standard_normal(200000).astype(np.float32),
+        (rng.standard_normal(20000) * 1e-38).astype(np.float32),   # subnormal range
+        (rng.standard_normal(20000) * 1e38).astype(np.float32),    # near overflow
+        np.array([0.0, -0.0, np.inf, -np.inf], dtype=np.float32),
+    ])
+    # force exact ties: low 16 bits = 0x8000
+    ties = (rng.integers(0, 1 << 31, 20000, dtype=np.uint32) & np.uint32(0x7F7F0000)) | np.uint32(0x8000)
+    x = np.concatenate([x, ties.view(np.float32)])
+    ours = R.round_bf16_rne(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_rne_single_rounding_from_fp64():
+    # A value just above a bf16 tie that rounds to the tie in binary32: one rounding (fp64 ->
+    # bf16) must go up; rounding through fp32 first would go to even (down).
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert int(R.round_bf16_rne(np.array([x]))[0]) == 0x3F81
+    assert np.float32(x) == np.float32(1.0 + 2.0 ** -8)
+
+
+def test_round_out_fp32():
+    x = np.array([1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 0.1])
+    assert np.array_equal(R.round_out(x, "fp32"), np.array([1.0, 1.0 + 2.0 ** -22, np.float32(0.1)], dtype=np.float32))
+
+
+# ------------------------------------------------------------------ special cases / invariants
+
+def test_identity_B_gives_gathered_shards():
+    rng = np.random.default_rng(11)
+    W, M_local, K = 4, 3, 16
+    shards = [rand_bf16_bits(rng, (M_local, K), False) for _ in range(W)]
+    eye = _bf16(np.eye(K))
+    C = R.ag_gemm(shards, eye, "bf16")
+    want = np.concatenate([R.decode_bf16(s) for s in shards])
+    assert np.array_equal(C, want)
+    assert np.array_equal(R.decode_bf16(R.round_out(C, "bf16")), want)   # bf16 values round to themselves
+
+
+def test_identity_B_gives_summed_slices():
+    rng = np.random.default_rng(12)
+    W, M, K = 4, 8, 8
+    A = [rand_bf16_bits(rng, (M, K), False) for _ in range(W)]
+    eye = [_bf16(np.eye(K)) for _ in range(W)]
+    out = R.gemm_rs(A, eye, "bf16")
+    for j in range(W):
+        for i in range(M // W):
+            for k in range(K):
+                want = sum((bf16_bits_to_fraction(int(A[r][j * (M // W) + i, k])) for r in range(W)),
+                           Fraction(0))
+                assert Fraction(out[j][i, k]) == want
+
+
+def test_ones_closed_form():
+    W, M_local, K, N = 3, 4, 37, 5
+    ones = _bf16(np.ones((M_local, K)))
+    C = R.ag_gemm([ones] * W, _bf16(np.ones((K, N))), "bf16")
+    assert np.array_equal(C, np.full((W * M_local, N), float(K)))
+    out = R.gemm_rs([_bf16(np.ones((8, K)))] * 2, [_bf16(np.ones((K, N)))] * 2, "bf16")
+    assert all(np.array_equal(o, np.full((4, N), 2.0 * K)) for o in out)
+
+
+def test_rank_permutation_equivariance():
+    rng = np.random.default_rng(13)
+    W, M_local, K, N = 4, 2, 9, 5
+    shards = [rand_bf16_bits(rng, (M_local, K), True) for _ in range(W)]
+    b = rand_bf16_bits(rng, (K, N), True)
+    C = R.ag_gemm(shards, b, "bf16")
+    perm = [2, 0, 3, 1]
+    Cp = R.ag_gemm([shards[p] for p in perm], b, "bf16")
+    for i, p in enumerate(perm):
+        assert np.array_equal(Cp[i * M_local:(i + 1) * M_local], C[p * M_local:(p + 1) * M_local])
+    # GEMM-RS output does not depend on the rank order (exact on integers)
+    A = [rand_bf16_bits(rng, (8, K), True) for _ in range(W)]
+    B = [rand_bf16_bits(rng, (K, N), True) for _ in range(W)]
+    o1 = R.gemm_rs(A, B, "bf16")
+    o2 = R.gemm_rs([A[p] for p in perm], [B[p] for p in perm], "bf16")
+    assert all(np.array_equal(x, y) for x, y in zip(o1, o2))
+
+
+def test_linearity_exact():
+    rng = np.random.default_rng(14)
+    shards = [rand_bf16_bits(rng, (3, 8), False) for _ in range(2)]
+    b = rand_bf16_bits(rng, (8, 4), False)
+    twice = [workloads.to_bf16_bits(2 * R.decode_bf16(s).astype(np.float32)) for s in shards]
+    assert np.array_equal(R.ag_gemm(twice, b, "bf16"), 2 * R.ag_gemm(shards, b, "bf16"))
+
+
+def test_scales_apply_per_rank():
+    codes = [np.full((2, 4), 0x38, dtype=np.uint8), np.full((2, 4), 0x40, dtype=np.uint8)]
+    b = np.full((4, 3), 0x38, dtype=np.uint8)
+    C = R.ag_gemm(codes, b, "e4m3", [2.0, 0.5], 0.25)
+    assert np.array_equal(C[:2], np.full((2, 3), 2.0 * 0.25 * 4))
+    assert np.array_equal(C[2:], np.full((2, 3), 0.5 * 0.25 * 8))
+
+
+def test_sampled_rows_match_full():
+    wl = workloads.with_shape(workloads.WORKLOADS["ag_w8"], W=3, M=8, K=32, N=16)
+    inp = workloads.make_inputs(wl)
+    full = R.ag_gemm(inp.a, inp.b[0], "bf16")
+    rows = [0, 5, 8, 23]
+    assert np.array_equal(R.ag_gemm_rows(inp.a, inp.b[0], rows, "bf16"), full[rows])
+    wl = workloads.with_shape(workloads.WORKLOADS["rs_w8"], W=4, M=8, K=16, N=8)
+    inp = workloads.make_inputs(wl)
+    shards = R.gemm_rs(inp.a, inp.b, "bf16")
+    S = np.concatenate(shards)
+    rows = [1, 2, 7]
+    assert np.allclose(R.gemm_rs_rows(inp.a, inp.b, rows, "bf16"), S[rows], rtol=1e-15, atol=0)
+
+
+def test_integer_mode_is_exact_at_config_magnitudes():
+    # Integer inputs in [-4, 4]: |sum| <= 16*K*W < 2**24, so every value is an exact integer
+    # and the bf16/fp32 rounding of it is deterministic.
+    wl = workloads.with_shape(workloads.WORKLOADS["rs_w8"], M=16, K=3584, N=8)
+    inp = workloads.make_inputs(wl, integer=True)
+    out = np.concatenate(R.gemm_rs(inp.a, inp.b, "bf16"))
+    assert np.array_equal(out, np.round(out))
+    assert np.abs(out).max() < 2 ** 24
+
+
+# ------------------------------------------------------------------ bookkeeping definitions
+
+def test_schedules_are_permutations_in_arrival_order():
+    W, M_local, chunk = 8, 1024, 128
+    order = R.ag_chunk_release_order(W, M_local, chunk, self_rank=3)
+    assert sorted(order) == [(r, c) for r in range(W) for c in range(M_local // chunk)]
+    assert [r for r, _ in order[:M_local // chunk]] == [4] * (M_local // chunk)
+    assert order[-1] == (3, M_local // chunk - 1)
+    sched = R.ag_tile_schedule(W, M_local, 3584, 128, 256, self_rank=3)
+    assert sorted(sched) == [(m, n) for m in range(64) for n in range(14)]
+    assert sched[0] == (24, 0) and sched[13] == (24, 13) and sched[14] == (25, 0)
+    assert sched[8 * 14] == (32, 0)
+    rs = R.rs_item_schedule(8, 8192, 8192, 128, 256)
+    assert len(rs) == 8 * 64 * 32 and rs[0] == (0, 0, 0) and rs[2048] == (1, 0, 0)
+    assert np.array_equal(R.expected_flags(3, 7), np.array([7, 7, 7], dtype=np.uint32))
+
+
+def test_tiny_schedule_tile_spans_ranks():
+    # tiny config: one 128-row M-tile covers both 64-row shards
+    assert R.ag_tile_schedule(2, 64, 256, 128, 256, self_rank=1) == [(0, 0)]
+
+
+# ------------------------------------------------------------------ planted mistakes
+
+def _mut_transposed_b(shards, b, dtype="bf16", scale_a=None, scale_b=None):
+    G = np.concatenate([R.decode(s, dtype) for s in shards])
+    Bd = R.decode(b, dtype)
+    return G @ Bd.T if Bd.shape[0] == Bd.shape[1] else G @ Bd[:, ::-1]
+
+
+def _mut_reversed_concat(shards, b, dtype="bf16", scale_a=None, scale_b=None):
+    return R.ag_gemm(list(reversed(shards)), b, dtype, scale_a, scale_b)
+
+
+def _mut_dropped_term(shards, b, dtype="bf16", scale_a=None, scale_b=None):
+    G = np.concatenate([R.decode(s, dtype) for s in shards])
+    return G[:, 1:] @ R.decode(b, dtype)[1:] if G.shape[1] > 1 else 0 * G @ R.decode(b, dtype)
+
+
+def _mut_rs_dropped_rank(a, b, dtype="bf16", scale_a=None, scale_b=None):
+    return R.gemm_rs(a[1:] + [a[0] * 0], b, dtype) if len(a) > 1 else R.gemm_rs(a, b, dtype)
+
+
+def _mut_rs_wrong_slice(a, b, dtype="bf16", scale_a=None, scale_b=None):
+    return list(reversed(R.gemm_rs(a, b, dtype)))
+
+
+def _mut_rs_sign(a, b, dtype="bf16", scale_a=None, scale_b=None):
+    out = R.gemm_rs(a[:1], b[:1], dtype)
+    rest = R.gemm_rs(a[1:], b[1:], dtype) if len(a) > 1 else None
+    if rest is None:
+        return out
+    # partial of rank >= 1 subtracted instead of added (shard count follows the full W)
+    full = np.concatenate(R.gemm_rs(a, b, dtype))
+    p0 = R.decode(a[0], dtype) @ R.decode(b[0], dtype)
+    wrong = 2 * p0 - full
+    h = wrong.shape[0] // len(a)
+    return [wrong[j * h:(j + 1) * h] for j in range(len(a))]
+
+
+@pytest.mark.parametrize("mut", [_mut_transposed_b, _mut_reversed_concat, _mut_dropped_term])
+def test_planted_ag_mistakes_are_caught(mut, golden):
+    caught = 0
+    try:
+        check_golden_ag(mut, golden)
+    except AssertionError:
+        caught += 1
+    try:
+        check_ag_brute(mut, 2, 2, 4, 4, True, 3)
+    except (AssertionError, ValueError):
+        caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("mut", [_mut_rs_dropped_rank, _mut_rs_wrong_slice, _mut_rs_sign])
+def test_planted_rs_mistakes_are_caught(mut, golden):
+    caught = 0
+    try:
+        check_golden_rs(mut, golden)
+    except AssertionError:
+        caught += 1
+    try:
+        check_rs_brute(mut, 3, 6, 4, 3, True, 4)
+    except AssertionError:
+        caught += 1
+    assert caught > 0
+
+
+def test_planted_format_mistakes_are_caught():
+    # wrong exponent bias in e4m3, and truncation instead of rounding in bf16
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    bad = R.decode_e4m3(codes) * 2.0
+    ok = ~np.isnan(ref)
+    assert not np.array_equal(bad[ok], ref[ok])
+    x = np.array([1.0 + 3 * 2.0 ** -8])
+    trunc = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert int(trunc[0]) != int(R.round_bf16_rne(x)[0])
+
+
+def test_oracle_package_exports():
+    for name in ["ag_gemm", "gemm_rs", "round_out", "ag_tile_schedule", "rs_item_schedule"]:
+        assert hasattr(oracle, name)
