@@ -1,0 +1,408 @@
+// Host side of the C ABI declared in include/tdx.h: argument validation, tiling choice, workspace
+// carving (status word, chunk flags, gathered buffer, running-sum buffer), TMA tensor maps and the
+// launch of the persistent fused kernel. No arithmetic of the operations happens here.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tdx.h"
+#include "tdx_internal.h"
+
+using namespace tdx;
+
+namespace {
+
+constexpr uint32_t kVersion = (1u << 16) | 0u;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elt_size(tdx_dtype d) { return d == TDX_BF16 ? 2 : d == TDX_FP8_E4M3 ? 1 : d == TDX_FP32 ? 4 : 0; }
+
+tdx_opts defaults() {
+  tdx_opts o;
+  std::memset(&o, 0, sizeof(o));
+  o.self_rank = 0;
+  o.chunk_rows = 0;
+  o.out_dtype = TDX_BF16;
+  o.scale_a = nullptr;
+  o.scale_b = nullptr;
+  o.mode = TDX_FUSED;
+  o.producer = TDX_PRODUCER_SM;
+  o.epoch = 0;
+  o.timeout_ns = 2000000000ull;
+  o.perturb_seed = 0;
+  o.trace = nullptr;
+  o.num_sms = 0;
+  o.split_k = 0;
+  o.block_n = 0;
+  return o;
+}
+
+// Everything the launch needs that follows from shapes and options alone (no device queries),
+// so that tdx_workspace_size and the calls carve the same layout.
+struct Plan {
+  int op = 0, W = 0, M = 0, M_local = 0, K = 0, N = 0, elt = 2;
+  int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
+  int chunk_rows = 0, n_chunks = 0;
+  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, ctrl_end = 0;
+  size_t off_G = 0, off_S = 0, total = 0;
+};
+
+bool valid_bn(int bn, bool fp8) { return fp8 ? (bn == 128 || bn == 256) : (bn == 64 || bn == 128 || bn == 256); }
+
+tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const tdx_opts& o, Plan* pl) {
+  if (op != OP_AG && op != OP_RS) return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW || Mx < 0 || K < 0 || N < 0) return TDX_ERR_INVALID_ARG;
+  if (dtype != TDX_BF16 && dtype != TDX_FP8_E4M3) return TDX_ERR_INVALID_ARG;
+  const bool fp8 = dtype == TDX_FP8_E4M3;
+  Plan p;
+  p.op = op;
+  p.W = W;
+  p.K = K;
+  p.N = N;
+  p.elt = elt_size(dtype);
+  if (op == OP_AG) {
+    p.M_local = Mx;
+    p.M = W * Mx;
+    int cr = o.chunk_rows > 0 ? o.chunk_rows : (Mx < 128 ? Mx : 128);
+    if (Mx > 0 && (cr <= 0 || Mx % cr != 0)) return TDX_ERR_INVALID_ARG;
+    p.chunk_rows = Mx > 0 ? cr : 1;
+    p.n_chunks = Mx > 0 ? Mx / cr : 0;
+  } else {
+    if (fp8) return TDX_ERR_UNSUPPORTED;
+    if (Mx % W != 0) return TDX_ERR_INVALID_ARG;
+    p.M = Mx;
+    p.M_local = Mx / W;
+  }
+  p.num_kb = (int)((static_cast<long long>(K) * p.elt + 127) / 128);
+  p.tiles_m = (p.M + kBM - 1) / kBM;
+  // tile width
+  int bn = o.block_n;
+  if (bn != 0 && !valid_bn(bn, fp8)) return TDX_ERR_UNSUPPORTED;
+  int L = 1;
+  if (op == OP_AG) {
+    const long long tiles256 = static_cast<long long>(p.tiles_m) * ((N + 255) / 256);
+    const bool small = tiles256 * 2 <= kRefSMs && p.num_kb >= 2;
+    if (bn == 0) {
+      if (small) bn = fp8 ? 128 : 64;
+      else bn = N > 128 ? 256 : (N > 64 || fp8 ? 128 : 64);
+    }
+    const long long tiles = static_cast<long long>(p.tiles_m) * ((N + bn - 1) / bn);
+    if (o.split_k > 0) {
+      L = o.split_k;
+    } else if (small && tiles > 0) {
+      L = static_cast<int>(kRefSMs / tiles);
+    }
+    if (L > kMaxSplitK) L = kMaxSplitK;
+    if (L > p.num_kb) L = p.num_kb;
+    if (L < 1) L = 1;
+  } else {
+    if (bn == 0) bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    L = W;
+  }
+  p.BN = bn;
+  p.L = L;
+  p.tiles_n = (N + bn - 1) / bn;
+  p.T = p.tiles_m * p.tiles_n;
+  // workspace layout
+  size_t off = kHeaderBytes;
+  const size_t n_chunk_words = op == OP_AG ? static_cast<size_t>(W) * p.n_chunks : 0;
+  p.off_chunk_flags = off;
+  off += n_chunk_words * 4;
+  p.off_chunk_cnt = off;
+  off += n_chunk_words * 4;
+  p.off_chain_flags = off;
+  off += static_cast<size_t>(L > 1 ? L - 1 : 0) * p.T * 4;
+  off = align_up(off, 1024);
+  p.ctrl_end = off;
+  if (op == OP_AG) {
+    p.off_G = off;
+    off = align_up(off + static_cast<size_t>(p.M) * K * p.elt, 1024);
+  }
+  if (L > 1) {
+    p.off_S = off;
+    off = align_up(off + static_cast<size_t>(p.T) * kBM * bn * 4, 1024);
+  }
+  p.total = off;
+  *pl = p;
+  return TDX_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2D map over a row-major (rows x cols) matrix with 128-byte swizzle; box = box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long long cols, int box_cols,
+              int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const int elt = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+tdx_status fill_zero(void* p, size_t bytes, cudaStream_t s) {
+  return launch_fill_zero(p, bytes, s) == cudaSuccess ? TDX_OK : TDX_ERR_CUDA;
+}
+
+tdx_status launch(const Plan& pl, KParams& kp, bool fp8, int grid, cudaStream_t stream) {
+  const cudaError_t e = fp8 ? launch_fused_fp8(pl.BN, kp, grid, stream) : launch_fused_bf16(pl.BN, kp, grid, stream);
+  if (e != cudaSuccess) {
+    if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
+    return TDX_ERR_CUDA;
+  }
+  return TDX_OK;
+}
+
+void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
+  kp.W = pl.W;
+  kp.M = pl.M;
+  kp.K = pl.K;
+  kp.N = pl.N;
+  kp.M_local = pl.M_local;
+  kp.tiles_m = pl.tiles_m;
+  kp.tiles_n = pl.tiles_n;
+  kp.T = pl.T;
+  kp.L = pl.L;
+  kp.num_kb = pl.num_kb;
+  kp.status = reinterpret_cast<uint32_t*>(ws);
+  kp.chunk_flags = reinterpret_cast<uint32_t*>(ws + pl.off_chunk_flags);
+  kp.chunk_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_chunk_cnt);
+  kp.chain_flags = reinterpret_cast<uint32_t*>(ws + pl.off_chain_flags);
+  kp.sbuf = pl.L > 1 ? reinterpret_cast<float*>(ws + pl.off_S) : nullptr;
+  kp.trace = static_cast<uint32_t*>(o.trace);
+  kp.epoch = o.epoch == 0 ? 1u : o.epoch;
+  kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
+  kp.perturb = o.perturb_seed;
+  kp.mode = o.mode;
+  kp.row_bytes = static_cast<long long>(pl.K) * pl.elt;
+}
+
+int grid_for(const tdx_opts& o, int items_or_zero) {
+  int sms = device_sms();
+  if (sms <= 0) return 0;
+  int g = o.num_sms > 0 && o.num_sms < sms ? o.num_sms : sms;
+  if (items_or_zero > 0 && items_or_zero < g) g = items_or_zero;
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+tdx_status tdx_opts_default(tdx_opts* opts) {
+  if (opts == nullptr) return TDX_ERR_INVALID_ARG;
+  *opts = defaults();
+  return TDX_OK;
+}
+
+tdx_status tdx_workspace_size(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype, const tdx_opts* opts,
+                              size_t* bytes) {
+  if (bytes == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  Plan pl;
+  tdx_status s = make_plan(op, W, M_local_or_M, K, N, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  *bytes = pl.total;
+  return TDX_OK;
+}
+
+tdx_status tdx_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TDX_ERR_WORKSPACE;
+  return fill_zero(workspace, bytes, static_cast<cudaStream_t>(stream));
+}
+
+tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* workspace, size_t workspace_bytes,
+                       int W, int M_local, int K, int N, tdx_dtype dtype, const tdx_opts* opts, void* stream) {
+  const tdx_opts o = opts ? *opts : defaults();
+  if (shards == nullptr || B == nullptr || C == nullptr) return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
+  for (int r = 0; r < W; ++r)
+    if (shards[r] == nullptr) return TDX_ERR_INVALID_ARG;
+  if (o.self_rank < 0 || o.self_rank >= W) return TDX_ERR_INVALID_ARG;
+  if (o.out_dtype != TDX_BF16 && o.out_dtype != TDX_FP32) return TDX_ERR_INVALID_ARG;
+  if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
+  if (o.producer != TDX_PRODUCER_SM && o.producer != TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_INVALID_ARG;
+  if (o.producer == TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_UNSUPPORTED;
+  Plan pl;
+  tdx_status s = make_plan(OP_AG, W, M_local, K, N, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  const bool fp8 = dtype == TDX_FP8_E4M3;
+  const int out_elt = o.out_dtype == TDX_FP32 ? 4 : 2;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(shards[r])) return TDX_ERR_ALIGNMENT;
+  if (!aligned16(B) || !aligned16(C)) return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(K) * pl.elt) % 16 != 0 || (static_cast<long long>(N) * pl.elt) % 16 != 0 ||
+      (static_cast<long long>(N) * out_elt) % 16 != 0)
+    return TDX_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.total)
+    return TDX_ERR_WORKSPACE;
+  if (M_local == 0 || N == 0) return TDX_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return fill_zero(C, static_cast<size_t>(pl.M) * N * out_elt, st);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  static thread_local KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(kp, pl, o, ws);
+  kp.op = OP_AG;
+  kp.self_rank = o.self_rank;
+  kp.chunk_rows = pl.chunk_rows;
+  kp.n_chunks = pl.n_chunks;
+  kp.out_fp32 = o.out_dtype == TDX_FP32;
+  kp.G = ws + pl.off_G;
+  kp.out[0] = static_cast<uint8_t*>(C);
+  for (int r = 0; r < W; ++r) {
+    kp.shard[r] = static_cast<const uint8_t*>(shards[r]);
+    const float sa = (fp8 && o.scale_a) ? o.scale_a[r] : 1.0f;
+    const float sb = (fp8 && o.scale_b) ? o.scale_b[0] : 1.0f;
+    kp.row_scale[r] = sa * sb;
+  }
+  kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
+  kp.ppc = static_cast<int>((kp.chunk_bytes + kPieceBytes - 1) / kPieceBytes);
+  kp.total_pieces = W * pl.n_chunks * kp.ppc;
+  kp.copy_active = (o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY) ? 1 : 0;
+  kp.wait_flags = (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY) ? 1 : 0;
+  const int bbox = fp8 ? 128 : 64;
+  if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, bbox, kBM) ||
+      !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, bbox, kBM) ||
+      !make_map(&kp.tm_b[0], B, fp8, K, N, bbox, bbox))
+    return TDX_ERR_CUDA;
+  if (o.epoch == 0) {
+    s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
+    if (s != TDX_OK) return s;
+  }
+  const int grid = grid_for(o, 0);
+  if (grid <= 0) return TDX_ERR_CUDA;
+  return launch(pl, kp, fp8, grid, st);
+}
+
+tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, void* const* out_shards,
+                       void* workspace, size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype,
+                       const tdx_opts* opts, void* stream) {
+  const tdx_opts o = opts ? *opts : defaults();
+  if (A_parts == nullptr || B_parts == nullptr || out_shards == nullptr) return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
+  for (int r = 0; r < W; ++r)
+    if (A_parts[r] == nullptr || B_parts[r] == nullptr || out_shards[r] == nullptr) return TDX_ERR_INVALID_ARG;
+  if (o.mode < TDX_FUSED || o.mode > TDX_MOVE_ONLY) return TDX_ERR_INVALID_ARG;
+  if (o.out_dtype != TDX_BF16) return TDX_ERR_UNSUPPORTED;
+  Plan pl;
+  tdx_status s = make_plan(OP_RS, W, M, K, N, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(A_parts[r]) || !aligned16(B_parts[r]) || !aligned16(out_shards[r])) return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(K) * 2) % 16 != 0 || (static_cast<long long>(N) * 2) % 16 != 0)
+    return TDX_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.total)
+    return TDX_ERR_WORKSPACE;
+  if (M == 0 || N == 0) return TDX_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    for (int r = 0; r < W; ++r) {
+      s = fill_zero(out_shards[r], static_cast<size_t>(pl.M_local) * N * 2, st);
+      if (s != TDX_OK) return s;
+    }
+    return TDX_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  static thread_local KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(kp, pl, o, ws);
+  kp.op = OP_RS;
+  for (int r = 0; r < W; ++r) {
+    kp.out[r] = static_cast<uint8_t*>(out_shards[r]);
+    if (!make_map(&kp.tm_a[r], A_parts[r], false, M, K, 64, kBM) ||
+        !make_map(&kp.tm_b[r], B_parts[r], false, K, N, 64, 64))
+      return TDX_ERR_CUDA;
+  }
+  if (o.epoch == 0) {
+    s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
+    if (s != TDX_OK) return s;
+  }
+  const int grid = grid_for(o, pl.L * pl.T);
+  if (grid <= 0) return TDX_ERR_CUDA;
+  return launch(pl, kp, false, grid, st);
+}
+
+tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_status* out, uint32_t* detail) {
+  if (workspace == nullptr || out == nullptr) return TDX_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t words[kStatusWords];
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TDX_ERR_CUDA;
+  if (cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return TDX_ERR_CUDA;
+  *out = static_cast<tdx_status>(words[0]);
+  if (detail != nullptr) std::memcpy(detail, words, sizeof(words));
+  return TDX_OK;
+}
+
+tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype, const tdx_opts* opts,
+                         int64_t* info) {
+  if (info == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  Plan pl;
+  tdx_status s = make_plan(op, W, M_local_or_M, K, N, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  const int64_t v[16] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
+                         (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
+                         (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total, 0, 0};
+  std::memcpy(info, v, sizeof(v));
+  return TDX_OK;
+}
+
+size_t tdx_trace_size(int grid, int items) {
+  if (grid <= 0 || items < 0) return 0;
+  const size_t per_cta = (static_cast<size_t>(items) + grid - 1) / grid;
+  return 4 * (4 + 4 * static_cast<size_t>(grid) + static_cast<size_t>(grid) * per_cta);
+}
+
+const char* tdx_status_string(tdx_status s) {
+  switch (s) {
+    case TDX_OK: return "TDX_OK";
+    case TDX_ERR_INVALID_ARG: return "TDX_ERR_INVALID_ARG: invalid argument";
+    case TDX_ERR_UNSUPPORTED: return "TDX_ERR_UNSUPPORTED: request not implemented by the kernels";
+    case TDX_ERR_ALIGNMENT: return "TDX_ERR_ALIGNMENT: pointer or row pitch not 16-byte aligned";
+    case TDX_ERR_WORKSPACE: return "TDX_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case TDX_ERR_CUDA: return "TDX_ERR_CUDA: a CUDA call failed";
+    case TDX_ERR_TIMEOUT: return "TDX_ERR_TIMEOUT: a bounded device wait ran out";
+    case TDX_ERR_STALE_EPOCH: return "TDX_ERR_STALE_EPOCH: a flag held an epoch >= the call's epoch";
+    default: return "unknown tdx_status";
+  }
+}
+
+uint32_t tdx_version(void) { return kVersion; }
+
+}  // extern "C"

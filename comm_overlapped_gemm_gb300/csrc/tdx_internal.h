@@ -1,0 +1,76 @@
+// Internal definitions shared by the host planner (tdx_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tdx {
+
+constexpr int kMaxW = 16;
+constexpr int kBM = 128;                 // rows of every output tile (one TMEM lane per row)
+constexpr int kNumThreads = 384;         // 12 warps, roles below
+constexpr int kTmaWarp = 0;              // lane 0 issues TMA loads (and waits on chunk flags)
+constexpr int kMmaWarp = 1;              // lane 0 issues tcgen05.mma; the warp owns TMEM
+constexpr int kCopyWarp0 = 2;            // warps 2-3: AllGather chunk producer
+constexpr int kNumCopyWarps = 2;
+constexpr int kEpiWarp0 = 4;             // warps 4-11: epilogue (TMEM -> registers -> global)
+constexpr int kNumEpiWarps = 8;
+constexpr int kEpiThreads = kNumEpiWarps * 32;
+constexpr int kCopyThreads = kNumCopyWarps * 32;
+constexpr int kPieceBytes = 16384;       // producer copy unit inside a chunk
+constexpr int kMaxSplitK = 16;
+constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
+
+enum Op { OP_AG = 0, OP_RS = 1 };
+enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };
+enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4 };
+enum DevStatus { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_STALE = 7 };
+
+// Word offsets in the workspace header (first 4 KiB).
+constexpr size_t kHeaderBytes = 4096;
+constexpr int kStatusWords = 8;
+
+struct KParams {
+  CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard. RS: A_r
+  CUtensorMap tm_b[kMaxW];       // AG: [0] B. RS: B_r
+  const uint8_t* shard[kMaxW];   // AG producer sources
+  uint8_t* out[kMaxW];           // AG: [0] = C. RS: output shards
+  uint8_t* G;                    // AG gathered buffer
+  uint32_t* status;              // kStatusWords words
+  uint32_t* chunk_flags;         // AG: [W * n_chunks], flag of chunk (rank, c) at rank*n_chunks + c
+  uint32_t* chunk_cnt;           // AG: pieces completed per chunk (reset by the last piece)
+  uint32_t* chain_flags;         // [(L-1) * T]: running sum of chain elements 0..c done for tile
+  float* sbuf;                   // [T][kBM*BN] running-sum buffer, thread-coalesced layout
+  uint32_t* trace;               // optional
+  float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r
+  int op, mode;
+  int W, M, K, N;                // M = total rows (AG: W * M_local)
+  int M_local;                   // AG: rows per shard. RS: rows per output shard (M / W)
+  int self_rank;
+  int chunk_rows, n_chunks;      // AG chunking (per rank)
+  int tiles_m, tiles_n, T;       // T = tiles_m * tiles_n
+  int L;                         // chain length: RS = W ranks, AG = split-K factor
+  int num_kb;                    // K blocks of 128 bytes
+  int out_fp32;
+  int copy_active;               // producer warps copy chunks (AG, SM producer, fused/move)
+  int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
+  uint32_t epoch;
+  uint64_t timeout_ns;
+  uint32_t perturb;
+  int ppc;                       // pieces per chunk
+  int total_pieces;
+  long long row_bytes;           // K * element size
+  long long chunk_bytes;
+};
+
+// Shared-memory footprint of one instantiation (host side, for the launch).
+int fused_smem_bytes(int block_n, bool fp8);
+
+// Launch the persistent fused kernel for (block_n, fp8) on `grid` CTAs.
+cudaError_t launch_fused_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_fp8(int block_n, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
+
+}  // namespace tdx

@@ -1,0 +1,601 @@
+// The persistent fused kernel: AllGather chunk producer + flag-gated tcgen05/TMEM GEMM, and
+// GEMM + rank-ordered ReduceScatter, in one launch per call.
+//
+// Roles (one CTA per SM, 12 warps):
+//   warp 0  lane 0  TMA issuer. For an AllGather tile it first acquire-waits the flags of every
+//                   chunk the tile's rows fall in (unless the rows are the local shard), then
+//                   streams 128-byte K slices of A and B into an S-stage shared-memory ring.
+//   warp 1  lane 0  MMA issuer: tcgen05.mma (bf16: kind::f16, e4m3: kind::f8f6f4) into one of two
+//                   TMEM accumulators of 128 x BN fp32; tcgen05.commit frees ring slots and
+//                   hands finished accumulators to the epilogue. Warp 1 allocates TMEM.
+//   warps 2-3       AllGather producer: copies 16 KiB pieces of shard chunks into the gathered
+//                   buffer; the last piece of a chunk releases the chunk's flag (= epoch).
+//   warps 4-11      epilogue: TMEM -> registers; either the output tile (rounded once) or, along
+//                   a chain (RS ranks or AG K-splits), the running sum: element c of the chain
+//                   acquires flag (c-1, tile), adds its partial to the fp32 running sum of
+//                   elements 0..c-1, stores it and releases flag (c, tile); the last element
+//                   rounds and stores the output. The order is fixed, so results are
+//                   bit-identical run to run.
+//
+// The chunk/flag pipeline follows the Triton-distributed article (cronfeed.work), section "The
+// first move was to expose the overlap" (chunks, compute on arrived chunks while others move,
+// communication and computation blocks coordinated in one kernel through symmetric memory and
+// signals) and section "DITRON adds three levels of tiling" (core-level tiles on tensor cores and
+// TMA; collectives split into chunks paired with compute tiles, with synchronisation inserted).
+//
+// Every wait is bounded by p.timeout_ns (%globaltimer); a wait that runs out records an error in
+// the workspace status word and sets a CTA-wide abort flag; all roles then stop issuing work, the
+// MMA issuer waits for its in-flight MMAs, the TMA issuer for its in-flight loads, TMEM is freed and
+// the kernel returns. Nothing traps.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "tdx_internal.h"
+#include "tdx_ptx.cuh"
+
+namespace tdx {
+
+template <int BN, bool FP8>
+struct Cfg {
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int BK = 128 / ELT;            // K elements per ring slot (128 bytes)
+  static constexpr int UMMA_K = 32 / ELT;         // K per tcgen05.mma (32 bytes)
+  static constexpr int K_STEPS = BK / UMMA_K;     // 4
+  static constexpr int A_BYTES = kBM * 128;       // 16 KiB
+  static constexpr int B_BOX_N = 128 / ELT;       // N elements per B box (128 bytes)
+  static constexpr int B_BOXES = BN / B_BOX_N;
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+  static constexpr int COLS_PER_WARP = BN / 2;    // 8 epilogue warps = 4 lane quarters x 2 halves
+  static constexpr int CHUNKS = COLS_PER_WARP / 32;
+  // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B type (bits 7-9, 10-12: bf16 = 1,
+  // e4m3 = 0), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 (bits 17-22),
+  // M >> 4 (bits 24-28).
+  static constexpr uint32_t IDESC = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
+                                    (1u << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                    (static_cast<uint32_t>(kBM >> 4) << 24);
+  static_assert(BN % B_BOX_N == 0 && B_BOXES >= 1, "tile width must cover whole 128-byte boxes");
+  static_assert(CHUNKS >= 1, "at least one 32-column chunk per epilogue warp");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct Item {
+  int c;      // chain element (RS rank, or AG K split)
+  int tile;   // tile id = mt * tiles_n + nt
+  int m0, n0;
+};
+
+__device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN) {
+  Item r;
+  r.c = it / p.T;
+  const int pos = it - r.c * p.T;
+  int mt, nt;
+  if (p.op == OP_AG) {
+    // rank-swizzled arrival order: M-tiles from the first tile whose first row belongs to
+    // self_rank, wrapping around; N-tiles innermost.
+    int start = (p.self_rank * p.M_local + kBM - 1) / kBM;
+    if (start >= p.tiles_m) start = 0;
+    mt = start + pos / p.tiles_n;
+    if (mt >= p.tiles_m) mt -= p.tiles_m;
+    nt = pos % p.tiles_n;
+  } else {
+    mt = pos / p.tiles_n;
+    nt = pos % p.tiles_n;
+  }
+  r.tile = mt * p.tiles_n + nt;
+  r.m0 = mt * kBM;
+  r.n0 = nt * BN;
+  return r;
+}
+
+// K blocks of one work item: an AllGather K split c covers [c*num_kb/L, (c+1)*num_kb/L); a
+// ReduceScatter item (chain element = rank) covers all of K. The host keeps L <= num_kb, so every
+// range is non-empty and the accumulator is always initialised.
+__device__ __forceinline__ void k_range(const KParams& p, const Item& w, int& kb0, int& kb1) {
+  if (p.op == OP_AG) {
+    kb0 = static_cast<int>((static_cast<long long>(w.c) * p.num_kb) / p.L);
+    kb1 = static_cast<int>((static_cast<long long>(w.c + 1) * p.num_kb) / p.L);
+  } else {
+    kb0 = 0;
+    kb1 = p.num_kb;
+  }
+}
+
+__device__ __forceinline__ void report_error(const KParams& p, uint32_t code, uint32_t role,
+                                             uint32_t idx, uint32_t seen, uint32_t want) {
+  if (atomicCAS(&p.status[0], 0u, code) == 0u) {
+    p.status[1] = role;
+    p.status[2] = blockIdx.x;
+    p.status[3] = idx;
+    p.status[4] = seen;
+    p.status[5] = want;
+    __threadfence();
+  }
+}
+
+__device__ __forceinline__ uint32_t perturb_hash(uint32_t seed, uint32_t x) {
+  uint32_t h = seed ^ (x * 0x9E3779B9u);
+  h ^= h >> 16;
+  h *= 0x7FEB352Du;
+  h ^= h >> 15;
+  return h;
+}
+
+// Bounded wait on an mbarrier phase. Gives up (false) when the CTA abort flag is raised or after
+// p.timeout_ns; a timeout is recorded as DEV_TIMEOUT / ROLE_PIPE.
+static __device__ __noinline__ bool wait_mbar(const KParams& p, uint32_t bar, uint32_t parity,
+                                       volatile int* abort_flag, uint32_t idx) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        report_error(p, DEV_TIMEOUT, ROLE_PIPE, idx, 0, parity);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while tearing down: ignores the abort flag, bounded by the timeout only.
+static __device__ __noinline__ bool wait_mbar_drain(const KParams& p, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > p.timeout_ns) {
+      report_error(p, DEV_TIMEOUT, ROLE_PIPE, 0xFFFFu, 0, parity);
+      return false;
+    }
+  }
+}
+
+// Bounded acquire-wait until *flag == epoch. A value above the epoch is a stale flag. Also gives
+// up when any CTA has already recorded an error (status word != 0) or this CTA aborted.
+static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* flag, uint32_t role,
+                                       uint32_t idx, volatile int* abort_flag, uint64_t* waited_ns) {
+  uint32_t v = ld_acquire_gpu(flag);
+  if (v == p.epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (v > p.epoch) {
+      report_error(p, DEV_STALE, role, idx, v, p.epoch);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(32);
+    v = ld_acquire_gpu(flag);
+    if (v == p.epoch) {
+      *waited_ns += globaltimer_ns() - t0;
+      return true;
+    }
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (ld_relaxed_gpu(p.status) != 0u) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        report_error(p, DEV_TIMEOUT, role, idx, v, p.epoch);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <int BN, bool FP8>
+__global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<BN, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  // misc[0] TMEM base, misc[1] abort flag, misc[2] TMA k-blocks issued, misc[3] MMA k-blocks
+  // consumed, misc[4] epilogue go/stop decision
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + C::STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * C::STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * C::STAGES + 2);
+  const uint32_t drain_bar = smem_u32(bars + 2 * C::STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 1);
+    }
+    mbar_init(drain_bar, 1);
+    misc[1] = 0;
+    misc[2] = 0;
+    misc[3] = 0;
+    misc[4] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&misc[0]), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == kTmaWarp * 32) {
+    for (int i = 0; i < (p.op == OP_AG ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
+    for (int i = 0; i < (p.op == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+
+  const bool ag = p.op == OP_AG;
+  const bool ag_move_only = ag && p.mode == MODE_MOVE_ONLY;
+  const bool rs_move_only = !ag && p.mode == MODE_MOVE_ONLY;
+  const int items = ag_move_only ? 0 : p.L * p.T;
+  const bool use_mma = !rs_move_only;  // RS move-only runs the chain on zero partials
+  const bool chain = p.L > 1 && !(!ag && p.mode == MODE_GEMM_ONLY);
+  const int grid = gridDim.x;
+  uint32_t* trace = p.trace;
+  const int per_cta = (items + grid - 1) / grid;
+
+  if (trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    trace[0] = grid;
+    trace[1] = items;
+    trace[2] = p.L;
+    trace[3] = p.T;
+  }
+
+  if (warp == kTmaWarp) {
+    // =============================================================== TMA issuer
+    if (lane == 0 && use_mma) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      uint64_t flag_ns = 0;
+      uint32_t n_waits = 0;
+      bool stop = false;
+      for (int it = blockIdx.x; it < items && !stop; it += grid) {
+        if (*abort_flag) break;
+        const Item w = decode_item(p, it, BN);
+        const CUtensorMap* map_a;
+        const CUtensorMap* map_b;
+        int arow = w.m0;
+        if (ag) {
+          map_b = &p.tm_b[0];
+          const int self_lo = p.self_rank * p.M_local;
+          const bool self_tile = w.m0 >= self_lo && w.m0 + kBM <= self_lo + p.M_local;
+          if (self_tile) {
+            map_a = &p.tm_a[1];
+            arow = w.m0 - self_lo;
+          } else {
+            map_a = &p.tm_a[0];
+            if (p.wait_flags) {
+              if (p.perturb) __nanosleep(perturb_hash(p.perturb, it) & 4095u);
+              const int last_row = min(w.m0 + kBM, p.M) - 1;
+              for (int gc = w.m0 / p.chunk_rows; gc <= last_row / p.chunk_rows; ++gc) {
+                ++n_waits;
+                if (!wait_flag(p, p.chunk_flags + gc, ROLE_FLAG, gc, abort_flag, &flag_ns)) {
+                  stop = true;
+                  break;
+                }
+              }
+              if (stop) break;
+              fence_proxy_async_global();
+            }
+          }
+        } else {
+          map_a = &p.tm_a[w.c];
+          map_b = &p.tm_b[w.c];
+        }
+        int kb0, kb1;
+        k_range(p, w, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_mbar(p, empty0 + 8 * stage, phase ^ 1u, abort_flag, 100 + stage)) {
+            stop = true;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow);
+#pragma unroll
+          for (int j = 0; j < C::B_BOXES; ++j)
+            tma_load_2d(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                        w.n0 + j * C::B_BOX_N, kb * C::BK);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      misc[2] = issued;
+      if (trace != nullptr) {
+        uint32_t* st = trace + 4 + 4 * blockIdx.x;
+        st[0] = static_cast<uint32_t>(flag_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : flag_ns);
+        st[1] = n_waits;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // =============================================================== MMA issuer
+    if (lane == 0 && use_mma) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t consumed = 0;
+      int local = 0;
+      bool stop = false;
+      for (int it = blockIdx.x; it < items && !stop; it += grid, ++local) {
+        const Item w = decode_item(p, it, BN);
+        const int acc = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!wait_mbar(p, tempty0 + 8 * acc, aph ^ 1u, abort_flag, 200 + acc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        int kb0, kb1;
+        k_range(p, w, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_mbar(p, full0 + 8 * stage, phase, abort_flag, 300 + stage)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < C::K_STEPS; ++k) {
+            const uint64_t adesc = sw128_desc(a_addr + k * 32, 16, 1024);
+            const uint64_t bdesc = sw128_desc(b_addr + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024);
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+            if constexpr (FP8)
+              umma_f8(d, adesc, bdesc, C::IDESC, accum);
+            else
+              umma_bf16(d, adesc, bdesc, C::IDESC, accum);
+          }
+          tc_commit(empty0 + 8 * stage);
+          ++consumed;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+        tc_commit(tfull0 + 8 * acc);
+      }
+      // every MMA issued by this thread has completed once the drain barrier flips
+      tc_commit(drain_bar);
+      wait_mbar_drain(p, drain_bar, 0);
+      misc[3] = consumed;
+    }
+  } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
+    // =============================================================== AllGather producer
+    if (p.copy_active) {
+      const int ct = threadIdx.x - kCopyWarp0 * 32;
+      constexpr int kVec = kPieceBytes / (16 * kCopyThreads);   // 16 vectors per thread
+      for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
+        const int q = piece / p.ppc;            // chunk position in release order
+        const int pc = piece - q * p.ppc;
+        const int rr = q / p.n_chunks;
+        const int rank = (p.self_rank + 1 + rr) % p.W;   // peers in ring order, self last
+        const int ck = q - rr * p.n_chunks;
+        const long long off = (long long)pc * kPieceBytes;
+        const long long rem = p.chunk_bytes - off;
+        const int n = rem < kPieceBytes ? static_cast<int>(rem) : kPieceBytes;
+        const uint8_t* src = p.shard[rank] + (long long)ck * p.chunk_bytes + off;
+        uint8_t* dst = p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off;
+        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
+        uint4 v[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const int b = (j * kCopyThreads + ct) * 16;
+          if (b < n) v[j] = ld_nc_v4(src + b);
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const int b = (j * kCopyThreads + ct) * 16;
+          if (b < n) st_v4(dst + b, v[j]);
+        }
+        named_bar_sync(2, kCopyThreads);
+        if (ct == 0) {
+          const int fi = rank * p.n_chunks + ck;
+          __threadfence();
+          const uint32_t old = atomicAdd(p.chunk_cnt + fi, 1u);
+          if (old == static_cast<uint32_t>(p.ppc - 1)) {
+            p.chunk_cnt[fi] = 0u;
+            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
+            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
+            __threadfence();
+            st_release_gpu(p.chunk_flags + fi, p.epoch);
+          }
+        }
+      }
+    }
+  } else {
+    // =============================================================== epilogue
+    const int e = warp - kEpiWarp0;           // 0..7
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int h = e >> 2;                     // column half
+    const int row_in_tile = q * 32 + lane;
+    const bool elected = threadIdx.x == kEpiWarp0 * 32;
+    volatile uint32_t* decision = misc + 4;
+    uint64_t chain_ns = 0;
+    int local = 0;
+    for (int it = blockIdx.x; it < items; it += grid, ++local) {
+      const Item w = decode_item(p, it, BN);
+      const int acc = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      const bool read_s = chain && w.c > 0;
+      const bool final_out = (!chain && !(!ag && p.mode == MODE_GEMM_ONLY)) || (chain && w.c == p.L - 1);
+      const bool write_s = (chain && w.c < p.L - 1) || (!ag && p.mode == MODE_GEMM_ONLY);
+      if (elected) {
+        bool ok = true;
+        if (use_mma) ok = wait_mbar(p, tfull0 + 8 * acc, aph, abort_flag, 400 + acc);
+        if (ok && read_s) {
+          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x20000u + it) & 4095u);
+          ok = wait_flag(p, p.chain_flags + (size_t)(w.c - 1) * p.T + w.tile, ROLE_CHAIN,
+                         (w.c - 1) * p.T + w.tile, abort_flag, &chain_ns);
+        }
+        if (*abort_flag) ok = false;
+        *decision = ok ? 1u : 0u;
+        if (trace != nullptr && ok) trace[4 + 4 * grid + blockIdx.x * per_cta + local] = (static_cast<uint32_t>(w.c) << 24) | static_cast<uint32_t>(w.tile);
+      }
+      named_bar_sync(1, kEpiThreads);
+      if (*decision == 0u) break;
+      tc_fence_after();
+
+      const int row = w.m0 + row_in_tile;
+      float* sb = p.sbuf + (size_t)w.tile * (kBM * BN);
+#pragma unroll 1
+      for (int ch = 0; ch < C::CHUNKS; ++ch) {
+        const int col0 = h * C::COLS_PER_WARP + ch * 32;   // column inside the tile
+        float v[32];
+        if (use_mma) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * BN + col0),
+                             r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        // running-sum layout: element (row i, col 32*cc + 4*j + t) of a tile sits at float
+        // ((cc*8 + j)*128 + i)*4 + t, so a warp's 32 rows read 512 contiguous bytes per vector
+        float* sp = sb + ((size_t)(col0 >> 5) * 8 * kBM + row_in_tile) * 4;
+        if (read_s) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 s = ld_cg_f4(sp + j * kBM * 4);
+            v[4 * j + 0] = s.x + v[4 * j + 0];
+            v[4 * j + 1] = s.y + v[4 * j + 1];
+            v[4 * j + 2] = s.z + v[4 * j + 2];
+            v[4 * j + 3] = s.w + v[4 * j + 3];
+          }
+        }
+        if (write_s) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_f4(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+        if (final_out && row < p.M) {
+          uint8_t* orow;
+          if (ag) {
+            if (FP8) {
+              const float s = p.row_scale[row / p.M_local];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= s;
+            }
+            orow = p.out[0] + (size_t)row * p.N * (p.out_fp32 ? 4 : 2);
+          } else {
+            const int j = row / p.M_local;
+            orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
+          }
+          const int col = w.n0 + col0;
+          if (p.out_fp32) {
+            float* o = reinterpret_cast<float*>(orow) + col;
+            if (col + 32 <= p.N) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                st_f4(o + 4 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col + i < p.N) o[i] = v[i];
+            }
+          } else {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(orow) + col;
+            if (col + 32 <= p.N) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 pk;
+                __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
+                __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+                __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+                pk.x = *reinterpret_cast<uint32_t*>(&b0);
+                pk.y = *reinterpret_cast<uint32_t*>(&b1);
+                pk.z = *reinterpret_cast<uint32_t*>(&b2);
+                pk.w = *reinterpret_cast<uint32_t*>(&b3);
+                st_v4(o + 8 * j, pk);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col + i < p.N) o[i] = __float2bfloat16_rn(v[i]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, kEpiThreads);
+      if (elected) {
+        if (use_mma) mbar_arrive(tempty0 + 8 * acc);
+        if (chain && write_s) {
+          __threadfence();
+          st_release_gpu(p.chain_flags + (size_t)w.c * p.T + w.tile, p.epoch);
+        }
+      }
+    }
+    if (elected && trace != nullptr) {
+      uint32_t* st = trace + 4 + 4 * blockIdx.x;
+      st[2] = static_cast<uint32_t>(chain_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : chain_ns);
+      st[3] = static_cast<uint32_t>(local);
+    }
+  }
+
+  // =============================================================== teardown
+  __syncthreads();
+  if (threadIdx.x == kTmaWarp * 32 && use_mma) {
+    // loads issued but never consumed by the MMA issuer (abort path) must land before exit
+    const uint32_t issued = misc[2];
+    const uint32_t consumed = misc[3];
+    uint32_t first = consumed;
+    if (issued > static_cast<uint32_t>(C::STAGES) && first < issued - C::STAGES) first = issued - C::STAGES;
+    for (uint32_t i = first; i < issued; ++i)
+      wait_mbar_drain(p, full0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, bool FP8>
+cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
+  using C = Cfg<BN, FP8>;
+  cudaError_t e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8>, p);
+}
+
+}  // namespace tdx

@@ -1,0 +1,170 @@
+/*
+ * tdx.h -- C ABI of the tile-pipelined AllGather+GEMM and GEMM+ReduceScatter library (sm_103a).
+ *
+ * What the operations are. The Triton-distributed article on cronfeed.work ("Triton-distributed
+ * is turning communication into compiler territory"), section "The first move was to expose the
+ * overlap", describes an AllGather that moves row shards into place feeding a GEMM, split into
+ * chunks so that the GEMM computes on one chunk while another is still moving, and the mirror
+ * operation GEMM-plus-ReduceScatter; communication and computation thread blocks of one kernel
+ * are coordinated through symmetric memory and signals. Section "DITRON adds three levels of
+ * tiling" adds that collectives such as AllGather and ReduceScatter are broken into chunks, paired
+ * with compute tiles, and synchronised. This library implements those two kernels for one GPU:
+ * the W ranks are logical, i.e. W shard buffers (and, for ReduceScatter, W partial products) in
+ * one device's memory; the "network" is a chunk producer that copies shard chunks into a
+ * symmetric gathered buffer and releases one flag per chunk, and the GEMM tiles acquire those
+ * flags before they read a chunk.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: every tensor and the workspace are device memory owned by the caller. The library
+ *    allocates nothing per call and keeps no pointer after a call returns.
+ *  - Layout: all matrices are dense and row-major with no padding (row pitch = columns * element
+ *    size). Each row pitch must be a multiple of 16 bytes and each pointer 16-byte aligned.
+ *  - Asynchrony: calls are stream-ordered on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return before the work runs. The returned status covers host-side validation and
+ *    launch errors only. Errors found on the device (a bounded wait that timed out, a stale epoch)
+ *    are recorded in the workspace's status word; read them with tdx_read_device_status. Kernels
+ *    never trap: a failed wait makes the kernel stop issuing work, drain what it started and exit.
+ *  - Threading: a workspace is used by one call at a time (calls that overlap on the GPU and share a
+ *    workspace race). Different workspaces may be used concurrently.
+ *  - No fallback: shapes the kernels cannot tile return TDX_ERR_UNSUPPORTED; nothing runs on the CPU.
+ */
+#ifndef TDX_H_
+#define TDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TDX_OK = 0,
+  TDX_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, W out of range, bad enum */
+  TDX_ERR_UNSUPPORTED = 2,   /* valid request the kernels do not implement (dtype combination, tiling) */
+  TDX_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned or row pitch not a multiple of 16 bytes */
+  TDX_ERR_WORKSPACE = 4,     /* workspace null, misaligned (256 B) or smaller than tdx_workspace_size */
+  TDX_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (launch, tensor map, memset) */
+  TDX_ERR_TIMEOUT = 6,       /* device: a bounded wait on a flag or pipeline barrier ran out */
+  TDX_ERR_STALE_EPOCH = 7    /* device: a flag already held an epoch >= the call's epoch */
+} tdx_status;
+
+typedef enum { TDX_BF16 = 0, TDX_FP8_E4M3 = 1, TDX_FP32 = 2 } tdx_dtype;
+
+typedef enum {
+  TDX_FUSED = 0,          /* producer and consumer overlapped in one persistent kernel (default) */
+  TDX_GEMM_ONLY = 1,      /* AG: GEMM on an already gathered buffer, no flag waits, no copies.
+                             RS: every rank's fp32 partial tile stored, no rank chain, no output */
+  TDX_MOVE_ONLY = 2,      /* AG: chunk copies and flag releases only. RS: the rank-order
+                             read-add-write chain over the running-sum buffer with zero partials */
+  TDX_CONSUMER_ONLY = 3   /* AG: consumers wait on flags that no producer releases (fault tests) */
+} tdx_mode;
+
+typedef enum {
+  TDX_PRODUCER_SM = 0,          /* chunk copies by producer warps of the persistent kernel */
+  TDX_PRODUCER_COPY_ENGINE = 1  /* chunk copies by cudaMemcpyAsync on a side stream + stream flag writes */
+} tdx_producer;
+
+/* Per-call options. Pass NULL for all defaults; tdx_opts_default fills the same values. */
+typedef struct tdx_opts {
+  int self_rank;             /* AG: rank whose shard is local; arrival order self, self+1, ... (default 0) */
+  int chunk_rows;            /* AG: rows per chunk and per flag; must divide M_local (default min(128, M_local)) */
+  tdx_dtype out_dtype;       /* AG: TDX_BF16 (default) or TDX_FP32. RS: TDX_BF16 only */
+  const float* scale_a;      /* host array [W]: per-shard dequantisation scales for e4m3 (NULL = 1) */
+  const float* scale_b;      /* host pointer to B's dequantisation scale for e4m3 (NULL = 1) */
+  tdx_mode mode;             /* default TDX_FUSED */
+  tdx_producer producer;     /* default TDX_PRODUCER_SM */
+  uint32_t epoch;            /* 0: the library clears the flags on `stream` and uses epoch 1.
+                                >0: flags are not cleared; the caller passes strictly increasing
+                                epochs on one workspace (after tdx_workspace_init) */
+  uint64_t timeout_ns;       /* bound of every device-side wait (default 2e9 ns) */
+  uint32_t perturb_seed;     /* test only: !=0 injects pseudo-random delays in producers/epilogues */
+  void* trace;               /* optional device buffer of tdx_trace_size() bytes, or NULL */
+  int num_sms;               /* persistent grid size; 0 = every SM of the device */
+  int split_k;               /* AG: K splits reduced in fixed order (0 = library choice, 1 = none) */
+  int block_n;               /* GEMM tile width 64/128/256 (0 = library choice) */
+} tdx_opts;
+
+/* Fill *opts with the defaults above. Returns TDX_ERR_INVALID_ARG if opts is NULL. */
+tdx_status tdx_opts_default(tdx_opts* opts);
+
+/* Bytes of workspace needed by one call. op = 0: AllGather+GEMM (M_local_or_M = rows per shard);
+ * op = 1: GEMM+ReduceScatter (M_local_or_M = rows of every A_r). The workspace holds the status
+ * word, the chunk flags, the symmetric gathered buffer G (AG, (W*M_local) x K of `dtype`) and the
+ * fp32 running-sum buffer with its rank-chain flags (RS, and AG with split K). Writes *bytes. */
+tdx_status tdx_workspace_size(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
+                              const tdx_opts* opts, size_t* bytes);
+
+/* Zero the control region of a workspace (status word, flags, counters) on `stream`. Call once
+ * after allocating a workspace, and again after a call reported a device-side error. */
+tdx_status tdx_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* AllGather+GEMM: C = concat_r(shards[r]) @ B, the shards gathered in rank order 0..W-1.
+ * (Triton-distributed article, section "The first move was to expose the overlap": the AllGather
+ * moves shards into place, split into chunks, and the GEMM consumes each chunk once it has arrived.)
+ *  shards     host array of W device pointers; shards[r] is M_local x K of `dtype`, row-major.
+ *  B          device, K x N of `dtype`, row-major.
+ *  C          device, (W*M_local) x N, row-major, of opts->out_dtype (bf16 or fp32). Row
+ *             r*M_local + i of C is row i of shards[r] times B, whatever the arrival order.
+ *  workspace  device, 256-byte aligned, workspace_bytes >= tdx_workspace_size(0, ...) with the
+ *             same shapes and opts (else TDX_ERR_WORKSPACE). After the call its gathered buffer
+ *             holds concat_r(shards[r]) and every chunk flag holds the epoch.
+ *  W          logical ranks, 1..16. M_local, K, N >= 0 (M_local or N == 0: nothing is launched;
+ *             K == 0: C is filled with zeros).
+ *  dtype      TDX_BF16, or TDX_FP8_E4M3 with per-tensor scales: C = scale_a[r]*scale_b*(shard @ B).
+ * Accumulation is fp32 on the tensor cores; the output is rounded once, to nearest even. */
+tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* workspace,
+                       size_t workspace_bytes, int W, int M_local, int K, int N, tdx_dtype dtype,
+                       const tdx_opts* opts, void* stream);
+
+/* GEMM+ReduceScatter: S = sum_{r=0}^{W-1} A_parts[r] @ B_parts[r], out_shards[j] = rows
+ * [j*M/W, (j+1)*M/W) of S. (Same article and section: "GEMM-plus-ReduceScatter"; section "DITRON
+ * adds three levels of tiling" lists ReduceScatter among the collectives split into chunks.)
+ *  A_parts    host array of W device pointers, each M x K bf16 row-major.
+ *  B_parts    host array of W device pointers, each K x N bf16 row-major.
+ *  out_shards host array of W device pointers, each (M/W) x N bf16 row-major.
+ *  workspace  device, 256-byte aligned, workspace_bytes >= tdx_workspace_size(1, ...) with the
+ *             same shapes and opts (else TDX_ERR_WORKSPACE).
+ *  W          1..16, and M must be a multiple of W.
+ * Rank r's fp32 partial tile is added to the running sum of ranks 0..r-1 in that fixed order,
+ * ((P_0 + P_1) + P_2) + ..., whatever the timing, so the result is identical run to run; the sum
+ * is rounded once to bf16 (nearest even). */
+tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
+                       void* const* out_shards, void* workspace, size_t workspace_bytes,
+                       int W, int M, int K, int N, tdx_dtype dtype,
+                       const tdx_opts* opts, void* stream);
+
+/* Synchronise `stream`, then read the workspace's device status word into *out (TDX_OK, or the
+ * first device-side error since tdx_workspace_init). If detail is not NULL it receives 8 words:
+ * [0] status, [1] role that failed (1 flag wait, 2 pipeline wait, 3 chain wait, 4 producer),
+ * [2] CTA index, [3] flag/barrier index, [4] value observed, [5] value expected, [6..7] reserved. */
+tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_status* out,
+                                  uint32_t* detail);
+
+/* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
+ * uses. Writes 16 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
+ * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] 128-byte K blocks, [6] chunk rows, [7] chunks per rank,
+ * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
+ * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
+ * buffer G, [12] fp32 running-sum buffer, [13] total workspace bytes; [14..15] reserved (0). */
+tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
+                         const tdx_opts* opts, int64_t* info);
+
+/* Bytes of the optional trace buffer for a call on `grid` CTAs taking `items` work items:
+ * words [0..3] = {grid, items, chain length, tiles}; then per CTA 4 statistics words {ns spent
+ * waiting on chunk flags, number of flag waits, ns spent waiting on rank-chain flags, items taken};
+ * then per CTA, in order, the work items it took, one word each: (chain element << 24) | tile id,
+ * tile id = m_tile * N-tiles + n_tile. CTA b takes items b, b + grid, b + 2*grid, ... */
+size_t tdx_trace_size(int grid, int items);
+
+/* Static description of a status code. Never NULL. */
+const char* tdx_status_string(tdx_status s);
+
+/* Library version, (major << 16) | minor. */
+uint32_t tdx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDX_H_ */

@@ -1,0 +1,134 @@
+"""Helpers for the GPU tests: move workloads.py inputs to the device, call the C ABI through the
+Python binding, bring outputs back as numpy, and compare them with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import comm_overlapped_gemm_gb300 as tdx
+from oracle import reference as R
+
+TOL = {"bf16": 1e-2, "e4m3": 4e-2}
+
+
+def dev_bits(a: np.ndarray) -> torch.Tensor:
+    """uint16 (bf16 bits) or uint8 (e4m3 codes) host array -> device tensor with the same bytes."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def workspace(op, W, Mx, K, N, dtype, opts=None) -> torch.Tensor:
+    n = tdx.tdx_workspace_size(op, W, Mx, K, N, dtype, opts)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    tdx.check(tdx.tdx_workspace_init(ws), "init")
+    return ws
+
+
+def dtype_code(name: str) -> int:
+    return tdx.TDX_BF16 if name == "bf16" else tdx.TDX_FP8_E4M3
+
+
+class AGCase:
+    """Device buffers of one AllGather+GEMM problem."""
+
+    def __init__(self, inp, out_dtype="bf16", opts=None):
+        wl = inp.wl
+        self.inp, self.wl = inp, wl
+        self.W, self.M_local, self.K, self.N = wl.W, wl.M, wl.K, wl.N
+        self.dt = dtype_code(wl.dtype)
+        self.shards = [dev_bits(a) for a in inp.a]
+        self.B = dev_bits(inp.b[0])
+        tdt = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+        self.C = torch.full((wl.W * wl.M, wl.N), float("nan"), dtype=tdt, device="cuda")
+        self.out_dtype = out_dtype
+        self.opts = opts
+        self.ws = workspace(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, self.dt, opts)
+
+    def run(self, opts=None):
+        o = opts if opts is not None else self.opts
+        return tdx.tdx_ag_gemm(self.shards, self.B, self.C, self.ws, self.W, self.M_local, self.K, self.N,
+                               self.dt, o)
+
+    def result(self) -> np.ndarray:
+        torch.cuda.synchronize()
+        if self.out_dtype == "fp32":
+            return self.C.cpu().numpy().astype(np.float64)
+        return R.decode_bf16(host_bits(self.C))
+
+    def result_bits(self) -> np.ndarray:
+        torch.cuda.synchronize()
+        return host_bits(self.C)
+
+    def oracle(self, rows=None):
+        i = self.inp
+        sa = i.scale_a if self.wl.dtype == "e4m3" else None
+        sb = i.scale_b[0] if self.wl.dtype == "e4m3" else None
+        if rows is None:
+            return R.ag_gemm(i.a, i.b[0], self.wl.dtype, sa, sb)
+        return R.ag_gemm_rows(i.a, i.b[0], rows, self.wl.dtype, sa, sb)
+
+
+class RSCase:
+    def __init__(self, inp, opts=None):
+        wl = inp.wl
+        self.inp, self.wl = inp, wl
+        self.W, self.M, self.K, self.N = wl.W, wl.M, wl.K, wl.N
+        self.A = [dev_bits(a) for a in inp.a]
+        self.B = [dev_bits(b) for b in inp.b]
+        self.out = [torch.full((wl.M // wl.W, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+                    for _ in range(wl.W)]
+        self.opts = opts
+        self.ws = workspace(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, opts)
+
+    def run(self, opts=None):
+        o = opts if opts is not None else self.opts
+        return tdx.tdx_gemm_rs(self.A, self.B, self.out, self.ws, self.W, self.M, self.K, self.N,
+                               tdx.TDX_BF16, o)
+
+    def result_bits(self) -> np.ndarray:
+        torch.cuda.synchronize()
+        return np.concatenate([host_bits(o) for o in self.out])
+
+    def result(self) -> np.ndarray:
+        return R.decode_bf16(self.result_bits())
+
+    def oracle(self, rows=None):
+        if rows is None:
+            return np.concatenate(R.gemm_rs(self.inp.a, self.inp.b, "bf16"))
+        return R.gemm_rs_rows(self.inp.a, self.inp.b, rows, "bf16")
+
+
+def assert_bit_exact(got_bits: np.ndarray, oracle_fp64: np.ndarray, out_dtype: str):
+    want = R.round_out(oracle_fp64, out_dtype)
+    if out_dtype == "fp32":
+        got_bits = np.asarray(got_bits, dtype=np.float32)
+        bad = np.argwhere(got_bits != want)
+    else:
+        bad = np.argwhere(got_bits != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+def assert_within_tol(got: np.ndarray, oracle_fp64: np.ndarray, dtype: str):
+    assert np.all(np.isfinite(got)), "non-finite output"
+    scale = float(np.max(np.abs(oracle_fp64)))
+    err = float(np.max(np.abs(got - oracle_fp64)))
+    assert err <= TOL[dtype] * scale, f"max err {err:.4g} > {TOL[dtype]} * {scale:.4g}"
+    return err / scale if scale else 0.0
+
+
+def sample_rows(M: int, chunk: int, extra_stride: int = 97) -> np.ndarray:
+    """First, second and last row of every chunk (and of every 128-row tile), plus a stride."""
+    rows = set()
+    for c0 in range(0, M, chunk):
+        rows.update({c0, c0 + 1, min(c0 + chunk, M) - 1})
+    for t0 in range(0, M, 128):
+        rows.update({t0, min(t0 + 128, M) - 1, min(t0 + 77, M - 1)})
+    rows.update(range(0, M, extra_stride))
+    return np.array(sorted(rows), dtype=np.int64)

@@ -1,0 +1,152 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every function declared in
+include/tdx.h, and its host-side validation returns the documented status codes without touching a
+device (every pointer below is a fake address that is never dereferenced on the host)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _load_build_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "tdx_build", os.path.join(ROOT, "comm_overlapped_gemm_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _lib_or_skip():
+    build = _load_build_module()
+    if not os.path.exists(build.LIB):
+        build.build()
+    import comm_overlapped_gemm_gb300 as tdx
+    return tdx
+
+
+@pytest.fixture(scope="module")
+def tdx():
+    return _lib_or_skip()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "tdx.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:tdx_status|size_t|uint32_t|const char\*)\s+(tdx_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["tdx_ag_gemm", "tdx_gemm_rs", "tdx_workspace_size", "tdx_read_device_status", "tdx_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(tdx):
+    lib = ctypes.CDLL(tdx.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(tdx.EXPORTED)
+
+
+def test_status_strings_and_version(tdx):
+    for s in range(8):
+        assert tdx.tdx_status_string(s).startswith("TDX_")
+    assert "unknown" in tdx.tdx_status_string(99)
+    assert tdx.tdx_version() >> 16 == 1
+
+
+def test_opts_default(tdx):
+    o = tdx.tdx_opts_default()
+    assert o.self_rank == 0 and o.mode == tdx.TDX_FUSED and o.timeout_ns == 2_000_000_000
+    assert o.epoch == 0 and o.out_dtype == tdx.TDX_BF16
+    assert ctypes.sizeof(tdx.tdx_opts) == 88
+
+
+def test_workspace_sizes(tdx):
+    # AG W=8: gathered buffer 8192 x 8192 bf16 = 128 MiB plus a small control region
+    ws = tdx.tdx_workspace_size(tdx.OP_AG, 8, 1024, 8192, 3584, tdx.TDX_BF16)
+    assert 128 << 20 < ws < (128 << 20) + (1 << 20)
+    # RS W=8: fp32 running sum of one 8192 x 8192 output = 256 MiB plus 7 x 2048 chain flags
+    ws = tdx.tdx_workspace_size(tdx.OP_RS, 8, 8192, 3584, 8192, tdx.TDX_BF16)
+    assert 256 << 20 < ws < (256 << 20) + (1 << 20)
+    # fp8 AG: 16384 x 8192 e4m3 gathered buffer = 128 MiB
+    ws = tdx.tdx_workspace_size(tdx.OP_AG, 8, 2048, 8192, 8192, tdx.TDX_FP8_E4M3)
+    assert 128 << 20 < ws < (128 << 20) + (1 << 20)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 0, 64, 128, 256, 0), 1),      # W = 0
+    ((0, 17, 64, 128, 256, 0), 1),     # W > 16
+    ((0, 2, -1, 128, 256, 0), 1),      # negative size
+    ((1, 3, 128, 128, 256, 0), 1),     # RS: M not a multiple of W
+    ((1, 2, 128, 128, 256, 1), 2),     # RS e4m3 not implemented
+    ((2, 2, 64, 128, 256, 0), 1),      # bad op
+    ((0, 2, 64, 128, 256, 7), 1),      # bad dtype
+])
+def test_workspace_size_rejects(tdx, args, code):
+    with pytest.raises(tdx.TdxError) as e:
+        tdx.tdx_workspace_size(*args)
+    assert e.value.status == code
+
+
+def test_chunk_rows_must_divide_shard(tdx):
+    o = tdx.make_opts(chunk_rows=48)
+    with pytest.raises(tdx.TdxError) as e:
+        tdx.tdx_workspace_size(tdx.OP_AG, 2, 64, 128, 256, tdx.TDX_BF16, o)
+    assert e.value.status == tdx.TDX_ERR_INVALID_ARG
+
+
+FAKE = 0x7F0000000000   # 256-byte aligned fake device address, never dereferenced on the host
+
+
+def _ag(tdx, shards=None, B=FAKE, C=FAKE, ws=FAKE, wsb=1 << 30, W=2, M_local=64, K=128, N=256,
+        dtype=0, opts=None):
+    shards = [FAKE] * W if shards is None else shards
+    return tdx.tdx_ag_gemm(shards, B, C, ws, W, M_local, K, N, dtype, opts, stream=0, workspace_bytes=wsb)
+
+
+def test_ag_validation_codes(tdx):
+    assert _ag(tdx, B=0) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, shards=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, W=0, shards=[FAKE]) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, shards=[FAKE + 8, FAKE]) == tdx.TDX_ERR_ALIGNMENT
+    assert _ag(tdx, C=FAKE + 4) == tdx.TDX_ERR_ALIGNMENT
+    assert _ag(tdx, K=100) == tdx.TDX_ERR_ALIGNMENT           # 200-byte rows
+    assert _ag(tdx, N=100) == tdx.TDX_ERR_ALIGNMENT
+    assert _ag(tdx, ws=0) == tdx.TDX_ERR_WORKSPACE
+    assert _ag(tdx, ws=FAKE + 16) == tdx.TDX_ERR_WORKSPACE
+    assert _ag(tdx, wsb=1024) == tdx.TDX_ERR_WORKSPACE
+    assert _ag(tdx, opts=tdx.make_opts(self_rank=2)) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, opts=tdx.make_opts(out_dtype=1)) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, opts=tdx.make_opts(mode=9)) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
+    assert _ag(tdx, dtype=1, opts=tdx.make_opts(block_n=64)) == tdx.TDX_ERR_UNSUPPORTED
+    # empty problems launch nothing and succeed
+    assert _ag(tdx, M_local=0) == tdx.TDX_OK
+    assert _ag(tdx, N=0) == tdx.TDX_OK
+
+
+def test_rs_validation_codes(tdx):
+    def rs(A=None, B=None, O=None, W=2, M=128, K=128, N=256, dtype=0, opts=None, wsb=1 << 30, ws=FAKE):
+        A = [FAKE] * W if A is None else A
+        B = [FAKE] * W if B is None else B
+        O = [FAKE] * W if O is None else O
+        return tdx.tdx_gemm_rs(A, B, O, ws, W, M, K, N, dtype, opts, stream=0, workspace_bytes=wsb)
+    assert rs(A=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert rs(O=[0, FAKE]) == tdx.TDX_ERR_INVALID_ARG
+    assert rs(M=129) == tdx.TDX_ERR_INVALID_ARG
+    assert rs(dtype=1) == tdx.TDX_ERR_UNSUPPORTED
+    assert rs(opts=tdx.make_opts(out_dtype=2)) == tdx.TDX_ERR_UNSUPPORTED
+    assert rs(B=[FAKE, FAKE + 2]) == tdx.TDX_ERR_ALIGNMENT
+    assert rs(wsb=100) == tdx.TDX_ERR_WORKSPACE
+    assert rs(M=0) == tdx.TDX_OK
+
+
+def test_trace_size(tdx):
+    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 4 * 3)
+    assert tdx.tdx_trace_size(0, 10) == 0

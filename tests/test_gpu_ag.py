@@ -1,0 +1,227 @@
+"""AllGather+GEMM on the GPU through the C ABI, element by element against the CPU oracle.
+
+Integer inputs (U{-4..4}, scales 1) must match the oracle's single rounding of the exact sum bit
+for bit; random inputs must satisfy max|gpu - oracle| <= 1e-2 * max|oracle| (bf16) or 4e-2 (e4m3),
+the bound applied to the fp64 oracle before rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import comm_overlapped_gemm_gb300 as tdx
+from oracle import reference as R
+import workloads as wls
+from gpu_util import AGCase, assert_bit_exact, assert_within_tol, sample_rows, host_bits
+
+pytestmark = pytest.mark.gpu
+
+TMO = int(5e8)   # 0.5 s bound on every device wait in these tests
+
+
+def opts(**kw):
+    return tdx.make_opts(timeout_ns=TMO, **kw)
+
+
+def status_ok(case):
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_OK, (tdx.tdx_status_string(st), detail)
+
+
+def gathered(case, plan):
+    g = case.ws[plan["off_G"]:plan["off_G"] + case.W * case.M_local * case.K * (1 if case.dt else 2)]
+    return g
+
+
+TINY = wls.WORKLOADS["ag_tiny"]
+
+
+@pytest.mark.parametrize("variant", [
+    {}, {"split_k": 1, "block_n": 256}, {"split_k": 1, "block_n": 128}, {"split_k": 1, "block_n": 64},
+    {"self_rank": 1}, {"split_k": 2, "block_n": 256}, {"perturb_seed": 7},
+])
+def test_ag_tiny_integer_bit_exact(variant):
+    inp = wls.make_inputs(TINY, integer=True)
+    o = opts(chunk_rows=32, out_dtype=tdx.TDX_FP32, **variant)
+    case = AGCase(inp, out_dtype="fp32", opts=o)
+    tdx.check(case.run(), "ag tiny")
+    assert_bit_exact(case.C.cpu().numpy(), case.oracle(), "fp32")
+    status_ok(case)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 2, 64, 128, 256, tdx.TDX_BF16, o)
+    g = gathered(case, plan)
+    assert torch.equal(g, torch.cat(case.shards).view(torch.uint8).flatten())
+    flags = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * 2 * plan["n_chunks"]].view(torch.int32)
+    assert np.array_equal(flags.cpu().numpy().astype(np.uint32), R.expected_flags(2 * plan["n_chunks"], 1))
+
+
+def test_ag_tiny_random_within_tolerance():
+    inp = wls.make_inputs(TINY, integer=False)
+    case = AGCase(inp, out_dtype="fp32", opts=opts(chunk_rows=32, out_dtype=tdx.TDX_FP32))
+    tdx.check(case.run())
+    got = case.result()
+    rel = assert_within_tol(got, case.oracle(), "bf16")
+    assert rel < 1e-5   # fp32 output of an fp32-accumulated 128-term sum
+
+
+@pytest.mark.parametrize("name", ["ag_w8", "ag_fp8_w8"])
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_full_size_sampled(name, integer):
+    wl = wls.WORKLOADS[name]
+    inp = wls.make_inputs(wl, integer=integer)
+    o = opts(scale_a=inp.scale_a, scale_b=inp.scale_b[0]) if wl.dtype == "e4m3" else opts()
+    case = AGCase(inp, opts=o)
+    tdx.check(case.run(), name)
+    status_ok(case)
+    rows = sample_rows(wl.W * wl.M, wl.chunk_rows)
+    got_bits = case.result_bits()[rows]
+    want = case.oracle(rows)
+    if integer:
+        assert_bit_exact(got_bits, want, "bf16")
+    else:
+        assert_within_tol(R.decode_bf16(got_bits), want, wl.dtype)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, case.dt, case.opts)
+    assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_small_m_full_output(integer):
+    wl = wls.WORKLOADS["ag_small"]
+    inp = wls.make_inputs(wl, integer=integer)
+    case = AGCase(inp, opts=opts())
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+
+
+@pytest.mark.parametrize("shape", [
+    dict(W=3, M=96, K=320, N=200, chunk_rows=32),     # tiles span ranks, ragged K and N
+    dict(W=1, M=200, K=136, N=264, chunk_rows=40),    # one rank, ragged M tile
+    dict(W=5, M=64, K=1024, N=72, chunk_rows=16),
+    dict(W=16, M=8, K=64, N=128, chunk_rows=8),       # maximum W
+])
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_ragged_shapes(shape, integer):
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    for variant in [{}, {"split_k": 1}, {"split_k": 3, "block_n": 128}]:
+        case = AGCase(inp, opts=opts(chunk_rows=shape["chunk_rows"], **variant))
+        tdx.check(case.run(), str(variant))
+        status_ok(case)
+        if integer:
+            assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+        else:
+            assert_within_tol(case.result(), case.oracle(), "bf16")
+
+
+def test_ag_fp8_ragged_and_scales():
+    wl = wls.with_shape(wls.WORKLOADS["ag_fp8_w8"], W=3, M=128, K=384, N=384, chunk_rows=64)
+    inp = wls.make_inputs(wl, integer=False)
+    case = AGCase(inp, opts=opts(chunk_rows=64, scale_a=inp.scale_a, scale_b=inp.scale_b[0]))
+    tdx.check(case.run())
+    status_ok(case)
+    assert_within_tol(case.result(), case.oracle(), "e4m3")
+
+
+@pytest.mark.parametrize("self_rank", [0, 3, 7])
+def test_ag_self_rank_and_trace_follow_the_oracle_schedule(self_rank):
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=512, N=512, chunk_rows=128)
+    inp = wls.make_inputs(wl, integer=True)
+    grid = 16
+    o = opts(self_rank=self_rank, num_sms=grid)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 512, 512, tdx.TDX_BF16, o)
+    items = plan["L"] * plan["T"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    o = opts(self_rank=self_rank, num_sms=grid, trace=trace)
+    case = AGCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    tr = trace.cpu().numpy().astype(np.uint32)
+    assert list(tr[:4]) == [grid, items, plan["L"], plan["T"]]
+    sched = R.ag_tile_schedule(8, 256, 512, 128, plan["BN"], self_rank)
+    per = (items + grid - 1) // grid
+    for b in range(grid):
+        mine = list(range(b, items, grid))
+        assert tr[4 + 4 * b + 3] == len(mine)
+        for k, it in enumerate(mine):
+            c, pos = divmod(it, plan["T"])
+            mt, nt = sched[pos]
+            assert tr[4 + 4 * grid + b * per + k] == (c << 24) | (mt * plan["tiles_n"] + nt)
+
+
+def test_ag_modes_and_epochs():
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=512, N=768, chunk_rows=64)
+    inp = wls.make_inputs(wl, integer=True)
+    case = AGCase(inp, opts=opts(chunk_rows=64))
+    want = R.round_out(case.oracle(), "bf16")
+    # epoch mode: strictly increasing epochs, no clearing between calls
+    for e in (5, 6, 9):
+        case.C.fill_(float("nan"))
+        tdx.check(case.run(opts(chunk_rows=64, epoch=e)))
+        assert np.array_equal(case.result_bits(), want)
+        plan = tdx.tdx_plan_info(tdx.OP_AG, 4, 256, 512, 768, tdx.TDX_BF16, case.opts)
+        n = 4 * plan["n_chunks"]
+        f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
+        assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, e))
+        status_ok(case)
+    # GEMM_ONLY reads the already gathered buffer
+    case.C.fill_(float("nan"))
+    tdx.check(case.run(opts(chunk_rows=64, mode=tdx.TDX_GEMM_ONLY)))
+    assert np.array_equal(case.result_bits(), want)
+    # MOVE_ONLY gathers and leaves C alone
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 4, 256, 512, 768, tdx.TDX_BF16, case.opts)
+    case.ws[plan["off_G"]:plan["off_G"] + 4 * 256 * 512 * 2].zero_()
+    case.C.fill_(0.0)
+    tdx.check(case.run(opts(chunk_rows=64, mode=tdx.TDX_MOVE_ONLY)))
+    torch.cuda.synchronize()
+    assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
+    assert int(torch.count_nonzero(case.C)) == 0
+    status_ok(case)
+
+
+def test_ag_degenerate_sizes():
+    # K == 0: C = 0 (empty sums); M_local == 0 and N == 0: nothing to do
+    B = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    shards = [torch.zeros((64, 0), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    C = torch.full((128, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    # zero-size tensors may share address 0; pass aligned dummy pointers instead
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    tdx.check(tdx.tdx_ag_gemm([dummy, dummy], dummy, C, ws, 2, 64, 0, 256, tdx.TDX_BF16, opts()))
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(C)) == 0
+    C2 = torch.full((4, 4), 3.0, dtype=torch.bfloat16, device="cuda")
+    assert tdx.tdx_ag_gemm([dummy], dummy, C2, ws, 1, 0, 128, 256, tdx.TDX_BF16, opts()) == tdx.TDX_OK
+    assert tdx.tdx_ag_gemm([dummy], dummy, C2, ws, 1, 4, 128, 0, tdx.TDX_BF16, opts()) == tdx.TDX_OK
+    torch.cuda.synchronize()
+    assert float(C2.float().sum()) == 48.0
+    del B, shards
+
+
+def test_ag_timeout_is_reported_and_workspace_recovers():
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=256, N=256, chunk_rows=128)
+    inp = wls.make_inputs(wl, integer=True)
+    case = AGCase(inp, opts=opts())
+    # no producer releases the flags: every remote tile's wait must run out (2 ms) and report
+    tdx.check(case.run(tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY, timeout_ns=2_000_000)))
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_ERR_TIMEOUT and detail[1] == 1
+    # after re-initialising the workspace a normal call succeeds
+    tdx.check(tdx.tdx_workspace_init(case.ws))
+    tdx.check(case.run(opts()))
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+
+
+def test_ag_stale_epoch_is_reported():
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=256, N=256, chunk_rows=128)
+    inp = wls.make_inputs(wl, integer=True)
+    case = AGCase(inp, opts=opts())
+    tdx.check(case.run(opts(epoch=10)))
+    status_ok(case)
+    tdx.check(case.run(opts(epoch=5, timeout_ns=2_000_000)))
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_ERR_STALE_EPOCH
+    assert detail[4] == 10 and detail[5] == 5

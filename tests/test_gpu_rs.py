@@ -1,0 +1,137 @@
+"""GEMM+ReduceScatter on the GPU through the C ABI against the CPU oracle, plus run-to-run
+bit-identity of the rank-ordered reduction under injected timing perturbation."""
+import numpy as np
+import pytest
+import torch
+
+import comm_overlapped_gemm_gb300 as tdx
+from oracle import reference as R
+import workloads as wls
+from gpu_util import RSCase, assert_bit_exact, assert_within_tol, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TMO = int(5e8)
+
+
+def opts(**kw):
+    return tdx.make_opts(timeout_ns=TMO, **kw)
+
+
+def status_ok(case):
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_OK, (tdx.tdx_status_string(st), detail)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(W=2, M=256, K=256, N=512),
+    dict(W=3, M=384, K=200, N=136),     # ragged K and N, shard = 128 rows
+    dict(W=4, M=200, K=64, N=264),      # shards of 50 rows: tiles span shards
+    dict(W=1, M=128, K=128, N=256),
+    dict(W=16, M=256, K=64, N=64),
+])
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_small_shapes(shape, integer):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    for bn in (0, 128):
+        case = RSCase(inp, opts=opts(block_n=bn))
+        tdx.check(case.run(), f"rs {shape} bn={bn}")
+        status_ok(case)
+        if integer:
+            assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+        else:
+            assert_within_tol(case.result(), case.oracle(), "bf16")
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_full_size_sampled(integer):
+    wl = wls.WORKLOADS["rs_w8"]
+    inp = wls.make_inputs(wl, integer=integer)
+    case = RSCase(inp, opts=opts())
+    tdx.check(case.run())
+    status_ok(case)
+    rows = sample_rows(wl.M, wl.M // wl.W)
+    got = case.result_bits()[rows]
+    want = case.oracle(rows)
+    if integer:
+        assert_bit_exact(got, want, "bf16")
+    else:
+        assert_within_tol(R.decode_bf16(got), want, "bf16")
+    if not integer:
+        # run-to-run bit identity, with and without injected delays
+        first = case.result_bits()
+        for seed in (0, 1234):
+            for o in case.out:
+                o.fill_(float("nan"))
+            tdx.check(case.run(opts(perturb_seed=seed)))
+            assert np.array_equal(case.result_bits(), first)
+        status_ok(case)
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_small_m_full_output(integer):
+    wl = wls.WORKLOADS["rs_small"]
+    inp = wls.make_inputs(wl, integer=integer)
+    case = RSCase(inp, opts=opts())
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+
+
+def test_rs_chain_flags_trace_and_order():
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
+    inp = wls.make_inputs(wl, integer=False)
+    grid = 8
+    o = opts(num_sms=grid)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, o)
+    items = plan["L"] * plan["T"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    case = RSCase(inp, opts=opts(num_sms=grid, trace=trace, epoch=3))
+    tdx.check(case.run())
+    status_ok(case)
+    assert_within_tol(case.result(), case.oracle(), "bf16")
+    n = (plan["L"] - 1) * plan["T"]
+    f = case.ws[plan["off_chain_flags"]:plan["off_chain_flags"] + 4 * n].view(torch.int32).cpu().numpy()
+    assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 3))
+    tr = trace.cpu().numpy().astype(np.uint32)
+    sched = R.rs_item_schedule(4, 512, 512, 128, plan["BN"])
+    per = (items + grid - 1) // grid
+    for b in range(grid):
+        for k, it in enumerate(range(b, items, grid)):
+            r, mt, nt = sched[it]
+            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)
+    # the running sum of ranks 0..W-2 left in the workspace is the left fold of the partials:
+    # with fp32 partials it matches the oracle's fp64 sum of ranks 0..W-2 to fp32 accuracy
+    S = case.ws[plan["off_S"]:plan["off_S"] + 4 * plan["T"] * 128 * plan["BN"]].view(torch.float32).cpu().numpy()
+    full3 = R.gemm_rs_rows(inp.a[:3], inp.b[:3], np.arange(512), "bf16")   # ranks 0..2 summed
+    BN = plan["BN"]
+    for (mt, nt) in [(0, 0), (3, 1)]:
+        tile = mt * plan["tiles_n"] + nt
+        T = S[tile * 128 * BN:(tile + 1) * 128 * BN]
+        # layout: ((cc*8 + j)*128 + i)*4 + t  ->  element (i, 32*cc + 4*j + t)
+        T = T.reshape(BN // 32, 8, 128, 4).transpose(2, 0, 1, 3).reshape(128, BN)
+        want = full3[mt * 128:(mt + 1) * 128, nt * BN:(nt + 1) * BN]
+        assert np.max(np.abs(T - want)) <= 1e-5 * np.max(np.abs(want))
+
+
+def test_rs_modes_run():
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
+    inp = wls.make_inputs(wl, integer=True)
+    case = RSCase(inp, opts=opts())
+    for mode in (tdx.TDX_GEMM_ONLY, tdx.TDX_MOVE_ONLY, tdx.TDX_FUSED):
+        tdx.check(case.run(opts(mode=mode)))
+        status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+
+
+def test_rs_degenerate_k_zero():
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    outs = [torch.full((64, 128), 2.0, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    tdx.check(tdx.tdx_gemm_rs([dummy] * 2, [dummy] * 2, outs, ws, 2, 128, 0, 128, tdx.TDX_BF16, opts()))
+    torch.cuda.synchronize()
+    assert all(int(torch.count_nonzero(o)) == 0 for o in outs)
