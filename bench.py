@@ -1,0 +1,435 @@
+"""Benchmark of the tile-pipelined AllGather+GEMM and GEMM+ReduceScatter on one GB300.
+
+One step = one fused AllGather+GEMM call (W=8 logical ranks, shards 1024x8192 bf16, B 8192x3584)
+followed by one fused GEMM+ReduceScatter call (W=8, A_r 8192x3584, B_r 3584x8192, bf16 output
+shards 1024x8192), i.e. every step of the hot path: chunk producer, flag-gated rank-swizzled
+tcgen05 GEMM, and the rank-ordered reduction. Inputs are seeded synthetic data (workloads.py).
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job TFLOP/s with inputs resident in HBM; ``e2e``
+repeats the step through the same C-ABI calls with pinned host inputs copied in and outputs copied
+back inside the timed region. ``roofline`` is for the dominant kernel (the GEMM+ReduceScatter
+launch), timed with CUDA events on its stream inside the timed region. ``cpu_baseline`` times the
+CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
+
+``--impl reference`` times the CPU oracle itself (the reference arm of this repository: the pages
+ship no runnable reference code) on a bounded sample of the same workload per step.
+
+Multi-GPU: launched under torchrun, every rank runs an independent replica of the step on its own
+GPU (weak scaling; the logical ranks of each replica live in that GPU's memory, so there is no
+data-path collective); the timed region is bracketed by a barrier and the maximum over ranks is
+reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AG-GEMM & GEMM-RS TFLOP/s (1 GB300), % tensor peak, overlap efficiency"
+WORKLOAD = ("AG-GEMM W=8 bf16 (8 shards 1024x8192, B 8192x3584, C 8192x3584, chunk 128) + "
+            "GEMM-RS W=8 bf16 (A_r 8192x3584, B_r 3584x8192, out 8 shards 1024x8192)")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(ag_inp, rs_inp, frac_rows: int = 8):
+    """The oracle on a bounded sample of the step: rows of rank 0's shard of C (1/8 of the AG
+    output) and output shard 0 of the GEMM-RS (1/8 of its rows). Returns (flops, seconds)."""
+    from oracle import reference as R
+    t0 = time.perf_counter()
+    wl = ag_inp.wl
+    rows = np.arange(wl.W * wl.M // frac_rows)
+    R.ag_gemm_rows(ag_inp.a, ag_inp.b[0], rows, "bf16")
+    f_ag = 2.0 * len(rows) * wl.K * wl.N
+    wr = rs_inp.wl
+    rrows = np.arange(wr.M // frac_rows)
+    R.gemm_rs_rows(rs_inp.a, rs_inp.b, rrows, "bf16")
+    f_rs = 2.0 * wr.W * len(rrows) * wr.K * wr.N
+    return f_ag + f_rs, time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import workloads as wls
+    ag = wls.make_inputs(wls.WORKLOADS["ag_w8"])
+    rs = wls.make_inputs(wls.WORKLOADS["rs_w8"])
+    for _ in range(args.warmup):
+        oracle_sample(ag, rs, frac_rows=128)
+    flops = 0.0
+    secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(ag, rs, frac_rows=128)
+        flops += f
+        secs += s
+    v = flops / secs / 1e12
+    sample = "per step: rows 0..63 of the AG-GEMM output (1/128) and rows 0..63 of the GEMM-RS sum (1/128), fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, workloads.py)",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------------- GPU arm
+class Step:
+    """Device buffers and the two C-ABI calls of one step."""
+
+    def __init__(self, tdx, torch, ag_inp, rs_inp, dev):
+        self.tdx, self.torch = tdx, torch
+        t = torch
+
+        def d(a):
+            return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+        wa, wr = ag_inp.wl, rs_inp.wl
+        self.wa, self.wr = wa, wr
+        self.shards = [d(a) for a in ag_inp.a]
+        self.B = d(ag_inp.b[0])
+        self.C = t.empty((wa.W * wa.M, wa.N), dtype=t.bfloat16, device=dev)
+        self.A = [d(a) for a in rs_inp.a]
+        self.Bs = [d(b) for b in rs_inp.b]
+        self.out = [t.empty((wr.M // wr.W, wr.N), dtype=t.bfloat16, device=dev) for _ in range(wr.W)]
+        self.ws_ag = t.empty(tdx.tdx_workspace_size(tdx.OP_AG, wa.W, wa.M, wa.K, wa.N, tdx.TDX_BF16),
+                             dtype=t.uint8, device=dev)
+        self.ws_rs = t.empty(tdx.tdx_workspace_size(tdx.OP_RS, wr.W, wr.M, wr.K, wr.N, tdx.TDX_BF16),
+                             dtype=t.uint8, device=dev)
+        tdx.check(tdx.tdx_workspace_init(self.ws_ag))
+        tdx.check(tdx.tdx_workspace_init(self.ws_rs))
+        self.epoch = 0
+
+    def ag(self, mode=0):
+        self.epoch += 1
+        o = self.tdx.make_opts(epoch=self.epoch, mode=mode)
+        wa = self.wa
+        return self.tdx.tdx_ag_gemm(self.shards, self.B, self.C, self.ws_ag, wa.W, wa.M, wa.K, wa.N,
+                                    self.tdx.TDX_BF16, o)
+
+    def rs(self, mode=0):
+        self.epoch += 1
+        o = self.tdx.make_opts(epoch=self.epoch, mode=mode)
+        wr = self.wr
+        return self.tdx.tdx_gemm_rs(self.A, self.Bs, self.out, self.ws_rs, wr.W, wr.M, wr.K, wr.N,
+                                    self.tdx.TDX_BF16, o)
+
+    def status(self):
+        for ws in (self.ws_ag, self.ws_rs):
+            st, detail = self.tdx.tdx_read_device_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {self.tdx.tdx_status_string(st)} {detail}")
+
+
+def time_mode(torch, fn, reps: int):
+    """Median of per-call CUDA-event times of fn() on the current stream (ms)."""
+    s = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import comm_overlapped_gemm_gb300 as tdx
+    import workloads as wls
+
+    ag_inp = wls.make_inputs(wls.WORKLOADS["ag_w8"])
+    rs_inp = wls.make_inputs(wls.WORKLOADS["rs_w8"])
+    st = Step(tdx, torch, ag_inp, rs_inp, dev)
+    fl_ag = wls.WORKLOADS["ag_w8"].flops
+    fl_rs = wls.WORKLOADS["rs_w8"].flops
+    fl_step = fl_ag + fl_rs
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        tdx.check(st.ag())
+        tdx.check(st.rs())
+    torch.cuda.synchronize()
+    st.status()
+
+    # timed region: K steps, per-launch events for the dominant kernel (GEMM-RS) on its stream
+    ev_rs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_ag = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin.record(stream)
+        for i in range(args.steps):
+            ev_ag[i][0].record(stream)
+            tdx.check(st.ag())
+            ev_ag[i][1].record(stream)
+            ev_rs[i][0].record(stream)
+            tdx.check(st.rs())
+            ev_rs[i][1].record(stream)
+            launches += 2
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = t_begin.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    st.status()
+    ms_rs = statistics.mean(a.elapsed_time(b) for a, b in ev_rs)
+    ms_ag = statistics.mean(a.elapsed_time(b) for a, b in ev_ag)
+    value = world * fl_step * args.steps / (ms_total * 1e-3) / 1e12
+
+    # overlap efficiency: fused vs GEMM-alone and movement-alone of the same kernel
+    reps = max(5, min(20, args.steps))
+    t_ag_f = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_FUSED)), reps)
+    t_ag_g = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_GEMM_ONLY)), reps)
+    t_ag_m = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_MOVE_ONLY)), reps)
+    t_rs_f = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_FUSED)), reps)
+    t_rs_g = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_GEMM_ONLY)), reps)
+    t_rs_m = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_MOVE_ONLY)), reps)
+    st.status()
+
+    # end to end through the same C-ABI calls with pinned host buffers
+    h_shards = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory() for a in ag_inp.a]
+    h_B = torch.from_numpy(np.ascontiguousarray(ag_inp.b[0]).view(np.int16)).pin_memory()
+    h_A = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory() for a in rs_inp.a]
+    h_Bs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).pin_memory() for b in rs_inp.b]
+    h_C = torch.empty(st.C.shape, dtype=torch.bfloat16).pin_memory()
+    h_out = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for o in st.out]
+    h2d = sum(t.numel() * 2 for t in h_shards + [h_B] + h_A + h_Bs)
+    d2h = h_C.numel() * 2 + sum(o.numel() * 2 for o in h_out)
+
+    def e2e_step():
+        for d, h in zip(st.shards, h_shards):
+            d.copy_(h.view(torch.int16), non_blocking=True)
+        st.B.copy_(h_B, non_blocking=True)
+        for d, h in zip(st.A, h_A):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(st.Bs, h_Bs):
+            d.copy_(h, non_blocking=True)
+        tdx.check(st.ag())
+        tdx.check(st.rs())
+        h_C.copy_(st.C, non_blocking=True)
+        for h, d in zip(h_out, st.out):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(tt.item())
+    st.status()
+    # the e2e outputs are the step's results: spot-check a few elements against the resident run
+    assert torch.equal(h_C[:4].to(dev), st.C[:4])
+
+    pk, pk_kind = peaks()
+    peak_tf = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK["bf16_tflops_sustained"])))
+    achieved = fl_rs / (ms_rs * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("rs_w8_fused_bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64, workloads.py)",
+        "config": {"workload": WORKLOAD, "logical_ranks": 8,
+                   "l2": "no flush; every step reads inputs larger than L2 (184 MiB AG + 896 MiB RS)",
+                   "parallelism": f"replicas x{world} (each GPU runs W=8 logical ranks)"},
+        "ag_gemm": {"tflops": fl_ag / (ms_ag * 1e-3) / 1e12, "ms": ms_ag, "ms_fused": t_ag_f,
+                    "ms_gemm_only": t_ag_g, "ms_move_only": t_ag_m,
+                    "overlap_efficiency": max(t_ag_g, t_ag_m) / t_ag_f,
+                    "frac_of_peak": fl_ag / (ms_ag * 1e-3) / 1e12 / peak_tf},
+        "gemm_rs": {"tflops": achieved, "ms": ms_rs, "ms_fused": t_rs_f, "ms_gemm_only": t_rs_g,
+                    "ms_move_only": t_rs_m, "overlap_efficiency": max(t_rs_g, t_rs_m) / t_rs_f,
+                    "frac_of_peak": achieved / peak_tf},
+        "roofline": {"kernel": "tdx_fused_kernel<256,bf16> (GEMM+ReduceScatter W=8)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "peak_source": f"{pk_kind} bf16 dense (sustained)", "traffic": traffic,
+                     "algorithmic_flops_per_launch": fl_rs},
+        "e2e": {"value": world * fl_step / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "device": {"name": torch.cuda.get_device_name(dev),
+                   "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s = oracle_sample(ag_inp, rs_inp, frac_rows=8)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "rows 0..1023 of the AG-GEMM output and rows 0..1023 of the GEMM-RS "
+                                          "sum (1/8 of each), fp64 numpy", "seconds": s}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_case(args):
+    """One op on a given shape (profiling helper): --case ag|rs --shape W,M,K,N."""
+    import torch
+    import comm_overlapped_gemm_gb300 as tdx
+    import workloads as wls
+    W, M, K, N = (int(x) for x in args.shape.split(","))
+    dev = torch.device("cuda", 0)
+    name = "ag_w8" if args.case == "ag" else "rs_w8"
+    inp = wls.make_inputs(wls.with_shape(wls.WORKLOADS[name], W=W, M=M, K=K, N=N))
+    ai = inp if args.case == "ag" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["ag_w8"], W=1, M=128, K=64, N=64))
+    ri = inp if args.case == "rs" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["rs_w8"], W=1, M=128, K=64, N=64))
+    st = Step(tdx, torch, ai, ri, dev)
+    fn = st.ag if args.case == "ag" else st.rs
+    for _ in range(args.warmup + args.steps):
+        tdx.check(fn())
+    torch.cuda.synchronize()
+    st.status()
+    ms = time_mode(torch, lambda: tdx.check(fn()), 5)
+    fl = inp.wl.flops
+    print(json.dumps({"case": args.case, "shape": [W, M, K, N], "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tdx", choices=["tdx", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["ag", "rs"], default=None)
+    ap.add_argument("--shape", default="8,1024,8192,3584")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.case is None:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.case is not None:
+        return run_case(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

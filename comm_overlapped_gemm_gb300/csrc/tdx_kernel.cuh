@@ -129,7 +129,9 @@ __device__ __forceinline__ uint32_t perturb_hash(uint32_t seed, uint32_t x) {
 }
 
 // Bounded wait on an mbarrier phase. Gives up (false) when the CTA abort flag is raised or after
-// p.timeout_ns; a timeout is recorded as DEV_TIMEOUT / ROLE_PIPE.
+// 2 * p.timeout_ns; a timeout is recorded as DEV_TIMEOUT / ROLE_PIPE. Pipeline stages only wait on
+// one another, so a stuck pipeline is normally caused by a flag wait upstream; the doubled bound
+// lets that flag wait run out (and report itself) first.
 static __device__ __noinline__ bool wait_mbar(const KParams& p, uint32_t bar, uint32_t parity,
                                        volatile int* abort_flag, uint32_t idx) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -138,7 +140,7 @@ static __device__ __noinline__ bool wait_mbar(const KParams& p, uint32_t bar, ui
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > p.timeout_ns) {
+      if (globaltimer_ns() - t0 > 2 * p.timeout_ns) {
         report_error(p, DEV_TIMEOUT, ROLE_PIPE, idx, 0, parity);
         *abort_flag = 1;
         return false;
