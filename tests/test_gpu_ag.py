@@ -221,7 +221,7 @@ def test_ag_stale_epoch_is_reported():
     case = AGCase(inp, opts=opts())
     tdx.check(case.run(opts(epoch=10)))
     status_ok(case)
-    tdx.check(case.run(opts(epoch=5, timeout_ns=2_000_000)))
+    tdx.check(case.run(tdx.make_opts(epoch=5, timeout_ns=2_000_000)))
     st, detail = tdx.tdx_read_device_status(case.ws)
     assert st == tdx.TDX_ERR_STALE_EPOCH
     assert detail[4] == 10 and detail[5] == 5
