@@ -22,7 +22,8 @@ TDX_PRODUCER_SM, TDX_PRODUCER_COPY_ENGINE = 0, 1
 OP_AG, OP_RS = 0, 1
 
 EXPORTED = ["tdx_opts_default", "tdx_workspace_size", "tdx_workspace_init", "tdx_ag_gemm", "tdx_gemm_rs",
-            "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info"]
+            "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info",
+            "tdx_ag_gemm_noalloc"]
 
 
 class tdx_opts(ctypes.Structure):
@@ -68,6 +69,7 @@ def _load():
         "tdx_status_string": (ctypes.c_char_p, [I]),
         "tdx_version": (U32, []),
         "tdx_plan_info": (I, [I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
+        "tdx_ag_gemm_noalloc": (I, [PP, P, P, I, I, I, I, I, OP, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -180,6 +182,17 @@ def tdx_ag_gemm(shards, B, C, workspace, W: int, M_local: int, K: int, N: int, d
     wsb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
     return int(_lib.tdx_ag_gemm(_ptr_array(shards), _ptr(B), _ptr(C), _ptr(workspace), wsb, W, M_local, K, N,
                                 dtype, _opts_ref(opts), _stream(stream)))
+
+
+TDX_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+
+
+def tdx_ag_gemm_noalloc(shards, B, C, W: int, M_local: int, K: int, N: int, dtype: int, opts=None,
+                        device_status=None, stream=None) -> int:
+    """AllGather+GEMM on the library's built-in scratch array (no workspace argument, nothing
+    allocated by the call); see include/tdx.h for its limit and sharing rules."""
+    return int(_lib.tdx_ag_gemm_noalloc(_ptr_array(shards), _ptr(B), _ptr(C), W, M_local, K, N, dtype,
+                                        _opts_ref(opts), _ptr(device_status), _stream(stream)))
 
 
 def tdx_gemm_rs(A_parts, B_parts, out_shards, workspace, W: int, M: int, K: int, N: int, dtype: int,

@@ -383,6 +383,69 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   return TDX_OK;
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free AllGather+GEMM: the workspace is this file-scope device array, shared by every
+// call on a device. Host code never dereferences or passes the symbol itself (on the host it is
+// only a stand-in); the device address is looked up with cudaGetSymbolAddress, once per device,
+// with that device current, and cached.
+static __device__ __align__(256) uint8_t g_tdx_noalloc_scratch[TDX_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+tdx_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TDX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tdx_noalloc_scratch) != cudaSuccess || p == nullptr) return TDX_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C, int W, int M_local, int K,
+                               int N, tdx_dtype dtype, const tdx_opts* opts, uint32_t* device_status,
+                               void* stream) {
+  tdx_opts o = opts ? *opts : defaults();
+  o.epoch = 0;   // the shared scratch is cleared by every call
+  size_t need = 0;
+  tdx_status s = tdx_workspace_size(OP_AG, W, M_local, K, N, dtype, &o, &need);
+  if (s != TDX_OK) return s;
+  if (need > TDX_NOALLOC_SCRATCH_BYTES) {
+    if (std::getenv("TDX_VERBOSE"))
+      std::fprintf(stderr, "tdx_ag_gemm_noalloc: problem needs %zu bytes of scratch, the built-in scratch holds %u\n",
+                   need, TDX_NOALLOC_SCRATCH_BYTES);
+    return TDX_ERR_WORKSPACE;
+  }
+  if (device_status != nullptr && !aligned16(device_status)) return TDX_ERR_ALIGNMENT;
+  void* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != TDX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // status word and details start at zero for this call (flags are cleared by the epoch-0 path)
+  s = fill_zero(scratch, kStatusWords * sizeof(uint32_t), st);
+  if (s != TDX_OK) return s;
+  s = tdx_ag_gemm(shards, B, C, scratch, TDX_NOALLOC_SCRATCH_BYTES, W, M_local, K, N, dtype, &o, stream);
+  if (s != TDX_OK) return s;
+  if (device_status != nullptr &&
+      cudaMemcpyAsync(device_status, scratch, kStatusWords * sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+    return TDX_ERR_CUDA;
+  return TDX_OK;
+}
+
 size_t tdx_trace_size(int grid, int items) {
   if (grid <= 0 || items < 0) return 0;
   const size_t per_cta = (static_cast<size_t>(items) + grid - 1) / grid;

@@ -134,6 +134,36 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
                        int W, int M, int K, int N, tdx_dtype dtype,
                        const tdx_opts* opts, void* stream);
 
+/* Size of the library's built-in scratch array used by tdx_ag_gemm_noalloc: 8 MiB per device. */
+#define TDX_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* AllGather+GEMM for callers that cannot allocate device memory themselves: for example code that
+ * runs inside a host framework which owns every device allocation and exposes no allocator to it
+ * (a plugin of an inference runtime with a fixed memory budget), or a latency-critical caller that
+ * cannot accept the device-wide synchronisation cudaMalloc may cause. The pages have no
+ * counterpart of this entry point; it is a convenience of this library.
+ *
+ * Computes exactly what tdx_ag_gemm computes (same shards, B, C, W, M_local, K, N, dtype and opts
+ * meaning), but instead of a caller-owned workspace it uses a scratch array that the library
+ * declares statically in device memory: TDX_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ * library, held until the process exits. The call itself allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *  - Limit: problems whose tdx_workspace_size(0, W, M_local, K, N, dtype, opts) exceeds
+ *    TDX_NOALLOC_SCRATCH_BYTES are rejected with TDX_ERR_WORKSPACE before anything is launched
+ *    (the small-M and tiny AllGather shapes fit; W=8 x 1024 x 8192 bf16 does not).
+ *  - First call on a device: it looks up the device address of the scratch array (with that
+ *    device current) and caches it; make this first call before any stream capture.
+ *  - Shared state: every call on a device uses the same array, which keeps the previous call's
+ *    contents. Each call clears, on `stream`, the status word and the flags that must start at
+ *    zero (opts->epoch is ignored; epoch 1 is used). Calls that overlap on the GPU (different
+ *    streams, or different host threads) race on the array: serialise them.
+ *  - device_status: optional device pointer to 8 uint32 words. If not NULL, the call copies the
+ *    scratch's status word and details (see tdx_read_device_status) there on `stream` once the
+ *    kernel has finished; if NULL, device-side errors of this call are not reported. */
+tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C,
+                               int W, int M_local, int K, int N, tdx_dtype dtype,
+                               const tdx_opts* opts, uint32_t* device_status, void* stream);
+
 /* Synchronise `stream`, then read the workspace's device status word into *out (TDX_OK, or the
  * first device-side error since tdx_workspace_init). If detail is not NULL it receives 8 words:
  * [0] status, [1] role that failed (1 flag wait, 2 pipeline wait, 3 chain wait, 4 producer),
