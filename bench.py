@@ -49,6 +49,23 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Maximum of x over all ranks (the job's time is its slowest rank's); identity at world 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Units all ranks processed (weak scaling: every rank runs the same step) over the slowest
+    rank's time."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
@@ -191,9 +208,9 @@ class Step:
         tdx.check(tdx.tdx_workspace_init(self.ws_rs))
         self.epoch = 0
 
-    def ag(self, mode=0):
+    def ag(self, mode=0, producer=0):
         self.epoch += 1
-        o = self.tdx.make_opts(epoch=self.epoch, mode=mode)
+        o = self.tdx.make_opts(epoch=self.epoch, mode=mode, producer=producer)
         wa = self.wa
         return self.tdx.tdx_ag_gemm(self.shards, self.B, self.C, self.ws_ag, wa.W, wa.M, wa.K, wa.N,
                                     self.tdx.TDX_BF16, o)
@@ -225,6 +242,107 @@ def time_mode(torch, fn, reps: int):
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))
     return statistics.median(ts)
+
+
+def ag_case(tdx, torch, wl, dev, integer=False):
+    """Device buffers + a timed call for one AllGather workload (extra configurations)."""
+    import workloads as wls
+    inp = wls.make_inputs(wl, integer=integer)
+    view = np.int16 if wl.dtype == "bf16" else np.uint8
+    shards = [torch.from_numpy(np.ascontiguousarray(a).view(view)).to(dev) for a in inp.a]
+    B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(view)).to(dev)
+    C = torch.empty((wl.W * wl.M, wl.N), dtype=torch.bfloat16, device=dev)
+    dt = tdx.TDX_BF16 if wl.dtype == "bf16" else tdx.TDX_FP8_E4M3
+    kw = dict(chunk_rows=wl.chunk_rows)
+    if wl.dtype == "e4m3":
+        kw.update(scale_a=inp.scale_a, scale_b=inp.scale_b[0])
+    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, dt, tdx.make_opts(**kw)),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    state = {"epoch": 0}
+
+    def call(mode=0, producer=0):
+        state["epoch"] += 1
+        o = tdx.make_opts(epoch=state["epoch"], mode=mode, producer=producer, **kw)
+        tdx.check(tdx.tdx_ag_gemm(shards, B, C, ws, wl.W, wl.M, wl.K, wl.N, dt, o))
+
+    def status():
+        st, d = tdx.tdx_read_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    return call, status
+
+
+def rs_case(tdx, torch, wl, dev):
+    import workloads as wls
+    inp = wls.make_inputs(wl)
+    A = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev) for a in inp.a]
+    Bs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev) for b in inp.b]
+    out = [torch.empty((wl.M // wl.W, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    state = {"epoch": 0}
+
+    def call(mode=0):
+        state["epoch"] += 1
+        o = tdx.make_opts(epoch=state["epoch"], mode=mode)
+        tdx.check(tdx.tdx_gemm_rs(A, Bs, out, ws, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o))
+
+    def status():
+        st, d = tdx.tdx_read_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    return call, status
+
+
+def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
+    """The other configurations, timed alone (median of CUDA-event times, warm): the AllGather
+    with the copy-engine producer, e4m3 AllGather, and the small-M latency cases."""
+    import workloads as wls
+    W = wls.WORKLOADS
+    res = {}
+    call, status = ag_case(tdx, torch, W["ag_w8"], dev)
+    for _ in range(3):
+        call(producer=1)
+    f = time_mode(torch, lambda: call(producer=1), reps)
+    g = time_mode(torch, lambda: call(mode=1), reps)
+    m = time_mode(torch, lambda: call(mode=2, producer=1), reps)
+    status()
+    res["ag_w8_copy_engine"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m,
+                                "overlap_efficiency": max(g, m) / f, "tflops": W["ag_w8"].flops / (f * 1e-3) / 1e12}
+    del call, status
+    call, status = ag_case(tdx, torch, W["ag_fp8_w8"], dev)
+    for _ in range(3):
+        call()
+    f = time_mode(torch, call, reps)
+    g = time_mode(torch, lambda: call(mode=1), reps)
+    m = time_mode(torch, lambda: call(mode=2), reps)
+    status()
+    tf = W["ag_fp8_w8"].flops / (f * 1e-3) / 1e12
+    res["ag_fp8_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
+                        "tflops": tf, "peak_fp8_tflops": 2 * peak_bf16, "frac_of_peak": tf / (2 * peak_bf16)}
+    del call, status
+    call, status = ag_case(tdx, torch, W["ag_small"], dev)
+    for _ in range(5):
+        call()
+    f = time_mode(torch, call, reps)
+    status()
+    wl = W["ag_small"]
+    byt = wl.W * wl.M * wl.K * 2 * 2 + wl.K * wl.N * 2 + wl.W * wl.M * wl.N * 2   # move r+w, B, C
+    res["ag_small"] = {"us_fused": 1e3 * f, "tflops": wl.flops / (f * 1e-3) / 1e12,
+                       "algorithmic_bytes": byt, "hbm_frac": byt / (f * 1e-3) / 1e9 / hbm_gbs}
+    del call, status
+    call, status = rs_case(tdx, torch, W["rs_small"], dev)
+    for _ in range(5):
+        call()
+    f = time_mode(torch, call, reps)
+    status()
+    wl = W["rs_small"]
+    byt = wl.W * (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 2
+    res["rs_small"] = {"us_fused": 1e3 * f, "tflops": wl.flops / (f * 1e-3) / 1e12,
+                       "algorithmic_bytes": byt, "hbm_frac": byt / (f * 1e-3) / 1e9 / hbm_gbs}
+    return res
 
 
 def run_gpu(args):
@@ -278,15 +396,11 @@ def run_gpu(args):
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = t_begin.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = reduce_max(t_begin.elapsed_time(t_end), world, dev)
     st.status()
     ms_rs = statistics.mean(a.elapsed_time(b) for a, b in ev_rs)
     ms_ag = statistics.mean(a.elapsed_time(b) for a, b in ev_ag)
-    value = world * fl_step * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(fl_step, args.steps, world, ms_total)
 
     # overlap efficiency: fused vs GEMM-alone and movement-alone of the same kernel
     reps = max(5, min(20, args.steps))
@@ -333,11 +447,7 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(tt.item())
+    ms_e2e = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
     st.status()
     # the e2e outputs are the step's results: spot-check a few elements against the resident run
     assert torch.equal(h_C[:4].to(dev), st.C[:4])
@@ -377,6 +487,8 @@ def run_gpu(args):
         "device": {"name": torch.cuda.get_device_name(dev),
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
     }
+    if not args.no_extra:
+        line["configs"] = extra_configs(tdx, torch, dev, peak_tf, float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"])))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, s = oracle_sample(ag_inp, rs_inp, frac_rows=8)
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
@@ -419,6 +531,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tdx", choices=["tdx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra configurations")
     ap.add_argument("--case", choices=["ag", "rs"], default=None)
     ap.add_argument("--shape", default="8,1024,8192,3584")
     args = ap.parse_args()

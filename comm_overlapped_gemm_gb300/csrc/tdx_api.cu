@@ -166,6 +166,44 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long l
   return r == CUDA_SUCCESS;
 }
 
+// Copy-engine producer: one side stream and a fork/join event pair per device, created on first
+// use and kept for the life of the process; cuStreamWriteValue32 through the driver entry point.
+typedef CUresult (*StreamWriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+struct CeState {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+StreamWriteValue32Fn get_write_value32() {
+  static StreamWriteValue32Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<StreamWriteValue32Fn>(ptr);
+  });
+  return fn;
+}
+
+bool ce_state(CeState** out) {
+  static std::mutex mu;
+  static CeState states[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  CeState& s = states[dev];
+  if (s.side == nullptr) {
+    if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return false;
+  }
+  *out = &s;
+  return true;
+}
+
 int device_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -179,7 +217,8 @@ tdx_status fill_zero(void* p, size_t bytes, cudaStream_t s) {
 }
 
 tdx_status launch(const Plan& pl, KParams& kp, bool fp8, int grid, cudaStream_t stream) {
-  const cudaError_t e = fp8 ? launch_fused_fp8(pl.BN, kp, grid, stream) : launch_fused_bf16(pl.BN, kp, grid, stream);
+  const cudaError_t e =
+      fp8 ? launch_fused_fp8(pl.op, pl.BN, kp, grid, stream) : launch_fused_bf16(pl.op, pl.BN, kp, grid, stream);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;
@@ -256,7 +295,6 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   if (o.out_dtype != TDX_BF16 && o.out_dtype != TDX_FP32) return TDX_ERR_INVALID_ARG;
   if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
   if (o.producer != TDX_PRODUCER_SM && o.producer != TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_INVALID_ARG;
-  if (o.producer == TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_UNSUPPORTED;
   Plan pl;
   tdx_status s = make_plan(OP_AG, W, M_local, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
@@ -292,9 +330,21 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
     kp.row_scale[r] = sa * sb;
   }
   kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
-  kp.ppc = static_cast<int>((kp.chunk_bytes + kPieceBytes - 1) / kPieceBytes);
+  const int grid = grid_for(o, 0);
+  if (grid <= 0) return TDX_ERR_CUDA;
+  // producer copy unit: about one piece per CTA, in 16 KiB rounds, at most 64 KiB per release
+  {
+    const long long total = static_cast<long long>(W) * pl.n_chunks * kp.chunk_bytes;
+    long long pb = (total / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;
+    if (pb < kCopyRoundBytes) pb = kCopyRoundBytes;
+    if (pb > kMaxPieceBytes) pb = kMaxPieceBytes;
+    kp.piece_bytes = static_cast<int>(pb);
+  }
+  kp.ppc = static_cast<int>((kp.chunk_bytes + kp.piece_bytes - 1) / kp.piece_bytes);
   kp.total_pieces = W * pl.n_chunks * kp.ppc;
-  kp.copy_active = (o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY) ? 1 : 0;
+  const bool ce = o.producer == TDX_PRODUCER_COPY_ENGINE;
+  const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
+  kp.copy_active = (moving && !ce) ? 1 : 0;
   kp.wait_flags = (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY) ? 1 : 0;
   const int bbox = fp8 ? 128 : 64;
   if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, bbox, kBM) ||
@@ -305,9 +355,35 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
     if (s != TDX_OK) return s;
   }
-  const int grid = grid_for(o, 0);
-  if (grid <= 0) return TDX_ERR_CUDA;
-  return launch(pl, kp, fp8, grid, st);
+  if (!(ce && moving)) return launch(pl, kp, fp8, grid, st);
+
+  // Copy-engine producer: the side stream starts after everything already on `st`, copies the
+  // chunks in release order (peers self+1, ..., self+W-1, then self) and writes each chunk's flag
+  // once its copy is done (the default write orders it after the preceding copy); the consumer
+  // kernel runs on `st` meanwhile, and `st` joins the side stream before returning.
+  CeState* ce_st = nullptr;
+  StreamWriteValue32Fn wv = get_write_value32();
+  if (!ce_state(&ce_st) || wv == nullptr) return TDX_ERR_CUDA;
+  if (cudaEventRecord(ce_st->fork, st) != cudaSuccess || cudaStreamWaitEvent(ce_st->side, ce_st->fork, 0) != cudaSuccess)
+    return TDX_ERR_CUDA;
+  for (int rr = 0; rr < W; ++rr) {
+    const int rank = (o.self_rank + 1 + rr) % W;
+    for (int ck = 0; ck < pl.n_chunks; ++ck) {
+      const uint8_t* src = static_cast<const uint8_t*>(shards[rank]) + static_cast<size_t>(ck) * kp.chunk_bytes;
+      uint8_t* dst = kp.G + (static_cast<size_t>(rank) * M_local + static_cast<size_t>(ck) * pl.chunk_rows) * kp.row_bytes;
+      if (cudaMemcpyAsync(dst, src, kp.chunk_bytes, cudaMemcpyDeviceToDevice, ce_st->side) != cudaSuccess)
+        return TDX_ERR_CUDA;
+      uint32_t* flag = kp.chunk_flags + rank * pl.n_chunks + ck;
+      if (wv(reinterpret_cast<CUstream>(ce_st->side), reinterpret_cast<CUdeviceptr>(flag), kp.epoch, 0) != CUDA_SUCCESS)
+        return TDX_ERR_CUDA;
+    }
+  }
+  if (cudaEventRecord(ce_st->join, ce_st->side) != cudaSuccess) return TDX_ERR_CUDA;
+  if (o.mode == TDX_FUSED) {
+    s = launch(pl, kp, fp8, grid, st);
+    if (s != TDX_OK) return s;
+  }
+  return cudaStreamWaitEvent(st, ce_st->join, 0) == cudaSuccess ? TDX_OK : TDX_ERR_CUDA;
 }
 
 tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, void* const* out_shards,
@@ -420,6 +496,7 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
                                void* stream) {
   tdx_opts o = opts ? *opts : defaults();
   o.epoch = 0;   // the shared scratch is cleared by every call
+  if (o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;   // the copy-engine producer creates a stream
   size_t need = 0;
   tdx_status s = tdx_workspace_size(OP_AG, W, M_local, K, N, dtype, &o, &need);
   if (s != TDX_OK) return s;

@@ -19,7 +19,8 @@ constexpr int kEpiWarp0 = 4;             // warps 4-11: epilogue (TMEM -> regist
 constexpr int kNumEpiWarps = 8;
 constexpr int kEpiThreads = kNumEpiWarps * 32;
 constexpr int kCopyThreads = kNumCopyWarps * 32;
-constexpr int kPieceBytes = 16384;       // producer copy unit inside a chunk
+constexpr int kCopyRoundBytes = 16384;   // producer: bytes in flight per CTA per round
+constexpr int kMaxPieceBytes = 65536;    // producer: largest copy unit released at once
 constexpr int kMaxSplitK = 16;
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
@@ -59,6 +60,7 @@ struct KParams {
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;
+  int piece_bytes;               // producer copy unit (multiple of kCopyRoundBytes)
   int ppc;                       // pieces per chunk
   int total_pieces;
   long long row_bytes;           // K * element size
@@ -69,8 +71,8 @@ struct KParams {
 int fused_smem_bytes(int block_n, bool fp8);
 
 // Launch the persistent fused kernel for (block_n, fp8) on `grid` CTAs.
-cudaError_t launch_fused_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_fused_fp8(int block_n, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_bf16(int op, int block_n, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_fp8(int op, int block_n, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
 }  // namespace tdx

@@ -72,12 +72,13 @@ struct Item {
   int m0, n0;
 };
 
+template <int OP>
 __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN) {
   Item r;
   r.c = it / p.T;
   const int pos = it - r.c * p.T;
   int mt, nt;
-  if (p.op == OP_AG) {
+  if constexpr (OP == OP_AG) {
     // rank-swizzled arrival order: M-tiles from the first tile whose first row belongs to
     // self_rank, wrapping around; N-tiles innermost.
     int start = (p.self_rank * p.M_local + kBM - 1) / kBM;
@@ -98,8 +99,9 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN) {
 // K blocks of one work item: an AllGather K split c covers [c*num_kb/L, (c+1)*num_kb/L); a
 // ReduceScatter item (chain element = rank) covers all of K. The host keeps L <= num_kb, so every
 // range is non-empty and the accumulator is always initialised.
+template <int OP>
 __device__ __forceinline__ void k_range(const KParams& p, const Item& w, int& kb0, int& kb1) {
-  if (p.op == OP_AG) {
+  if constexpr (OP == OP_AG) {
     kb0 = static_cast<int>((static_cast<long long>(w.c) * p.num_kb) / p.L);
     kb1 = static_cast<int>((static_cast<long long>(w.c + 1) * p.num_kb) / p.L);
   } else {
@@ -195,7 +197,7 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
   }
 }
 
-template <int BN, bool FP8>
+template <int BN, bool FP8, int OP>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
   using C = Cfg<BN, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -239,15 +241,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     tmem_relinquish();
   }
   if (threadIdx.x == kTmaWarp * 32) {
-    for (int i = 0; i < (p.op == OP_AG ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
-    for (int i = 0; i < (p.op == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
+    for (int i = 0; i < (OP == OP_AG ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
+    for (int i = 0; i < (OP == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
 
-  const bool ag = p.op == OP_AG;
+  constexpr bool ag = OP == OP_AG;
   const bool ag_move_only = ag && p.mode == MODE_MOVE_ONLY;
   const bool rs_move_only = !ag && p.mode == MODE_MOVE_ONLY;
   const int items = ag_move_only ? 0 : p.L * p.T;
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       bool stop = false;
       for (int it = blockIdx.x; it < items && !stop; it += grid) {
         if (*abort_flag) break;
-        const Item w = decode_item(p, it, BN);
+        const Item w = decode_item<OP>(p, it, BN);
         const CUtensorMap* map_a;
         const CUtensorMap* map_b;
         int arow = w.m0;
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           map_b = &p.tm_b[w.c];
         }
         int kb0, kb1;
-        k_range(p, w, kb0, kb1);
+        k_range<OP>(p, w, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_mbar(p, empty0 + 8 * stage, phase ^ 1u, abort_flag, 100 + stage)) {
             stop = true;
@@ -343,14 +345,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       int local = 0;
       bool stop = false;
       for (int it = blockIdx.x; it < items && !stop; it += grid, ++local) {
-        const Item w = decode_item(p, it, BN);
+        const Item w = decode_item<OP>(p, it, BN);
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!wait_mbar(p, tempty0 + 8 * acc, aph ^ 1u, abort_flag, 200 + acc)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         int kb0, kb1;
-        k_range(p, w, kb0, kb1);
+        k_range<OP>(p, w, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_mbar(p, full0 + 8 * stage, phase, abort_flag, 300 + stage)) {
             stop = true;
@@ -386,31 +388,37 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
     // =============================================================== AllGather producer
-    if (p.copy_active) {
+    if (ag && p.copy_active) {
+      // A piece (p.piece_bytes, a multiple of 16 KiB) is copied in rounds of 16 KiB: each of the
+      // 64 producer threads keeps 16 vector loads in flight, stores them, and the next round
+      // starts at once; the synchronisation that releases a chunk (barrier, fence, counter
+      // atomic) is paid once per piece.
       const int ct = threadIdx.x - kCopyWarp0 * 32;
-      constexpr int kVec = kPieceBytes / (16 * kCopyThreads);   // 16 vectors per thread
+      constexpr int kVec = kCopyRoundBytes / (16 * kCopyThreads);   // 16 vectors per thread
       for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
         const int q = piece / p.ppc;            // chunk position in release order
         const int pc = piece - q * p.ppc;
         const int rr = q / p.n_chunks;
         const int rank = (p.self_rank + 1 + rr) % p.W;   // peers in ring order, self last
         const int ck = q - rr * p.n_chunks;
-        const long long off = (long long)pc * kPieceBytes;
+        const long long off = (long long)pc * p.piece_bytes;
         const long long rem = p.chunk_bytes - off;
-        const int n = rem < kPieceBytes ? static_cast<int>(rem) : kPieceBytes;
+        const int n = rem < p.piece_bytes ? static_cast<int>(rem) : p.piece_bytes;
         const uint8_t* src = p.shard[rank] + (long long)ck * p.chunk_bytes + off;
         uint8_t* dst = p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off;
         if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
-        uint4 v[kVec];
+        for (int r0 = 0; r0 < n; r0 += kCopyRoundBytes) {
+          uint4 v[kVec];
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-          const int b = (j * kCopyThreads + ct) * 16;
-          if (b < n) v[j] = ld_nc_v4(src + b);
-        }
+          for (int j = 0; j < kVec; ++j) {
+            const int b = r0 + (j * kCopyThreads + ct) * 16;
+            if (b < n) v[j] = ld_nc_v4(src + b);
+          }
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-          const int b = (j * kCopyThreads + ct) * 16;
-          if (b < n) st_v4(dst + b, v[j]);
+          for (int j = 0; j < kVec; ++j) {
+            const int b = r0 + (j * kCopyThreads + ct) * 16;
+            if (b < n) st_v4(dst + b, v[j]);
+          }
         }
         named_bar_sync(2, kCopyThreads);
         if (ct == 0) {
@@ -438,7 +446,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     uint64_t chain_ns = 0;
     int local = 0;
     for (int it = blockIdx.x; it < items; it += grid, ++local) {
-      const Item w = decode_item(p, it, BN);
+      const Item w = decode_item<OP>(p, it, BN);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const bool read_s = chain && w.c > 0;
@@ -581,10 +589,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   }
 }
 
-template <int BN, bool FP8>
+template <int BN, bool FP8, int OP>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8>,
+  cudaError_t e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -597,7 +605,7 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8>, p);
+  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP>, p);
 }
 
 }  // namespace tdx

@@ -3,11 +3,19 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_bf16(int op, int block_n, const KParams& p, int grid, cudaStream_t stream) {
+  if (op == OP_AG) {
+    switch (block_n) {
+      case 64: return launch_fused_t<64, false, OP_AG>(p, grid, stream);
+      case 128: return launch_fused_t<128, false, OP_AG>(p, grid, stream);
+      case 256: return launch_fused_t<256, false, OP_AG>(p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (block_n) {
-    case 64: return launch_fused_t<64, false>(p, grid, stream);
-    case 128: return launch_fused_t<128, false>(p, grid, stream);
-    case 256: return launch_fused_t<256, false>(p, grid, stream);
+    case 64: return launch_fused_t<64, false, OP_RS>(p, grid, stream);
+    case 128: return launch_fused_t<128, false, OP_RS>(p, grid, stream);
+    case 256: return launch_fused_t<256, false, OP_RS>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

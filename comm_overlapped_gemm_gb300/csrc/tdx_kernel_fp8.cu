@@ -4,10 +4,11 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_fp8(int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_fp8(int op, int block_n, const KParams& p, int grid, cudaStream_t stream) {
+  if (op != OP_AG) return cudaErrorInvalidValue;
   switch (block_n) {
-    case 128: return launch_fused_t<128, true>(p, grid, stream);
-    case 256: return launch_fused_t<256, true>(p, grid, stream);
+    case 128: return launch_fused_t<128, true, OP_AG>(p, grid, stream);
+    case 256: return launch_fused_t<256, true, OP_AG>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -62,7 +62,9 @@ typedef enum {
 
 typedef enum {
   TDX_PRODUCER_SM = 0,          /* chunk copies by producer warps of the persistent kernel */
-  TDX_PRODUCER_COPY_ENGINE = 1  /* chunk copies by cudaMemcpyAsync on a side stream + stream flag writes */
+  TDX_PRODUCER_COPY_ENGINE = 1  /* chunk copies by cudaMemcpyAsync on a library-owned side stream (created
+                                   once per device), each followed by a stream write of its flag; the
+                                   caller's stream waits for the side stream before the call returns */
 } tdx_producer;
 
 /* Per-call options. Pass NULL for all defaults; tdx_opts_default fills the same values. */
@@ -157,6 +159,7 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
  *    contents. Each call clears, on `stream`, the status word and the flags that must start at
  *    zero (opts->epoch is ignored; epoch 1 is used). Calls that overlap on the GPU (different
  *    streams, or different host threads) race on the array: serialise them.
+ *  - opts->producer must be TDX_PRODUCER_SM (else TDX_ERR_UNSUPPORTED).
  *  - device_status: optional device pointer to 8 uint32 words. If not NULL, the call copies the
  *    scratch's status word and details (see tdx_read_device_status) there on `stream` once the
  *    kernel has finished; if NULL, device-side errors of this call are not reported. */

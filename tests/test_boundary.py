@@ -150,3 +150,14 @@ def test_rs_validation_codes(tdx):
 def test_trace_size(tdx):
     assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 4 * 3)
     assert tdx.tdx_trace_size(0, 10) == 0
+
+
+def test_noalloc_rejects_copy_engine_producer_before_any_device_work(tdx):
+    o = tdx.make_opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE)
+    rc = tdx.tdx_ag_gemm_noalloc([FAKE] * 2, FAKE, FAKE, 2, 64, 128, 256, tdx.TDX_BF16, o, stream=0)
+    assert rc == tdx.TDX_ERR_UNSUPPORTED
+
+
+def test_noalloc_rejects_oversized_problem_before_any_device_work(tdx):
+    rc = tdx.tdx_ag_gemm_noalloc([FAKE] * 8, FAKE, FAKE, 8, 1024, 8192, 3584, tdx.TDX_BF16, None, stream=0)
+    assert rc == tdx.TDX_ERR_WORKSPACE
