@@ -42,6 +42,7 @@ class tdx_opts(ctypes.Structure):
         ("num_sms", ctypes.c_int),
         ("split_k", ctypes.c_int),
         ("block_n", ctypes.c_int),
+        ("reduce_mode", ctypes.c_int),
     ]
 
 
@@ -166,7 +167,7 @@ def tdx_workspace_init(workspace, nbytes: int | None = None, stream=None) -> int
 
 
 PLAN_KEYS = ["BN", "L", "tiles_m", "tiles_n", "T", "num_kb", "chunk_rows", "n_chunks", "off_chunk_flags",
-             "off_chunk_cnt", "off_chain_flags", "off_G", "off_S", "total"]
+             "off_chunk_cnt", "off_chain_flags", "off_G", "off_S", "total", "reduce_mode", "off_tile_cnt"]
 
 
 def tdx_plan_info(op: int, W: int, M_local_or_M: int, K: int, N: int, dtype: int, opts=None) -> dict:

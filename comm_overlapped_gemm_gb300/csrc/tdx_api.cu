@@ -38,6 +38,7 @@ tdx_opts defaults() {
   o.num_sms = 0;
   o.split_k = 0;
   o.block_n = 0;
+  o.reduce_mode = 0;
   return o;
 }
 
@@ -47,7 +48,8 @@ struct Plan {
   int op = 0, W = 0, M = 0, M_local = 0, K = 0, N = 0, elt = 2;
   int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
   int chunk_rows = 0, n_chunks = 0;
-  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, ctrl_end = 0;
+  int reduce_last = 0;
+  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
 };
 
@@ -100,13 +102,25 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     if (L > p.num_kb) L = p.num_kb;
     if (L < 1) L = 1;
   } else {
-    if (bn == 0) bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    if (bn == 0) {
+      bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+      // few output tiles: narrower tiles spread the ranks' partial reductions over more CTAs
+      if (bn == 256 && static_cast<long long>(p.tiles_m) * ((N + 255) / 256) < 2 * kRefSMs) bn = 128;
+    }
     L = W;
   }
   p.BN = bn;
   p.L = L;
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
+  // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
+  // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
+  if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
+  if (L > 1) {
+    if (o.reduce_mode == 1) p.reduce_last = 0;
+    else if (o.reduce_mode == 2) p.reduce_last = 1;
+    else p.reduce_last = (op == OP_AG || p.T < 2 * kRefSMs) ? 1 : 0;
+  }
   // workspace layout
   size_t off = kHeaderBytes;
   const size_t n_chunk_words = op == OP_AG ? static_cast<size_t>(W) * p.n_chunks : 0;
@@ -115,7 +129,9 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.off_chunk_cnt = off;
   off += n_chunk_words * 4;
   p.off_chain_flags = off;
-  off += static_cast<size_t>(L > 1 ? L - 1 : 0) * p.T * 4;
+  off += static_cast<size_t>(L > 1 && !p.reduce_last ? L - 1 : 0) * p.T * 4;
+  p.off_tile_cnt = off;
+  off += static_cast<size_t>(p.reduce_last ? p.T : 0) * 4;
   off = align_up(off, 1024);
   p.ctrl_end = off;
   if (op == OP_AG) {
@@ -124,7 +140,8 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   }
   if (L > 1) {
     p.off_S = off;
-    off = align_up(off + static_cast<size_t>(p.T) * kBM * bn * 4, 1024);
+    const size_t slots = p.reduce_last ? static_cast<size_t>(L) : 1;
+    off = align_up(off + slots * static_cast<size_t>(p.T) * kBM * bn * 4, 1024);
   }
   p.total = off;
   *pl = p;
@@ -242,6 +259,8 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.chunk_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_chunk_cnt);
   kp.chain_flags = reinterpret_cast<uint32_t*>(ws + pl.off_chain_flags);
   kp.sbuf = pl.L > 1 ? reinterpret_cast<float*>(ws + pl.off_S) : nullptr;
+  kp.tile_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tile_cnt);
+  kp.reduce_last = pl.reduce_last;
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;
   kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
@@ -454,7 +473,8 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   if (s != TDX_OK) return s;
   const int64_t v[16] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
-                         (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total, 0, 0};
+                         (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

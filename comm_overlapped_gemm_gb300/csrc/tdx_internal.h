@@ -43,7 +43,9 @@ struct KParams {
   uint32_t* chunk_flags;         // AG: [W * n_chunks], flag of chunk (rank, c) at rank*n_chunks + c
   uint32_t* chunk_cnt;           // AG: pieces completed per chunk (reset by the last piece)
   uint32_t* chain_flags;         // [(L-1) * T]: running sum of chain elements 0..c done for tile
-  float* sbuf;                   // [T][kBM*BN] running-sum buffer, thread-coalesced layout
+  float* sbuf;                   // chained: [T][kBM*BN] running sum; slotted: [L][T][kBM*BN] partials
+  uint32_t* tile_cnt;            // slotted: partials stored per tile (reset by the last arriver)
+  int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
   float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r
   int op, mode;

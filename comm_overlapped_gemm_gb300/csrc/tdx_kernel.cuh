@@ -11,11 +11,16 @@
 //   warps 2-3       AllGather producer: copies 16 KiB pieces of shard chunks into the gathered
 //                   buffer; the last piece of a chunk releases the chunk's flag (= epoch).
 //   warps 4-11      epilogue: TMEM -> registers; either the output tile (rounded once) or, along
-//                   a chain (RS ranks or AG K-splits), the running sum: element c of the chain
-//                   acquires flag (c-1, tile), adds its partial to the fp32 running sum of
-//                   elements 0..c-1, stores it and releases flag (c, tile); the last element
-//                   rounds and stores the output. The order is fixed, so results are
-//                   bit-identical run to run.
+//                   a chain (RS ranks or AG K-splits) of L elements, the fixed-order fp32 sum
+//                   ((P_0 + P_1) + P_2) + ... of the elements' partial tiles, in one of two ways:
+//                   "chained": element c acquires flag (c-1, tile), adds its partial to the
+//                   running sum of elements 0..c-1, stores it and releases flag (c, tile); the
+//                   last element rounds and stores the output (large problems: the elements of a
+//                   tile run far apart in time, one running-sum buffer). "slotted": every element
+//                   stores its partial in its own slot and bumps the tile's arrival counter; the
+//                   element that completes the count folds the slots in order 0..L-1 (small
+//                   problems: the elements of a tile run concurrently, nothing waits). Either way
+//                   the order is fixed, so results are bit-identical run to run.
 //
 // The chunk/flag pipeline follows the Triton-distributed article (cronfeed.work), section "The
 // first move was to expose the overlap" (chunks, compute on arrived chunks while others move,
@@ -197,6 +202,59 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
   }
 }
 
+// Round 32 consecutive fp32 values of one output row (columns col..col+31) once to the output type
+// and store them: AllGather -> C (bf16 or fp32, e4m3 inputs scaled by scale_a[rank]*scale_b);
+// ReduceScatter -> output shard row / (M/W). Rows >= M and columns >= N are skipped.
+template <int OP, bool FP8>
+__device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int col, float (&v)[32]) {
+  if (row >= p.M) return;
+  uint8_t* orow;
+  if constexpr (OP == OP_AG) {
+    if constexpr (FP8) {
+      const float s = p.row_scale[row / p.M_local];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= s;
+    }
+    orow = p.out[0] + (size_t)row * p.N * (p.out_fp32 ? 4 : 2);
+  } else {
+    const int j = row / p.M_local;
+    orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
+  }
+  if (p.out_fp32) {
+    float* o = reinterpret_cast<float*>(orow) + col;
+    if (col + 32 <= p.N) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_f4(o + 4 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col + i < p.N) o[i] = v[i];
+    }
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(orow) + col;
+    if (col + 32 <= p.N) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 pk;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+        pk.x = *reinterpret_cast<uint32_t*>(&b0);
+        pk.y = *reinterpret_cast<uint32_t*>(&b1);
+        pk.z = *reinterpret_cast<uint32_t*>(&b2);
+        pk.w = *reinterpret_cast<uint32_t*>(&b3);
+        st_v4(o + 8 * j, pk);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col + i < p.N) o[i] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
 template <int BN, bool FP8, int OP>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
   using C = Cfg<BN, FP8>;
@@ -208,7 +266,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] TMA k-blocks issued, misc[3] MMA k-blocks
-  // consumed, misc[4] epilogue go/stop decision
+  // consumed, misc[4] epilogue go/stop decision, misc[5] epilogue "last arriver" decision
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   const uint32_t full0 = smem_u32(bars);
@@ -234,6 +292,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     misc[2] = 0;
     misc[3] = 0;
     misc[4] = 0;
+    misc[5] = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -442,16 +501,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const int h = e >> 2;                     // column half
     const int row_in_tile = q * 32 + lane;
     const bool elected = threadIdx.x == kEpiWarp0 * 32;
-    volatile uint32_t* decision = misc + 4;
+    volatile uint32_t* decision = misc + 4;    // written before barrier 1, read after it
+    volatile uint32_t* is_last = misc + 5;     // written between barriers 2 and 3, read after 3
+    const bool rs_gemm_only = !ag && p.mode == MODE_GEMM_ONLY;
+    const bool chained = chain && !p.reduce_last;   // running sum handed from element to element
+    const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
     int local = 0;
     for (int it = blockIdx.x; it < items; it += grid, ++local) {
       const Item w = decode_item<OP>(p, it, BN);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      const bool read_s = chain && w.c > 0;
-      const bool final_out = (!chain && !(!ag && p.mode == MODE_GEMM_ONLY)) || (chain && w.c == p.L - 1);
-      const bool write_s = (chain && w.c < p.L - 1) || (!ag && p.mode == MODE_GEMM_ONLY);
+      const bool read_s = chained && w.c > 0;
+      const bool write_s = (chained && w.c < p.L - 1) || slotted || rs_gemm_only;
+      const bool direct_out = (!chain && !rs_gemm_only) || (chained && w.c == p.L - 1);
       if (elected) {
         bool ok = true;
         if (use_mma) ok = wait_mbar(p, tfull0 + 8 * acc, aph, abort_flag, 400 + acc);
@@ -462,14 +525,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
         if (*abort_flag) ok = false;
         *decision = ok ? 1u : 0u;
-        if (trace != nullptr && ok) trace[4 + 4 * grid + blockIdx.x * per_cta + local] = (static_cast<uint32_t>(w.c) << 24) | static_cast<uint32_t>(w.tile);
+        if (trace != nullptr && ok)
+          trace[4 + 4 * grid + blockIdx.x * per_cta + local] =
+              (static_cast<uint32_t>(w.c) << 24) | static_cast<uint32_t>(w.tile);
       }
       named_bar_sync(1, kEpiThreads);
       if (*decision == 0u) break;
       tc_fence_after();
 
       const int row = w.m0 + row_in_tile;
-      float* sb = p.sbuf + (size_t)w.tile * (kBM * BN);
+      const size_t slot = slotted ? (size_t)w.c * p.T + w.tile : (size_t)w.tile;
+      float* sb = p.sbuf + slot * (kBM * BN);
 #pragma unroll 1
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
         const int col0 = h * C::COLS_PER_WARP + ch * 32;   // column inside the tile
@@ -504,62 +570,60 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           for (int j = 0; j < 8; ++j)
             st_f4(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
         }
-        if (final_out && row < p.M) {
-          uint8_t* orow;
-          if (ag) {
-            if (FP8) {
-              const float s = p.row_scale[row / p.M_local];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= s;
-            }
-            orow = p.out[0] + (size_t)row * p.N * (p.out_fp32 ? 4 : 2);
-          } else {
-            const int j = row / p.M_local;
-            orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
-          }
-          const int col = w.n0 + col0;
-          if (p.out_fp32) {
-            float* o = reinterpret_cast<float*>(orow) + col;
-            if (col + 32 <= p.N) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                st_f4(o + 4 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col + i < p.N) o[i] = v[i];
-            }
-          } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(orow) + col;
-            if (col + 32 <= p.N) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 pk;
-                __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
-                __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
-                __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
-                pk.x = *reinterpret_cast<uint32_t*>(&b0);
-                pk.y = *reinterpret_cast<uint32_t*>(&b1);
-                pk.z = *reinterpret_cast<uint32_t*>(&b2);
-                pk.w = *reinterpret_cast<uint32_t*>(&b3);
-                st_v4(o + 8 * j, pk);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col + i < p.N) o[i] = __float2bfloat16_rn(v[i]);
-            }
-          }
-        }
+        if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v);
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
       if (elected) {
         if (use_mma) mbar_arrive(tempty0 + 8 * acc);
-        if (chain && write_s) {
+        if (chained && write_s) {
           __threadfence();
           st_release_gpu(p.chain_flags + (size_t)w.c * p.T + w.tile, p.epoch);
+        }
+        if (slotted) {
+          // count this tile's stored partials; the element that completes the count folds them
+          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x30000u + it) & 4095u);
+          __threadfence();
+          const uint32_t old = atomicAdd(p.tile_cnt + w.tile, 1u);
+          const bool last = old == static_cast<uint32_t>(p.L - 1);
+          if (last) {
+            p.tile_cnt[w.tile] = 0u;
+            __threadfence();
+          }
+          *is_last = last ? 1u : 0u;
+        }
+      }
+      if (slotted) {
+        named_bar_sync(1, kEpiThreads);
+        if (*is_last) {
+          // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ...
+#pragma unroll 1
+          for (int ch = 0; ch < C::CHUNKS; ++ch) {
+            const int col0 = h * C::COLS_PER_WARP + ch * 32;
+            const size_t off = ((size_t)(col0 >> 5) * 8 * kBM + row_in_tile) * 4;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 s = ld_cg_f4(p.sbuf + (size_t)w.tile * (kBM * BN) + off + j * kBM * 4);
+              v[4 * j + 0] = s.x;
+              v[4 * j + 1] = s.y;
+              v[4 * j + 2] = s.z;
+              v[4 * j + 3] = s.w;
+            }
+#pragma unroll 1
+            for (int c = 1; c < p.L; ++c) {
+              const float* sp = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 s = ld_cg_f4(sp + j * kBM * 4);
+                v[4 * j + 0] = v[4 * j + 0] + s.x;
+                v[4 * j + 1] = v[4 * j + 1] + s.y;
+                v[4 * j + 2] = v[4 * j + 2] + s.z;
+                v[4 * j + 3] = v[4 * j + 3] + s.w;
+              }
+            }
+            store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v);
+          }
         }
       }
     }

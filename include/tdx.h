@@ -85,6 +85,11 @@ typedef struct tdx_opts {
   int num_sms;               /* persistent grid size; 0 = every SM of the device */
   int split_k;               /* AG: K splits reduced in fixed order (0 = library choice, 1 = none) */
   int block_n;               /* GEMM tile width 64/128/256 (0 = library choice) */
+  int reduce_mode;           /* fixed-order reduction of RS ranks / AG K splits: 0 = library choice,
+                                1 = chained (element c adds its partial to the running sum of
+                                elements 0..c-1 and hands it on), 2 = slotted (each element stores its
+                                partial; the last to arrive folds them in order 0..L-1). Both give
+                                the same bits. */
 } tdx_opts;
 
 /* Fill *opts with the defaults above. Returns TDX_ERR_INVALID_ARG if opts is NULL. */
@@ -179,7 +184,8 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] 128-byte K blocks, [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
- * buffer G, [12] fp32 running-sum buffer, [13] total workspace bytes; [14..15] reserved (0). */
+ * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
+ * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -37,7 +37,7 @@ TINY = wls.WORKLOADS["ag_tiny"]
 
 @pytest.mark.parametrize("variant", [
     {}, {"split_k": 1, "block_n": 256}, {"split_k": 1, "block_n": 128}, {"split_k": 1, "block_n": 64},
-    {"self_rank": 1}, {"split_k": 2, "block_n": 256}, {"perturb_seed": 7},
+    {"self_rank": 1}, {"split_k": 2, "block_n": 256}, {"perturb_seed": 7}, {"split_k": 2, "reduce_mode": 1},
 ])
 def test_ag_tiny_integer_bit_exact(variant):
     inp = wls.make_inputs(TINY, integer=True)
@@ -105,7 +105,8 @@ def test_ag_small_m_full_output(integer):
 def test_ag_ragged_shapes(shape, integer):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], **shape)
     inp = wls.make_inputs(wl, integer=integer)
-    for variant in [{}, {"split_k": 1}, {"split_k": 3, "block_n": 128}]:
+    for variant in [{}, {"split_k": 1}, {"split_k": 3, "block_n": 128, "reduce_mode": 1},
+                    {"split_k": 4, "block_n": 256, "reduce_mode": 2}]:
         case = AGCase(inp, opts=opts(chunk_rows=shape["chunk_rows"], **variant))
         tdx.check(case.run(), str(variant))
         status_ok(case)
@@ -262,3 +263,15 @@ def test_ag_full_size_copy_engine_sampled():
     status_ok(case)
     rows = sample_rows(wl.W * wl.M, wl.chunk_rows)
     assert_within_tol(R.decode_bf16(case.result_bits()[rows]), case.oracle(rows), "bf16")
+
+
+def test_ag_split_k_chained_and_slotted_identical():
+    wl = wls.WORKLOADS["ag_small"]
+    inp = wls.make_inputs(wl, integer=False)
+    bits = []
+    for rm in (1, 2):
+        case = AGCase(inp, opts=opts(reduce_mode=rm, perturb_seed=5))
+        tdx.check(case.run())
+        status_ok(case)
+        bits.append(case.result_bits())
+    assert np.array_equal(bits[0], bits[1])

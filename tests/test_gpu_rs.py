@@ -34,9 +34,9 @@ def status_ok(case):
 def test_rs_small_shapes(shape, integer):
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
     inp = wls.make_inputs(wl, integer=integer)
-    for bn in (0, 128):
-        case = RSCase(inp, opts=opts(block_n=bn))
-        tdx.check(case.run(), f"rs {shape} bn={bn}")
+    for bn, rm in ((0, 0), (128, 1), (256, 2)):
+        case = RSCase(inp, opts=opts(block_n=bn, reduce_mode=rm))
+        tdx.check(case.run(), f"rs {shape} bn={bn} reduce_mode={rm}")
         status_ok(case)
         if integer:
             assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
@@ -86,11 +86,12 @@ def test_rs_chain_flags_trace_and_order():
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
     inp = wls.make_inputs(wl, integer=False)
     grid = 8
-    o = opts(num_sms=grid)
+    o = opts(num_sms=grid, reduce_mode=1)
     plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, o)
+    assert plan["reduce_mode"] == 1
     items = plan["L"] * plan["T"]
     trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    case = RSCase(inp, opts=opts(num_sms=grid, trace=trace, epoch=3))
+    case = RSCase(inp, opts=opts(num_sms=grid, trace=trace, epoch=3, reduce_mode=1))
     tdx.check(case.run())
     status_ok(case)
     assert_within_tol(case.result(), case.oracle(), "bf16")
@@ -135,3 +136,63 @@ def test_rs_degenerate_k_zero():
     tdx.check(tdx.tdx_gemm_rs([dummy] * 2, [dummy] * 2, outs, ws, 2, 128, 0, 128, tdx.TDX_BF16, opts()))
     torch.cuda.synchronize()
     assert all(int(torch.count_nonzero(o)) == 0 for o in outs)
+
+
+@pytest.mark.parametrize("shape", [dict(W=8, M=1024, K=512, N=1024), dict(W=3, M=384, K=200, N=136)])
+def test_rs_chained_and_slotted_give_identical_bits(shape):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=False)
+    outs = []
+    for rm in (1, 2):
+        case = RSCase(inp, opts=opts(reduce_mode=rm, perturb_seed=99))
+        tdx.check(case.run())
+        status_ok(case)
+        outs.append(case.result_bits())
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_rs_slotted_bookkeeping():
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
+    inp = wls.make_inputs(wl, integer=True)
+    o = opts(reduce_mode=2, epoch=7)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, o)
+    assert plan["reduce_mode"] == 2
+    case = RSCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    # every tile's arrival counter is back to zero for the next call
+    T = plan["T"]
+    cnt = case.ws[plan["off_tile_cnt"]:plan["off_tile_cnt"] + 4 * T].view(torch.int32).cpu().numpy()
+    assert not cnt.any()
+    # slot r of a tile holds rank r's partial A_r @ B_r (fp32, exact on integers)
+    BN = plan["BN"]
+    S = case.ws[plan["off_S"]:plan["off_S"] + 4 * 4 * T * 128 * BN].view(torch.float32).cpu().numpy()
+    for r in range(4):
+        P = R.gemm_rs_rows([inp.a[r]], [inp.b[r]], np.arange(512), "bf16")
+        for (mt, nt) in [(0, 0), (2, 3)]:
+            tile = mt * plan["tiles_n"] + nt
+            blk = S[(r * T + tile) * 128 * BN:(r * T + tile + 1) * 128 * BN]
+            blk = blk.reshape(BN // 32, 8, 128, 4).transpose(2, 0, 1, 3).reshape(128, BN)
+            assert np.array_equal(blk, P[mt * 128:(mt + 1) * 128, nt * BN:(nt + 1) * BN])
+    # a second call with the next epoch gives the same result (counters were reset)
+    for x in case.out:
+        x.fill_(float("nan"))
+    tdx.check(case.run(opts(reduce_mode=2, epoch=8)))
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+
+
+def test_rs_full_size_slotted_matches_chained():
+    wl = wls.WORKLOADS["rs_w8"]
+    inp = wls.make_inputs(wl, integer=False)
+    bits = []
+    for rm in (1, 2):
+        case = RSCase(inp, opts=opts(reduce_mode=rm))
+        tdx.check(case.run())
+        status_ok(case)
+        bits.append(case.result_bits())
+        del case
+        torch.cuda.empty_cache()
+    assert np.array_equal(bits[0], bits[1])
