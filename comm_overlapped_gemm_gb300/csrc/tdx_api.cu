@@ -222,10 +222,13 @@ bool ce_state(CeState** out) {
 }
 
 int device_sms() {
+  static int cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
   return n;
 }
 

@@ -656,9 +656,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 template <int BN, bool FP8, int OP>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // the dynamic shared-memory limit is raised once per device for each instantiation
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
