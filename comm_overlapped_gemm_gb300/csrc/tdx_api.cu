@@ -39,6 +39,7 @@ tdx_opts defaults() {
   o.split_k = 0;
   o.block_n = 0;
   o.reduce_mode = 0;
+  o.cluster = 0;
   return o;
 }
 
@@ -49,6 +50,7 @@ struct Plan {
   int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
+  int CL = 1;
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
 };
@@ -113,6 +115,15 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.L = L;
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
+  // pairs of CTAs sharing the B slice: large problems with 256-wide tiles and an even M-tile count
+  if (o.cluster < 0 || o.cluster > 2) return TDX_ERR_INVALID_ARG;
+  const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
+  if (o.cluster == 2) {
+    if (!pair_ok) return TDX_ERR_UNSUPPORTED;
+    p.CL = 2;
+  } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs) {
+    p.CL = 2;
+  }
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
   if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
@@ -237,8 +248,8 @@ tdx_status fill_zero(void* p, size_t bytes, cudaStream_t s) {
 }
 
 tdx_status launch(const Plan& pl, KParams& kp, bool fp8, int grid, cudaStream_t stream) {
-  const cudaError_t e =
-      fp8 ? launch_fused_fp8(pl.op, pl.BN, kp, grid, stream) : launch_fused_bf16(pl.op, pl.BN, kp, grid, stream);
+  const cudaError_t e = fp8 ? launch_fused_fp8(pl.op, pl.BN, pl.CL, kp, grid, stream)
+                            : launch_fused_bf16(pl.op, pl.BN, pl.CL, kp, grid, stream);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;
@@ -272,11 +283,16 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.row_bytes = static_cast<long long>(pl.K) * pl.elt;
 }
 
-int grid_for(const tdx_opts& o, int items_or_zero) {
+// Persistent grid: every CTA resident at once (one per SM; for pairs, the clusters that fit), capped
+// by opts.num_sms and, when given, by the number of work items; a multiple of the cluster size.
+int grid_for(const tdx_opts& o, const Plan& pl, bool fp8, int items_or_zero) {
   int sms = device_sms();
   if (sms <= 0) return 0;
-  int g = o.num_sms > 0 && o.num_sms < sms ? o.num_sms : sms;
+  int g = fp8 ? fused_max_grid_fp8(pl.op, pl.CL, sms) : fused_max_grid_bf16(pl.op, pl.CL, sms);
+  if (g <= 0) return 0;
+  if (o.num_sms > 0 && o.num_sms < g) g = o.num_sms;
   if (items_or_zero > 0 && items_or_zero < g) g = items_or_zero;
+  g -= g % pl.CL;
   return g;
 }
 
@@ -352,7 +368,7 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
     kp.row_scale[r] = sa * sb;
   }
   kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
-  const int grid = grid_for(o, 0);
+  const int grid = grid_for(o, pl, fp8, 0);
   if (grid <= 0) return TDX_ERR_CUDA;
   // producer copy unit: about one piece per CTA, in 16 KiB rounds, at most 64 KiB per release
   {
@@ -451,7 +467,7 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
     if (s != TDX_OK) return s;
   }
-  const int grid = grid_for(o, pl.L * pl.T);
+  const int grid = grid_for(o, pl, false, pl.L * pl.T);
   if (grid <= 0) return TDX_ERR_CUDA;
   return launch(pl, kp, false, grid, st);
 }
@@ -474,10 +490,10 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   Plan pl;
   tdx_status s = make_plan(op, W, M_local_or_M, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const int64_t v[16] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
+  const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.CL, 0, 0, 0};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

@@ -72,9 +72,12 @@ struct KParams {
 // Shared-memory footprint of one instantiation (host side, for the launch).
 int fused_smem_bytes(int block_n, bool fp8);
 
-// Launch the persistent fused kernel for (block_n, fp8) on `grid` CTAs.
-cudaError_t launch_fused_bf16(int op, int block_n, const KParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_fused_fp8(int op, int block_n, const KParams& p, int grid, cudaStream_t stream);
+// Launch the persistent fused kernel for (op, block_n, cluster size cl) on `grid` CTAs.
+cudaError_t launch_fused_bf16(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_fp8(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream);
+// Largest grid whose CTAs are resident together (cl = 2: twice the 2-CTA clusters that fit).
+int fused_max_grid_bf16(int op, int cl, int sms);
+int fused_max_grid_fp8(int op, int cl, int sms);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
 }  // namespace tdx

@@ -77,24 +77,30 @@ struct Item {
   int m0, n0;
 };
 
-template <int OP>
-__device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN) {
+// Work item `it` of a CTA whose rank in its cluster is `crank`. With CL CTAs per cluster, items
+// index (chain element, group of CL consecutive M-tiles, N-tile) and the CTA of cluster rank r takes
+// M-tile CL*group + r (the host keeps tiles_m a multiple of CL). AllGather groups are taken in the
+// rank-swizzled arrival order: from the first group whose first row belongs to self_rank,
+// wrapping around; N-tiles innermost.
+template <int OP, int CL>
+__device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, int crank) {
   Item r;
-  r.c = it / p.T;
-  const int pos = it - r.c * p.T;
-  int mt, nt;
+  const int tiles_g = p.tiles_m / CL;
+  const int Tg = tiles_g * p.tiles_n;
+  r.c = it / Tg;
+  const int pos = it - r.c * Tg;
+  int mg, nt;
   if constexpr (OP == OP_AG) {
-    // rank-swizzled arrival order: M-tiles from the first tile whose first row belongs to
-    // self_rank, wrapping around; N-tiles innermost.
-    int start = (p.self_rank * p.M_local + kBM - 1) / kBM;
-    if (start >= p.tiles_m) start = 0;
-    mt = start + pos / p.tiles_n;
-    if (mt >= p.tiles_m) mt -= p.tiles_m;
+    int start = (p.self_rank * p.M_local + CL * kBM - 1) / (CL * kBM);
+    if (start >= tiles_g) start = 0;
+    mg = start + pos / p.tiles_n;
+    if (mg >= tiles_g) mg -= tiles_g;
     nt = pos % p.tiles_n;
   } else {
-    mt = pos / p.tiles_n;
+    mg = pos / p.tiles_n;
     nt = pos % p.tiles_n;
   }
+  const int mt = mg * CL + crank;
   r.tile = mt * p.tiles_n + nt;
   r.m0 = mt * kBM;
   r.n0 = nt * BN;
@@ -255,8 +261,9 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
   }
 }
 
-template <int BN, bool FP8, int OP>
+template <int BN, bool FP8, int OP, int CL>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
+  static_assert(CL == 1 || (CL == 2 && Cfg<BN, FP8>::B_BOXES % 2 == 0), "pairs split B into two halves");
   using C = Cfg<BN, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CL);   // a slot is free once every CTA of the cluster consumed it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -304,23 +311,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     for (int i = 0; i < (OP == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync_all();   // the peer's barriers are initialised before any multicast targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
+  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = blockIdx.x / CL;          // cluster index
+  const int ncl = gridDim.x / CL;           // clusters in the grid
 
   constexpr bool ag = OP == OP_AG;
   const bool ag_move_only = ag && p.mode == MODE_MOVE_ONLY;
   const bool rs_move_only = !ag && p.mode == MODE_MOVE_ONLY;
-  const int items = ag_move_only ? 0 : p.L * p.T;
+  const int items_all = ag_move_only ? 0 : p.L * p.T;   // (element, tile) work items
+  const int items = items_all / CL;                       // items of one cluster-wide sequence
   const bool use_mma = !rs_move_only;  // RS move-only runs the chain on zero partials
   const bool chain = p.L > 1 && !(!ag && p.mode == MODE_GEMM_ONLY);
   const int grid = gridDim.x;
   uint32_t* trace = p.trace;
-  const int per_cta = (items + grid - 1) / grid;
+  const int per_cta = (items_all + grid - 1) / grid;
 
   if (trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
     trace[0] = grid;
-    trace[1] = items;
+    trace[1] = items_all;
     trace[2] = p.L;
     trace[3] = p.T;
   }
@@ -334,9 +348,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       uint64_t flag_ns = 0;
       uint32_t n_waits = 0;
       bool stop = false;
-      for (int it = blockIdx.x; it < items && !stop; it += grid) {
+      for (int it = cid; it < items && !stop; it += ncl) {
         if (*abort_flag) break;
-        const Item w = decode_item<OP>(p, it, BN);
+        const Item w = decode_item<OP, CL>(p, it, BN, crank);
         const CUtensorMap* map_a;
         const CUtensorMap* map_b;
         int arow = w.m0;
@@ -377,10 +391,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow);
+          if constexpr (CL == 1) {
 #pragma unroll
-          for (int j = 0; j < C::B_BOXES; ++j)
-            tma_load_2d(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                        w.n0 + j * C::B_BOX_N, kb * C::BK);
+            for (int j = 0; j < C::B_BOXES; ++j)
+              tma_load_2d(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                          w.n0 + j * C::B_BOX_N, kb * C::BK);
+          } else {
+            // both CTAs of the pair compute the same N-tile: each loads its half of the B slice
+            // into the slot of both CTAs (multicast); the slot's barrier in each CTA expects the
+            // whole stage (own A + both halves of B)
+#pragma unroll
+            for (int jj = 0; jj < C::B_BOXES / 2; ++jj) {
+              const int j = crank * (C::B_BOXES / 2) + jj;
+              tma_load_2d_multicast(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                                    w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3));
+            }
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -403,8 +429,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       uint32_t consumed = 0;
       int local = 0;
       bool stop = false;
-      for (int it = blockIdx.x; it < items && !stop; it += grid, ++local) {
-        const Item w = decode_item<OP>(p, it, BN);
+      for (int it = cid; it < items && !stop; it += ncl, ++local) {
+        const Item w = decode_item<OP, CL>(p, it, BN, crank);
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!wait_mbar(p, tempty0 + 8 * acc, aph ^ 1u, abort_flag, 200 + acc)) break;
@@ -430,7 +456,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             else
               umma_bf16(d, adesc, bdesc, C::IDESC, accum);
           }
-          tc_commit(empty0 + 8 * stage);
+          if constexpr (CL == 1)
+            tc_commit(empty0 + 8 * stage);
+          else
+            tc_commit_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));   // free it in both CTAs
           ++consumed;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -508,8 +537,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
     int local = 0;
-    for (int it = blockIdx.x; it < items; it += grid, ++local) {
-      const Item w = decode_item<OP>(p, it, BN);
+    for (int it = cid; it < items; it += ncl, ++local) {
+      const Item w = decode_item<OP, CL>(p, it, BN, crank);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const bool read_s = chained && w.c > 0;
@@ -646,14 +675,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       wait_mbar_drain(p, full0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1u);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync_all();   // no CTA leaves while its peer may still multicast into it or arrive on it
+  else
+    __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <int BN, bool FP8, int OP>
+template <int BN, bool FP8, int OP, int CL>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8>;
   // the dynamic shared-memory limit is raised once per device for each instantiation
@@ -662,7 +694,7 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -673,11 +705,54 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if constexpr (CL == 1) {
+    // CTAs wait on flags other CTAs release: all of them must be resident at once
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    // pairs of CTAs; the host sizes the grid to the clusters that fit at once
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP>, p);
+  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP, CL>, p);
+}
+
+// Largest grid whose CTAs are all resident at once: one CTA per SM, or for pairs twice the number
+// of 2-CTA clusters the device can hold simultaneously.
+template <int BN, bool FP8, int OP, int CL>
+int max_grid_t(int sms) {
+  if constexpr (CL == 1) {
+    return sms;
+  } else {
+    using C = Cfg<BN, FP8>;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sms, 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tdx_fused_kernel<BN, FP8, OP, CL>, &cfg) != cudaSuccess) return 0;
+    const int g = n * CL;
+    if (dev >= 0 && dev < 64) cache[dev] = g;
+    return g;
+  }
 }
 
 }  // namespace tdx

@@ -3,21 +3,31 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_bf16(int op, int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_bf16(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream) {
+  if (cl == 2) {
+    if (block_n != 256) return cudaErrorInvalidValue;
+    return op == OP_AG ? launch_fused_t<256, false, OP_AG, 2>(p, grid, stream)
+                       : launch_fused_t<256, false, OP_RS, 2>(p, grid, stream);
+  }
   if (op == OP_AG) {
     switch (block_n) {
-      case 64: return launch_fused_t<64, false, OP_AG>(p, grid, stream);
-      case 128: return launch_fused_t<128, false, OP_AG>(p, grid, stream);
-      case 256: return launch_fused_t<256, false, OP_AG>(p, grid, stream);
+      case 64: return launch_fused_t<64, false, OP_AG, 1>(p, grid, stream);
+      case 128: return launch_fused_t<128, false, OP_AG, 1>(p, grid, stream);
+      case 256: return launch_fused_t<256, false, OP_AG, 1>(p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (block_n) {
-    case 64: return launch_fused_t<64, false, OP_RS>(p, grid, stream);
-    case 128: return launch_fused_t<128, false, OP_RS>(p, grid, stream);
-    case 256: return launch_fused_t<256, false, OP_RS>(p, grid, stream);
+    case 64: return launch_fused_t<64, false, OP_RS, 1>(p, grid, stream);
+    case 128: return launch_fused_t<128, false, OP_RS, 1>(p, grid, stream);
+    case 256: return launch_fused_t<256, false, OP_RS, 1>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int fused_max_grid_bf16(int op, int cl, int sms) {
+  if (cl != 2) return sms;
+  return op == OP_AG ? max_grid_t<256, false, OP_AG, 2>(sms) : max_grid_t<256, false, OP_RS, 2>(sms);
 }
 
 // Zero-fill used for the degenerate K == 0 product (C = 0).

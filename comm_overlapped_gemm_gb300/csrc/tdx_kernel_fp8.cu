@@ -4,13 +4,22 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_fp8(int op, int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_fp8(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream) {
   if (op != OP_AG) return cudaErrorInvalidValue;
+  if (cl == 2) {
+    if (block_n != 256) return cudaErrorInvalidValue;
+    return launch_fused_t<256, true, OP_AG, 2>(p, grid, stream);
+  }
   switch (block_n) {
-    case 128: return launch_fused_t<128, true, OP_AG>(p, grid, stream);
-    case 256: return launch_fused_t<256, true, OP_AG>(p, grid, stream);
+    case 128: return launch_fused_t<128, true, OP_AG, 1>(p, grid, stream);
+    case 256: return launch_fused_t<256, true, OP_AG, 1>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int fused_max_grid_fp8(int op, int cl, int sms) {
+  if (cl != 2 || op != OP_AG) return sms;
+  return max_grid_t<256, true, OP_AG, 2>(sms);
 }
 
 }  // namespace tdx

@@ -90,6 +90,10 @@ typedef struct tdx_opts {
                                 elements 0..c-1 and hands it on), 2 = slotted (each element stores its
                                 partial; the last to arrive folds them in order 0..L-1). Both give
                                 the same bits. */
+  int cluster;               /* CTAs per cluster for the GEMM: 0 = library choice, 1 = single CTAs,
+                                2 = pairs of CTAs on vertically adjacent 128 x 256 tiles that share
+                                the B slice (each loads half of it into both CTAs' shared memory).
+                                2 needs tile width 256 and an even number of 128-row M-tiles. */
 } tdx_opts;
 
 /* Fill *opts with the defaults above. Returns TDX_ERR_INVALID_ARG if opts is NULL. */
@@ -180,12 +184,13 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
                                   uint32_t* detail);
 
 /* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
- * uses. Writes 16 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
+ * uses. Writes 20 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
  * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] 128-byte K blocks, [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
- * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters. */
+ * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters,
+ * [16] CTAs per cluster (1 or 2), [17..19] reserved (0). */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -203,24 +203,30 @@ def ag_chunk_release_order(W: int, M_local: int, chunk: int, self_rank: int = 0)
     return [(r, c) for r in ranks for c in range(n_chunks)]
 
 
-def ag_tile_schedule(W: int, M_local: int, N: int, BM: int, BN: int, self_rank: int = 0):
+def ag_tile_schedule(W: int, M_local: int, N: int, BM: int, BN: int, self_rank: int = 0, group: int = 1):
     """Order in which the consumer GEMM takes output tiles: M-tiles grouped by the rank that owns
     the tile's first row, in arrival order self, self+1, ..., self+W-1 (mod W); M-tiles ascending
-    within a rank; N-tiles innermost. Returns (m_tile, n_tile) pairs."""
+    within a rank; N-tiles innermost. Returns (m_tile, n_tile) pairs.
+
+    With ``group`` > 1, ``group`` consecutive M-tiles are taken together (one per CTA of a cluster):
+    the groups follow the same rule keyed by the rank owning the group's first row, and the list
+    holds (m_group, n_tile) pairs; the CTA of cluster rank r takes M-tile ``group*m_group + r``."""
     M = W * M_local
     tiles_m = (M + BM - 1) // BM
     tiles_n = (N + BN - 1) // BN
-    key = lambda mt: (((mt * BM) // M_local - self_rank) % W, mt)
-    return [(mt, nt) for mt in sorted(range(tiles_m), key=key) for nt in range(tiles_n)]
+    n_groups = tiles_m // group
+    key = lambda mg: (((mg * group * BM) // M_local - self_rank) % W, mg)
+    return [(mg, nt) for mg in sorted(range(n_groups), key=key) for nt in range(tiles_n)]
 
 
-def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int):
+def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1):
     """Order of GEMM+ReduceScatter work items: rank-outer (0..W-1, the reduction order), M-tiles,
     N-tiles innermost. Item (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1.
-    Returns (rank, m_tile, n_tile) triples."""
+    Returns (rank, m_tile, n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group
+    (see :func:`ag_tile_schedule`)."""
     tiles_m = (M + BM - 1) // BM
     tiles_n = (N + BN - 1) // BN
-    return [(r, mt, nt) for r in range(W) for mt in range(tiles_m) for nt in range(tiles_n)]
+    return [(r, mg, nt) for r in range(W) for mg in range(tiles_m // group) for nt in range(tiles_n)]
 
 
 def expected_flags(n: int, epoch: int) -> np.ndarray:

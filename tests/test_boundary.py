@@ -64,7 +64,7 @@ def test_opts_default(tdx):
     o = tdx.tdx_opts_default()
     assert o.self_rank == 0 and o.mode == tdx.TDX_FUSED and o.timeout_ns == 2_000_000_000
     assert o.epoch == 0 and o.out_dtype == tdx.TDX_BF16
-    assert ctypes.sizeof(tdx.tdx_opts) == 88 and o.reduce_mode == 0
+    assert ctypes.sizeof(tdx.tdx_opts) == 96 and o.reduce_mode == 0 and o.cluster == 0
 
 
 def test_workspace_sizes(tdx):

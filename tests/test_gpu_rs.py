@@ -196,3 +196,32 @@ def test_rs_full_size_slotted_matches_chained():
         del case
         torch.cuda.empty_cache()
     assert np.array_equal(bits[0], bits[1])
+
+
+@pytest.mark.parametrize("rm", [1, 2])
+def test_rs_pairs_parity_trace_and_identity(rm):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=512, N=512)
+    inp = wls.make_inputs(wl, integer=False)
+    grid = 8
+    o = opts(num_sms=grid, cluster=2, block_n=256, reduce_mode=rm)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 512, 512, tdx.TDX_BF16, o)
+    assert plan["cluster"] == 2
+    items = plan["L"] * plan["T"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    case = RSCase(inp, opts=opts(num_sms=grid, cluster=2, block_n=256, reduce_mode=rm, trace=trace))
+    tdx.check(case.run())
+    status_ok(case)
+    assert_within_tol(case.result(), case.oracle(), "bf16")
+    paired = case.result_bits()
+    tr = trace.cpu().numpy().astype(np.uint32)
+    sched = R.rs_item_schedule(4, 512, 512, 128, 256, group=2)
+    per = (items + grid - 1) // grid
+    for b in range(grid):
+        cid, crank = divmod(b, 2)
+        for k, it in enumerate(range(cid, items // 2, grid // 2)):
+            r, mg, nt = sched[it]
+            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | ((2 * mg + crank) * plan["tiles_n"] + nt)
+    single = RSCase(inp, opts=opts(cluster=1, block_n=256, reduce_mode=rm))
+    tdx.check(single.run())
+    status_ok(single)
+    assert np.array_equal(single.result_bits(), paired)

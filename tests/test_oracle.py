@@ -407,3 +407,16 @@ def test_planted_format_mistakes_are_caught():
 def test_oracle_package_exports():
     for name in ["ag_gemm", "gemm_rs", "round_out", "ag_tile_schedule", "rs_item_schedule"]:
         assert hasattr(oracle, name)
+
+
+def test_grouped_schedules():
+    # groups of 2 M-tiles: a permutation of all groups, keyed by the owner of the group's first row
+    g = R.ag_tile_schedule(8, 1024, 3584, 128, 256, self_rank=3, group=2)
+    assert sorted(g) == [(m, n) for m in range(32) for n in range(14)]
+    assert g[0] == (12, 0) and g[14] == (13, 0) and g[4 * 14] == (16, 0)
+    assert R.ag_tile_schedule(8, 1024, 3584, 128, 256, 5, group=1) == R.ag_tile_schedule(8, 1024, 3584, 128, 256, 5)
+    # the tiles taken by the two CTAs of a cluster cover the ungrouped schedule's tile set
+    tiles = sorted((2 * mg + r, nt) for mg, nt in g for r in range(2))
+    assert tiles == sorted(R.ag_tile_schedule(8, 1024, 3584, 128, 256, 3))
+    rs = R.rs_item_schedule(8, 8192, 8192, 128, 256, group=2)
+    assert len(rs) == 8 * 32 * 32 and rs[1024] == (1, 0, 0)
