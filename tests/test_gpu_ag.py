@@ -282,12 +282,12 @@ def test_ag_pairs_parity_and_trace(self_rank):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=1024, N=768, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
     grid = 16
-    o = opts(self_rank=self_rank, num_sms=grid, cluster=2)
+    o = opts(self_rank=self_rank, num_sms=grid, cluster=2, block_n=256)
     plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 1024, 768, tdx.TDX_BF16, o)
     assert plan["cluster"] == 2 and plan["BN"] == 256
     items = plan["L"] * plan["T"]
     trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=2, trace=trace))
+    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=2, block_n=256, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
@@ -325,11 +325,11 @@ def test_ag_pairs_and_singles_give_identical_bits(name):
 def test_ag_pairs_timeout_recovers():
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=256, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
-    case = AGCase(inp, opts=opts(cluster=2))
-    tdx.check(case.run(tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY, timeout_ns=2_000_000, cluster=2)))
+    case = AGCase(inp, opts=opts(cluster=2, block_n=256))
+    tdx.check(case.run(tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY, timeout_ns=2_000_000, cluster=2, block_n=256)))
     st, detail = tdx.tdx_read_device_status(case.ws)
     assert st == tdx.TDX_ERR_TIMEOUT and detail[1] == 1
     tdx.check(tdx.tdx_workspace_init(case.ws))
-    tdx.check(case.run(opts(cluster=2)))
+    tdx.check(case.run(opts(cluster=2, block_n=256)))
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
