@@ -51,6 +51,7 @@ struct Plan {
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
   int CL = 1;
+  int group_n = 1;
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
 };
@@ -115,6 +116,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.L = L;
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
+  p.group_n = op == OP_RS ? (p.tiles_n < kRsGroupN ? (p.tiles_n > 0 ? p.tiles_n : 1) : kRsGroupN) : p.tiles_n;
   // pairs of CTAs sharing the B slice: large problems with 256-wide tiles and an even M-tile count
   if (o.cluster < 0 || o.cluster > 2) return TDX_ERR_INVALID_ARG;
   const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
@@ -266,6 +268,7 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.tiles_m = pl.tiles_m;
   kp.tiles_n = pl.tiles_n;
   kp.T = pl.T;
+  kp.group_n = pl.group_n;
   kp.L = pl.L;
   kp.num_kb = pl.num_kb;
   kp.status = reinterpret_cast<uint32_t*>(ws);
@@ -493,7 +496,7 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.CL, 0, 0, 0};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.CL, pl.group_n, 0, 0};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

@@ -22,6 +22,7 @@ constexpr int kCopyThreads = kNumCopyWarps * 32;
 constexpr int kCopyRoundBytes = 16384;   // producer: bytes in flight per CTA per round
 constexpr int kMaxPieceBytes = 65536;    // producer: largest copy unit released at once
 constexpr int kMaxSplitK = 16;
+constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
 enum Op { OP_AG = 0, OP_RS = 1 };
@@ -54,6 +55,7 @@ struct KParams {
   int self_rank;
   int chunk_rows, n_chunks;      // AG chunking (per rank)
   int tiles_m, tiles_n, T;       // T = tiles_m * tiles_n
+  int group_n;                   // RS raster: N-tiles per group (1..tiles_n)
   int L;                         // chain length: RS = W ranks, AG = split-K factor
   int num_kb;                    // K blocks of 128 bytes
   int out_fp32;

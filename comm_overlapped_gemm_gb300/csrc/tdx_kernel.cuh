@@ -97,8 +97,23 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, in
     if (mg >= tiles_g) mg -= tiles_g;
     nt = pos % p.tiles_n;
   } else {
-    mg = pos / p.tiles_n;
-    nt = pos % p.tiles_n;
+    // ReduceScatter: within a rank, N-tiles in groups of group_n (the last group may be narrower);
+    // group-outer, M groups, N-tiles of the group innermost, so that a wave of tiles touches few
+    // rows of A_r and few columns of B_r
+    const int gn = p.group_n;
+    const int full = p.tiles_n / gn;
+    const int per_group = tiles_g * gn;
+    if (pos < full * per_group) {
+      const int ng = pos / per_group;
+      const int q = pos - ng * per_group;
+      mg = q / gn;
+      nt = ng * gn + (q - mg * gn);
+    } else {
+      const int rem = p.tiles_n - full * gn;
+      const int q = pos - full * per_group;
+      mg = q / rem;
+      nt = full * gn + (q - mg * rem);
+    }
   }
   const int mt = mg * CL + crank;
   r.tile = mt * p.tiles_n + nt;
@@ -212,7 +227,7 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
 // and store them: AllGather -> C (bf16 or fp32, e4m3 inputs scaled by scale_a[rank]*scale_b);
 // ReduceScatter -> output shard row / (M/W). Rows >= M and columns >= N are skipped.
 template <int OP, bool FP8>
-__device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int col, float (&v)[32]) {
+__device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int col, float (&v)[32], uint64_t pol) {
   if (row >= p.M) return;
   uint8_t* orow;
   if constexpr (OP == OP_AG) {
@@ -231,7 +246,7 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
     if (col + 32 <= p.N) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        st_f4(o + 4 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        st_f4_hint(o + 4 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -251,7 +266,7 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
         pk.y = *reinterpret_cast<uint32_t*>(&b1);
         pk.z = *reinterpret_cast<uint32_t*>(&b2);
         pk.w = *reinterpret_cast<uint32_t*>(&b3);
-        st_v4(o + 8 * j, pk);
+        st_v4_hint(o + 8 * j, pk, pol);
       }
     } else {
 #pragma unroll
@@ -345,6 +360,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
+      const uint64_t keep = policy_evict_last();   // operand tiles are re-read by other tiles
       uint64_t flag_ns = 0;
       uint32_t n_waits = 0;
       bool stop = false;
@@ -390,12 +406,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow);
+          tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
           if constexpr (CL == 1) {
 #pragma unroll
             for (int j = 0; j < C::B_BOXES; ++j)
-              tma_load_2d(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                          w.n0 + j * C::B_BOX_N, kb * C::BK);
+              tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                               w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
           } else {
             // both CTAs of the pair compute the same N-tile: each loads its half of the B slice
             // into the slot of both CTAs (multicast); the slot's barrier in each CTA expects the
@@ -403,8 +419,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 #pragma unroll
             for (int jj = 0; jj < C::B_BOXES / 2; ++jj) {
               const int j = crank * (C::B_BOXES / 2) + jj;
-              tma_load_2d_multicast(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                    w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3));
+              tma_load_2d_multicast_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b,
+                                         fb, w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3),
+                                         keep);
             }
           }
           ++issued;
@@ -482,6 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       // starts at once; the synchronisation that releases a chunk (barrier, fence, counter
       // atomic) is paid once per piece.
       const int ct = threadIdx.x - kCopyWarp0 * 32;
+      const uint64_t stream_pol = policy_evict_first();   // each shard byte is read once
       constexpr int kVec = kCopyRoundBytes / (16 * kCopyThreads);   // 16 vectors per thread
       for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
         const int q = piece / p.ppc;            // chunk position in release order
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 #pragma unroll
           for (int j = 0; j < kVec; ++j) {
             const int b = r0 + (j * kCopyThreads + ct) * 16;
-            if (b < n) v[j] = ld_nc_v4(src + b);
+            if (b < n) v[j] = ld_nc_v4_hint(src + b, stream_pol);
           }
 #pragma unroll
           for (int j = 0; j < kVec; ++j) {
@@ -536,6 +554,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const bool chained = chain && !p.reduce_last;   // running sum handed from element to element
     const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
+    const uint64_t once = policy_evict_first();   // running sums and outputs: touched once per pass
     int local = 0;
     for (int it = cid; it < items; it += ncl, ++local) {
       const Item w = decode_item<OP, CL>(p, it, BN, crank);
@@ -587,7 +606,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         if (read_s) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 s = ld_cg_f4(sp + j * kBM * 4);
+            const float4 s = ld_cg_f4_hint(sp + j * kBM * 4, once);
             v[4 * j + 0] = s.x + v[4 * j + 0];
             v[4 * j + 1] = s.y + v[4 * j + 1];
             v[4 * j + 2] = s.z + v[4 * j + 2];
@@ -597,9 +616,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         if (write_s) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_f4(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), once);
         }
-        if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v);
+        if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             float v[32];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float4 s = ld_cg_f4(p.sbuf + (size_t)w.tile * (kBM * BN) + off + j * kBM * 4);
+              const float4 s = ld_cg_f4_hint(p.sbuf + (size_t)w.tile * (kBM * BN) + off + j * kBM * 4, once);
               v[4 * j + 0] = s.x;
               v[4 * j + 1] = s.y;
               v[4 * j + 2] = s.z;
@@ -644,14 +663,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               const float* sp = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float4 s = ld_cg_f4(sp + j * kBM * 4);
+                const float4 s = ld_cg_f4_hint(sp + j * kBM * 4, once);
                 v[4 * j + 0] = v[4 * j + 0] + s.x;
                 v[4 * j + 1] = v[4 * j + 1] + s.y;
                 v[4 * j + 2] = v[4 * j + 2] + s.z;
                 v[4 * j + 3] = v[4 * j + 3] + s.w;
               }
             }
-            store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v);
+            store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
           }
         }
       }

@@ -190,7 +190,8 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
  * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters,
- * [16] CTAs per cluster (1 or 2), [17..19] reserved (0). */
+ * [16] CTAs per cluster (1 or 2), [17] ReduceScatter raster: N-tiles per group (within a rank the
+ * tiles are taken group by group, M-tiles, then the group's N-tiles), [18..19] reserved (0). */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -219,14 +219,23 @@ def ag_tile_schedule(W: int, M_local: int, N: int, BM: int, BN: int, self_rank: 
     return [(mg, nt) for mg in sorted(range(n_groups), key=key) for nt in range(tiles_n)]
 
 
-def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1):
-    """Order of GEMM+ReduceScatter work items: rank-outer (0..W-1, the reduction order), M-tiles,
-    N-tiles innermost. Item (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1.
-    Returns (rank, m_tile, n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group
-    (see :func:`ag_tile_schedule`)."""
+def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1, group_n=None):
+    """Order of GEMM+ReduceScatter work items: rank-outer (0..W-1, the reduction order); within a
+    rank the N-tiles are taken in groups of ``group_n`` (default: one group of all N-tiles; the last
+    group may be narrower): group by group, M-tiles ascending, the group's N-tiles innermost. Item
+    (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1. Returns (rank, m_tile,
+    n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group (see
+    :func:`ag_tile_schedule`)."""
     tiles_m = (M + BM - 1) // BM
     tiles_n = (N + BN - 1) // BN
-    return [(r, mg, nt) for r in range(W) for mg in range(tiles_m // group) for nt in range(tiles_n)]
+    gn = tiles_n if group_n is None else max(1, min(group_n, tiles_n))
+    out = []
+    for r in range(W):
+        for n0 in range(0, tiles_n, gn):
+            for mg in range(tiles_m // group):
+                for nt in range(n0, min(n0 + gn, tiles_n)):
+                    out.append((r, mg, nt))
+    return out
 
 
 def expected_flags(n: int, epoch: int) -> np.ndarray:

@@ -99,7 +99,7 @@ def test_rs_chain_flags_trace_and_order():
     f = case.ws[plan["off_chain_flags"]:plan["off_chain_flags"] + 4 * n].view(torch.int32).cpu().numpy()
     assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 3))
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(4, 512, 512, 128, plan["BN"])
+    sched = R.rs_item_schedule(4, 512, 512, 128, plan["BN"], group_n=plan["group_n"])
     per = (items + grid - 1) // grid
     for b in range(grid):
         for k, it in enumerate(range(b, items, grid)):
@@ -214,7 +214,7 @@ def test_rs_pairs_parity_trace_and_identity(rm):
     assert_within_tol(case.result(), case.oracle(), "bf16")
     paired = case.result_bits()
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(4, 512, 512, 128, 256, group=2)
+    sched = R.rs_item_schedule(4, 512, 512, 128, 256, group=2, group_n=plan["group_n"])
     per = (items + grid - 1) // grid
     for b in range(grid):
         cid, crank = divmod(b, 2)
@@ -225,3 +225,26 @@ def test_rs_pairs_parity_trace_and_identity(rm):
     tdx.check(single.run())
     status_ok(single)
     assert np.array_equal(single.result_bits(), paired)
+
+
+def test_rs_grouped_raster_trace():
+    # 10 N-tiles of 128: groups of 8 and 2 within each rank
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=2, M=256, K=128, N=1280)
+    inp = wls.make_inputs(wl, integer=True)
+    grid = 6
+    o = opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 2, 256, 128, 1280, tdx.TDX_BF16, o)
+    assert plan["group_n"] == 8 and plan["tiles_n"] == 10
+    items = plan["L"] * plan["T"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    case = RSCase(inp, opts=opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1, trace=trace))
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    tr = trace.cpu().numpy().astype(np.uint32)
+    sched = R.rs_item_schedule(2, 256, 1280, 128, 128, group_n=8)
+    per = (items + grid - 1) // grid
+    for b in range(grid):
+        for k, it in enumerate(range(b, items, grid)):
+            r, mt, nt = sched[it]
+            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)

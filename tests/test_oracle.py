@@ -420,3 +420,11 @@ def test_grouped_schedules():
     assert tiles == sorted(R.ag_tile_schedule(8, 1024, 3584, 128, 256, 3))
     rs = R.rs_item_schedule(8, 8192, 8192, 128, 256, group=2)
     assert len(rs) == 8 * 32 * 32 and rs[1024] == (1, 0, 0)
+
+
+def test_rs_schedule_n_groups():
+    s = R.rs_item_schedule(2, 256, 2560, 128, 256, group_n=4)    # 2 M-tiles, 10 N-tiles: groups 4, 4, 2
+    assert sorted(s) == sorted(R.rs_item_schedule(2, 256, 2560, 128, 256))
+    assert s[:9] == [(0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 0, 3), (0, 1, 0), (0, 1, 1), (0, 1, 2), (0, 1, 3), (0, 0, 4)]
+    assert s[16:20] == [(0, 0, 8), (0, 0, 9), (0, 1, 8), (0, 1, 9)] and s[20] == (1, 0, 0)
+    assert R.rs_item_schedule(3, 512, 512, 128, 256, group_n=8) == R.rs_item_schedule(3, 512, 512, 128, 256)
