@@ -41,6 +41,12 @@
 
 namespace tdx {
 
+// Upper bound of the shared-memory ring depth (the budget below usually binds first); a build may
+// lower it with -DTDX_MAX_STAGES=n to study how latency hiding scales with depth.
+#ifndef TDX_MAX_STAGES
+#define TDX_MAX_STAGES 8
+#endif
+
 template <int BN, bool FP8>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
@@ -54,7 +60,7 @@ struct Cfg {
   static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
