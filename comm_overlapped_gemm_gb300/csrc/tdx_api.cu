@@ -82,7 +82,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     p.M = Mx;
     p.M_local = Mx / W;
   }
-  p.num_kb = (int)((static_cast<long long>(K) * p.elt + 127) / 128);
+  const int kb128 = (int)((static_cast<long long>(K) * p.elt + 127) / 128);   // 128-byte K blocks
   p.tiles_m = (p.M + kBM - 1) / kBM;
   // tile width
   int bn = o.block_n;
@@ -90,7 +90,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   int L = 1;
   if (op == OP_AG) {
     const long long tiles256 = static_cast<long long>(p.tiles_m) * ((N + 255) / 256);
-    const bool small = tiles256 * 2 <= kRefSMs && p.num_kb >= 2;
+    const bool small = tiles256 * 2 <= kRefSMs && kb128 >= 2;
     if (bn == 0) {
       if (small) bn = fp8 ? 128 : 64;
       else bn = N > 128 ? 256 : (N > 64 || fp8 ? 128 : 64);
@@ -101,8 +101,9 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     } else if (small && tiles > 0) {
       L = static_cast<int>(kRefSMs / tiles);
     }
+    const int kb_bn = (int)((static_cast<long long>(K) * p.elt + k_slice_bytes(bn) - 1) / k_slice_bytes(bn));
     if (L > kMaxSplitK) L = kMaxSplitK;
-    if (L > p.num_kb) L = p.num_kb;
+    if (L > kb_bn) L = kb_bn;
     if (L < 1) L = 1;
   } else {
     if (bn == 0) {
@@ -114,6 +115,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   }
   p.BN = bn;
   p.L = L;
+  p.num_kb = (int)((static_cast<long long>(K) * p.elt + k_slice_bytes(bn) - 1) / k_slice_bytes(bn));
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
   p.group_n = op == OP_RS ? (p.tiles_n < kRsGroupN ? (p.tiles_n > 0 ? p.tiles_n : 1) : kRsGroupN) : p.tiles_n;
@@ -179,9 +181,9 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-// 2D map over a row-major (rows x cols) matrix with 128-byte swizzle; box = box_cols x box_rows.
+// 2D map over a row-major (rows x cols) matrix; box = box_cols x box_rows; 128- or 64-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long long cols, int box_cols,
-              int box_rows) {
+              int box_rows, int swizzle_bytes = 128) {
   EncodeTiledFn enc = get_encode();
   if (enc == nullptr) return false;
   const int elt = fp8 ? 1 : 2;
@@ -191,7 +193,8 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long l
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -387,10 +390,12 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
   kp.copy_active = (moving && !ce) ? 1 : 0;
   kp.wait_flags = (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY) ? 1 : 0;
-  const int bbox = fp8 ? 128 : 64;
-  if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, bbox, kBM) ||
-      !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, bbox, kBM) ||
-      !make_map(&kp.tm_b[0], B, fp8, K, N, bbox, bbox))
+  // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
+  const int ks = k_slice_bytes(pl.BN);
+  const int a_box = ks / pl.elt, b_box_n = 128 / pl.elt, b_box_k = ks / pl.elt;
+  if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, a_box, kBM, ks) ||
+      !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, a_box, kBM, ks) ||
+      !make_map(&kp.tm_b[0], B, fp8, K, N, b_box_n, b_box_k))
     return TDX_ERR_CUDA;
   if (o.epoch == 0) {
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
@@ -462,8 +467,9 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   kp.op = OP_RS;
   for (int r = 0; r < W; ++r) {
     kp.out[r] = static_cast<uint8_t*>(out_shards[r]);
-    if (!make_map(&kp.tm_a[r], A_parts[r], false, M, K, 64, kBM) ||
-        !make_map(&kp.tm_b[r], B_parts[r], false, K, N, 64, 64))
+    const int ks = k_slice_bytes(pl.BN);
+    if (!make_map(&kp.tm_a[r], A_parts[r], false, M, K, ks / 2, kBM, ks) ||
+        !make_map(&kp.tm_b[r], B_parts[r], false, K, N, 64, ks / 2))
       return TDX_ERR_CUDA;
   }
   if (o.epoch == 0) {

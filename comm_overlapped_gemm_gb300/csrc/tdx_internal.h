@@ -25,6 +25,9 @@ constexpr int kMaxSplitK = 16;
 constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
+// K bytes per shared-memory ring slot for a tile width (host and device agree on it).
+constexpr int k_slice_bytes(int block_n) { return block_n == 256 ? 64 : 128; }
+
 enum Op { OP_AG = 0, OP_RS = 1 };
 enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };
 enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4 };

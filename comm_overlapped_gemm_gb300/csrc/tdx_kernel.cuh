@@ -44,22 +44,28 @@ namespace tdx {
 // Upper bound of the shared-memory ring depth (the budget below usually binds first); a build may
 // lower it with -DTDX_MAX_STAGES=n to study how latency hiding scales with depth.
 #ifndef TDX_MAX_STAGES
-#define TDX_MAX_STAGES 8
+#define TDX_MAX_STAGES 12
 #endif
 
 template <int BN, bool FP8>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
-  static constexpr int BK = 128 / ELT;            // K elements per ring slot (128 bytes)
+  // K bytes per ring slot: 64 for 256-wide tiles (24 KiB slots, 9 of them: more latency hidden per
+  // byte of shared memory), 128 otherwise. A rows in a slot are KB bytes long (64- or 128-byte
+  // swizzle); B keeps 128-byte MN rows with KB/ELT K rows per box.
+  static constexpr int KB = k_slice_bytes(BN);
+  static constexpr int BK = KB / ELT;             // K elements per ring slot
   static constexpr int UMMA_K = 32 / ELT;         // K per tcgen05.mma (32 bytes)
-  static constexpr int K_STEPS = BK / UMMA_K;     // 4
-  static constexpr int A_BYTES = kBM * 128;       // 16 KiB
+  static constexpr int K_STEPS = BK / UMMA_K;     // 2 or 4
+  static constexpr int A_BYTES = kBM * KB;        // 8 or 16 KiB
+  static constexpr uint32_t A_SBO = 8 * KB;       // next group of 8 rows
+  static constexpr uint32_t A_LAYOUT = KB == 128 ? 2u : 4u;   // descriptor swizzle: 128 B or 64 B
   static constexpr int B_BOX_N = 128 / ELT;       // N elements per B box (128 bytes)
   static constexpr int B_BOXES = BN / B_BOX_N;
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES_RAW = (216 * 1024) / STAGE_BYTES;   // ring budget: 216 KiB
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
   static constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -471,8 +477,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < C::K_STEPS; ++k) {
-            const uint64_t adesc = sw128_desc(a_addr + k * 32, 16, 1024);
-            const uint64_t bdesc = sw128_desc(b_addr + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024);
+            const uint64_t adesc = smem_desc(a_addr + k * 32, 16, C::A_SBO, C::A_LAYOUT);
+            const uint64_t bdesc = smem_desc(b_addr + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024, 2u);
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
             if constexpr (FP8)
               umma_f8(d, adesc, bdesc, C::IDESC, accum);

@@ -267,21 +267,21 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (layout type 2 in bits
-// 61-63), descriptor version 1 (bit 46). Start address, leading-dimension byte offset (LBO) and
-// stride-dimension byte offset (SBO) are stored without their 4 least significant bits.
-//  K-major operand: rows of 128 B (one K slice of 64 bf16 / 128 e4m3), 8-row atoms of 1 KiB;
-//    SBO = 1024 (next 8 rows), LBO unused (1).
-//  MN-major operand: 128 B of MN per K row, 8 K rows per 1 KiB atom; SBO = 1024 (next 8 K rows),
-//    LBO = byte distance between consecutive 128-byte MN blocks.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes,
-                                               uint32_t sbo_bytes) {
+// Shared-memory matrix descriptor for tcgen05.mma: start address, leading-dimension byte offset
+// (LBO) and stride-dimension byte offset (SBO), each stored without its 4 least significant bits,
+// descriptor version 1 (bit 46) and the swizzle layout in bits 61-63 (2 = 128-byte, 4 = 64-byte).
+//  K-major operand with R-byte rows (R = 128 or 64, swizzle R): 8-row atoms of 8*R bytes;
+//    SBO = 8*R (next 8 rows), LBO unused (1).
+//  MN-major operand, 128-byte swizzle: 128 bytes of MN per K row, 8 K rows per 1 KiB atom;
+//    SBO = 1024 (next 8 K rows), LBO = byte distance between consecutive 128-byte MN blocks.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(layout & 0x7u) << 61;
   return d;
 }
 

@@ -185,7 +185,7 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
 
 /* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
  * uses. Writes 20 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
- * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] 128-byte K blocks, [6] chunk rows, [7] chunks per rank,
+ * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] K blocks (64 bytes of K for BN = 256, else 128), [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
