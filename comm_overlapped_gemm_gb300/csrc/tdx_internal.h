@@ -25,8 +25,10 @@ constexpr int kMaxSplitK = 16;
 constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
-// K bytes per shared-memory ring slot for a tile width (host and device agree on it).
-constexpr int k_slice_bytes(int block_n) { return block_n == 256 ? 64 : 128; }
+// K bytes per shared-memory ring slot (host and device agree on it). 128 for every tile width: a
+// 64-byte slice doubles the ring depth in the same shared memory but measured slower on GB300
+// (per-slot barrier/commit overhead and a 64-byte-swizzled A operand cost more than the depth buys).
+constexpr int k_slice_bytes(int /*block_n*/) { return 128; }
 
 enum Op { OP_AG = 0, OP_RS = 1 };
 enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };

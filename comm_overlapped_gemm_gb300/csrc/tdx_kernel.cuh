@@ -46,6 +46,11 @@ namespace tdx {
 #ifndef TDX_MAX_STAGES
 #define TDX_MAX_STAGES 12
 #endif
+// The TMA issuer prefetches into L2 the K slice this many slices ahead of the one it loads (0 = no
+// prefetch), so that slices missing in L2 are on their way before their ring slot frees up.
+#ifndef TDX_PREFETCH_AHEAD
+#define TDX_PREFETCH_AHEAD 0
+#endif
 
 template <int BN, bool FP8>
 struct Cfg {
@@ -415,6 +420,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if (!wait_mbar(p, empty0 + 8 * stage, phase ^ 1u, abort_flag, 100 + stage)) {
             stop = true;
             break;
+          }
+          if constexpr (TDX_PREFETCH_AHEAD > 0) {
+            const int kp = kb + TDX_PREFETCH_AHEAD;
+            if (kp < kb1) {
+              tma_prefetch_2d(map_a, kp * C::BK, arow);
+              if constexpr (CL == 1) {
+#pragma unroll
+                for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_2d(map_b, w.n0 + j * C::B_BOX_N, kp * C::BK);
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < C::B_BOXES / 2; ++jj)
+                  tma_prefetch_2d(map_b, w.n0 + (crank * (C::B_BOXES / 2) + jj) * C::B_BOX_N, kp * C::BK);
+              }
+            }
           }
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);

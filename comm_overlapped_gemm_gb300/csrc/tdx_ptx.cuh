@@ -91,6 +91,13 @@ __device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const C
       : "memory");
 }
 
+// Bring a box into L2 ahead of its load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Multicast form: the box is written at the same shared-memory offset in every CTA of the cluster
 // named in cta_mask, and each destination CTA's barrier at `bar`'s offset receives the bytes.
 __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
