@@ -50,7 +50,8 @@ struct Plan {
   int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
-  int CL = 1;
+  int CL = 1;            // CTAs per cluster (1 or 2)
+  int PM = 0;            // pair mode: 0 single, 1 B multicast, 2 two-SM MMA
   int group_n = 1;
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
@@ -119,15 +120,17 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
   p.group_n = op == OP_RS ? (p.tiles_n < kRsGroupN ? (p.tiles_n > 0 ? p.tiles_n : 1) : kRsGroupN) : p.tiles_n;
-  // pairs of CTAs sharing the B slice: large problems with 256-wide tiles and an even M-tile count
-  if (o.cluster < 0 || o.cluster > 2) return TDX_ERR_INVALID_ARG;
+  // CTA pairs on vertically adjacent 128 x 256 tiles: large problems with 256-wide tiles and an
+  // even M-tile count; by default the 2-SM MMA pair (mode 3), else on request the multicast pair (2)
+  if (o.cluster < 0 || o.cluster > 3) return TDX_ERR_INVALID_ARG;
   const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
-  if (o.cluster == 2) {
+  if (o.cluster >= 2) {
     if (!pair_ok) return TDX_ERR_UNSUPPORTED;
-    p.CL = 2;
+    p.PM = o.cluster - 1;
   } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs) {
-    p.CL = 2;
+    p.PM = 2;
   }
+  p.CL = p.PM == 0 ? 1 : 2;
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
   if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
@@ -253,8 +256,8 @@ tdx_status fill_zero(void* p, size_t bytes, cudaStream_t s) {
 }
 
 tdx_status launch(const Plan& pl, KParams& kp, bool fp8, int grid, cudaStream_t stream) {
-  const cudaError_t e = fp8 ? launch_fused_fp8(pl.op, pl.BN, pl.CL, kp, grid, stream)
-                            : launch_fused_bf16(pl.op, pl.BN, pl.CL, kp, grid, stream);
+  const cudaError_t e = fp8 ? launch_fused_fp8(pl.op, pl.BN, pl.PM, kp, grid, stream)
+                            : launch_fused_bf16(pl.op, pl.BN, pl.PM, kp, grid, stream);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;
@@ -294,7 +297,7 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
 int grid_for(const tdx_opts& o, const Plan& pl, bool fp8, int items_or_zero) {
   int sms = device_sms();
   if (sms <= 0) return 0;
-  int g = fp8 ? fused_max_grid_fp8(pl.op, pl.CL, sms) : fused_max_grid_bf16(pl.op, pl.CL, sms);
+  int g = fp8 ? fused_max_grid_fp8(pl.op, pl.PM, sms) : fused_max_grid_bf16(pl.op, pl.PM, sms);
   if (g <= 0) return 0;
   if (o.num_sms > 0 && o.num_sms < g) g = o.num_sms;
   if (items_or_zero > 0 && items_or_zero < g) g = items_or_zero;
@@ -502,7 +505,7 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.CL, pl.group_n, 0, 0};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, 0, 0};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

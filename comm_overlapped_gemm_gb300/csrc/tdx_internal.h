@@ -79,12 +79,13 @@ struct KParams {
 // Shared-memory footprint of one instantiation (host side, for the launch).
 int fused_smem_bytes(int block_n, bool fp8);
 
-// Launch the persistent fused kernel for (op, block_n, cluster size cl) on `grid` CTAs.
-cudaError_t launch_fused_bf16(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_fused_fp8(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream);
-// Largest grid whose CTAs are resident together (cl = 2: twice the 2-CTA clusters that fit).
-int fused_max_grid_bf16(int op, int cl, int sms);
-int fused_max_grid_fp8(int op, int cl, int sms);
+// Launch the persistent fused kernel for (op, block_n, pair mode pm) on `grid` CTAs. pm: 0 single
+// CTAs, 1 CTA pairs sharing B by multicast, 2 CTA pairs running one 2-SM MMA stream.
+cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
+// Largest grid whose CTAs are resident together (pairs: twice the 2-CTA clusters that fit).
+int fused_max_grid_bf16(int op, int pm, int sms);
+int fused_max_grid_fp8(int op, int pm, int sms);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
 }  // namespace tdx

@@ -52,12 +52,14 @@ namespace tdx {
 #define TDX_PREFETCH_AHEAD 0
 #endif
 
-template <int BN, bool FP8>
+// PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
+// 256 x BN tile with one instruction stream issued by the leader; each CTA stages its own 128 rows
+// of A and its half (BN/2 columns) of the B slice, and holds its 128 x BN accumulator in TMEM.
+template <int BN, bool FP8, bool PAIR_MMA = false>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
-  // K bytes per ring slot: 64 for 256-wide tiles (24 KiB slots, 9 of them: more latency hidden per
-  // byte of shared memory), 128 otherwise. A rows in a slot are KB bytes long (64- or 128-byte
-  // swizzle); B keeps 128-byte MN rows with KB/ELT K rows per box.
+  // K bytes per ring slot (k_slice_bytes): A rows in a slot are KB bytes long; B keeps 128-byte MN
+  // rows with KB/ELT K rows per box.
   static constexpr int KB = k_slice_bytes(BN);
   static constexpr int BK = KB / ELT;             // K elements per ring slot
   static constexpr int UMMA_K = 32 / ELT;         // K per tcgen05.mma (32 bytes)
@@ -66,9 +68,10 @@ struct Cfg {
   static constexpr uint32_t A_SBO = 8 * KB;       // next group of 8 rows
   static constexpr uint32_t A_LAYOUT = KB == 128 ? 2u : 4u;   // descriptor swizzle: 128 B or 64 B
   static constexpr int B_BOX_N = 128 / ELT;       // N elements per B box (128 bytes)
-  static constexpr int B_BOXES = BN / B_BOX_N;
+  static constexpr int B_BOXES = BN / B_BOX_N;              // boxes across the tile width
+  static constexpr int B_BOXES_CTA = PAIR_MMA ? B_BOXES / 2 : B_BOXES;   // boxes this CTA stages
   static constexpr int B_BOX_BYTES = BK * 128;
-  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int B_BYTES = B_BOXES_CTA * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (216 * 1024) / STAGE_BYTES;   // ring budget: 216 KiB
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
@@ -80,10 +83,12 @@ struct Cfg {
   // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B type (bits 7-9, 10-12: bf16 = 1,
   // e4m3 = 0), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 (bits 17-22),
   // M >> 4 (bits 24-28).
+  static constexpr int MMA_M = PAIR_MMA ? 2 * kBM : kBM;
   static constexpr uint32_t IDESC = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
                                     (1u << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                                    (static_cast<uint32_t>(kBM >> 4) << 24);
+                                    (static_cast<uint32_t>(MMA_M >> 4) << 24);
   static_assert(BN % B_BOX_N == 0 && B_BOXES >= 1, "tile width must cover whole 128-byte boxes");
+  static_assert(!PAIR_MMA || B_BOXES % 2 == 0, "a 2-SM pair splits B into two halves");
   static_assert(CHUNKS >= 1, "at least one 32-column chunk per epilogue warp");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -293,10 +298,13 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
   }
 }
 
-template <int BN, bool FP8, int OP, int CL>
+// PM (pair mode): 0 = single CTAs; 1 = CTA pairs sharing the B slice by TMA multicast, each CTA
+// running its own 128-row MMA; 2 = CTA pairs running one 2-SM (cta_group::2) MMA stream.
+template <int BN, bool FP8, int OP, int PM>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
-  static_assert(CL == 1 || (CL == 2 && Cfg<BN, FP8>::B_BOXES % 2 == 0), "pairs split B into two halves");
-  using C = Cfg<BN, FP8>;
+  constexpr int CL = PM == 0 ? 1 : 2;      // CTAs per cluster
+  static_assert(PM == 0 || Cfg<BN, FP8>::B_BOXES % 2 == 0, "pairs split B into two halves");
+  using C = Cfg<BN, FP8, PM == 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -320,11 +328,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CL);   // a slot is free once every CTA of the cluster consumed it
+      mbar_init(empty0 + 8 * s, PM == 1 ? 2 : 1);   // PM 1: freed once both CTAs' MMAs used it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, PM == 2 ? 2 : 1);   // PM 2: both CTAs' epilogues free the leader's
     }
     mbar_init(drain_bar, 1);
     misc[1] = 0;
@@ -335,8 +343,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&misc[0]), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PM == 2) {
+      tmem_alloc_pair(smem_u32(&misc[0]), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&misc[0]), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (threadIdx.x == kTmaWarp * 32) {
     for (int i = 0; i < (OP == OP_AG ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
@@ -350,6 +363,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = crank == 0;           // PM 2: the CTA that issues the pair's MMAs
   const int cid = blockIdx.x / CL;          // cluster index
   const int ncl = gridDim.x / CL;           // clusters in the grid
 
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             stop = true;
             break;
           }
-          if constexpr (TDX_PREFETCH_AHEAD > 0) {
+          if constexpr (TDX_PREFETCH_AHEAD > 0 && PM != 2) {
             const int kp = kb + TDX_PREFETCH_AHEAD;
             if (kp < kb1) {
               tma_prefetch_2d(map_a, kp * C::BK, arow);
@@ -436,23 +450,34 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
           const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
-          if constexpr (CL == 1) {
+          if constexpr (PM == 2) {
+            // both CTAs' slices count on the leader's slot barrier, armed once for the pair
+            if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+            const uint32_t fbl = mapa_shared(fb, 0);
+            tma_load_2d_pair_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fbl, kb * C::BK, arow, keep);
 #pragma unroll
-            for (int j = 0; j < C::B_BOXES; ++j)
-              tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                               w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
+            for (int jj = 0; jj < C::B_BOXES_CTA; ++jj)
+              tma_load_2d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
+                                    w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep);
           } else {
-            // both CTAs of the pair compute the same N-tile: each loads its half of the B slice
-            // into the slot of both CTAs (multicast); the slot's barrier in each CTA expects the
-            // whole stage (own A + both halves of B)
-#pragma unroll
-            for (int jj = 0; jj < C::B_BOXES / 2; ++jj) {
-              const int j = crank * (C::B_BOXES / 2) + jj;
-              tma_load_2d_multicast_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b,
-                                         fb, w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3),
-                                         keep);
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
+            if constexpr (CL == 1) {
+  #pragma unroll
+              for (int j = 0; j < C::B_BOXES; ++j)
+                tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
+            } else {
+              // both CTAs of the pair compute the same N-tile: each loads its half of the B slice
+              // into the slot of both CTAs (multicast); the slot's barrier in each CTA expects the
+              // whole stage (own A + both halves of B)
+  #pragma unroll
+              for (int jj = 0; jj < C::B_BOXES / 2; ++jj) {
+                const int j = crank * (C::B_BOXES / 2) + jj;
+                tma_load_2d_multicast_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b,
+                                           fb, w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3),
+                                           keep);
+              }
             }
           }
           ++issued;
@@ -471,7 +496,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   } else if (warp == kMmaWarp) {
     // =============================================================== MMA issuer
-    if (lane == 0 && use_mma) {
+    if (lane == 0 && use_mma && (PM != 2 || leader)) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t consumed = 0;
@@ -499,15 +524,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             const uint64_t adesc = smem_desc(a_addr + k * 32, 16, C::A_SBO, C::A_LAYOUT);
             const uint64_t bdesc = smem_desc(b_addr + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024, 2u);
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-            if constexpr (FP8)
+            if constexpr (PM == 2) {
+              if constexpr (FP8)
+                umma_f8_pair(d, adesc, bdesc, C::IDESC, accum);
+              else
+                umma_bf16_pair(d, adesc, bdesc, C::IDESC, accum);
+            } else if constexpr (FP8) {
               umma_f8(d, adesc, bdesc, C::IDESC, accum);
-            else
+            } else {
               umma_bf16(d, adesc, bdesc, C::IDESC, accum);
+            }
           }
-          if constexpr (CL == 1)
+          if constexpr (PM == 0)
             tc_commit(empty0 + 8 * stage);
-          else
+          else if constexpr (PM == 1)
             tc_commit_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));   // free it in both CTAs
+          else
+            tc_commit_pair_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));
           ++consumed;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -515,10 +548,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
         if (stop) break;
-        tc_commit(tfull0 + 8 * acc);
+        if constexpr (PM == 2)
+          tc_commit_pair_multicast(tfull0 + 8 * acc, static_cast<uint16_t>(0x3));   // both halves ready
+        else
+          tc_commit(tfull0 + 8 * acc);
       }
       // every MMA issued by this thread has completed once the drain barrier flips
-      tc_commit(drain_bar);
+      if constexpr (PM == 2)
+        tc_commit_pair(drain_bar);
+      else
+        tc_commit(drain_bar);
       wait_mbar_drain(p, drain_bar, 0);
       misc[3] = consumed;
     }
@@ -654,7 +693,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
       if (elected) {
-        if (use_mma) mbar_arrive(tempty0 + 8 * acc);
+        if (use_mma) {
+          if constexpr (PM == 2) {
+            if (leader)
+              mbar_arrive(tempty0 + 8 * acc);
+            else
+              mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));   // free the leader's accumulator
+          } else {
+            mbar_arrive(tempty0 + 8 * acc);
+          }
+        }
         if (chained && write_s) {
           __threadfence();
           st_release_gpu(p.chain_flags + (size_t)w.c * p.T + w.tile, p.epoch);
@@ -715,7 +763,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 
   // =============================================================== teardown
   __syncthreads();
-  if (threadIdx.x == kTmaWarp * 32 && use_mma) {
+  if (PM == 2 && !leader && threadIdx.x == kTmaWarp * 32 && use_mma &&
+      (*abort_flag || ld_relaxed_gpu(p.status) != 0u)) {
+    // abort path of a pair's second CTA: its loads are counted on the leader's barriers, which this
+    // CTA cannot observe; give any load still in flight ample time to land before leaving
+    for (int i = 0; i < 64; ++i) __nanosleep(1000);
+  }
+  if (threadIdx.x == kTmaWarp * 32 && use_mma && (PM != 2 || leader)) {
     // loads issued but never consumed by the MMA issuer (abort path) must land before exit
     const uint32_t issued = misc[2];
     const uint32_t consumed = misc[3];
@@ -731,20 +785,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PM == 2)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <int BN, bool FP8, int OP, int CL>
+template <int BN, bool FP8, int OP, int PM>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, FP8>;
+  using C = Cfg<BN, FP8, PM == 2>;
+  constexpr int CL = PM == 0 ? 1 : 2;
   // the dynamic shared-memory limit is raised once per device for each instantiation
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -768,22 +826,23 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP, CL>, p);
+  return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP, PM>, p);
 }
 
 // Largest grid whose CTAs are all resident at once: one CTA per SM, or for pairs twice the number
 // of 2-CTA clusters the device can hold simultaneously.
-template <int BN, bool FP8, int OP, int CL>
+template <int BN, bool FP8, int OP, int PM>
 int max_grid_t(int sms) {
+  constexpr int CL = PM == 0 ? 1 : 2;
   if constexpr (CL == 1) {
     return sms;
   } else {
-    using C = Cfg<BN, FP8>;
+    using C = Cfg<BN, FP8, PM == 2>;
     static int cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
-    if (cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg = {};
@@ -798,7 +857,7 @@ int max_grid_t(int sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tdx_fused_kernel<BN, FP8, OP, CL>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tdx_fused_kernel<BN, FP8, OP, PM>, &cfg) != cudaSuccess) return 0;
     const int g = n * CL;
     if (dev >= 0 && dev < 64) cache[dev] = g;
     return g;

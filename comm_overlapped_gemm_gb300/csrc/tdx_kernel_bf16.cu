@@ -3,30 +3,34 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_bf16(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream) {
-  if (cl == 2) {
+cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
+  if (pm != 0) {
     if (block_n != 256) return cudaErrorInvalidValue;
+    if (pm == 1)
+      return op == OP_AG ? launch_fused_t<256, false, OP_AG, 1>(p, grid, stream)
+                         : launch_fused_t<256, false, OP_RS, 1>(p, grid, stream);
     return op == OP_AG ? launch_fused_t<256, false, OP_AG, 2>(p, grid, stream)
                        : launch_fused_t<256, false, OP_RS, 2>(p, grid, stream);
   }
   if (op == OP_AG) {
     switch (block_n) {
-      case 64: return launch_fused_t<64, false, OP_AG, 1>(p, grid, stream);
-      case 128: return launch_fused_t<128, false, OP_AG, 1>(p, grid, stream);
-      case 256: return launch_fused_t<256, false, OP_AG, 1>(p, grid, stream);
+      case 64: return launch_fused_t<64, false, OP_AG, 0>(p, grid, stream);
+      case 128: return launch_fused_t<128, false, OP_AG, 0>(p, grid, stream);
+      case 256: return launch_fused_t<256, false, OP_AG, 0>(p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (block_n) {
-    case 64: return launch_fused_t<64, false, OP_RS, 1>(p, grid, stream);
-    case 128: return launch_fused_t<128, false, OP_RS, 1>(p, grid, stream);
-    case 256: return launch_fused_t<256, false, OP_RS, 1>(p, grid, stream);
+    case 64: return launch_fused_t<64, false, OP_RS, 0>(p, grid, stream);
+    case 128: return launch_fused_t<128, false, OP_RS, 0>(p, grid, stream);
+    case 256: return launch_fused_t<256, false, OP_RS, 0>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int fused_max_grid_bf16(int op, int cl, int sms) {
-  if (cl != 2) return sms;
+int fused_max_grid_bf16(int op, int pm, int sms) {
+  if (pm == 0) return sms;
+  if (pm == 1) return op == OP_AG ? max_grid_t<256, false, OP_AG, 1>(sms) : max_grid_t<256, false, OP_RS, 1>(sms);
   return op == OP_AG ? max_grid_t<256, false, OP_AG, 2>(sms) : max_grid_t<256, false, OP_RS, 2>(sms);
 }
 
@@ -50,7 +54,7 @@ cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int fused_smem_bytes(int block_n, bool fp8) {
+int fused_smem_bytes(int block_n, bool fp8) {   // single-CTA configurations
   if (fp8) {
     switch (block_n) {
       case 128: return Cfg<128, true>::SMEM_BYTES;

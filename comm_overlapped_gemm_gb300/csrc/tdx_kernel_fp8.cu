@@ -4,22 +4,23 @@
 
 namespace tdx {
 
-cudaError_t launch_fused_fp8(int op, int block_n, int cl, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
   if (op != OP_AG) return cudaErrorInvalidValue;
-  if (cl == 2) {
+  if (pm != 0) {
     if (block_n != 256) return cudaErrorInvalidValue;
-    return launch_fused_t<256, true, OP_AG, 2>(p, grid, stream);
+    return pm == 1 ? launch_fused_t<256, true, OP_AG, 1>(p, grid, stream)
+                   : launch_fused_t<256, true, OP_AG, 2>(p, grid, stream);
   }
   switch (block_n) {
-    case 128: return launch_fused_t<128, true, OP_AG, 1>(p, grid, stream);
-    case 256: return launch_fused_t<256, true, OP_AG, 1>(p, grid, stream);
+    case 128: return launch_fused_t<128, true, OP_AG, 0>(p, grid, stream);
+    case 256: return launch_fused_t<256, true, OP_AG, 0>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int fused_max_grid_fp8(int op, int cl, int sms) {
-  if (cl != 2 || op != OP_AG) return sms;
-  return max_grid_t<256, true, OP_AG, 2>(sms);
+int fused_max_grid_fp8(int op, int pm, int sms) {
+  if (pm == 0 || op != OP_AG) return sms;
+  return pm == 1 ? max_grid_t<256, true, OP_AG, 1>(sms) : max_grid_t<256, true, OP_AG, 2>(sms);
 }
 
 }  // namespace tdx

@@ -90,10 +90,12 @@ typedef struct tdx_opts {
                                 elements 0..c-1 and hands it on), 2 = slotted (each element stores its
                                 partial; the last to arrive folds them in order 0..L-1). Both give
                                 the same bits. */
-  int cluster;               /* CTAs per cluster for the GEMM: 0 = library choice, 1 = single CTAs,
-                                2 = pairs of CTAs on vertically adjacent 128 x 256 tiles that share
-                                the B slice (each loads half of it into both CTAs' shared memory).
-                                2 needs tile width 256 and an even number of 128-row M-tiles. */
+  int cluster;               /* how CTAs cooperate on the GEMM: 0 = library choice, 1 = single CTAs,
+                                2 = pairs of CTAs on vertically adjacent 128 x 256 tiles sharing the B
+                                slice (each loads half of it into both CTAs' shared memory),
+                                3 = pairs running one 2-SM MMA stream on a 256 x 256 tile (each CTA
+                                stages its 128 rows of A and half of B). 2 and 3 need tile width 256
+                                and an even number of 128-row M-tiles. */
 } tdx_opts;
 
 /* Fill *opts with the defaults above. Returns TDX_ERR_INVALID_ARG if opts is NULL. */
@@ -190,7 +192,7 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
  * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters,
- * [16] CTAs per cluster (1 or 2), [17] ReduceScatter raster: N-tiles per group (within a rank the
+ * [16] CTA cooperation in use (1 single, 2 multicast pair, 3 2-SM pair), [17] ReduceScatter raster: N-tiles per group (within a rank the
  * tiles are taken group by group, M-tiles, then the group's N-tiles), [18..19] reserved (0). */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);

@@ -125,6 +125,8 @@ def test_ag_validation_codes(tdx):
     assert _ag(tdx, opts=tdx.make_opts(out_dtype=1)) == tdx.TDX_ERR_INVALID_ARG
     assert _ag(tdx, opts=tdx.make_opts(mode=9)) == tdx.TDX_ERR_INVALID_ARG
     assert _ag(tdx, opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
+    assert _ag(tdx, opts=tdx.make_opts(cluster=4)) == tdx.TDX_ERR_INVALID_ARG
+    assert _ag(tdx, opts=tdx.make_opts(cluster=3, block_n=128)) == tdx.TDX_ERR_UNSUPPORTED
     assert _ag(tdx, dtype=1, opts=tdx.make_opts(block_n=64)) == tdx.TDX_ERR_UNSUPPORTED
     # empty problems launch nothing and succeed
     assert _ag(tdx, M_local=0) == tdx.TDX_OK

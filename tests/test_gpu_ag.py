@@ -277,17 +277,18 @@ def test_ag_split_k_chained_and_slotted_identical():
     assert np.array_equal(bits[0], bits[1])
 
 
+@pytest.mark.parametrize("cluster", [2, 3])
 @pytest.mark.parametrize("self_rank", [0, 5])
-def test_ag_pairs_parity_and_trace(self_rank):
+def test_ag_pairs_parity_and_trace(self_rank, cluster):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=1024, N=768, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
     grid = 16
-    o = opts(self_rank=self_rank, num_sms=grid, cluster=2, block_n=256)
+    o = opts(self_rank=self_rank, num_sms=grid, cluster=cluster, block_n=256)
     plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 1024, 768, tdx.TDX_BF16, o)
-    assert plan["cluster"] == 2 and plan["BN"] == 256
+    assert plan["cluster"] == cluster and plan["BN"] == 256
     items = plan["L"] * plan["T"]
     trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=2, block_n=256, trace=trace))
+    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=cluster, block_n=256, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
@@ -310,7 +311,7 @@ def test_ag_pairs_and_singles_give_identical_bits(name):
     wl = wls.with_shape(wls.WORKLOADS[name], W=4, M=256, K=1024, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=False)
     bits = []
-    for cl in (1, 2):
+    for cl in (1, 2, 3):
         kw = dict(cluster=cl, block_n=256)
         if wl.dtype == "e4m3":
             kw.update(scale_a=inp.scale_a, scale_b=inp.scale_b[0])
@@ -320,16 +321,19 @@ def test_ag_pairs_and_singles_give_identical_bits(name):
         bits.append(case.result_bits())
         assert_within_tol(case.result(), case.oracle(), wl.dtype)
     assert np.array_equal(bits[0], bits[1])
+    assert np.array_equal(bits[0], bits[2])
 
 
-def test_ag_pairs_timeout_recovers():
+@pytest.mark.parametrize("cluster", [2, 3])
+def test_ag_pairs_timeout_recovers(cluster):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=256, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
-    case = AGCase(inp, opts=opts(cluster=2, block_n=256))
-    tdx.check(case.run(tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY, timeout_ns=2_000_000, cluster=2, block_n=256)))
+    case = AGCase(inp, opts=opts(cluster=cluster, block_n=256))
+    tdx.check(case.run(tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY, timeout_ns=2_000_000, cluster=cluster,
+                                     block_n=256)))
     st, detail = tdx.tdx_read_device_status(case.ws)
     assert st == tdx.TDX_ERR_TIMEOUT and detail[1] == 1
     tdx.check(tdx.tdx_workspace_init(case.ws))
-    tdx.check(case.run(opts(cluster=2, block_n=256)))
+    tdx.check(case.run(opts(cluster=cluster, block_n=256)))
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")

@@ -198,17 +198,18 @@ def test_rs_full_size_slotted_matches_chained():
     assert np.array_equal(bits[0], bits[1])
 
 
+@pytest.mark.parametrize("cluster", [2, 3])
 @pytest.mark.parametrize("rm", [1, 2])
-def test_rs_pairs_parity_trace_and_identity(rm):
+def test_rs_pairs_parity_trace_and_identity(rm, cluster):
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=512, N=512)
     inp = wls.make_inputs(wl, integer=False)
     grid = 8
-    o = opts(num_sms=grid, cluster=2, block_n=256, reduce_mode=rm)
+    o = opts(num_sms=grid, cluster=cluster, block_n=256, reduce_mode=rm)
     plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 512, 512, tdx.TDX_BF16, o)
-    assert plan["cluster"] == 2
+    assert plan["cluster"] == cluster
     items = plan["L"] * plan["T"]
     trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    case = RSCase(inp, opts=opts(num_sms=grid, cluster=2, block_n=256, reduce_mode=rm, trace=trace))
+    case = RSCase(inp, opts=opts(num_sms=grid, cluster=cluster, block_n=256, reduce_mode=rm, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_within_tol(case.result(), case.oracle(), "bf16")
