@@ -49,6 +49,30 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources of the library (identifies the kernel an ncu capture measured)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "comm_overlapped_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def kernel_traffic():
+    """DRAM bytes (read + written) per GEMM-RS W=8 launch from the committed ncu summary, or None
+    when the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "tdx_fused_rs_w8_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 def reduce_max(x: float, world: int, device=None) -> float:
     """Maximum of x over all ranks (the job's time is its slowest rank's); identity at world 1."""
     if world <= 1:
@@ -488,11 +512,7 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     peak_tf = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK["bf16_tflops_sustained"])))
     achieved = fl_rs / (ms_rs * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("rs_w8_fused_bytes_per_launch")
+    traffic = kernel_traffic()
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -567,9 +587,13 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the extra configurations")
     ap.add_argument("--case", choices=["ag", "rs"], default=None)
     ap.add_argument("--shape", default="8,1024,8192,3584")
+    ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.case is None:
         ap.error("--warmup must be >= 3")
+    if args.source_hash:
+        print(kernel_source_hash())
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     if args.case is not None:
