@@ -234,7 +234,7 @@ class Step:
 
     def ag(self, mode=0, producer=0):
         self.epoch += 1
-        o = self.tdx.make_opts(epoch=self.epoch, mode=mode, producer=producer)
+        o = self.tdx.make_opts(epoch=self.epoch, mode=mode, producer=producer, chunk_rows=self.wa.chunk_rows)
         wa = self.wa
         return self.tdx.tdx_ag_gemm(self.shards, self.B, self.C, self.ws_ag, wa.W, wa.M, wa.K, wa.N,
                                     self.tdx.TDX_BF16, o)
@@ -479,19 +479,35 @@ def run_gpu(args):
     h2d = sum(t.numel() * 2 for t in h_shards + [h_B] + h_A + h_Bs)
     d2h = h_C.numel() * 2 + sum(o.numel() * 2 for o in h_out)
 
+    copy_stream = torch.cuda.Stream(device=dev)
+    rs_done = torch.cuda.Event()
+    rs_done.record(stream)
+
     def e2e_step():
+        # AllGather inputs on the compute stream; ReduceScatter inputs on a copy stream while the
+        # AllGather kernel runs (after the previous step's ReduceScatter finished reading them);
+        # C goes back on the copy stream while the ReduceScatter kernel runs.
         for d, h in zip(st.shards, h_shards):
-            d.copy_(h.view(torch.int16), non_blocking=True)
+            d.copy_(h, non_blocking=True)
         st.B.copy_(h_B, non_blocking=True)
-        for d, h in zip(st.A, h_A):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(st.Bs, h_Bs):
-            d.copy_(h, non_blocking=True)
+        copy_stream.wait_event(rs_done)
+        with torch.cuda.stream(copy_stream):
+            for d, h in zip(st.A, h_A):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(st.Bs, h_Bs):
+                d.copy_(h, non_blocking=True)
+        rs_in = copy_stream.record_event()
         tdx.check(st.ag())
+        ag_done = stream.record_event()
+        stream.wait_event(rs_in)
         tdx.check(st.rs())
-        h_C.copy_(st.C, non_blocking=True)
+        rs_done.record(stream)
+        copy_stream.wait_event(ag_done)
+        with torch.cuda.stream(copy_stream):
+            h_C.copy_(st.C, non_blocking=True)
         for h, d in zip(h_out, st.out):
             h.copy_(d, non_blocking=True)
+        stream.wait_stream(copy_stream)
 
     e2e_steps = max(3, min(args.steps, 20))
     e2e_step()
@@ -562,7 +578,7 @@ def run_case(args):
     W, M, K, N = (int(x) for x in args.shape.split(","))
     dev = torch.device("cuda", 0)
     name = "ag_w8" if args.case == "ag" else "rs_w8"
-    inp = wls.make_inputs(wls.with_shape(wls.WORKLOADS[name], W=W, M=M, K=K, N=N))
+    inp = wls.make_inputs(wls.with_shape(wls.WORKLOADS[name], W=W, M=M, K=K, N=N, chunk_rows=min(128, M)))
     ai = inp if args.case == "ag" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["ag_w8"], W=1, M=128, K=64, N=64))
     ri = inp if args.case == "rs" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["rs_w8"], W=1, M=128, K=64, N=64))
     st = Step(tdx, torch, ai, ri, dev)
