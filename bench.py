@@ -232,16 +232,19 @@ class Step:
         tdx.check(tdx.tdx_workspace_init(self.ws_rs))
         self.epoch = 0
 
-    def ag(self, mode=0, producer=0):
+    extra: dict = {}
+
+    def ag(self, mode=0, producer=0, epoch=None):
         self.epoch += 1
-        o = self.tdx.make_opts(epoch=self.epoch, mode=mode, producer=producer, chunk_rows=self.wa.chunk_rows)
+        o = self.tdx.make_opts(epoch=self.epoch if epoch is None else epoch, mode=mode, producer=producer,
+                               chunk_rows=self.wa.chunk_rows, **self.extra)
         wa = self.wa
         return self.tdx.tdx_ag_gemm(self.shards, self.B, self.C, self.ws_ag, wa.W, wa.M, wa.K, wa.N,
                                     self.tdx.TDX_BF16, o)
 
-    def rs(self, mode=0):
+    def rs(self, mode=0, epoch=None):
         self.epoch += 1
-        o = self.tdx.make_opts(epoch=self.epoch, mode=mode)
+        o = self.tdx.make_opts(epoch=self.epoch if epoch is None else epoch, mode=mode, **self.extra)
         wr = self.wr
         return self.tdx.tdx_gemm_rs(self.A, self.Bs, self.out, self.ws_rs, wr.W, wr.M, wr.K, wr.N,
                                     self.tdx.TDX_BF16, o)
@@ -582,6 +585,11 @@ def run_case(args):
     ai = inp if args.case == "ag" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["ag_w8"], W=1, M=128, K=64, N=64))
     ri = inp if args.case == "rs" else wls.make_inputs(wls.with_shape(wls.WORKLOADS["rs_w8"], W=1, M=128, K=64, N=64))
     st = Step(tdx, torch, ai, ri, dev)
+    extra = {}
+    for kv in filter(None, args.opts.split(",")):
+        k, v = kv.split("=")
+        extra[k] = int(v)
+    st.extra = extra
     fn = st.ag if args.case == "ag" else st.rs
     for _ in range(args.warmup + args.steps):
         tdx.check(fn())
@@ -589,7 +597,12 @@ def run_case(args):
     st.status()
     ms = time_mode(torch, lambda: tdx.check(fn()), 5)
     fl = inp.wl.flops
-    print(json.dumps({"case": args.case, "shape": [W, M, K, N], "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}))
+    gus = graph_time_us(torch, lambda: fn(epoch=0))
+    plan = tdx.tdx_plan_info(tdx.OP_AG if args.case == "ag" else tdx.OP_RS, W, M, K, N, tdx.TDX_BF16,
+                             tdx.make_opts(chunk_rows=min(128, M), **extra) if args.case == "ag" else tdx.make_opts(**extra))
+    print(json.dumps({"case": args.case, "shape": [W, M, K, N], "opts": extra, "ms": ms, "us_gpu_graph": gus,
+                      "tflops": fl / (ms * 1e-3) / 1e12,
+                      "plan": {k: plan[k] for k in ("BN", "L", "T", "reduce_mode", "cluster")}}))
     return 0
 
 
@@ -603,6 +616,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the extra configurations")
     ap.add_argument("--case", choices=["ag", "rs"], default=None)
     ap.add_argument("--shape", default="8,1024,8192,3584")
+    ap.add_argument("--opts", default="", help="--case only: tdx_opts fields, e.g. block_n=256,split_k=4")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.case is None:
