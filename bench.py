@@ -224,13 +224,22 @@ class Step:
         self.A = [d(a) for a in rs_inp.a]
         self.Bs = [d(b) for b in rs_inp.b]
         self.out = [t.empty((wr.M // wr.W, wr.N), dtype=t.bfloat16, device=dev) for _ in range(wr.W)]
-        self.ws_ag = t.empty(tdx.tdx_workspace_size(tdx.OP_AG, wa.W, wa.M, wa.K, wa.N, tdx.TDX_BF16),
+        self.ws_ag = t.empty(1, dtype=t.uint8, device=dev)
+        self.ws_rs = t.empty(1, dtype=t.uint8, device=dev)
+        self.size_workspaces({})
+        self.epoch = 0
+
+    def size_workspaces(self, extra):
+        """(Re)allocate the two workspaces for the tiling options in `extra`."""
+        tdx, t, wa, wr = self.tdx, self.torch, self.wa, self.wr
+        dev = self.ws_ag.device
+        self.ws_ag = t.empty(tdx.tdx_workspace_size(tdx.OP_AG, wa.W, wa.M, wa.K, wa.N, tdx.TDX_BF16,
+                                                    tdx.make_opts(chunk_rows=wa.chunk_rows, **extra)),
                              dtype=t.uint8, device=dev)
-        self.ws_rs = t.empty(tdx.tdx_workspace_size(tdx.OP_RS, wr.W, wr.M, wr.K, wr.N, tdx.TDX_BF16),
-                             dtype=t.uint8, device=dev)
+        self.ws_rs = t.empty(tdx.tdx_workspace_size(tdx.OP_RS, wr.W, wr.M, wr.K, wr.N, tdx.TDX_BF16,
+                                                    tdx.make_opts(**extra)), dtype=t.uint8, device=dev)
         tdx.check(tdx.tdx_workspace_init(self.ws_ag))
         tdx.check(tdx.tdx_workspace_init(self.ws_rs))
-        self.epoch = 0
 
     extra: dict = {}
 
@@ -590,6 +599,7 @@ def run_case(args):
         k, v = kv.split("=")
         extra[k] = int(v)
     st.extra = extra
+    st.size_workspaces(extra)
     fn = st.ag if args.case == "ag" else st.rs
     for _ in range(args.warmup + args.steps):
         tdx.check(fn())

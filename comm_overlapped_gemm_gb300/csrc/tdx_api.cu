@@ -53,6 +53,7 @@ struct Plan {
   int CL = 1;            // CTAs per cluster (1 or 2)
   int PM = 0;            // pair mode: 0 single, 1 B multicast, 2 two-SM MMA
   int group_n = 1;
+  int rank_block = 1;    // RS: positions (in tile groups) per rank block
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
 };
@@ -131,6 +132,10 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     p.PM = 2;
   }
   p.CL = p.PM == 0 ? 1 : 2;
+  {
+    const int tg = (p.tiles_m / p.CL) * p.tiles_n;
+    p.rank_block = op == OP_RS ? (tg < kRefSMs ? (tg > 0 ? tg : 1) : kRefSMs) : (tg > 0 ? tg : 1);
+  }
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
   if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
@@ -275,6 +280,7 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.tiles_n = pl.tiles_n;
   kp.T = pl.T;
   kp.group_n = pl.group_n;
+  kp.rank_block = pl.rank_block;
   kp.L = pl.L;
   kp.num_kb = pl.num_kb;
   kp.status = reinterpret_cast<uint32_t*>(ws);
@@ -505,7 +511,7 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, 0, 0};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, 0};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

@@ -61,6 +61,7 @@ struct KParams {
   int chunk_rows, n_chunks;      // AG chunking (per rank)
   int tiles_m, tiles_n, T;       // T = tiles_m * tiles_n
   int group_n;                   // RS raster: N-tiles per group (1..tiles_n)
+  int rank_block;                // RS order: positions per rank block (1..tiles per rank in groups)
   int L;                         // chain length: RS = W ranks, AG = split-K factor
   int num_kb;                    // K blocks of 128 bytes
   int out_fp32;

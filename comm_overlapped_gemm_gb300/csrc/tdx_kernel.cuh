@@ -109,8 +109,29 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, in
   Item r;
   const int tiles_g = p.tiles_m / CL;
   const int Tg = tiles_g * p.tiles_n;
-  r.c = it / Tg;
-  const int pos = it - r.c * Tg;
+  int pos;
+  if constexpr (OP == OP_AG) {
+    r.c = it / Tg;
+    pos = it - r.c * Tg;
+  } else {
+    // ReduceScatter, rank-blocked: positions of a rank's tile order are taken in blocks of
+    // rank_block; a block is done for ranks 0..L-1 before the next block starts, so the running sum
+    // of a tile is handed to the next rank about one block (two waves) later, while it is in L2
+    const int P = p.rank_block;
+    const int nfull = Tg / P;
+    const int full_items = nfull * p.L * P;
+    if (it < full_items) {
+      const int b = it / (p.L * P);
+      const int rem = it - b * p.L * P;
+      r.c = rem / P;
+      pos = b * P + (rem - r.c * P);
+    } else {
+      const int Pl = Tg - nfull * P;
+      const int rem = it - full_items;
+      r.c = rem / Pl;
+      pos = nfull * P + (rem - r.c * Pl);
+    }
+  }
   int mg, nt;
   if constexpr (OP == OP_AG) {
     int start = (p.self_rank * p.M_local + CL * kBM - 1) / (CL * kBM);
@@ -692,6 +713,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
+      if (chained && read_s && w.c == p.L - 1) {
+        // the running sum of this tile is dead after the last element read it: drop it from L2
+        const int et = threadIdx.x - kEpiWarp0 * 32;
+        for (int l = et; l < 4 * BN; l += kEpiThreads) discard_l2_line(sb + (size_t)l * 32);
+      }
       if (elected) {
         if (use_mma) {
           if constexpr (PM == 2) {
@@ -751,6 +777,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
             store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
           }
+          // every slot of this tile is dead now: drop the lines from L2
+          named_bar_sync(1, kEpiThreads);
+          const int et = threadIdx.x - kEpiWarp0 * 32;
+          for (int c = 0; c < p.L; ++c)
+            for (int l = et; l < 4 * BN; l += kEpiThreads)
+              discard_l2_line(p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + (size_t)l * 32);
         }
       }
     }

@@ -207,6 +207,10 @@ __device__ __forceinline__ void st_f4_hint(void* p, float4 v, uint64_t pol) {
                "f"(v.z), "f"(v.w), "l"(pol)
                : "memory");
 }
+// Drop a dead 128-byte line from L2 without writing it back (its contents become undefined).
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)

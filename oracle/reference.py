@@ -219,22 +219,29 @@ def ag_tile_schedule(W: int, M_local: int, N: int, BM: int, BN: int, self_rank: 
     return [(mg, nt) for mg in sorted(range(n_groups), key=key) for nt in range(tiles_n)]
 
 
-def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1, group_n=None):
-    """Order of GEMM+ReduceScatter work items: rank-outer (0..W-1, the reduction order); within a
-    rank the N-tiles are taken in groups of ``group_n`` (default: one group of all N-tiles; the last
-    group may be narrower): group by group, M-tiles ascending, the group's N-tiles innermost. Item
-    (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1. Returns (rank, m_tile,
-    n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group (see
+def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1, group_n=None, rank_block=None):
+    """Order of GEMM+ReduceScatter work items. Within a rank, the tile order ("positions") takes the
+    N-tiles in groups of ``group_n`` (default: one group of all N-tiles; the last group may be
+    narrower): group by group, M-tiles ascending, the group's N-tiles innermost. Ranks are
+    interleaved in blocks of ``rank_block`` positions (default: one block of all positions, i.e.
+    rank-outer): for each block, ranks 0..W-1 (the reduction order), the block's positions in
+    order. Item (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1. Returns
+    (rank, m_tile, n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group (see
     :func:`ag_tile_schedule`)."""
     tiles_m = (M + BM - 1) // BM
     tiles_n = (N + BN - 1) // BN
     gn = tiles_n if group_n is None else max(1, min(group_n, tiles_n))
+    order = []
+    for n0 in range(0, tiles_n, gn):
+        for mg in range(tiles_m // group):
+            for nt in range(n0, min(n0 + gn, tiles_n)):
+                order.append((mg, nt))
+    P = len(order) if rank_block is None else max(1, min(rank_block, len(order)))
     out = []
-    for r in range(W):
-        for n0 in range(0, tiles_n, gn):
-            for mg in range(tiles_m // group):
-                for nt in range(n0, min(n0 + gn, tiles_n)):
-                    out.append((r, mg, nt))
+    for b0 in range(0, len(order), P):
+        for r in range(W):
+            for pos in range(b0, min(b0 + P, len(order))):
+                out.append((r,) + order[pos])
     return out
 
 

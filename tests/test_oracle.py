@@ -428,3 +428,16 @@ def test_rs_schedule_n_groups():
     assert s[:9] == [(0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 0, 3), (0, 1, 0), (0, 1, 1), (0, 1, 2), (0, 1, 3), (0, 0, 4)]
     assert s[16:20] == [(0, 0, 8), (0, 0, 9), (0, 1, 8), (0, 1, 9)] and s[20] == (1, 0, 0)
     assert R.rs_item_schedule(3, 512, 512, 128, 256, group_n=8) == R.rs_item_schedule(3, 512, 512, 128, 256)
+
+
+def test_rs_schedule_rank_blocks():
+    # 2 ranks, 3 M-tiles x 2 N-tiles = 6 positions per rank, blocks of 4: positions 0-3 for ranks
+    # 0 and 1, then positions 4-5 for ranks 0 and 1
+    s = R.rs_item_schedule(2, 384, 512, 128, 256, rank_block=4)
+    order = [(m, n) for m in range(3) for n in range(2)]
+    want = [(r,) + order[p] for r in range(2) for p in range(4)] + [(r,) + order[p] for r in range(2) for p in range(4, 6)]
+    assert s == want
+    assert sorted(s) == sorted(R.rs_item_schedule(2, 384, 512, 128, 256))
+    # the running sum of a tile is always handed to the next rank later in the order
+    idx = {it: i for i, it in enumerate(R.rs_item_schedule(8, 8192, 8192, 128, 256, group=2, group_n=8, rank_block=148))}
+    assert all(idx[(r, m, n)] > idx[(r - 1, m, n)] for (r, m, n) in idx if r > 0)
