@@ -51,6 +51,14 @@ namespace tdx {
 #ifndef TDX_PREFETCH_AHEAD
 #define TDX_PREFETCH_AHEAD 0
 #endif
+// L2 eviction policy of operand tile loads and of running-sum / output traffic: 0 = evict_first,
+// 1 = evict_last, 2 = evict_normal.
+#ifndef TDX_OPERAND_POLICY
+#define TDX_OPERAND_POLICY 1
+#endif
+#ifndef TDX_SUM_POLICY
+#define TDX_SUM_POLICY 0
+#endif
 
 // PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
 // 256 x BN tile with one instruction stream issued by the leader; each CTA stages its own 128 rows
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      const uint64_t keep = policy_evict_last();   // operand tiles are re-read by other tiles
+      const uint64_t keep = policy_of(TDX_OPERAND_POLICY);   // operand tiles are re-read by other tiles
       uint64_t flag_ns = 0;
       uint32_t n_waits = 0;
       bool stop = false;
@@ -645,7 +653,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const bool chained = chain && !p.reduce_last;   // running sum handed from element to element
     const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
-    const uint64_t once = policy_evict_first();   // running sums and outputs: touched once per pass
+    const uint64_t once = policy_of(TDX_SUM_POLICY);   // running sums and outputs
     int local = 0;
     for (int it = cid; it < items; it += ncl, ++local) {
       const Item w = decode_item<OP, CL>(p, it, BN, crank);

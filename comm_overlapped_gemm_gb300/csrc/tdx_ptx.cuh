@@ -74,6 +74,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 0 = evict_first, 1 = evict_last, 2 = evict_normal
+__device__ __forceinline__ uint64_t policy_of(int kind) {
+  return kind == 0 ? policy_evict_first() : kind == 1 ? policy_evict_last() : policy_evict_normal();
+}
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                                  int y, uint64_t pol) {
   asm volatile(
