@@ -23,6 +23,13 @@ constexpr int kCopyRoundBytes = 16384;   // producer: bytes in flight per CTA pe
 constexpr int kMaxPieceBytes = 65536;    // producer: largest copy unit released at once
 constexpr int kMaxSplitK = 16;
 constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
+// RS order: tiles per rank block (divided by the CTAs per cluster to count positions); a block is
+// processed for every rank before the next, so a tile's running sum is re-read by the next rank
+// about one block later.
+#ifndef TDX_RS_RANK_BLOCK
+#define TDX_RS_RANK_BLOCK 296
+#endif
+constexpr int kRsRankBlock = TDX_RS_RANK_BLOCK;
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
 // K bytes per shared-memory ring slot (host and device agree on it). 128 for every tile width: a
