@@ -134,7 +134,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.CL = p.PM == 0 ? 1 : 2;
   {
     const int tg = (p.tiles_m / p.CL) * p.tiles_n;
-    const int rb = kRsRankBlock / p.CL;   // about one wave of tiles
+    const int rb = kRsRankBlock / p.CL;
     p.rank_block = op == OP_RS ? (tg < rb ? (tg > 0 ? tg : 1) : rb) : (tg > 0 ? tg : 1);
   }
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
