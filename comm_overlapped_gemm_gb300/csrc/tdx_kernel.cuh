@@ -59,6 +59,10 @@ namespace tdx {
 #ifndef TDX_SUM_POLICY
 #define TDX_SUM_POLICY 0
 #endif
+// Drop dead running-sum / partial-slot lines from L2 after their last read (1) or leave them (0).
+#ifndef TDX_DISCARD_DEAD
+#define TDX_DISCARD_DEAD 1
+#endif
 
 // PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
 // 256 x BN tile with one instruction stream issued by the leader; each CTA stages its own 128 rows
@@ -274,6 +278,56 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
   }
 }
 
+// Bounded wait until every chunk flag gc0..gc1 equals the epoch. The flags are polled with
+// independent relaxed loads (one round trip for all of them, not one per flag), then a single
+// acquire fence orders the data reads after them. Stale values and timeouts are reported like
+// wait_flag's, for the first chunk not yet released.
+static __device__ __noinline__ bool wait_flags_all(const KParams& p, int gc0, int gc1, volatile int* abort_flag,
+                                                   uint64_t* waited_ns) {
+  constexpr int kBatch = 16;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    int pending = -1;
+    uint32_t seen = 0;
+    for (int b = gc0; b <= gc1 && pending < 0; b += kBatch) {
+      uint32_t v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = (b + j <= gc1) ? ld_relaxed_gpu(p.chunk_flags + b + j) : p.epoch;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (v[j] > p.epoch) {
+          report_error(p, DEV_STALE, ROLE_FLAG, b + j, v[j], p.epoch);
+          *abort_flag = 1;
+          return false;
+        }
+        if (pending < 0 && v[j] != p.epoch) {
+          pending = b + j;
+          seen = v[j];
+        }
+      }
+    }
+    if (pending < 0) {
+      fence_acq_rel_gpu();
+      if (it > 0) *waited_ns += globaltimer_ns() - t0;
+      return true;
+    }
+    if (it == 0) t0 = globaltimer_ns();
+    __nanosleep(32);
+    if ((it & 15u) == 15u) {
+      if (*abort_flag) return false;
+      if (ld_relaxed_gpu(p.status) != 0u) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        report_error(p, DEV_TIMEOUT, ROLE_FLAG, pending, seen, p.epoch);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Round 32 consecutive fp32 values of one output row (columns col..col+31) once to the output type
 // and store them: AllGather -> C (bf16 or fp32, e4m3 inputs scaled by scale_a[rank]*scale_b);
 // ReduceScatter -> output shard row / (M/W). Rows >= M and columns >= N are skipped.
@@ -442,14 +496,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             if (p.wait_flags) {
               if (p.perturb) __nanosleep(perturb_hash(p.perturb, it) & 4095u);
               const int last_row = min(w.m0 + kBM, p.M) - 1;
-              for (int gc = w.m0 / p.chunk_rows; gc <= last_row / p.chunk_rows; ++gc) {
-                ++n_waits;
-                if (!wait_flag(p, p.chunk_flags + gc, ROLE_FLAG, gc, abort_flag, &flag_ns)) {
-                  stop = true;
-                  break;
-                }
-              }
-              if (stop) break;
+              const int gc0 = w.m0 / p.chunk_rows;
+              const int gc1 = last_row / p.chunk_rows;
+              ++n_waits;
+              if (!wait_flags_all(p, gc0, gc1, abort_flag, &flag_ns)) break;
               fence_proxy_async_global();
             }
           }
@@ -721,7 +771,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
-      if (chained && read_s && w.c == p.L - 1) {
+      if (TDX_DISCARD_DEAD && chained && read_s && w.c == p.L - 1) {
         // the running sum of this tile is dead after the last element read it: drop it from L2
         const int et = threadIdx.x - kEpiWarp0 * 32;
         for (int l = et; l < 4 * BN; l += kEpiThreads) discard_l2_line(sb + (size_t)l * 32);
@@ -785,12 +835,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
             store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
           }
-          // every slot of this tile is dead now: drop the lines from L2
-          named_bar_sync(1, kEpiThreads);
-          const int et = threadIdx.x - kEpiWarp0 * 32;
-          for (int c = 0; c < p.L; ++c)
-            for (int l = et; l < 4 * BN; l += kEpiThreads)
-              discard_l2_line(p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + (size_t)l * 32);
+          if (TDX_DISCARD_DEAD) {
+            // every slot of this tile is dead now: drop the lines from L2
+            named_bar_sync(1, kEpiThreads);
+            const int et = threadIdx.x - kEpiWarp0 * 32;
+            for (int c = 0; c < p.L; ++c)
+              for (int l = et; l < 4 * BN; l += kEpiThreads)
+                discard_l2_line(p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + (size_t)l * 32);
+          }
         }
       }
     }
