@@ -54,6 +54,7 @@ struct Plan {
   int PM = 0;            // pair mode: 0 single, 1 B multicast, 2 two-SM MMA
   int group_n = 1;
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
+  int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
   size_t off_G = 0, off_S = 0, total = 0;
 };
@@ -137,6 +138,9 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     const int rb = kRsRankBlock / p.CL;
     p.rank_block = op == OP_RS ? (tg < rb ? (tg > 0 ? tg : 1) : rb) : (tg > 0 ? tg : 1);
   }
+  // AllGather with shards smaller than a tile (whole shards per 128-row tile, 8-row aligned): the
+  // consumers read A from the shards themselves instead of waiting for the gathered copy
+  p.pull_a = (op == OP_AG && p.PM == 0 && Mx > 0 && Mx < kBM && kBM % Mx == 0 && Mx % 8 == 0) ? 1 : 0;
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
   if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
@@ -145,6 +149,9 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     else if (o.reduce_mode == 2) p.reduce_last = 1;
     else p.reduce_last = (op == OP_AG || p.T < 2 * kRefSMs) ? 1 : 0;
   }
+  // slotted ReduceScatter: rank-inner order (blocks of one position), so that the elements of a
+  // tile run together and their last arriver's fold is spread over the waves
+  if (op == OP_RS && p.reduce_last) p.rank_block = 1;
   // workspace layout
   size_t off = kHeaderBytes;
   const size_t n_chunk_words = op == OP_AG ? static_cast<size_t>(W) * p.n_chunks : 0;
@@ -399,14 +406,20 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   const bool ce = o.producer == TDX_PRODUCER_COPY_ENGINE;
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
   kp.copy_active = (moving && !ce) ? 1 : 0;
-  kp.wait_flags = (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY) ? 1 : 0;
+  kp.pull_a = pl.pull_a;
+  kp.wait_flags = (!pl.pull_a && (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY)) ? 1 : 0;
   // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
   const int ks = k_slice_bytes(pl.BN);
   const int a_box = ks / pl.elt, b_box_n = 128 / pl.elt, b_box_k = ks / pl.elt;
-  if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, a_box, kBM, ks) ||
-      !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, a_box, kBM, ks) ||
-      !make_map(&kp.tm_b[0], B, fp8, K, N, b_box_n, b_box_k))
+  if (pl.pull_a) {
+    // one map per shard, a box of the whole shard's M_local rows
+    for (int r = 0; r < W; ++r)
+      if (!make_map(&kp.tm_a[r], shards[r], fp8, M_local, K, a_box, M_local, ks)) return TDX_ERR_CUDA;
+  } else if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, a_box, kBM, ks) ||
+             !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, a_box, kBM, ks)) {
     return TDX_ERR_CUDA;
+  }
+  if (!make_map(&kp.tm_b[0], B, fp8, K, N, b_box_n, b_box_k)) return TDX_ERR_CUDA;
   if (o.epoch == 0) {
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
     if (s != TDX_OK) return s;
@@ -512,7 +525,7 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, 0};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, pl.pull_a};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

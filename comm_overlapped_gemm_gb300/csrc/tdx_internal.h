@@ -49,7 +49,7 @@ constexpr size_t kHeaderBytes = 4096;
 constexpr int kStatusWords = 8;
 
 struct KParams {
-  CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard. RS: A_r
+  CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard (pull mode: shard r). RS: A_r
   CUtensorMap tm_b[kMaxW];       // AG: [0] B. RS: B_r
   const uint8_t* shard[kMaxW];   // AG producer sources
   uint8_t* out[kMaxW];           // AG: [0] = C. RS: output shards
@@ -76,6 +76,7 @@ struct KParams {
   int out_fp32;
   int copy_active;               // producer warps copy chunks (AG, SM producer, fused/move)
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
+  int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;

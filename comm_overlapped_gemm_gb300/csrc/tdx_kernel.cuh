@@ -60,8 +60,9 @@ namespace tdx {
 #define TDX_SUM_POLICY 0
 #endif
 // Drop dead running-sum / partial-slot lines from L2 after their last read (1) or leave them (0).
+// Measured neutral on GB300, so off: the workspace then keeps the last call's sums and partials.
 #ifndef TDX_DISCARD_DEAD
-#define TDX_DISCARD_DEAD 1
+#define TDX_DISCARD_DEAD 0
 #endif
 
 // PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   }
   if (threadIdx.x == kTmaWarp * 32) {
-    for (int i = 0; i < (OP == OP_AG ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
+    for (int i = 0; i < (OP == OP_AG && !p.pull_a ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
     for (int i = 0; i < (OP == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
   }
   tc_fence_before();
@@ -484,7 +485,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         const CUtensorMap* map_a;
         const CUtensorMap* map_b;
         int arow = w.m0;
-        if (ag) {
+        int a_bytes = C::A_BYTES;   // A bytes this CTA loads per K slice
+        int pull_r0 = 0, pull_nr = 0;
+        if (ag && p.pull_a) {
+          // remote data access: the tile's rows are whole shards (128/M_local of them); each is read
+          // straight from its shard, so nothing waits on the gathered copy
+          map_a = &p.tm_a[0];
+          map_b = &p.tm_b[0];
+          pull_r0 = w.m0 / p.M_local;
+          pull_nr = min(kBM / p.M_local, p.W - pull_r0);
+          a_bytes = pull_nr * p.M_local * 128;
+        } else if (ag) {
           map_b = &p.tm_b[0];
           const int self_lo = p.self_rank * p.M_local;
           const bool self_tile = w.m0 >= self_lo && w.m0 + kBM <= self_lo + p.M_local;
@@ -529,6 +540,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
           const uint32_t fb = full0 + 8 * stage;
+          if constexpr (PM == 0) {
+            if (ag && p.pull_a) {
+              mbar_arrive_expect_tx(fb, a_bytes + C::B_BYTES);
+              for (int q = 0; q < pull_nr; ++q)
+                tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES + q * p.M_local * 128), &p.tm_a[pull_r0 + q], fb,
+                                 kb * C::BK, 0, keep);
+#pragma unroll
+              for (int j = 0; j < C::B_BOXES; ++j)
+                tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
+              goto issued_slice;
+            }
+          }
           if constexpr (PM == 2) {
             // both CTAs' slices count on the leader's slot barrier, armed once for the pair
             if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
@@ -559,6 +583,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               }
             }
           }
+        issued_slice:
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -807,7 +832,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       if (slotted) {
         named_bar_sync(1, kEpiThreads);
         if (*is_last) {
-          // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ...
+          // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ..., two slots' loads in
+          // flight at a time
 #pragma unroll 1
           for (int ch = 0; ch < C::CHUNKS; ++ch) {
             const int col0 = h * C::COLS_PER_WARP + ch * 32;
@@ -821,8 +847,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               v[4 * j + 2] = s.z;
               v[4 * j + 3] = s.w;
             }
+            int c = 1;
 #pragma unroll 1
-            for (int c = 1; c < p.L; ++c) {
+            for (; c + 1 < p.L; c += 2) {
+              const float* sp0 = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
+              const float* sp1 = sp0 + (size_t)p.T * (kBM * BN);
+              float4 s0[8], s1[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                s0[j] = ld_cg_f4_hint(sp0 + j * kBM * 4, once);
+                s1[j] = ld_cg_f4_hint(sp1 + j * kBM * 4, once);
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                v[4 * j + 0] = (v[4 * j + 0] + s0[j].x) + s1[j].x;
+                v[4 * j + 1] = (v[4 * j + 1] + s0[j].y) + s1[j].y;
+                v[4 * j + 2] = (v[4 * j + 2] + s0[j].z) + s1[j].z;
+                v[4 * j + 3] = (v[4 * j + 3] + s0[j].w) + s1[j].w;
+              }
+            }
+            if (c < p.L) {
               const float* sp = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
 #pragma unroll
               for (int j = 0; j < 8; ++j) {

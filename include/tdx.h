@@ -105,8 +105,8 @@ tdx_status tdx_opts_default(tdx_opts* opts);
  * op = 1: GEMM+ReduceScatter (M_local_or_M = rows of every A_r). The workspace holds the status
  * word, the chunk flags, the symmetric gathered buffer G (AG, (W*M_local) x K of `dtype`) and the
  * fp32 running-sum buffer with its rank-chain flags (RS, and AG with split K). Writes *bytes.
- * After a call the running-sum region's contents are undefined (dead lines are dropped from L2
- * without being written back). */
+ * After a call the running-sum region holds the last call's fp32 sums (chained: ranks/splits
+ * 0..L-2 of every tile) or partials (slotted: one slot per rank/split). */
 tdx_status tdx_workspace_size(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                               const tdx_opts* opts, size_t* bytes);
 
@@ -197,7 +197,10 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * [16] CTA cooperation in use (1 single, 2 multicast pair, 3 2-SM pair), [17] ReduceScatter raster: N-tiles per group (within a rank the
  * tiles are taken group by group, M-tiles, then the group's N-tiles), [18] ReduceScatter rank block:
  * that many positions of a rank's tile order are processed for ranks 0..W-1 before the next block
- * (positions count tiles, or tile pairs when [16] >= 2), [19] reserved (0). */
+ * (positions count tiles, or tile pairs when [16] >= 2), [19] 1 if AllGather tiles read A straight
+ * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
+ * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
+ * its flags), else 0. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -337,3 +337,23 @@ def test_ag_pairs_timeout_recovers(cluster):
     tdx.check(case.run(opts(cluster=cluster, block_n=256)))
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+
+
+def test_ag_small_shards_pull_and_flag_paths_agree():
+    # shards smaller than a tile: tiles read A straight from the shards (pull), while the gathered
+    # copy still completes G and releases every flag; a 96-row shard (not a divisor of 128) takes
+    # the flag-waiting path. Both match the oracle bit for bit on integers.
+    for shape, chunk in ((dict(W=8, M=16, K=2048, N=512), 16), (dict(W=4, M=96, K=512, N=512), 32)):
+        wl = wls.with_shape(wls.WORKLOADS["ag_w8"], chunk_rows=chunk, **shape)
+        inp = wls.make_inputs(wl, integer=True)
+        o = opts(chunk_rows=chunk, epoch=4)
+        plan = tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o)
+        assert plan["pull_a"] == (1 if wl.M == 16 else 0)
+        case = AGCase(inp, opts=o)
+        tdx.check(case.run())
+        status_ok(case)
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+        assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
+        n = wl.W * plan["n_chunks"]
+        f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
+        assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 4))

@@ -105,6 +105,18 @@ def test_rs_chain_flags_trace_and_order():
         for k, it in enumerate(range(b, items, grid)):
             r, mt, nt = sched[it]
             assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)
+    # the running sum of ranks 0..W-2 left in the workspace is the left fold of the partials:
+    # with fp32 partials it matches the oracle's fp64 sum of ranks 0..W-2 to fp32 accuracy
+    S = case.ws[plan["off_S"]:plan["off_S"] + 4 * plan["T"] * 128 * plan["BN"]].view(torch.float32).cpu().numpy()
+    full3 = R.gemm_rs_rows(inp.a[:3], inp.b[:3], np.arange(512), "bf16")   # ranks 0..2 summed
+    BN = plan["BN"]
+    for (mt, nt) in [(0, 0), (3, 1)]:
+        tile = mt * plan["tiles_n"] + nt
+        T = S[tile * 128 * BN:(tile + 1) * 128 * BN]
+        # layout: ((cc*8 + j)*128 + i)*4 + t  ->  element (i, 32*cc + 4*j + t)
+        T = T.reshape(BN // 32, 8, 128, 4).transpose(2, 0, 1, 3).reshape(128, BN)
+        want = full3[mt * 128:(mt + 1) * 128, nt * BN:(nt + 1) * BN]
+        assert np.max(np.abs(T - want)) <= 1e-5 * np.max(np.abs(want))
 
 
 def test_rs_modes_run():
@@ -154,6 +166,16 @@ def test_rs_slotted_bookkeeping():
     T = plan["T"]
     cnt = case.ws[plan["off_tile_cnt"]:plan["off_tile_cnt"] + 4 * T].view(torch.int32).cpu().numpy()
     assert not cnt.any()
+    # slot r of a tile holds rank r's partial A_r @ B_r (fp32, exact on integers)
+    BN = plan["BN"]
+    S = case.ws[plan["off_S"]:plan["off_S"] + 4 * 4 * T * 128 * BN].view(torch.float32).cpu().numpy()
+    for r in range(4):
+        P = R.gemm_rs_rows([inp.a[r]], [inp.b[r]], np.arange(512), "bf16")
+        for (mt, nt) in [(0, 0), (2, 3)]:
+            tile = mt * plan["tiles_n"] + nt
+            blk = S[(r * T + tile) * 128 * BN:(r * T + tile + 1) * 128 * BN]
+            blk = blk.reshape(BN // 32, 8, 128, 4).transpose(2, 0, 1, 3).reshape(128, BN)
+            assert np.array_equal(blk, P[mt * 128:(mt + 1) * 128, nt * BN:(nt + 1) * BN])
     # a second call with the next epoch gives the same result (counters were reset)
     for x in case.out:
         x.fill_(float("nan"))
