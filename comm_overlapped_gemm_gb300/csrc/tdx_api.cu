@@ -151,7 +151,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   }
   // slotted ReduceScatter: rank-inner order (blocks of one position), so that the elements of a
   // tile run together and their last arriver's fold is spread over the waves
-  if (op == OP_RS && p.reduce_last) p.rank_block = 1;
+  if (op == OP_RS && p.reduce_last && kSlottedRankInner) p.rank_block = 1;
   // workspace layout
   size_t off = kHeaderBytes;
   const size_t n_chunk_words = op == OP_AG ? static_cast<size_t>(W) * p.n_chunks : 0;

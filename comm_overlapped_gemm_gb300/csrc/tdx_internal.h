@@ -32,6 +32,11 @@ constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
 #define TDX_RS_RANK_BLOCK (1 << 30)
 #endif
 constexpr int kRsRankBlock = TDX_RS_RANK_BLOCK;
+// Slotted ReduceScatter order: rank-inner (1) or the rank-outer order of the chained mode (0).
+#ifndef TDX_SLOTTED_RANK_INNER
+#define TDX_SLOTTED_RANK_INNER 1
+#endif
+constexpr bool kSlottedRankInner = TDX_SLOTTED_RANK_INNER != 0;
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
 
 // K bytes per shared-memory ring slot (host and device agree on it). 128 for every tile width: a

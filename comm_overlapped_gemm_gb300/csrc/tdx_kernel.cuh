@@ -729,6 +729,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
     const uint64_t once = policy_of(TDX_SUM_POLICY);   // running sums and outputs
+    const uint64_t keep_slot = policy_evict_last();     // slotted partials, folded soon after
     int local = 0;
     for (int it = cid; it < items; it += ncl, ++local) {
       const Item w = decode_item<OP, CL>(p, it, BN, crank);
@@ -788,9 +789,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
         if (write_s) {
+          // slotted partials are folded soon after (keep them in L2); a chained running sum is read
+          // by the next element much later
+          const uint64_t pol = slotted ? keep_slot : once;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), once);
+            st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
         }
         if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
       }
