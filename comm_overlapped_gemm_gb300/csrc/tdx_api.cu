@@ -149,8 +149,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     else if (o.reduce_mode == 2) p.reduce_last = 1;
     else p.reduce_last = (op == OP_AG || p.T < 2 * kRefSMs) ? 1 : 0;
   }
-  // slotted ReduceScatter: rank-inner order (blocks of one position), so that the elements of a
-  // tile run together and their last arriver's fold is spread over the waves
+  // slotted ReduceScatter may take a rank-inner order (blocks of one position) instead
   if (op == OP_RS && p.reduce_last && kSlottedRankInner) p.rank_block = 1;
   // workspace layout
   size_t off = kHeaderBytes;

@@ -33,8 +33,9 @@ constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
 #endif
 constexpr int kRsRankBlock = TDX_RS_RANK_BLOCK;
 // Slotted ReduceScatter order: rank-inner (1) or the rank-outer order of the chained mode (0).
+// Rank-outer measured faster on GB300 for the small-M case (48.6 vs 57.9 us).
 #ifndef TDX_SLOTTED_RANK_INNER
-#define TDX_SLOTTED_RANK_INNER 1
+#define TDX_SLOTTED_RANK_INNER 0
 #endif
 constexpr bool kSlottedRankInner = TDX_SLOTTED_RANK_INNER != 0;
 constexpr int kRefSMs = 148;             // fixed SM count used only for the (host) tiling choice
