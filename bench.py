@@ -388,6 +388,29 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     res["ag_fp8_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
                         "tflops": tf, "peak_fp8_tflops": 2 * peak_bf16, "frac_of_peak": tf / (2 * peak_bf16)}
     del call, status
+    wl = W["rs_fp8_w8"]
+    inp = wls.make_inputs(wl)
+    A = [torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in inp.a]
+    Bs = [torch.from_numpy(np.ascontiguousarray(x)).to(dev) for x in inp.b]
+    out = [torch.empty((wl.M // wl.W, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_FP8_E4M3),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    ep = {"e": 0}
+
+    def rs8(mode=0):
+        ep["e"] += 1
+        o = tdx.make_opts(epoch=ep["e"], mode=mode, scale_a=inp.scale_a, scale_b=inp.scale_b)
+        tdx.check(tdx.tdx_gemm_rs(A, Bs, out, ws, wl.W, wl.M, wl.K, wl.N, tdx.TDX_FP8_E4M3, o))
+    for _ in range(3):
+        rs8()
+    f = time_mode(torch, rs8, reps)
+    st8, d8 = tdx.tdx_read_device_status(ws)
+    if st8 != 0:
+        raise RuntimeError(f"device status {tdx.tdx_status_string(st8)} {d8}")
+    tf = wl.flops / (f * 1e-3) / 1e12
+    res["rs_fp8_w8"] = {"ms_fused": f, "tflops": tf, "peak_fp8_tflops": 2 * peak_bf16, "frac_of_peak": tf / (2 * peak_bf16)}
+    del A, Bs, out, ws
     call, status = ag_case(tdx, torch, W["ag_small"], dev)
     for _ in range(5):
         call()

@@ -112,7 +112,8 @@ def _stream(stream) -> int:
 
 def make_opts(**kw) -> tdx_opts:
     """A tdx_opts filled with the library defaults, then the given fields. ``scale_a`` (list of W
-    floats) and ``scale_b`` (float) are converted to host arrays kept alive by the struct."""
+    floats) and ``scale_b`` (a float for AllGather, a list of W floats for ReduceScatter) are
+    converted to host arrays kept alive by the struct."""
     o = tdx_opts()
     _lib.tdx_opts_default(ctypes.byref(o))
     keep = []
@@ -122,7 +123,8 @@ def make_opts(**kw) -> tdx_opts:
             keep.append(arr)
             o.scale_a = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
         elif k == "scale_b" and v is not None:
-            arr = (ctypes.c_float * 1)(float(v))
+            vals = [float(s) for s in v] if isinstance(v, (list, tuple)) else [float(v)]
+            arr = (ctypes.c_float * len(vals))(*vals)
             keep.append(arr)
             o.scale_b = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
         elif k == "trace":

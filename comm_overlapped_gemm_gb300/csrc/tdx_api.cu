@@ -80,7 +80,6 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     p.chunk_rows = Mx > 0 ? cr : 1;
     p.n_chunks = Mx > 0 ? Mx / cr : 0;
   } else {
-    if (fp8) return TDX_ERR_UNSUPPORTED;
     if (Mx % W != 0) return TDX_ERR_INVALID_ARG;
     p.M = Mx;
     p.M_local = Mx / W;
@@ -110,7 +109,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     if (L < 1) L = 1;
   } else {
     if (bn == 0) {
-      bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+      bn = N > 128 ? 256 : ((N > 64 || fp8) ? 128 : 64);
       // few output tiles: narrower tiles spread the ranks' partial reductions over more CTAs
       if (bn == 256 && static_cast<long long>(p.tiles_m) * ((N + 255) / 256) < 2 * kRefSMs) bn = 128;
     }
@@ -127,7 +126,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   if (o.cluster < 0 || o.cluster > 3) return TDX_ERR_INVALID_ARG;
   const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
   if (o.cluster >= 2) {
-    if (!pair_ok) return TDX_ERR_UNSUPPORTED;
+    if (!pair_ok || (op == OP_RS && fp8 && o.cluster == 2)) return TDX_ERR_UNSUPPORTED;
     p.PM = o.cluster - 1;
   } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs) {
     p.PM = 2;
@@ -467,9 +466,11 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   Plan pl;
   tdx_status s = make_plan(OP_RS, W, M, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
+  const bool fp8 = dtype == TDX_FP8_E4M3;
   for (int r = 0; r < W; ++r)
     if (!aligned16(A_parts[r]) || !aligned16(B_parts[r]) || !aligned16(out_shards[r])) return TDX_ERR_ALIGNMENT;
-  if ((static_cast<long long>(K) * 2) % 16 != 0 || (static_cast<long long>(N) * 2) % 16 != 0)
+  if ((static_cast<long long>(K) * pl.elt) % 16 != 0 || (static_cast<long long>(N) * pl.elt) % 16 != 0 ||
+      (static_cast<long long>(N) * 2) % 16 != 0)
     return TDX_ERR_ALIGNMENT;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.total)
     return TDX_ERR_WORKSPACE;
@@ -490,17 +491,20 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   for (int r = 0; r < W; ++r) {
     kp.out[r] = static_cast<uint8_t*>(out_shards[r]);
     const int ks = k_slice_bytes(pl.BN);
-    if (!make_map(&kp.tm_a[r], A_parts[r], false, M, K, ks / 2, kBM, ks) ||
-        !make_map(&kp.tm_b[r], B_parts[r], false, K, N, 64, ks / 2))
+    if (!make_map(&kp.tm_a[r], A_parts[r], fp8, M, K, ks / pl.elt, kBM, ks) ||
+        !make_map(&kp.tm_b[r], B_parts[r], fp8, K, N, 128 / pl.elt, ks / pl.elt))
       return TDX_ERR_CUDA;
+    const float sa = (fp8 && o.scale_a) ? o.scale_a[r] : 1.0f;
+    const float sb = (fp8 && o.scale_b) ? o.scale_b[r] : 1.0f;
+    kp.elem_scale[r] = sa * sb;
   }
   if (o.epoch == 0) {
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
     if (s != TDX_OK) return s;
   }
-  const int grid = grid_for(o, pl, false, pl.L * pl.T);
+  const int grid = grid_for(o, pl, fp8, pl.L * pl.T);
   if (grid <= 0) return TDX_ERR_CUDA;
-  return launch(pl, kp, false, grid, st);
+  return launch(pl, kp, fp8, grid, st);
 }
 
 tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_status* out, uint32_t* detail) {

@@ -69,6 +69,7 @@ struct KParams {
   int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
   float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r
+  float elem_scale[kMaxW];       // RS e4m3: scale_a[r] * scale_b[r] for rank r's partial
   int op, mode;
   int W, M, K, N;                // M = total rows (AG: W * M_local)
   int M_local;                   // AG: rows per shard. RS: rows per output shard (M / W)

@@ -771,6 +771,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           tmem_ld_wait(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if constexpr (FP8 && OP == OP_RS) {
+            // rank r's partial enters the fold dequantised: scale_a[r] * scale_b[r]
+            const float s = p.elem_scale[w.c];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= s;
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.0f;

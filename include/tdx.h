@@ -72,8 +72,8 @@ typedef struct tdx_opts {
   int self_rank;             /* AG: rank whose shard is local; arrival order self, self+1, ... (default 0) */
   int chunk_rows;            /* AG: rows per chunk and per flag; must divide M_local (default min(128, M_local)) */
   tdx_dtype out_dtype;       /* AG: TDX_BF16 (default) or TDX_FP32. RS: TDX_BF16 only */
-  const float* scale_a;      /* host array [W]: per-shard dequantisation scales for e4m3 (NULL = 1) */
-  const float* scale_b;      /* host pointer to B's dequantisation scale for e4m3 (NULL = 1) */
+  const float* scale_a;      /* host array [W]: per-shard (AG) / per-A_r (RS) e4m3 dequantisation scales (NULL = 1) */
+  const float* scale_b;      /* host array: AG [1] B's scale; RS [W] the B_r scales; e4m3 only (NULL = 1) */
   tdx_mode mode;             /* default TDX_FUSED */
   tdx_producer producer;     /* default TDX_PRODUCER_SM */
   uint32_t epoch;            /* 0: the library clears the flags on `stream` and uses epoch 1.
@@ -135,12 +135,13 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
 /* GEMM+ReduceScatter: S = sum_{r=0}^{W-1} A_parts[r] @ B_parts[r], out_shards[j] = rows
  * [j*M/W, (j+1)*M/W) of S. (Same article and section: "GEMM-plus-ReduceScatter"; section "DITRON
  * adds three levels of tiling" lists ReduceScatter among the collectives split into chunks.)
- *  A_parts    host array of W device pointers, each M x K bf16 row-major.
- *  B_parts    host array of W device pointers, each K x N bf16 row-major.
+ *  A_parts    host array of W device pointers, each M x K of `dtype`, row-major.
+ *  B_parts    host array of W device pointers, each K x N of `dtype`, row-major.
  *  out_shards host array of W device pointers, each (M/W) x N bf16 row-major.
  *  workspace  device, 256-byte aligned, workspace_bytes >= tdx_workspace_size(1, ...) with the
  *             same shapes and opts (else TDX_ERR_WORKSPACE).
  *  W          1..16, and M must be a multiple of W.
+ *  dtype      TDX_BF16, or TDX_FP8_E4M3 with per-rank scales: P_r = scale_a[r]*scale_b[r]*(A_r @ B_r).
  * Rank r's fp32 partial tile is added to the running sum of ranks 0..r-1 in that fixed order,
  * ((P_0 + P_1) + P_2) + ..., whatever the timing, so the result is identical run to run; the sum
  * is rounded once to bf16 (nearest even). */

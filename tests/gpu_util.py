@@ -80,17 +80,18 @@ class RSCase:
         wl = inp.wl
         self.inp, self.wl = inp, wl
         self.W, self.M, self.K, self.N = wl.W, wl.M, wl.K, wl.N
+        self.dt = dtype_code(wl.dtype)
         self.A = [dev_bits(a) for a in inp.a]
         self.B = [dev_bits(b) for b in inp.b]
         self.out = [torch.full((wl.M // wl.W, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
                     for _ in range(wl.W)]
         self.opts = opts
-        self.ws = workspace(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, opts)
+        self.ws = workspace(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, self.dt, opts)
 
     def run(self, opts=None):
         o = opts if opts is not None else self.opts
         return tdx.tdx_gemm_rs(self.A, self.B, self.out, self.ws, self.W, self.M, self.K, self.N,
-                               tdx.TDX_BF16, o)
+                               self.dt, o)
 
     def result_bits(self) -> np.ndarray:
         torch.cuda.synchronize()
@@ -100,9 +101,12 @@ class RSCase:
         return R.decode_bf16(self.result_bits())
 
     def oracle(self, rows=None):
+        i, dt = self.inp, self.wl.dtype
+        sa = i.scale_a if dt == "e4m3" else None
+        sb = i.scale_b if dt == "e4m3" else None
         if rows is None:
-            return np.concatenate(R.gemm_rs(self.inp.a, self.inp.b, "bf16"))
-        return R.gemm_rs_rows(self.inp.a, self.inp.b, rows, "bf16")
+            return np.concatenate(R.gemm_rs(i.a, i.b, dt, sa, sb))
+        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb)
 
 
 def assert_bit_exact(got_bits: np.ndarray, oracle_fp64: np.ndarray, out_dtype: str):

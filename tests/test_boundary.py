@@ -84,7 +84,6 @@ def test_workspace_sizes(tdx):
     ((0, 17, 64, 128, 256, 0), 1),     # W > 16
     ((0, 2, -1, 128, 256, 0), 1),      # negative size
     ((1, 3, 128, 128, 256, 0), 1),     # RS: M not a multiple of W
-    ((1, 2, 128, 128, 256, 1), 2),     # RS e4m3 not implemented
     ((2, 2, 64, 128, 256, 0), 1),      # bad op
     ((0, 2, 64, 128, 256, 7), 1),      # bad dtype
 ])
@@ -142,7 +141,8 @@ def test_rs_validation_codes(tdx):
     assert rs(A=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
     assert rs(O=[0, FAKE]) == tdx.TDX_ERR_INVALID_ARG
     assert rs(M=129) == tdx.TDX_ERR_INVALID_ARG
-    assert rs(dtype=1) == tdx.TDX_ERR_UNSUPPORTED
+    assert rs(dtype=1, M=256, opts=tdx.make_opts(cluster=2, block_n=256)) == tdx.TDX_ERR_UNSUPPORTED
+    assert rs(dtype=1, K=120) == tdx.TDX_ERR_ALIGNMENT      # 120-byte e4m3 rows
     assert rs(opts=tdx.make_opts(out_dtype=2)) == tdx.TDX_ERR_UNSUPPORTED
     assert rs(B=[FAKE, FAKE + 2]) == tdx.TDX_ERR_ALIGNMENT
     assert rs(wsb=100) == tdx.TDX_ERR_WORKSPACE

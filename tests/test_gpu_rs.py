@@ -249,3 +249,32 @@ def test_rs_grouped_raster_trace():
         for k, it in enumerate(range(b, items, grid)):
             r, mt, nt = sched[it]
             assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(reduce_mode=1), dict(reduce_mode=2, block_n=256),
+                                     dict(cluster=3, block_n=256, reduce_mode=1)])
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_e4m3(variant, integer):
+    wl = wls.with_shape(wls.WORKLOADS["rs_fp8_w8"], W=4, M=512, K=1024, N=1024)
+    inp = wls.make_inputs(wl, integer=integer)
+    o = opts(scale_a=inp.scale_a, scale_b=inp.scale_b, **variant)
+    case = RSCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "e4m3")
+
+
+def test_rs_e4m3_full_size_sampled_and_deterministic():
+    wl = wls.WORKLOADS["rs_fp8_w8"]
+    inp = wls.make_inputs(wl, integer=False)
+    case = RSCase(inp, opts=opts(scale_a=inp.scale_a, scale_b=inp.scale_b))
+    tdx.check(case.run())
+    status_ok(case)
+    rows = sample_rows(wl.M, wl.M // wl.W)
+    first = case.result_bits()
+    assert_within_tol(R.decode_bf16(first[rows]), case.oracle(rows), "e4m3")
+    tdx.check(case.run(opts(scale_a=inp.scale_a, scale_b=inp.scale_b, perturb_seed=3)))
+    assert np.array_equal(case.result_bits(), first)

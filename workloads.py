@@ -69,6 +69,9 @@ WORKLOADS = {
     "ag_fp8_w8": Workload("ag_fp8_w8", 3, "ag", W=8, M=2048, K=8192, N=8192, dtype="e4m3",
                           out_dtype="bf16", chunk_rows=128, b_dist=("normal", 1.0),
                           note="W=8, shard 2048x8192 e4m3, B 8192x8192 e4m3, per-tensor scales"),
+    "rs_fp8_w8": Workload("rs_fp8_w8", 6, "rs", W=8, M=8192, K=3584, N=8192, dtype="e4m3", out_dtype="bf16",
+                          chunk_rows=0, b_dist=("normal", 1.0),
+                          note="W=8, A_r 8192x3584 e4m3, B_r 3584x8192 e4m3, per-tensor scales, bf16 shards"),
     "ag_small": Workload("ag_small", 4, "ag", W=8, M=16, K=8192, N=1024, dtype="bf16",
                          out_dtype="bf16", chunk_rows=16,
                          note="small-M latency: shard 16x8192, B 8192x1024, chunk 16"),
