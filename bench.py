@@ -363,7 +363,8 @@ def graph_time_us(torch, fn, reps: int = 50):
 
 def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     """The other configurations, timed alone (median of CUDA-event times, warm): the AllGather
-    with the copy-engine producer, e4m3 AllGather, and the small-M latency cases."""
+    with the copy-engine producer, e4m3 AllGather and ReduceScatter, GEMM+AllReduce, and the
+    small-M latency cases."""
     import workloads as wls
     W = wls.WORKLOADS
     res = {}
@@ -410,6 +411,30 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
         raise RuntimeError(f"device status {tdx.tdx_status_string(st8)} {d8}")
     tf = wl.flops / (f * 1e-3) / 1e12
     res["rs_fp8_w8"] = {"ms_fused": f, "tflops": tf, "peak_fp8_tflops": 2 * peak_bf16, "frac_of_peak": tf / (2 * peak_bf16)}
+    del A, Bs, out, ws
+    # GEMM+AllReduce: the ReduceScatter's fold writes each reduced tile into all W full outputs
+    wl = W["ar_w8"]
+    inp = wls.make_inputs(wl)
+    A = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev) for a in inp.a]
+    Bs = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev) for x in inp.b]
+    out = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_AR, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+
+    def ar(mode=0):
+        ep["e"] += 1
+        o = tdx.make_opts(epoch=ep["e"], mode=mode)
+        tdx.check(tdx.tdx_gemm_ar(A, Bs, out, ws, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o))
+    for _ in range(3):
+        ar()
+    f = time_mode(torch, ar, reps)
+    st, d = tdx.tdx_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    tf = wl.flops / (f * 1e-3) / 1e12
+    res["ar_w8"] = {"ms_fused": f, "tflops": tf, "frac_of_peak": tf / peak_bf16,
+                    "output_bytes": wl.W * wl.M * wl.N * 2}
     del A, Bs, out, ws
     call, status = ag_case(tdx, torch, W["ag_small"], dev)
     for _ in range(5):

@@ -19,11 +19,11 @@ TDX_ERR_WORKSPACE, TDX_ERR_CUDA, TDX_ERR_TIMEOUT, TDX_ERR_STALE_EPOCH = 4, 5, 6,
 TDX_BF16, TDX_FP8_E4M3, TDX_FP32 = 0, 1, 2
 TDX_FUSED, TDX_GEMM_ONLY, TDX_MOVE_ONLY, TDX_CONSUMER_ONLY = 0, 1, 2, 3
 TDX_PRODUCER_SM, TDX_PRODUCER_COPY_ENGINE = 0, 1
-OP_AG, OP_RS = 0, 1
+OP_AG, OP_RS, OP_AR = 0, 1, 2
 
 EXPORTED = ["tdx_opts_default", "tdx_workspace_size", "tdx_workspace_init", "tdx_ag_gemm", "tdx_gemm_rs",
             "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info",
-            "tdx_ag_gemm_noalloc"]
+            "tdx_ag_gemm_noalloc", "tdx_gemm_ar"]
 
 
 class tdx_opts(ctypes.Structure):
@@ -66,6 +66,7 @@ def _load():
         "tdx_workspace_init": (I, [P, SZ, P]),
         "tdx_ag_gemm": (I, [PP, P, P, P, SZ, I, I, I, I, I, OP, P]),
         "tdx_gemm_rs": (I, [PP, PP, PP, P, SZ, I, I, I, I, I, OP, P]),
+        "tdx_gemm_ar": (I, [PP, PP, PP, P, SZ, I, I, I, I, I, OP, P]),
         "tdx_read_device_status": (I, [P, P, ctypes.POINTER(I), ctypes.POINTER(U32)]),
         "tdx_trace_size": (SZ, [I, I]),
         "tdx_status_string": (ctypes.c_char_p, [I]),
@@ -204,6 +205,13 @@ def tdx_gemm_rs(A_parts, B_parts, out_shards, workspace, W: int, M: int, K: int,
                 opts=None, stream=None, workspace_bytes: int | None = None) -> int:
     wsb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
     return int(_lib.tdx_gemm_rs(_ptr_array(A_parts), _ptr_array(B_parts), _ptr_array(out_shards), _ptr(workspace),
+                                wsb, W, M, K, N, dtype, _opts_ref(opts), _stream(stream)))
+
+
+def tdx_gemm_ar(A_parts, B_parts, out_full, workspace, W: int, M: int, K: int, N: int, dtype: int,
+                opts=None, stream=None, workspace_bytes: int | None = None) -> int:
+    wsb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    return int(_lib.tdx_gemm_ar(_ptr_array(A_parts), _ptr_array(B_parts), _ptr_array(out_full), _ptr(workspace),
                                 wsb, W, M, K, N, dtype, _opts_ref(opts), _stream(stream)))
 
 

@@ -47,6 +47,7 @@ tdx_opts defaults() {
 // so that tdx_workspace_size and the calls carve the same layout.
 struct Plan {
   int op = 0, W = 0, M = 0, M_local = 0, K = 0, N = 0, elt = 2;
+  int allreduce = 0;     // op code 2: the ReduceScatter kernel writes every rank's full output
   int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
@@ -62,12 +63,15 @@ struct Plan {
 bool valid_bn(int bn, bool fp8) { return fp8 ? (bn == 128 || bn == 256) : (bn == 64 || bn == 128 || bn == 256); }
 
 tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const tdx_opts& o, Plan* pl) {
+  const bool allreduce = op == kOpAllReduce;
+  if (allreduce) op = OP_RS;
   if (op != OP_AG && op != OP_RS) return TDX_ERR_INVALID_ARG;
   if (W < 1 || W > kMaxW || Mx < 0 || K < 0 || N < 0) return TDX_ERR_INVALID_ARG;
   if (dtype != TDX_BF16 && dtype != TDX_FP8_E4M3) return TDX_ERR_INVALID_ARG;
   const bool fp8 = dtype == TDX_FP8_E4M3;
   Plan p;
   p.op = op;
+  p.allreduce = allreduce ? 1 : 0;
   p.W = W;
   p.K = K;
   p.N = N;
@@ -80,9 +84,9 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     p.chunk_rows = Mx > 0 ? cr : 1;
     p.n_chunks = Mx > 0 ? Mx / cr : 0;
   } else {
-    if (Mx % W != 0) return TDX_ERR_INVALID_ARG;
+    if (!allreduce && Mx % W != 0) return TDX_ERR_INVALID_ARG;
     p.M = Mx;
-    p.M_local = Mx / W;
+    p.M_local = allreduce ? Mx : Mx / W;
   }
   const int kb128 = (int)((static_cast<long long>(K) * p.elt + 127) / 128);   // 128-byte K blocks
   p.tiles_m = (p.M + kBM - 1) / kBM;
@@ -453,9 +457,15 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   return cudaStreamWaitEvent(st, ce_st->join, 0) == cudaSuccess ? TDX_OK : TDX_ERR_CUDA;
 }
 
-tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, void* const* out_shards,
-                       void* workspace, size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype,
-                       const tdx_opts* opts, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// GEMM+ReduceScatter (allreduce = false: out[j] is output shard j) or GEMM+AllReduce (allreduce =
+// true: out[r] is rank r's full M x N output).
+tdx_status rs_call(const void* const* A_parts, const void* const* B_parts, void* const* out_shards, void* workspace,
+                   size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype, const tdx_opts* opts,
+                   void* stream, bool allreduce) {
   const tdx_opts o = opts ? *opts : defaults();
   if (A_parts == nullptr || B_parts == nullptr || out_shards == nullptr) return TDX_ERR_INVALID_ARG;
   if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
@@ -464,7 +474,7 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   if (o.mode < TDX_FUSED || o.mode > TDX_MOVE_ONLY) return TDX_ERR_INVALID_ARG;
   if (o.out_dtype != TDX_BF16) return TDX_ERR_UNSUPPORTED;
   Plan pl;
-  tdx_status s = make_plan(OP_RS, W, M, K, N, dtype, o, &pl);
+  tdx_status s = make_plan(allreduce ? kOpAllReduce : OP_RS, W, M, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
   const bool fp8 = dtype == TDX_FP8_E4M3;
   for (int r = 0; r < W; ++r)
@@ -478,7 +488,7 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) {
     for (int r = 0; r < W; ++r) {
-      s = fill_zero(out_shards[r], static_cast<size_t>(pl.M_local) * N * 2, st);
+      s = fill_zero(out_shards[r], static_cast<size_t>(allreduce ? M : pl.M_local) * N * 2, st);
       if (s != TDX_OK) return s;
     }
     return TDX_OK;
@@ -488,6 +498,7 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   std::memset(&kp, 0, sizeof(kp));
   fill_common(kp, pl, o, ws);
   kp.op = OP_RS;
+  kp.allreduce = pl.allreduce;
   for (int r = 0; r < W; ++r) {
     kp.out[r] = static_cast<uint8_t*>(out_shards[r]);
     const int ks = k_slice_bytes(pl.BN);
@@ -505,6 +516,22 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, v
   const int grid = grid_for(o, pl, fp8, pl.L * pl.T);
   if (grid <= 0) return TDX_ERR_CUDA;
   return launch(pl, kp, fp8, grid, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts, void* const* out_shards,
+                       void* workspace, size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype,
+                       const tdx_opts* opts, void* stream) {
+  return rs_call(A_parts, B_parts, out_shards, workspace, workspace_bytes, W, M, K, N, dtype, opts, stream, false);
+}
+
+tdx_status tdx_gemm_ar(const void* const* A_parts, const void* const* B_parts, void* const* out_full, void* workspace,
+                       size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype, const tdx_opts* opts,
+                       void* stream) {
+  return rs_call(A_parts, B_parts, out_full, workspace, workspace_bytes, W, M, K, N, dtype, opts, stream, true);
 }
 
 tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_status* out, uint32_t* detail) {

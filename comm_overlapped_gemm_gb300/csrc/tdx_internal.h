@@ -46,6 +46,7 @@ constexpr int kRefSMs = 148;             // fixed SM count used only for the (ho
 constexpr int k_slice_bytes(int /*block_n*/) { return 128; }
 
 enum Op { OP_AG = 0, OP_RS = 1 };
+constexpr int kOpAllReduce = 2;          // API op code: GEMM+AllReduce (runs the OP_RS kernel)
 enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };
 enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4 };
 enum DevStatus { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_STALE = 7 };
@@ -58,7 +59,7 @@ struct KParams {
   CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard (pull mode: shard r). RS: A_r
   CUtensorMap tm_b[kMaxW];       // AG: [0] B. RS: B_r
   const uint8_t* shard[kMaxW];   // AG producer sources
-  uint8_t* out[kMaxW];           // AG: [0] = C. RS: output shards
+  uint8_t* out[kMaxW];           // AG: [0] = C. RS: output shards. AllReduce: every rank's M x N output
   uint8_t* G;                    // AG gathered buffer
   uint32_t* status;              // kStatusWords words
   uint32_t* chunk_flags;         // AG: [W * n_chunks], flag of chunk (rank, c) at rank*n_chunks + c
@@ -84,6 +85,7 @@ struct KParams {
   int copy_active;               // producer warps copy chunks (AG, SM producer, fused/move)
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
   int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
+  int allreduce;                 // RS kernel as GEMM+AllReduce: out[r] are full M x N outputs
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;

@@ -329,24 +329,25 @@ static __device__ __noinline__ bool wait_flags_all(const KParams& p, int gc0, in
   }
 }
 
-// Round 32 consecutive fp32 values of one output row (columns col..col+31) once to the output type
-// and store them: AllGather -> C (bf16 or fp32, e4m3 inputs scaled by scale_a[rank]*scale_b);
-// ReduceScatter -> output shard row / (M/W). Rows >= M and columns >= N are skipped.
-template <int OP, bool FP8>
-__device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int col, float (&v)[32], uint64_t pol) {
-  if (row >= p.M) return;
-  uint8_t* orow;
-  if constexpr (OP == OP_AG) {
-    if constexpr (FP8) {
-      const float s = p.row_scale[row / p.M_local];
+// 32 fp32 values -> 32 bf16 (round to nearest even) packed in four 16-byte words.
+__device__ __forceinline__ void pack_bf16x32(const float (&v)[32], uint4 (&pk)[4]) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= s;
-    }
-    orow = p.out[0] + (size_t)row * p.N * (p.out_fp32 ? 4 : 2);
-  } else {
-    const int j = row / p.M_local;
-    orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+    pk[j].x = *reinterpret_cast<uint32_t*>(&b0);
+    pk[j].y = *reinterpret_cast<uint32_t*>(&b1);
+    pk[j].z = *reinterpret_cast<uint32_t*>(&b2);
+    pk[j].w = *reinterpret_cast<uint32_t*>(&b3);
   }
+}
+
+// Store 32 fp32 values (columns col..col+31 of one row starting at orow) rounded once to the
+// output type; columns >= N are skipped.
+__device__ __forceinline__ void store_row_chunk(uint8_t* orow, const KParams& p, int col, const float (&v)[32],
+                                                uint64_t pol) {
   if (p.out_fp32) {
     float* o = reinterpret_cast<float*>(orow) + col;
     if (col + 32 <= p.N) {
@@ -361,25 +362,53 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
   } else {
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(orow) + col;
     if (col + 32 <= p.N) {
+      uint4 pk[4];
+      pack_bf16x32(v, pk);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 pk;
-        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
-        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
-        __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&b0);
-        pk.y = *reinterpret_cast<uint32_t*>(&b1);
-        pk.z = *reinterpret_cast<uint32_t*>(&b2);
-        pk.w = *reinterpret_cast<uint32_t*>(&b3);
-        st_v4_hint(o + 8 * j, pk, pol);
-      }
+      for (int j = 0; j < 4; ++j) st_v4_hint(o + 8 * j, pk[j], pol);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (col + i < p.N) o[i] = __float2bfloat16_rn(v[i]);
     }
   }
+}
+
+// Round 32 consecutive fp32 values of one output row (columns col..col+31) once to the output type
+// and store them: AllGather -> C (bf16 or fp32, e4m3 inputs scaled by scale_a[rank]*scale_b);
+// ReduceScatter -> output shard row / (M/W); AllReduce -> row of every rank's full output (bf16).
+// Rows >= M and columns >= N are skipped.
+template <int OP, bool FP8>
+__device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int col, float (&v)[32], uint64_t pol) {
+  if (row >= p.M) return;
+  uint8_t* orow;
+  if constexpr (OP == OP_AG) {
+    if constexpr (FP8) {
+      const float s = p.row_scale[row / p.M_local];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= s;
+    }
+    orow = p.out[0] + (size_t)row * p.N * (p.out_fp32 ? 4 : 2);
+  } else if (p.allreduce) {
+    // AllReduce: the reduced tile, rounded once, goes to every rank's full output (the fused
+    // AllGather of the reduced shards)
+    if (col + 32 <= p.N) {
+      uint4 pk[4];
+      pack_bf16x32(v, pk);
+      for (int r = 0; r < p.W; ++r) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[r] + (size_t)row * p.N * 2) + col;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_v4_hint(o + 8 * j, pk[j], pol);
+      }
+      return;
+    }
+    for (int r = 1; r < p.W; ++r) store_row_chunk(p.out[r] + (size_t)row * p.N * 2, p, col, v, pol);
+    orow = p.out[0] + (size_t)row * p.N * 2;
+  } else {
+    const int j = row / p.M_local;
+    orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
+  }
+  store_row_chunk(orow, p, col, v, pol);
 }
 
 // PM (pair mode): 0 = single CTAs; 1 = CTA pairs sharing the B slice by TMA multicast, each CTA

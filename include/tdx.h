@@ -102,7 +102,7 @@ typedef struct tdx_opts {
 tdx_status tdx_opts_default(tdx_opts* opts);
 
 /* Bytes of workspace needed by one call. op = 0: AllGather+GEMM (M_local_or_M = rows per shard);
- * op = 1: GEMM+ReduceScatter (M_local_or_M = rows of every A_r). The workspace holds the status
+ * op = 1: GEMM+ReduceScatter, op = 2: GEMM+AllReduce (M_local_or_M = rows of every A_r). The workspace holds the status
  * word, the chunk flags, the symmetric gathered buffer G (AG, (W*M_local) x K of `dtype`) and the
  * fp32 running-sum buffer with its rank-chain flags (RS, and AG with split K). Writes *bytes.
  * After a call the running-sum region holds the last call's fp32 sums (chained: ranks/splits
@@ -180,6 +180,19 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
 tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C,
                                int W, int M_local, int K, int N, tdx_dtype dtype,
                                const tdx_opts* opts, uint32_t* device_status, void* stream);
+
+/* GEMM+AllReduce: every rank r receives the whole S = sum_{r'} A_parts[r'] @ B_parts[r'] in
+ * out_full[r]. (Triton-distributed article, section "DITRON adds three levels of tiling": AllReduce is
+ * among the collectives broken into chunks and paired with compute tiles.) Realised as the chunked
+ * ReduceScatter above fused with an AllGather: the element that completes a tile's fixed-order fold
+ * ((P_0 + P_1) + ...) rounds the tile once to bf16 and writes it into every rank's output, so all W
+ * outputs are bit-identical.
+ *  A_parts, B_parts, workspace, dtype, scales: as tdx_gemm_rs (workspace sized with op = 2).
+ *  out_full   host array of W device pointers, each M x N bf16 row-major. M need not be a multiple
+ *             of W. */
+tdx_status tdx_gemm_ar(const void* const* A_parts, const void* const* B_parts, void* const* out_full,
+                       void* workspace, size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype,
+                       const tdx_opts* opts, void* stream);
 
 /* Synchronise `stream`, then read the workspace's device status word into *out (TDX_OK, or the
  * first device-side error since tdx_workspace_init). If detail is not NULL it receives 8 words:

@@ -17,6 +17,8 @@ reach is the plain definition:
   type.
 * GEMM+ReduceScatter: ``S = sum_{r=0}^{W-1} A_r @ B_r`` (ascending r) and output shard j is rows
   ``[j*M/W, (j+1)*M/W)`` of S, rounded once to bf16.
+* GEMM+AllReduce (AllReduce is listed among the chunked collectives in "DITRON adds three levels of
+  tiling"): every rank receives the whole of the same S, rounded once to bf16; M is any size.
 
 Where the pages are silent this file takes the plainest reading: inputs are decoded exactly to
 fp64, products and sums are fp64 (a library fp64 matmul serves as the GEMM step; on the integer
@@ -171,6 +173,19 @@ def gemm_rs(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None):
         S = P if S is None else S + P
     h = M // W
     return [S[j * h:(j + 1) * h] for j in range(W)]
+
+
+def gemm_ar(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None):
+    """GEMM+AllReduce, unrounded fp64: the full ``S = sum_r s_r * A_r @ B_r`` (ascending r), one
+    entry per rank (every rank holds the same S). ``s_r`` as in :func:`gemm_rs`; M need not be a
+    multiple of W."""
+    W = len(a_parts)
+    S = None
+    for r in range(W):
+        s = (1.0 if scale_a is None else float(scale_a[r])) * (1.0 if scale_b is None else float(scale_b[r]))
+        P = (decode(a_parts[r], dtype) @ decode(b_parts[r], dtype)) * s
+        S = P if S is None else S + P
+    return [S.copy() for _ in range(W)]
 
 
 def gemm_rs_rows(a_parts, b_parts, rows, dtype: str = "bf16", scale_a=None, scale_b=None):

@@ -109,6 +109,39 @@ class RSCase:
         return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb)
 
 
+class ARCase:
+    """Device buffers of one GEMM+AllReduce problem: W full M x N outputs."""
+
+    def __init__(self, inp, opts=None):
+        wl = inp.wl
+        self.inp, self.wl = inp, wl
+        self.W, self.M, self.K, self.N = wl.W, wl.M, wl.K, wl.N
+        self.dt = dtype_code(wl.dtype)
+        self.A = [dev_bits(a) for a in inp.a]
+        self.B = [dev_bits(b) for b in inp.b]
+        self.out = [torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+                    for _ in range(wl.W)]
+        self.opts = opts
+        self.ws = workspace(tdx.OP_AR, wl.W, wl.M, wl.K, wl.N, self.dt, opts)
+
+    def run(self, opts=None):
+        o = opts if opts is not None else self.opts
+        return tdx.tdx_gemm_ar(self.A, self.B, self.out, self.ws, self.W, self.M, self.K, self.N,
+                               self.dt, o)
+
+    def result_bits(self, rank: int) -> np.ndarray:
+        torch.cuda.synchronize()
+        return host_bits(self.out[rank])
+
+    def oracle(self, rows=None):
+        i, dt = self.inp, self.wl.dtype
+        sa = i.scale_a if dt == "e4m3" else None
+        sb = i.scale_b if dt == "e4m3" else None
+        if rows is None:
+            return R.gemm_ar(i.a, i.b, dt, sa, sb)[0]
+        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb)
+
+
 def assert_bit_exact(got_bits: np.ndarray, oracle_fp64: np.ndarray, out_dtype: str):
     want = R.round_out(oracle_fp64, out_dtype)
     if out_dtype == "fp32":

@@ -79,12 +79,20 @@ def test_workspace_sizes(tdx):
     assert 128 << 20 < ws < (128 << 20) + (1 << 20)
 
 
+def test_allreduce_workspace_any_m(tdx):
+    # GEMM+AllReduce keeps every row on every rank, so M need not be a multiple of W
+    ws = tdx.tdx_workspace_size(tdx.OP_AR, 3, 200, 136, 264, tdx.TDX_BF16)
+    assert ws > 0
+    info = tdx.tdx_plan_info(tdx.OP_AR, 3, 200, 136, 264, tdx.TDX_BF16)
+    assert info["tiles_m"] == 2 and info["L"] == 3
+
+
 @pytest.mark.parametrize("args,code", [
     ((0, 0, 64, 128, 256, 0), 1),      # W = 0
     ((0, 17, 64, 128, 256, 0), 1),     # W > 16
     ((0, 2, -1, 128, 256, 0), 1),      # negative size
     ((1, 3, 128, 128, 256, 0), 1),     # RS: M not a multiple of W
-    ((2, 2, 64, 128, 256, 0), 1),      # bad op
+    ((3, 2, 64, 128, 256, 0), 1),      # bad op
     ((0, 2, 64, 128, 256, 7), 1),      # bad dtype
 ])
 def test_workspace_size_rejects(tdx, args, code):
@@ -147,6 +155,21 @@ def test_rs_validation_codes(tdx):
     assert rs(B=[FAKE, FAKE + 2]) == tdx.TDX_ERR_ALIGNMENT
     assert rs(wsb=100) == tdx.TDX_ERR_WORKSPACE
     assert rs(M=0) == tdx.TDX_OK
+
+
+def test_ar_validation_codes(tdx):
+    def ar(A=None, B=None, O=None, W=2, M=128, K=128, N=256, dtype=0, opts=None, wsb=1 << 30, ws=FAKE):
+        A = [FAKE] * W if A is None else A
+        B = [FAKE] * W if B is None else B
+        O = [FAKE] * W if O is None else O
+        return tdx.tdx_gemm_ar(A, B, O, ws, W, M, K, N, dtype, opts, stream=0, workspace_bytes=wsb)
+    assert ar(A=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert ar(O=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert ar(O=[FAKE, FAKE + 4]) == tdx.TDX_ERR_ALIGNMENT
+    assert ar(opts=tdx.make_opts(out_dtype=2)) == tdx.TDX_ERR_UNSUPPORTED
+    assert ar(wsb=100) == tdx.TDX_ERR_WORKSPACE
+    assert ar(W=17, A=[FAKE] * 17, B=[FAKE] * 17, O=[FAKE] * 17) == tdx.TDX_ERR_INVALID_ARG
+    assert ar(M=0) == tdx.TDX_OK
 
 
 def test_trace_size(tdx):

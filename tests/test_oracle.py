@@ -107,6 +107,71 @@ def test_rs_brute_force(W, integer):
     check_rs_brute(R.gemm_rs, W, M=2 * W, K=5 + W, N=6, integer=integer, seed=77 + W + integer)
 
 
+def check_ar_brute(gemm_ar, W, M, K, N, integer, seed):
+    """Every rank's output of GEMM+AllReduce is the exact sum of the W products (any M)."""
+    rng = np.random.default_rng(seed)
+    A = [rand_bf16_bits(rng, (M, K), integer) for _ in range(W)]
+    B = [rand_bf16_bits(rng, (K, N), integer) for _ in range(W)]
+    exact = [[Fraction(0)] * N for _ in range(M)]
+    mag = [[Fraction(0)] * N for _ in range(M)]
+    for r in range(W):
+        Aq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in A[r]]
+        Bq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in B[r]]
+        P = brute_gemm(Aq, Bq)
+        for i in range(M):
+            for n in range(N):
+                exact[i][n] += P[i][n]
+                mag[i][n] += sum(abs(Aq[i][k] * Bq[k][n]) for k in range(K))
+    outs = gemm_ar(A, B, "bf16")
+    assert len(outs) == W
+    for o in outs:
+        assert o.shape == (M, N)
+        for i in range(M):
+            for n in range(N):
+                if integer:
+                    assert o[i, n] == exact[i][n]
+                else:
+                    assert abs(Fraction(o[i, n]) - exact[i][n]) <= mag[i][n] * Fraction(W * K + W, 2 ** 52)
+
+
+@pytest.mark.parametrize("W,M", [(1, 3), (2, 3), (3, 5), (4, 2)])
+@pytest.mark.parametrize("integer", [True, False])
+def test_ar_brute_force(W, M, integer):
+    # M = 3, 5, 2 against W = 2, 3, 4: row counts that do not divide among the ranks
+    check_ar_brute(R.gemm_ar, W, M, K=4 + W, N=5, integer=integer, seed=91 + 7 * W + integer)
+
+
+def test_ar_is_reducescatter_then_allgather():
+    # AllReduce = ReduceScatter followed by AllGather of the shards (where M divides by W)
+    wl = workloads.with_shape(workloads.WORKLOADS["rs_w8"], W=4, M=64, K=48, N=40)
+    inp = workloads.make_inputs(wl)
+    outs = R.gemm_ar(inp.a, inp.b)
+    gathered = np.concatenate(R.gemm_rs(inp.a, inp.b))
+    for o in outs:
+        assert np.array_equal(o, gathered)
+    rows = np.array([0, 17, 63])
+    assert np.array_equal(R.gemm_rs_rows(inp.a, inp.b, rows), outs[2][rows])
+
+
+def _mut_ar_one_rank_missing(a, b, dtype="bf16", scale_a=None, scale_b=None):
+    outs = R.gemm_ar(a, b, dtype)
+    outs[-1] = R.gemm_ar(a[:-1], b[:-1], dtype)[0] if len(a) > 1 else outs[-1] * 0
+    return outs
+
+
+def _mut_ar_shard_only(a, b, dtype="bf16", scale_a=None, scale_b=None):
+    S = R.gemm_ar(a, b, dtype)[0]
+    outs = [S.copy() for _ in a]
+    outs[0][1:] = 0          # rank 0 keeps only its own first row, as if the AllGather were skipped
+    return outs
+
+
+@pytest.mark.parametrize("mut", [_mut_ar_one_rank_missing, _mut_ar_shard_only])
+def test_planted_ar_mistakes_are_caught(mut):
+    with pytest.raises(AssertionError):
+        check_ar_brute(mut, 3, 4, 3, 3, True, 5)
+
+
 # ------------------------------------------------------------------ hand-worked fixtures
 
 def _bf16(a):
@@ -405,7 +470,7 @@ def test_planted_format_mistakes_are_caught():
 
 
 def test_oracle_package_exports():
-    for name in ["ag_gemm", "gemm_rs", "round_out", "ag_tile_schedule", "rs_item_schedule"]:
+    for name in ["ag_gemm", "gemm_rs", "gemm_ar", "round_out", "ag_tile_schedule", "rs_item_schedule"]:
         assert hasattr(oracle, name)
 
 

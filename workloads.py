@@ -27,16 +27,17 @@ import torch
 class Workload:
     """One synthetic configuration.
 
-    ``op`` is ``"ag"`` (AllGather+GEMM: W shards of M_local x K, B is K x N, C is (W*M_local) x N)
-    or ``"rs"`` (GEMM+ReduceScatter: W pairs A_r (M x K), B_r (K x N); the output is split into
-    W row shards of (M/W) x N).
+    ``op`` is ``"ag"`` (AllGather+GEMM: W shards of M_local x K, B is K x N, C is (W*M_local) x N),
+    ``"rs"`` (GEMM+ReduceScatter: W pairs A_r (M x K), B_r (K x N); the output is split into
+    W row shards of (M/W) x N) or ``"ar"`` (GEMM+AllReduce: inputs as ``"rs"``, every rank
+    receives the full M x N sum).
     """
 
     name: str
     index: int
     op: str
     W: int
-    M: int            # ag: M_local (rows per shard); rs: M (rows of every A_r)
+    M: int            # ag: M_local (rows per shard); rs, ar: M (rows of every A_r)
     K: int
     N: int
     dtype: str        # "bf16" or "e4m3"
@@ -72,6 +73,8 @@ WORKLOADS = {
     "rs_fp8_w8": Workload("rs_fp8_w8", 6, "rs", W=8, M=8192, K=3584, N=8192, dtype="e4m3", out_dtype="bf16",
                           chunk_rows=0, b_dist=("normal", 1.0),
                           note="W=8, A_r 8192x3584 e4m3, B_r 3584x8192 e4m3, per-tensor scales, bf16 shards"),
+    "ar_w8": Workload("ar_w8", 7, "ar", W=8, M=8192, K=3584, N=8192, dtype="bf16", out_dtype="bf16",
+                      chunk_rows=0, note="W=8, A_r 8192x3584 N(0,1), B_r 3584x8192 N(0,0.02), full sum on every rank"),
     "ag_small": Workload("ag_small", 4, "ag", W=8, M=16, K=8192, N=1024, dtype="bf16",
                          out_dtype="bf16", chunk_rows=16,
                          note="small-M latency: shard 16x8192, B 8192x1024, chunk 16"),
