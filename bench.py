@@ -49,12 +49,17 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+FUSED_KERNEL_SOURCES = ["tdx_api.cu", "tdx_internal.h", "tdx_kernel.cuh", "tdx_kernel_bf16.cu",
+                        "tdx_kernel_fp8.cu", "tdx_ptx.cuh"]
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources of the library (identifies the kernel an ncu capture measured)."""
+    """sha256 over the sources of the fused GEMM kernel and its host launch code (identifies the
+    kernel an ncu capture measured)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "comm_overlapped_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in FUSED_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
@@ -309,20 +314,21 @@ def ag_case(tdx, torch, wl, dev, integer=False):
     return call, status
 
 
-def rs_case(tdx, torch, wl, dev):
+def rs_case(tdx, torch, wl, dev, **kw):
+    """Device buffers + a timed call for one bf16 ReduceScatter workload; ``kw`` are extra options."""
     import workloads as wls
     inp = wls.make_inputs(wl)
     A = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev) for a in inp.a]
     Bs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev) for b in inp.b]
     out = [torch.empty((wl.M // wl.W, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
-    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16),
+    ws = torch.empty(tdx.tdx_workspace_size(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, tdx.make_opts(**kw)),
                      dtype=torch.uint8, device=dev)
     tdx.check(tdx.tdx_workspace_init(ws))
     state = {"epoch": 0}
 
     def call(mode=0, epoch=None):
         state["epoch"] += 1
-        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode)
+        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode, **kw)
         tdx.check(tdx.tdx_gemm_rs(A, Bs, out, ws, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o))
 
     def status():
@@ -436,6 +442,15 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     res["ar_w8"] = {"ms_fused": f, "tflops": tf, "frac_of_peak": tf / peak_bf16,
                     "output_bytes": wl.W * wl.M * wl.N * 2}
     del A, Bs, out, ws
+    # ReduceScatter with bf16 partials (slotted fold of rounded partials: half the slot bytes)
+    call, status = rs_case(tdx, torch, W["rs_w8"], dev, bf16_partials=1)
+    for _ in range(3):
+        call()
+    f = time_mode(torch, call, reps)
+    status()
+    tf = W["rs_w8"].flops / (f * 1e-3) / 1e12
+    res["rs_w8_bf16_partials"] = {"ms_fused": f, "tflops": tf, "frac_of_peak": tf / peak_bf16}
+    del call, status
     call, status = ag_case(tdx, torch, W["ag_small"], dev)
     for _ in range(5):
         call()

@@ -44,6 +44,7 @@ class tdx_opts(ctypes.Structure):
         ("block_n", ctypes.c_int),
         ("reduce_mode", ctypes.c_int),
         ("cluster", ctypes.c_int),
+        ("bf16_partials", ctypes.c_int),
     ]
 
 
@@ -172,11 +173,11 @@ def tdx_workspace_init(workspace, nbytes: int | None = None, stream=None) -> int
 
 PLAN_KEYS = ["BN", "L", "tiles_m", "tiles_n", "T", "num_kb", "chunk_rows", "n_chunks", "off_chunk_flags",
              "off_chunk_cnt", "off_chain_flags", "off_G", "off_S", "total", "reduce_mode", "off_tile_cnt",
-             "cluster", "group_n", "rank_block", "pull_a"]
+             "cluster", "group_n", "rank_block", "pull_a", "partial_bytes"]
 
 
 def tdx_plan_info(op: int, W: int, M_local_or_M: int, K: int, N: int, dtype: int, opts=None) -> dict:
-    info = (ctypes.c_int64 * 20)()
+    info = (ctypes.c_int64 * len(PLAN_KEYS))()
     st = _lib.tdx_plan_info(op, W, M_local_or_M, K, N, dtype, _opts_ref(opts), info)
     if st != TDX_OK:
         raise TdxError(st, "tdx_plan_info")

@@ -40,6 +40,7 @@ tdx_opts defaults() {
   o.block_n = 0;
   o.reduce_mode = 0;
   o.cluster = 0;
+  o.bf16_partials = 0;
   return o;
 }
 
@@ -48,6 +49,7 @@ tdx_opts defaults() {
 struct Plan {
   int op = 0, W = 0, M = 0, M_local = 0, K = 0, N = 0, elt = 2;
   int allreduce = 0;     // op code 2: the ReduceScatter kernel writes every rank's full output
+  int bf16_partials = 0; // slotted partials rounded to bf16
   int BN = 256, L = 1, tiles_m = 0, tiles_n = 0, T = 0, num_kb = 0;
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
@@ -147,9 +149,14 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
   if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
+  if (o.bf16_partials < 0 || o.bf16_partials > 1) return TDX_ERR_INVALID_ARG;
+  // bf16 partials: a rank's partial is rounded before the fold, which the slotted reduction does
+  // (a chained running sum would be rounded at every hand-over instead)
+  if (o.bf16_partials && (op != OP_RS || o.reduce_mode == 1)) return TDX_ERR_UNSUPPORTED;
+  p.bf16_partials = o.bf16_partials;
   if (L > 1) {
     if (o.reduce_mode == 1) p.reduce_last = 0;
-    else if (o.reduce_mode == 2) p.reduce_last = 1;
+    else if (o.reduce_mode == 2 || p.bf16_partials) p.reduce_last = 1;
     else p.reduce_last = (op == OP_AG || p.T < 2 * kRefSMs) ? 1 : 0;
   }
   // slotted ReduceScatter may take a rank-inner order (blocks of one position) instead
@@ -174,7 +181,7 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   if (L > 1) {
     p.off_S = off;
     const size_t slots = p.reduce_last ? static_cast<size_t>(L) : 1;
-    off = align_up(off + slots * static_cast<size_t>(p.T) * kBM * bn * 4, 1024);
+    off = align_up(off + slots * static_cast<size_t>(p.T) * kBM * bn * (p.bf16_partials ? 2 : 4), 1024);
   }
   p.total = off;
   *pl = p;
@@ -499,6 +506,7 @@ tdx_status rs_call(const void* const* A_parts, const void* const* B_parts, void*
   fill_common(kp, pl, o, ws);
   kp.op = OP_RS;
   kp.allreduce = pl.allreduce;
+  kp.bf16_partials = pl.bf16_partials;
   for (int r = 0; r < W; ++r) {
     kp.out[r] = static_cast<uint8_t*>(out_shards[r]);
     const int ks = k_slice_bytes(pl.BN);
@@ -552,10 +560,11 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   Plan pl;
   tdx_status s = make_plan(op, W, M_local_or_M, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const int64_t v[20] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
+  const int64_t v[21] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
-                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, pl.pull_a};
+                         pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, pl.pull_a,
+                         pl.bf16_partials ? 2 : 4};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

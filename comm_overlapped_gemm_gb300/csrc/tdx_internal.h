@@ -86,6 +86,7 @@ struct KParams {
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
   int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
   int allreduce;                 // RS kernel as GEMM+AllReduce: out[r] are full M x N outputs
+  int bf16_partials;        // slotted RS/AR: partials rounded to bf16 in their slots (else fp32)
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;

@@ -344,6 +344,18 @@ __device__ __forceinline__ void pack_bf16x32(const float (&v)[32], uint4 (&pk)[4
   }
 }
 
+// 8 bf16 in a 16-byte word -> 8 fp32 (exact)
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x << 16);
+  f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(u.y << 16);
+  f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(u.z << 16);
+  f[5] = __uint_as_float(u.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(u.w << 16);
+  f[7] = __uint_as_float(u.w & 0xFFFF0000u);
+}
+
 // Store 32 fp32 values (columns col..col+31 of one row starting at orow) rounded once to the
 // output type; columns >= N are skipped.
 __device__ __forceinline__ void store_row_chunk(uint8_t* orow, const KParams& p, int col, const float (&v)[32],
@@ -827,9 +839,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           // slotted partials are folded soon after (keep them in L2); a chained running sum is read
           // by the next element much later
           const uint64_t pol = slotted ? keep_slot : once;
+          if (p.bf16_partials) {
+            // bf16 slot layout: element (row i, col 32*cc + 8*j + t) at bf16 ((cc*4 + j)*128 + i)*8 + t
+            uint4 pk[4];
+            pack_bf16x32(v, pk);
+            uint8_t* bp = reinterpret_cast<uint8_t*>(p.sbuf) + slot * (kBM * BN * 2) +
+                          ((size_t)(col0 >> 5) * 4 * kBM + row_in_tile) * 16;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
+            for (int j = 0; j < 4; ++j) st_v4_hint(bp + j * kBM * 16, pk[j], pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
+          }
         }
         if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
       }
@@ -874,7 +896,47 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ..., two slots' loads in
           // flight at a time
 #pragma unroll 1
-          for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          for (int ch = 0; ch < C::CHUNKS && p.bf16_partials; ++ch) {
+            // bf16 partials: widened exactly to fp32, folded in fp32
+            const int col0 = h * C::COLS_PER_WARP + ch * 32;
+            const size_t off = ((size_t)(col0 >> 5) * 4 * kBM + row_in_tile) * 16;
+            const uint8_t* base = reinterpret_cast<const uint8_t*>(p.sbuf) + (size_t)w.tile * (kBM * BN * 2) + off;
+            const size_t slot_stride = (size_t)p.T * (kBM * BN * 2);
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) unpack_bf16x8(ld_cg_v4_hint(base + j * kBM * 16, once), v + 8 * j);
+            int c = 1;
+#pragma unroll 1
+            for (; c + 1 < p.L; c += 2) {
+              const uint8_t* b0 = base + (size_t)c * slot_stride;
+              uint4 u0[4], u1[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                u0[j] = ld_cg_v4_hint(b0 + j * kBM * 16, once);
+                u1[j] = ld_cg_v4_hint(b0 + slot_stride + j * kBM * 16, once);
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float f0[8], f1[8];
+                unpack_bf16x8(u0[j], f0);
+                unpack_bf16x8(u1[j], f1);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[8 * j + t] = (v[8 * j + t] + f0[t]) + f1[t];
+              }
+            }
+            if (c < p.L) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float f0[8];
+                unpack_bf16x8(ld_cg_v4_hint(base + (size_t)c * slot_stride + j * kBM * 16, once), f0);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[8 * j + t] = v[8 * j + t] + f0[t];
+              }
+            }
+            store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
+          }
+#pragma unroll 1
+          for (int ch = 0; ch < C::CHUNKS && !p.bf16_partials; ++ch) {
             const int col0 = h * C::COLS_PER_WARP + ch * 32;
             const size_t off = ((size_t)(col0 >> 5) * 8 * kBM + row_in_tile) * 4;
             float v[32];
@@ -922,9 +984,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             // every slot of this tile is dead now: drop the lines from L2
             named_bar_sync(1, kEpiThreads);
             const int et = threadIdx.x - kEpiWarp0 * 32;
+            const size_t sbytes = (size_t)kBM * BN * (p.bf16_partials ? 2 : 4);
             for (int c = 0; c < p.L; ++c)
-              for (int l = et; l < 4 * BN; l += kEpiThreads)
-                discard_l2_line(p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + (size_t)l * 32);
+              for (int l = et; l < (int)(sbytes / 128); l += kEpiThreads)
+                discard_l2_line(reinterpret_cast<uint8_t*>(p.sbuf) + ((size_t)c * p.T + w.tile) * sbytes + (size_t)l * 128);
           }
         }
       }

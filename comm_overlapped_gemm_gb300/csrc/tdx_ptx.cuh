@@ -211,6 +211,14 @@ __device__ __forceinline__ float4 ld_cg_f4_hint(const void* p, uint64_t pol) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint4 ld_cg_v4_hint(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_v4_hint(void* p, uint4 v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(pol)

@@ -96,6 +96,11 @@ typedef struct tdx_opts {
                                 3 = pairs running one 2-SM MMA stream on a 256 x 256 tile (each CTA
                                 stages its 128 rows of A and half of B). 2 and 3 need tile width 256
                                 and an even number of 128-row M-tiles. */
+  int bf16_partials;         /* ReduceScatter / AllReduce: 0 (default) = each rank's partial enters
+                                the fold in fp32; 1 = each partial is rounded once to bf16 (RNE, the
+                                type a rank would send) before the fp32 fold, which halves the
+                                partial-slot traffic. Needs the slotted reduction (reduce_mode 0 or 2);
+                                AllGather: must be 0. */
 } tdx_opts;
 
 /* Fill *opts with the defaults above. Returns TDX_ERR_INVALID_ARG if opts is NULL. */
@@ -202,7 +207,7 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
                                   uint32_t* detail);
 
 /* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
- * uses. Writes 20 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
+ * uses. Writes 21 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
  * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] K blocks (64 bytes of K for BN = 256, else 128), [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
@@ -214,7 +219,8 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * (positions count tiles, or tile pairs when [16] >= 2), [19] 1 if AllGather tiles read A straight
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
  * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
- * its flags), else 0. */
+ * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
+ * 2 bf16 partials). */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -19,6 +19,10 @@ reach is the plain definition:
   ``[j*M/W, (j+1)*M/W)`` of S, rounded once to bf16.
 * GEMM+AllReduce (AllReduce is listed among the chunked collectives in "DITRON adds three levels of
   tiling"): every rank receives the whole of the same S, rounded once to bf16; M is any size.
+* Both with ``partials="bf16"``: every rank's partial ``P_r = s_r * A_r @ B_r`` is first rounded to
+  bf16 (the type a rank would put on the wire), then the rounded partials are summed exactly and
+  the sum rounded once more to bf16. The pages do not say in which type partials travel; fp32 is
+  the default reading and bf16 the variant real ReduceScatters send.
 
 Where the pages are silent this file takes the plainest reading: inputs are decoded exactly to
 fp64, products and sums are fp64 (a library fp64 matmul serves as the GEMM step; on the integer
@@ -155,9 +159,20 @@ def ag_gemm_rows(shards, b, rows, dtype: str = "bf16", scale_a=None, scale_b=Non
 # ----------------------------------------------------------------------------------------------
 
 
-def gemm_rs(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None):
+def _partial(P: np.ndarray, partials: str) -> np.ndarray:
+    """A rank's partial as it enters the sum: exact (``"fp32"``: the kernels keep it in fp32, and
+    the fp64 value is the exact one it approximates) or rounded once to bf16 (``"bf16"``)."""
+    if partials == "fp32":
+        return P
+    if partials == "bf16":
+        return decode_bf16(round_bf16_rne(P))
+    raise ValueError(partials)
+
+
+def gemm_rs(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None, partials: str = "fp32"):
     """GEMM+ReduceScatter, unrounded fp64: ``S = sum_r s_r * A_r @ B_r`` (ascending r), returned
-    as the list of W row shards ``S[j*M/W:(j+1)*M/W]``. ``s_r = scale_a[r]*scale_b[r]`` (None = 1)."""
+    as the list of W row shards ``S[j*M/W:(j+1)*M/W]``. ``s_r = scale_a[r]*scale_b[r]`` (None = 1).
+    ``partials="bf16"`` rounds every term of the sum to bf16 first."""
     W = len(a_parts)
     M = a_parts[0].shape[0]
     if M % W:
@@ -169,26 +184,26 @@ def gemm_rs(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None):
             s *= float(scale_a[r])
         if scale_b is not None:
             s *= float(scale_b[r])
-        P = (decode(a_parts[r], dtype) @ decode(b_parts[r], dtype)) * s
+        P = _partial((decode(a_parts[r], dtype) @ decode(b_parts[r], dtype)) * s, partials)
         S = P if S is None else S + P
     h = M // W
     return [S[j * h:(j + 1) * h] for j in range(W)]
 
 
-def gemm_ar(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None):
+def gemm_ar(a_parts, b_parts, dtype: str = "bf16", scale_a=None, scale_b=None, partials: str = "fp32"):
     """GEMM+AllReduce, unrounded fp64: the full ``S = sum_r s_r * A_r @ B_r`` (ascending r), one
-    entry per rank (every rank holds the same S). ``s_r`` as in :func:`gemm_rs`; M need not be a
-    multiple of W."""
+    entry per rank (every rank holds the same S). ``s_r`` and ``partials`` as in :func:`gemm_rs`;
+    M need not be a multiple of W."""
     W = len(a_parts)
     S = None
     for r in range(W):
         s = (1.0 if scale_a is None else float(scale_a[r])) * (1.0 if scale_b is None else float(scale_b[r]))
-        P = (decode(a_parts[r], dtype) @ decode(b_parts[r], dtype)) * s
+        P = _partial((decode(a_parts[r], dtype) @ decode(b_parts[r], dtype)) * s, partials)
         S = P if S is None else S + P
     return [S.copy() for _ in range(W)]
 
 
-def gemm_rs_rows(a_parts, b_parts, rows, dtype: str = "bf16", scale_a=None, scale_b=None):
+def gemm_rs_rows(a_parts, b_parts, rows, dtype: str = "bf16", scale_a=None, scale_b=None, partials: str = "fp32"):
     """Rows ``rows`` (indices into the M rows of S) of the reduced sum, before scattering."""
     rows = np.asarray(rows, dtype=np.int64)
     S = None
@@ -198,7 +213,7 @@ def gemm_rs_rows(a_parts, b_parts, rows, dtype: str = "bf16", scale_a=None, scal
             s *= float(scale_a[r])
         if scale_b is not None:
             s *= float(scale_b[r])
-        P = (decode(a_parts[r][rows], dtype) @ decode(b_parts[r], dtype)) * s
+        P = _partial((decode(a_parts[r][rows], dtype) @ decode(b_parts[r], dtype)) * s, partials)
         S = P if S is None else S + P
     return S
 

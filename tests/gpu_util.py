@@ -100,13 +100,13 @@ class RSCase:
     def result(self) -> np.ndarray:
         return R.decode_bf16(self.result_bits())
 
-    def oracle(self, rows=None):
+    def oracle(self, rows=None, partials="fp32"):
         i, dt = self.inp, self.wl.dtype
         sa = i.scale_a if dt == "e4m3" else None
         sb = i.scale_b if dt == "e4m3" else None
         if rows is None:
-            return np.concatenate(R.gemm_rs(i.a, i.b, dt, sa, sb))
-        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb)
+            return np.concatenate(R.gemm_rs(i.a, i.b, dt, sa, sb, partials=partials))
+        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb, partials=partials)
 
 
 class ARCase:
@@ -133,13 +133,13 @@ class ARCase:
         torch.cuda.synchronize()
         return host_bits(self.out[rank])
 
-    def oracle(self, rows=None):
+    def oracle(self, rows=None, partials="fp32"):
         i, dt = self.inp, self.wl.dtype
         sa = i.scale_a if dt == "e4m3" else None
         sb = i.scale_b if dt == "e4m3" else None
         if rows is None:
-            return R.gemm_ar(i.a, i.b, dt, sa, sb)[0]
-        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb)
+            return R.gemm_ar(i.a, i.b, dt, sa, sb, partials=partials)[0]
+        return R.gemm_rs_rows(i.a, i.b, rows, dt, sa, sb, partials=partials)
 
 
 def assert_bit_exact(got_bits: np.ndarray, oracle_fp64: np.ndarray, out_dtype: str):

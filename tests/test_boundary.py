@@ -170,6 +170,19 @@ def test_ar_validation_codes(tdx):
     assert ar(wsb=100) == tdx.TDX_ERR_WORKSPACE
     assert ar(W=17, A=[FAKE] * 17, B=[FAKE] * 17, O=[FAKE] * 17) == tdx.TDX_ERR_INVALID_ARG
     assert ar(M=0) == tdx.TDX_OK
+    assert ar(opts=tdx.make_opts(bf16_partials=1, reduce_mode=1)) == tdx.TDX_ERR_UNSUPPORTED
+    assert ar(opts=tdx.make_opts(bf16_partials=2)) == tdx.TDX_ERR_INVALID_ARG
+
+
+def test_bf16_partials_plan(tdx):
+    # the partial slots shrink to half, and the slotted reduction is chosen even for many tiles
+    full = tdx.tdx_plan_info(tdx.OP_RS, 8, 8192, 3584, 8192, tdx.TDX_BF16)
+    half = tdx.tdx_plan_info(tdx.OP_RS, 8, 8192, 3584, 8192, tdx.TDX_BF16, tdx.make_opts(bf16_partials=1))
+    assert full["reduce_mode"] == 1 and full["partial_bytes"] == 4
+    assert half["reduce_mode"] == 2 and half["partial_bytes"] == 2
+    assert half["total"] - half["off_S"] == 8 * half["T"] * 128 * half["BN"] * 2
+    with pytest.raises(tdx.TdxError):
+        tdx.tdx_workspace_size(tdx.OP_AG, 2, 64, 128, 256, tdx.TDX_BF16, tdx.make_opts(bf16_partials=1))
 
 
 def test_trace_size(tdx):

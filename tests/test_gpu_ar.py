@@ -141,3 +141,18 @@ def test_ar_modes_run():
         status_ok(case)
     assert_bit_exact(case.result_bits(2), R.gemm_ar(inp.a, inp.b)[2], "bf16")
     assert host_bits(case.out[0]).shape == (512, 512)
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_ar_bf16_partials(integer):
+    wl = wls.with_shape(wls.WORKLOADS["ar_w8"], W=4, M=300, K=1024, N=512)
+    inp = wls.make_inputs(wl, integer=integer)
+    case = ARCase(inp, opts=opts(bf16_partials=1))
+    tdx.check(case.run())
+    status_ok(case)
+    want = case.oracle(partials="bf16")
+    if integer:
+        assert_bit_exact(case.result_bits(2), want, "bf16")
+    else:
+        assert_within_tol(R.decode_bf16(case.result_bits(2)), want, "bf16")
+    all_ranks_identical(case)

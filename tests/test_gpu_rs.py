@@ -278,3 +278,78 @@ def test_rs_e4m3_full_size_sampled_and_deterministic():
     assert_within_tol(R.decode_bf16(first[rows]), case.oracle(rows), "e4m3")
     tdx.check(case.run(opts(scale_a=inp.scale_a, scale_b=inp.scale_b, perturb_seed=3)))
     assert np.array_equal(case.result_bits(), first)
+
+
+# ------------------------------------------------------------------ bf16 partials
+
+
+@pytest.mark.parametrize("shape", [
+    dict(W=2, M=256, K=256, N=512),
+    dict(W=3, M=384, K=200, N=136),
+    dict(W=4, M=200, K=64, N=264),
+    dict(W=8, M=1024, K=512, N=1024),
+])
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_bf16_partials(shape, integer):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    for bn in (0, 256):
+        case = RSCase(inp, opts=opts(bf16_partials=1, block_n=bn))
+        plan = tdx.tdx_plan_info(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, case.opts)
+        assert plan["partial_bytes"] == 2 and plan["reduce_mode"] == 2
+        tdx.check(case.run())
+        status_ok(case)
+        want = case.oracle(partials="bf16")
+        if integer:
+            assert_bit_exact(case.result_bits(), want, "bf16")
+        else:
+            assert_within_tol(case.result(), want, "bf16")
+            # the rounded partials stay close to the fp32-partial result too
+            assert_within_tol(case.result(), case.oracle(), "bf16")
+
+
+def test_rs_bf16_partial_slots_hold_rounded_partials():
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=1024, N=512)
+    inp = wls.make_inputs(wl, integer=True)      # partials up to 16384: many need rounding in bf16
+    o = opts(bf16_partials=1, block_n=128, epoch=4)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 1024, 512, tdx.TDX_BF16, o)
+    case = RSCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(partials="bf16"), "bf16")
+    T, BN = plan["T"], plan["BN"]
+    S = case.ws[plan["off_S"]:plan["off_S"] + 2 * 4 * T * 128 * BN].view(torch.int16).cpu().numpy().view(np.uint16)
+    for r in (0, 3):
+        P = R.gemm_rs_rows([inp.a[r]], [inp.b[r]], np.arange(512), "bf16")
+        want = R.round_bf16_rne(P)
+        for (mt, nt) in [(0, 0), (3, 2)]:
+            tile = mt * plan["tiles_n"] + nt
+            blk = S[(r * T + tile) * 128 * BN:(r * T + tile + 1) * 128 * BN]
+            # layout: ((cc*4 + j)*128 + i)*8 + t  ->  element (i, 32*cc + 8*j + t)
+            blk = blk.reshape(BN // 32, 4, 128, 8).transpose(2, 0, 1, 3).reshape(128, BN)
+            assert np.array_equal(blk, want[mt * 128:(mt + 1) * 128, nt * BN:(nt + 1) * BN])
+
+
+def test_rs_bf16_partials_full_size_sampled_and_deterministic():
+    wl = wls.WORKLOADS["rs_w8"]
+    inp = wls.make_inputs(wl, integer=False)
+    case = RSCase(inp, opts=opts(bf16_partials=1))
+    tdx.check(case.run())
+    status_ok(case)
+    rows = sample_rows(wl.M, wl.M // wl.W)
+    first = case.result_bits()
+    assert_within_tol(R.decode_bf16(first[rows]), case.oracle(rows, partials="bf16"), "bf16")
+    for o in case.out:
+        o.fill_(float("nan"))
+    tdx.check(case.run(opts(bf16_partials=1, perturb_seed=21)))
+    status_ok(case)
+    assert np.array_equal(case.result_bits(), first)
+
+
+def test_rs_e4m3_bf16_partials():
+    wl = wls.with_shape(wls.WORKLOADS["rs_fp8_w8"], W=4, M=512, K=1024, N=1024)
+    inp = wls.make_inputs(wl, integer=True)
+    case = RSCase(inp, opts=opts(scale_a=inp.scale_a, scale_b=inp.scale_b, bf16_partials=1))
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(partials="bf16"), "bf16")

@@ -198,6 +198,126 @@ def check_golden_rs(gemm_rs, golden):
             assert np.array_equal(got[j], np.asarray(want, dtype=np.float64))
 
 
+def test_golden_rs_bf16_partials(golden):
+    ex = golden["gemm_rs_bf16_partials"]
+    A = [_bf16(a) for a in ex["A"]]
+    B = [_bf16(b) for b in ex["B"]]
+    for mode, key in (("fp32", "out_fp32_partials"), ("bf16", "out_bf16_partials")):
+        got = R.gemm_rs(A, B, "bf16", partials=mode)
+        for j, want in enumerate(ex[key]):
+            assert np.array_equal(R.decode_bf16(R.round_out(got[j], "bf16")), np.asarray(want, dtype=np.float64))
+    ar = R.gemm_ar(A, B, "bf16", partials="bf16")
+    assert R.decode_bf16(R.round_out(ar[1], "bf16"))[0, 0] == 256
+
+
+def fraction_to_bf16(x: Fraction) -> Fraction:
+    """Round an exact rational to the nearest bf16 value, ties to an even significand (8 significant
+    bits), by exact rational arithmetic: an independent restatement for the pins."""
+    if x == 0:
+        return Fraction(0)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = 0
+    while a >= 2:
+        a /= 2
+        e += 1
+    while a < 1:
+        a *= 2
+        e -= 1
+    e = max(e, -126)                       # subnormals share the smallest exponent's spacing
+    ulp = Fraction(2) ** (e - 7)
+    q = abs(x) / ulp
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def test_fraction_bf16_rounding_agrees_with_torch():
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 6, 2000),
+                        np.arange(250, 270, dtype=np.float64)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    for xi, wi in zip(x, want):
+        assert fraction_to_bf16(Fraction(float(xi))) == Fraction(float(wi))
+
+
+def check_rs_bf16_partials_brute(gemm_rs, W, seed):
+    rng = np.random.default_rng(seed)
+    M, K, N = W, 3, 4
+    A = [rand_bf16_bits(rng, (M, K), False) for _ in range(W)]
+    B = [rand_bf16_bits(rng, (K, N), False) for _ in range(W)]
+    exact = [[Fraction(0)] * N for _ in range(M)]
+    for r in range(W):
+        Aq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in A[r]]
+        Bq = [[bf16_bits_to_fraction(int(v)) for v in row] for row in B[r]]
+        P = brute_gemm(Aq, Bq)
+        for i in range(M):
+            for n in range(N):
+                exact[i][n] += fraction_to_bf16(P[i][n])
+    shards = gemm_rs(A, B, "bf16", partials="bf16")
+    for j in range(W):
+        for n in range(N):
+            # the sum of W bf16 values is exact in fp64 here (few terms, close exponents)
+            assert Fraction(shards[j][0, n]) == exact[j][n]
+    # the final rounding of the exact sum, also by the independent rule
+    out = R.decode_bf16(R.round_out(np.concatenate(shards), "bf16"))
+    for i in range(M):
+        for n in range(N):
+            assert Fraction(out[i, n]) == fraction_to_bf16(exact[i][n])
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_rs_bf16_partials_brute_force(W):
+    check_rs_bf16_partials_brute(R.gemm_rs, W, 500 + W)
+    check_rs_bf16_partials_brute(
+        lambda a, b, dt, partials: [R.gemm_ar(a, b, dt, partials=partials)[W - 1][j:j + 1] for j in range(W)],
+        W, 600 + W)
+
+
+def test_bf16_partials_equal_fp32_when_partials_are_representable():
+    wl = workloads.with_shape(workloads.WORKLOADS["rs_w8"], W=4, M=8, K=2, N=8)
+    inp = workloads.make_inputs(wl, integer=True)     # |P_r| <= 32: every integer partial fits bf16
+    a = np.concatenate(R.gemm_rs(inp.a, inp.b, partials="fp32"))
+    b = np.concatenate(R.gemm_rs(inp.a, inp.b, partials="bf16"))
+    assert np.array_equal(a, b)
+    rows = np.array([1, 6])
+    assert np.array_equal(R.gemm_rs_rows(inp.a, inp.b, rows, partials="bf16"), b[rows])
+
+
+def _mut_round_running_sum(a, b, dtype="bf16", partials="fp32"):
+    # a ring's rounding: the running sum is rounded at every hand-over instead of each partial
+    S = None
+    for r in range(len(a)):
+        P = R.decode(a[r], dtype) @ R.decode(b[r], dtype)
+        S = P if S is None else S + P
+        S = R.decode_bf16(R.round_bf16_rne(S))
+    h = S.shape[0] // len(a)
+    return [S[j * h:(j + 1) * h] for j in range(len(a))]
+
+
+def _mut_truncated_partials(a, b, dtype="bf16", partials="fp32"):
+    S = None
+    for r in range(len(a)):
+        P = (R.decode(a[r], dtype) @ R.decode(b[r], dtype)).astype(np.float32)
+        P = (P.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+        S = P if S is None else S + P
+    h = S.shape[0] // len(a)
+    return [S[j * h:(j + 1) * h] for j in range(len(a))]
+
+
+def _mut_fp32_partials(a, b, dtype="bf16", partials="fp32"):
+    return R.gemm_rs(a, b, dtype)
+
+
+@pytest.mark.parametrize("mut", [_mut_round_running_sum, _mut_truncated_partials, _mut_fp32_partials])
+def test_planted_partial_rounding_mistakes_are_caught(mut):
+    with pytest.raises(AssertionError):
+        for seed in range(5):
+            check_rs_bf16_partials_brute(mut, 3, 700 + seed)
+
+
 def test_golden_ag(golden):
     check_golden_ag(R.ag_gemm, golden)
 
