@@ -1,4 +1,5 @@
-"""CPU oracle for tile-pipelined AllGather+GEMM and GEMM+ReduceScatter.
+"""CPU oracle for tile-pipelined AllGather+GEMM, GEMM+ReduceScatter / AllReduce and the
+AllToAll-overlapped grouped GEMM of a mixture-of-experts layer (``moe.py``).
 
 TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
@@ -7,7 +8,8 @@ helpers, tables or constants); both sides take their inputs from ``workloads.py`
 none of the method's arithmetic.
 
 The oracle computes what the overlapped kernels must produce, written as the plain definition in
-fp64 (see ``reference.py``). Every function there is pinned by ``tests/test_oracle.py`` against
+fp64 (see ``reference.py`` and ``moe.py``). Every function there is pinned by
+``tests/test_oracle.py`` / ``tests/test_oracle_moe.py`` against
 brute force in exact rational arithmetic, closed forms, the identity-matrix special cases, a
 hand-worked fixture and library routines (torch's bf16 and e4m3 casts).
 """

@@ -29,8 +29,11 @@ class Workload:
 
     ``op`` is ``"ag"`` (AllGather+GEMM: W shards of M_local x K, B is K x N, C is (W*M_local) x N),
     ``"rs"`` (GEMM+ReduceScatter: W pairs A_r (M x K), B_r (K x N); the output is split into
-    W row shards of (M/W) x N) or ``"ar"`` (GEMM+AllReduce: inputs as ``"rs"``, every rank
-    receives the full M x N sum).
+    W row shards of (M/W) x N), ``"ar"`` (GEMM+AllReduce: inputs as ``"rs"``, every rank
+    receives the full M x N sum), ``"moe"`` (AllToAll dispatch + grouped GEMM: rank s holds M
+    tokens X_s (M x K) routed to ``topk`` of E experts, expert weights E x K x N) or
+    ``"moe_combine"`` (grouped GEMM + AllToAll combine: the dispatched rows (W*M*topk x K) times
+    expert weights E x K x N, summed back per token with the gates).
     """
 
     name: str
@@ -46,16 +49,21 @@ class Workload:
     a_dist: tuple = ("normal", 1.0)
     b_dist: tuple = ("normal", 0.02)
     note: str = ""
+    E: int = 0        # moe: experts (a multiple of W)
+    topk: int = 0     # moe: experts per token
 
     @property
     def M_total(self) -> int:
+        if self.op in ("moe", "moe_combine"):
+            return self.W * self.M * self.topk
         return self.W * self.M if self.op == "ag" else self.M
 
     @property
     def flops(self) -> float:
-        """Algorithmic FLOP of one call: 2*M*N*K summed over the GEMMs the op defines."""
-        if self.op == "ag":
-            return 2.0 * self.W * self.M * self.N * self.K
+        """Algorithmic FLOP of one call: 2*M*N*K summed over the GEMMs the op defines (moe: one
+        GEMM row per routed token-expert pair)."""
+        if self.op in ("moe", "moe_combine"):
+            return 2.0 * self.M_total * self.N * self.K
         return 2.0 * self.W * self.M * self.N * self.K
 
 
@@ -75,6 +83,17 @@ WORKLOADS = {
                           note="W=8, A_r 8192x3584 e4m3, B_r 3584x8192 e4m3, per-tensor scales, bf16 shards"),
     "ar_w8": Workload("ar_w8", 7, "ar", W=8, M=8192, K=3584, N=8192, dtype="bf16", out_dtype="bf16",
                       chunk_rows=0, note="W=8, A_r 8192x3584 N(0,1), B_r 3584x8192 N(0,0.02), full sum on every rank"),
+    "moe_w8": Workload("moe_w8", 8, "moe", W=8, M=4096, K=7168, N=2048, dtype="bf16", out_dtype="bf16",
+                       chunk_rows=128, E=64, topk=8,
+                       note="W=8, 4096 tokens/rank of 7168, top-8 of 64 experts (8 per rank), expert weights "
+                            "7168x2048 N(0,0.02); 262144 dispatched rows"),
+    "moe_w8_decode": Workload("moe_w8_decode", 9, "moe", W=8, M=128, K=7168, N=2048, dtype="bf16",
+                              out_dtype="bf16", chunk_rows=128, E=64, topk=8,
+                              note="W=8, 128 tokens/rank, top-8 of 64 experts; 8192 dispatched rows"),
+    "moe_combine_w8": Workload("moe_combine_w8", 10, "moe_combine", W=8, M=4096, K=2048, N=7168, dtype="bf16",
+                               out_dtype="bf16", chunk_rows=128, E=64, topk=8,
+                               note="W=8, 262144 dispatched rows of 2048, expert weights 2048x7168, combined "
+                                    "back to 4096x7168 per rank with top-8 gates"),
     "ag_small": Workload("ag_small", 4, "ag", W=8, M=16, K=8192, N=1024, dtype="bf16",
                          out_dtype="bf16", chunk_rows=16,
                          note="small-M latency: shard 16x8192, B 8192x1024, chunk 16"),
@@ -86,6 +105,12 @@ WORKLOADS = {
 
 def seed_for(wl: Workload, rank: int, is_b: bool) -> int:
     return 20260 + 100 * wl.index + rank + (50 if is_b else 0)
+
+
+def route_seed_for(wl: Workload, rank: int) -> int:
+    """Seed of rank ``rank``'s routing scores (moe). Expert e's weights use
+    ``20260 + 100*index + 50 + 1000*(e + 1)``."""
+    return 20260 + 100 * wl.index + 25 + rank
 
 
 def _draw(rng: np.random.Generator, shape, dist, integer: bool) -> np.ndarray:
@@ -125,6 +150,9 @@ class Inputs:
     rs: ``a[r]`` is A_r (M x K), ``b[r]`` is B_r (K x N).
     bf16 tensors are uint16 bit patterns, e4m3 tensors uint8 codes; ``scale_a[r]``/``scale_b[r]``
     are the per-tensor dequantisation scales (1.0 for bf16 or integer mode).
+    moe: ``a[s]`` X_s (M x K) for "moe" / the dispatched rows (W*M*topk x K, one array) for
+    "moe_combine"; ``b[0]`` the E x K x N expert weights; ``route[s]`` int32 (M x topk) expert ids
+    and ``gates[s]`` fp32 (M x topk) gate weights of rank s's tokens.
     """
 
     wl: Workload
@@ -133,6 +161,8 @@ class Inputs:
     b: list = field(default_factory=list)
     scale_a: list = field(default_factory=list)
     scale_b: list = field(default_factory=list)
+    route: list = field(default_factory=list)
+    gates: list = field(default_factory=list)
 
 
 def make_inputs(wl: Workload, integer: bool = False, shape_override: dict | None = None) -> Inputs:
@@ -143,6 +173,8 @@ def make_inputs(wl: Workload, integer: bool = False, shape_override: dict | None
     """
     if shape_override:
         wl = Workload(**{**wl.__dict__, **shape_override})
+    if wl.op in ("moe", "moe_combine"):
+        return _make_moe_inputs(wl, integer)
     out = Inputs(wl=wl, integer=integer)
     nb = 1 if wl.op == "ag" else wl.W
     for r in range(wl.W):
@@ -171,3 +203,56 @@ def make_inputs(wl: Workload, integer: bool = False, shape_override: dict | None
 def with_shape(wl: Workload, **kw) -> Workload:
     """A copy of ``wl`` with some of W/M/K/N/chunk_rows replaced (same seeds and recipe)."""
     return Workload(**{**wl.__dict__, **kw})
+
+
+def make_routing(wl: Workload, integer: bool = False):
+    """Seeded top-k routing of every rank's tokens: each token draws E standard-normal scores (a
+    stand-in for router logits) and picks the ``topk`` largest (descending score; ties cannot occur
+    with continuous draws). Gates are the softmax of the chosen scores (fp32), or in integer mode
+    powers of two drawn from {1/4, 1/2, 1, 2} (exact products). Returns (route, gates): lists of W
+    arrays (M x topk), int32 and fp32."""
+    route, gates = [], []
+    for s in range(wl.W):
+        rng = np.random.Generator(np.random.PCG64(route_seed_for(wl, s)))
+        scores = rng.standard_normal(size=(wl.M, wl.E), dtype=np.float32)
+        idx = np.argsort(-scores, axis=1, kind="stable")[:, :wl.topk].astype(np.int32)
+        top = np.take_along_axis(scores, idx, axis=1).astype(np.float64)
+        if integer:
+            g = (2.0 ** rng.integers(-2, 2, size=idx.shape)).astype(np.float32)
+        else:
+            ex = np.exp(top - top.max(axis=1, keepdims=True))
+            g = (ex / ex.sum(axis=1, keepdims=True)).astype(np.float32)
+        route.append(np.ascontiguousarray(idx))
+        gates.append(np.ascontiguousarray(g))
+    return route, gates
+
+
+def _cast(x: np.ndarray, dtype: str, integer: bool):
+    if dtype == "bf16":
+        return to_bf16_bits(x), 1.0
+    if integer:
+        return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy(), 1.0
+    return quantize_e4m3(x)
+
+
+def _make_moe_inputs(wl: Workload, integer: bool) -> Inputs:
+    out = Inputs(wl=wl, integer=integer)
+    out.route, out.gates = make_routing(wl, integer)
+    if wl.op == "moe":
+        for s in range(wl.W):
+            rng = np.random.Generator(np.random.PCG64(seed_for(wl, s, False)))
+            q, sc = _cast(_draw(rng, (wl.M, wl.K), wl.a_dist, integer), wl.dtype, integer)
+            out.a.append(q); out.scale_a.append(sc)
+    else:
+        rng = np.random.Generator(np.random.PCG64(seed_for(wl, 0, False)))
+        q, sc = _cast(_draw(rng, (wl.M_total, wl.K), wl.a_dist, integer), wl.dtype, integer)
+        out.a.append(q); out.scale_a.append(sc)
+    dt = np.uint16 if wl.dtype == "bf16" else np.uint8
+    b = np.empty((wl.E, wl.K, wl.N), dtype=dt)
+    for e in range(wl.E):
+        rng = np.random.Generator(np.random.PCG64(20260 + 100 * wl.index + 50 + 1000 * (e + 1)))
+        q, sc = _cast(_draw(rng, (wl.K, wl.N), wl.b_dist, integer), wl.dtype, integer)
+        b[e] = q
+        out.scale_b.append(sc)
+    out.b.append(b)
+    return out
