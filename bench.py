@@ -338,6 +338,33 @@ def rs_case(tdx, torch, wl, dev, **kw):
     return call, status
 
 
+def moe_case(tdx, torch, wl, dev):
+    """Device buffers + a timed call for one MoE dispatch + grouped GEMM workload."""
+    import workloads as wls
+    inp = wls.make_inputs(wl)
+    X = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev) for a in inp.a]
+    route = [torch.from_numpy(np.ascontiguousarray(r)).to(dev) for r in inp.route]
+    B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(np.int16)).to(dev)
+    Y = torch.empty((wl.M_total, wl.N), dtype=torch.bfloat16, device=dev)
+    dest = torch.empty((wl.W, wl.M, wl.topk), dtype=torch.int32, device=dev)
+    ws = torch.empty(tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    state = {"epoch": 0}
+
+    def call(mode=0, epoch=None):
+        state["epoch"] += 1
+        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode)
+        tdx.check(tdx.tdx_moe_dispatch_gemm(X, route, B, Y, dest, None, ws, wl.W, wl.M, wl.K, wl.N, wl.E,
+                                            wl.topk, tdx.TDX_BF16, o))
+
+    def status():
+        st, d = tdx.tdx_read_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    return call, status
+
+
 def graph_time_us(torch, fn, reps: int = 50):
     """GPU time per call (us) of fn captured in a CUDA graph of `reps` back-to-back calls (no host
     submission cost inside the timed region); None if the call cannot be captured."""
@@ -450,6 +477,34 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     status()
     tf = W["rs_w8"].flops / (f * 1e-3) / 1e12
     res["rs_w8_bf16_partials"] = {"ms_fused": f, "tflops": tf, "frac_of_peak": tf / peak_bf16}
+    del call, status
+    # MoE AllToAll dispatch + grouped GEMM: fused, GEMM alone (receive buffer already filled), dispatch alone
+    wl = W["moe_w8"]
+    call, status = moe_case(tdx, torch, wl, dev)
+    for _ in range(3):
+        call()
+    f = time_mode(torch, call, reps)
+    m = time_mode(torch, lambda: call(mode=2), reps)
+    g = time_mode(torch, lambda: call(mode=1), reps)
+    status()
+    tf = wl.flops / (f * 1e-3) / 1e12
+    moved = 2 * wl.M_total * wl.K * 2                       # dispatched rows read + written
+    res["moe_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
+                     "tflops": tf, "frac_of_peak": tf / peak_bf16, "dispatch_bytes": moved,
+                     "dispatch_gbs_alone": moved / (m * 1e-3) / 1e9}
+    del call, status
+    wl = W["moe_w8_decode"]
+    call, status = moe_case(tdx, torch, wl, dev)
+    for _ in range(5):
+        call()
+    f = time_mode(torch, call, reps)
+    gus = graph_time_us(torch, lambda: call(epoch=0))
+    status()
+    byt = wl.E * wl.K * wl.N * 2 + 2 * wl.M_total * wl.K * 2 + wl.M_total * wl.N * 2   # weights, dispatch r+w, Y
+    t_us = gus or 1e3 * f
+    res["moe_w8_decode"] = {"us_call": 1e3 * f, "us_gpu_graph": gus, "algorithmic_bytes": byt,
+                            "tflops": wl.flops / (t_us * 1e-6) / 1e12,
+                            "hbm_frac": byt / (t_us * 1e-6) / 1e9 / hbm_gbs}
     del call, status
     call, status = ag_case(tdx, torch, W["ag_small"], dev)
     for _ in range(5):

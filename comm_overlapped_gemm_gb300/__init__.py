@@ -23,7 +23,8 @@ OP_AG, OP_RS, OP_AR = 0, 1, 2
 
 EXPORTED = ["tdx_opts_default", "tdx_workspace_size", "tdx_workspace_init", "tdx_ag_gemm", "tdx_gemm_rs",
             "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info",
-            "tdx_ag_gemm_noalloc", "tdx_gemm_ar"]
+            "tdx_ag_gemm_noalloc", "tdx_gemm_ar", "tdx_moe_workspace_size", "tdx_moe_plan_info",
+            "tdx_moe_dispatch_gemm"]
 
 
 class tdx_opts(ctypes.Structure):
@@ -74,6 +75,9 @@ def _load():
         "tdx_version": (U32, []),
         "tdx_plan_info": (I, [I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
         "tdx_ag_gemm_noalloc": (I, [PP, P, P, I, I, I, I, I, OP, P, P]),
+        "tdx_moe_workspace_size": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(SZ)]),
+        "tdx_moe_plan_info": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
+        "tdx_moe_dispatch_gemm": (I, [PP, PP, P, P, P, P, P, SZ, I, I, I, I, I, I, I, OP, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -230,3 +234,33 @@ def check(status: int, what: str = "tdx") -> None:
     """Raise TdxError unless status is TDX_OK."""
     if status != TDX_OK:
         raise TdxError(status, what)
+
+
+# ------------------------------------------------------------------ mixture-of-experts dispatch
+MOE_PLAN_KEYS = ["BN", "tiles_n", "max_tiles", "n_chunks", "total_rows", "off_chunk_flags", "off_ntiles",
+                 "off_offsets", "off_src", "off_tiles", "off_R", "total", "num_kb"]
+
+
+def tdx_moe_workspace_size(W: int, T: int, H: int, F: int, E: int, topk: int, dtype: int, opts=None) -> int:
+    out = ctypes.c_size_t(0)
+    st = _lib.tdx_moe_workspace_size(W, T, H, F, E, topk, dtype, _opts_ref(opts), ctypes.byref(out))
+    if st != TDX_OK:
+        raise TdxError(st, "tdx_moe_workspace_size")
+    return int(out.value)
+
+
+def tdx_moe_plan_info(W: int, T: int, H: int, F: int, E: int, topk: int, dtype: int, opts=None) -> dict:
+    info = (ctypes.c_int64 * len(MOE_PLAN_KEYS))()
+    st = _lib.tdx_moe_plan_info(W, T, H, F, E, topk, dtype, _opts_ref(opts), info)
+    if st != TDX_OK:
+        raise TdxError(st, "tdx_moe_plan_info")
+    return {k: int(info[i]) for i, k in enumerate(MOE_PLAN_KEYS)}
+
+
+def tdx_moe_dispatch_gemm(X, topk_idx, B_experts, Y, dest, expert_offsets, workspace, W: int, T: int, H: int,
+                          F: int, E: int, topk: int, dtype: int, opts=None, stream=None,
+                          workspace_bytes: int | None = None) -> int:
+    wsb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    return int(_lib.tdx_moe_dispatch_gemm(_ptr_array(X), _ptr_array(topk_idx), _ptr(B_experts), _ptr(Y), _ptr(dest),
+                                          _ptr(expert_offsets), _ptr(workspace), wsb, W, T, H, F, E, topk, dtype,
+                                          _opts_ref(opts), _stream(stream)))

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libtdx.so")
-SOURCES = ["tdx_api.cu", "tdx_kernel_bf16.cu", "tdx_kernel_fp8.cu"]
+SOURCES = ["tdx_api.cu", "tdx_kernel_bf16.cu", "tdx_kernel_fp8.cu", "tdx_moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]

@@ -656,3 +656,226 @@ const char* tdx_status_string(tdx_status s) {
 uint32_t tdx_version(void) { return kVersion; }
 
 }  // extern "C"
+
+// ================================================================================================
+// Mixture-of-experts AllToAll dispatch + grouped GEMM
+// ================================================================================================
+namespace {
+
+struct MoePlan {
+  int W = 0, T = 0, H = 0, F = 0, E = 0, k = 0, BN = 0, tiles_n = 0, num_kb = 0;
+  long long total = 0;              // dispatched rows = W * T * k
+  int n_chunks = 0, max_tiles = 0;  // 128-row chunks of the receive buffer; tile-table bound
+  size_t off_flags = 0, off_cnt = 0, off_ntiles = 0, ctrl_end = 0;
+  size_t off_offsets = 0, off_src = 0, off_tiles = 0, off_R = 0, bytes = 0;
+};
+
+tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dtype, const tdx_opts& o, MoePlan* out) {
+  if (W < 1 || W > kMaxW || T < 0 || H < 0 || F < 0 || E < 1 || k < 1 || k > E) return TDX_ERR_INVALID_ARG;
+  if (E > kMoeMaxExperts) return TDX_ERR_UNSUPPORTED;
+  if (dtype == TDX_FP8_E4M3) return TDX_ERR_UNSUPPORTED;
+  if (dtype != TDX_BF16) return TDX_ERR_INVALID_ARG;
+  if (o.split_k > 1 || o.cluster > 1 || o.bf16_partials != 0 || o.out_dtype != TDX_BF16) return TDX_ERR_UNSUPPORTED;
+  MoePlan p;
+  p.W = W;
+  p.T = T;
+  p.H = H;
+  p.F = F;
+  p.E = E;
+  p.k = k;
+  p.total = static_cast<long long>(W) * T * k;
+  if (p.total > (1ll << 30)) return TDX_ERR_INVALID_ARG;
+  int bn = o.block_n;
+  if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return TDX_ERR_UNSUPPORTED;
+  if (bn == 0) bn = F > 128 ? 256 : (F > 64 ? 128 : 64);
+  p.BN = bn;
+  p.tiles_n = (F + bn - 1) / bn;
+  p.num_kb = static_cast<int>((static_cast<long long>(H) * 2 + 127) / 128);
+  p.n_chunks = static_cast<int>((p.total + kBM - 1) / kBM);
+  p.max_tiles = p.n_chunks + E;     // every expert adds at most one partial tile
+  size_t off = kHeaderBytes;
+  p.off_flags = off;
+  off += static_cast<size_t>(p.n_chunks) * 4;
+  p.off_cnt = off;
+  off += static_cast<size_t>(p.n_chunks) * 4;
+  p.off_ntiles = off;
+  off += 8;
+  p.ctrl_end = off = align_up(off, 1024);
+  p.off_offsets = off;
+  off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
+  p.off_src = off;
+  off = align_up(off + static_cast<size_t>(p.total) * 4, 256);
+  p.off_tiles = off;
+  off = align_up(off + static_cast<size_t>(p.max_tiles) * 16, 1024);
+  p.off_R = off;
+  off = align_up(off + static_cast<size_t>(p.total) * H * 2, 1024);
+  p.bytes = off;
+  *out = p;
+  return TDX_OK;
+}
+
+// 3D map over a stack of `depth` row-major (rows x cols) bf16 matrices; box = box_cols x box_rows x 1,
+// 128-byte swizzle (the same shared-memory image as the 2D box of one matrix).
+bool make_map_3d(CUtensorMap* m, const void* base, long long depth, long long rows, long long cols, int box_cols,
+                 int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(depth)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(rows * cols) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+tdx_status tdx_moe_workspace_size(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype, const tdx_opts* opts,
+                                  size_t* bytes) {
+  if (bytes == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, H, F, E, topk, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  *bytes = pl.bytes;
+  return TDX_OK;
+}
+
+tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype, const tdx_opts* opts,
+                             int64_t* info) {
+  if (info == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, H, F, E, topk, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  const int64_t v[13] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
+                         (int64_t)pl.off_ntiles, (int64_t)pl.off_offsets, (int64_t)pl.off_src, (int64_t)pl.off_tiles,
+                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb};
+  std::memcpy(info, v, sizeof(v));
+  return TDX_OK;
+}
+
+tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* topk_idx, const void* B_experts, void* Y,
+                                 int32_t* dest, int32_t* expert_offsets, void* workspace, size_t workspace_bytes, int W,
+                                 int T, int H, int F, int E, int topk, tdx_dtype dtype, const tdx_opts* opts,
+                                 void* stream) {
+  const tdx_opts o = opts ? *opts : defaults();
+  if (X == nullptr || topk_idx == nullptr || B_experts == nullptr || Y == nullptr || dest == nullptr)
+    return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
+  for (int s = 0; s < W; ++s)
+    if (X[s] == nullptr || topk_idx[s] == nullptr) return TDX_ERR_INVALID_ARG;
+  if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
+  if (o.mode == TDX_CONSUMER_ONLY || o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, H, F, E, topk, dtype, o, &pl);
+  if (s != TDX_OK) return s;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(X[r]) || (reinterpret_cast<uintptr_t>(topk_idx[r]) & 3u) != 0) return TDX_ERR_ALIGNMENT;
+  if (!aligned16(B_experts) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(dest) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
+    return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(H) * 2) % 16 != 0 || (static_cast<long long>(F) * 2) % 16 != 0) return TDX_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.bytes)
+    return TDX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (pl.total == 0) {
+    return expert_offsets != nullptr ? fill_zero(expert_offsets, static_cast<size_t>(E + 1) * 4, st) : TDX_OK;
+  }
+  const uint32_t epoch = o.epoch == 0 ? 1u : o.epoch;
+  if (o.epoch == 0) {
+    s = fill_zero(ws + pl.off_flags, pl.ctrl_end - pl.off_flags, st);
+    if (s != TDX_OK) return s;
+  }
+  // 1. routing layout on the device
+  static thread_local MoeLayoutParams lq;
+  std::memset(&lq, 0, sizeof(lq));
+  for (int r = 0; r < W; ++r) lq.topk[r] = topk_idx[r];
+  lq.dest = dest;
+  lq.src = reinterpret_cast<int32_t*>(ws + pl.off_src);
+  lq.offsets = reinterpret_cast<int32_t*>(ws + pl.off_offsets);
+  lq.user_offsets = expert_offsets;
+  lq.tiles = reinterpret_cast<int4*>(ws + pl.off_tiles);
+  lq.ntiles = reinterpret_cast<int32_t*>(ws + pl.off_ntiles);
+  lq.status = reinterpret_cast<uint32_t*>(ws);
+  lq.W = W;
+  lq.T = T;
+  lq.k = topk;
+  lq.E = E;
+  lq.max_tiles = pl.max_tiles;
+  if (launch_moe_layout(lq, st) != cudaSuccess) return TDX_ERR_CUDA;
+  if (F == 0) return TDX_OK;
+  if (H == 0) return fill_zero(Y, static_cast<size_t>(pl.total) * F * 2, st);
+
+  // 2. fused dispatch + grouped GEMM
+  static thread_local KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.op = OP_MOE;
+  kp.mode = o.mode;
+  kp.W = W;
+  kp.M = static_cast<int>(pl.total);
+  kp.K = H;
+  kp.N = F;
+  kp.M_local = kp.M;
+  kp.tiles_m = pl.n_chunks;
+  kp.tiles_n = pl.tiles_n;
+  kp.T = pl.max_tiles;
+  kp.group_n = pl.tiles_n;
+  kp.rank_block = 1;
+  kp.L = 1;
+  kp.num_kb = pl.num_kb;
+  kp.status = reinterpret_cast<uint32_t*>(ws);
+  kp.chunk_flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags);
+  kp.chunk_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
+  kp.trace = static_cast<uint32_t*>(o.trace);
+  kp.epoch = epoch;
+  kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
+  kp.perturb = o.perturb_seed;
+  kp.row_bytes = static_cast<long long>(H) * 2;
+  kp.chunk_rows = kBM;
+  kp.n_chunks = pl.n_chunks;
+  kp.chunk_bytes = kBM * kp.row_bytes;
+  kp.G = ws + pl.off_R;
+  kp.out[0] = static_cast<uint8_t*>(Y);
+  for (int r = 0; r < W; ++r) kp.shard[r] = static_cast<const uint8_t*>(X[r]);
+  kp.moe_src = lq.src;
+  kp.moe_tiles = lq.tiles;
+  kp.moe_ntiles = lq.ntiles;
+  kp.moe_T = T;
+  int grid = device_sms();
+  if (grid <= 0) return TDX_ERR_CUDA;
+  if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
+  {
+    // producer copy unit: about one piece per CTA, whole rows, at most 64 KiB (one row if larger)
+    const long long bytes_all = pl.total * kp.row_bytes;
+    long long pb = (bytes_all / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;
+    if (pb < kCopyRoundBytes) pb = kCopyRoundBytes;
+    if (pb > kMaxPieceBytes) pb = kMaxPieceBytes;
+    long long rpp = pb / kp.row_bytes;
+    if (rpp < 1) rpp = 1;
+    if (rpp > kBM) rpp = kBM;
+    kp.moe_rpp = static_cast<int>(rpp);
+    kp.piece_bytes = static_cast<int>(rpp * kp.row_bytes);
+  }
+  kp.ppc = (kBM + kp.moe_rpp - 1) / kp.moe_rpp;
+  kp.total_pieces = pl.n_chunks * kp.ppc;
+  const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
+  kp.copy_active = moving ? 1 : 0;
+  kp.wait_flags = o.mode == TDX_FUSED ? 1 : 0;
+  if (!make_map(&kp.tm_a[0], kp.G, false, pl.total, H, 64, kBM) ||
+      !make_map_3d(&kp.tm_b[0], B_experts, E, H, F, 64, 64))
+    return TDX_ERR_CUDA;
+  const cudaError_t e = launch_fused_moe_bf16(pl.BN, kp, grid, st);
+  if (e != cudaSuccess) {
+    if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
+    return TDX_ERR_CUDA;
+  }
+  return TDX_OK;
+}
+
+}  // extern "C"

@@ -45,11 +45,12 @@ constexpr int kRefSMs = 148;             // fixed SM count used only for the (ho
 // (per-slot barrier/commit overhead and a 64-byte-swizzled A operand cost more than the depth buys).
 constexpr int k_slice_bytes(int /*block_n*/) { return 128; }
 
-enum Op { OP_AG = 0, OP_RS = 1 };
+enum Op { OP_AG = 0, OP_RS = 1, OP_MOE = 3 };   // OP_MOE: AllToAll dispatch + grouped GEMM
 constexpr int kOpAllReduce = 2;          // API op code: GEMM+AllReduce (runs the OP_RS kernel)
+constexpr int kMoeMaxExperts = 512;      // layout kernel: per-expert tables live in shared memory
 enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };
-enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4 };
-enum DevStatus { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_STALE = 7 };
+enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4, ROLE_LAYOUT = 5 };
+enum DevStatus { DEV_OK = 0, DEV_BAD_INPUT = 1, DEV_TIMEOUT = 6, DEV_STALE = 7 };
 
 // Word offsets in the workspace header (first 4 KiB).
 constexpr size_t kHeaderBytes = 4096;
@@ -86,7 +87,12 @@ struct KParams {
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
   int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
   int allreduce;                 // RS kernel as GEMM+AllReduce: out[r] are full M x N outputs
-  int bf16_partials;        // slotted RS/AR: partials rounded to bf16 in their slots (else fp32)
+  int bf16_partials;             // slotted RS/AR: partials rounded to bf16 in their slots (else fp32)
+  const int32_t* moe_src;        // MoE: source token of every dispatched row, s * moe_T + t
+  const int4* moe_tiles;         // MoE: tile table {first row, end row of its expert, expert, 0}
+  const int32_t* moe_ntiles;     // MoE: [0] tiles in the table, [1] nonzero if the routing was invalid
+  int moe_T;                     // MoE: tokens per rank
+  int moe_rpp;                   // MoE producer: dispatched rows per piece
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;
@@ -108,5 +114,23 @@ cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int 
 int fused_max_grid_bf16(int op, int pm, int sms);
 int fused_max_grid_fp8(int op, int pm, int sms);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
+
+// MoE: the fused dispatch + grouped GEMM kernel (bf16, single CTAs).
+cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
+
+// MoE routing layout: from every rank's top-k expert ids, the dispatched row of every (rank, token,
+// slot), the source of every dispatched row, the expert row offsets and the GEMM tile table.
+struct MoeLayoutParams {
+  const int32_t* topk[kMaxW];    // [W] T x k expert ids
+  int32_t* dest;                 // W x T x k dispatched rows (output)
+  int32_t* src;                  // total rows: s * T + t (output)
+  int32_t* offsets;              // E + 1 expert row offsets (output)
+  int32_t* user_offsets;         // optional copy of offsets for the caller (may be null)
+  int4* tiles;                   // tile table (output)
+  int32_t* ntiles;               // [0] tiles, [1] invalid routing (output)
+  uint32_t* status;              // workspace status words
+  int W, T, k, E, max_tiles;
+};
+cudaError_t launch_moe_layout(const MoeLayoutParams& q, cudaStream_t stream);
 
 }  // namespace tdx

@@ -108,8 +108,10 @@ struct Cfg {
 
 struct Item {
   int c;      // chain element (RS rank, or AG K split)
-  int tile;   // tile id = mt * tiles_n + nt
+  int tile;   // tile id = mt * tiles_n + nt (MoE: the item index)
   int m0, n0;
+  int mend;   // MoE: end row of the tile's expert (rows >= mend are not stored)
+  int e;      // MoE: expert
 };
 
 // Work item `it` of a CTA whose rank in its cluster is `crank`. With CL CTAs per cluster, items
@@ -120,6 +122,21 @@ struct Item {
 template <int OP, int CL>
 __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, int crank) {
   Item r;
+  if constexpr (OP == OP_MOE) {
+    // MoE: the tile table lists each expert's 128-row tiles in dispatched-row order (experts
+    // ascending), which is the order the producers fill the receive buffer in; N-tiles innermost
+    const int t = it / p.tiles_n;
+    const int4 ti = p.moe_tiles[t];
+    r.c = 0;
+    r.tile = it;
+    r.m0 = ti.x;
+    r.mend = ti.y;
+    r.e = ti.z;
+    r.n0 = (it - t * p.tiles_n) * BN;
+    return r;
+  }
+  r.mend = 0;
+  r.e = 0;
   const int tiles_g = p.tiles_m / CL;
   const int Tg = tiles_g * p.tiles_n;
   int pos;
@@ -416,6 +433,8 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
     }
     for (int r = 1; r < p.W; ++r) store_row_chunk(p.out[r] + (size_t)row * p.N * 2, p, col, v, pol);
     orow = p.out[0] + (size_t)row * p.N * 2;
+  } else if constexpr (OP == OP_MOE) {
+    orow = p.out[0] + (size_t)row * p.N * 2;    // rows past the tile's expert arrive as row >= M
   } else {
     const int j = row / p.M_local;
     orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
@@ -477,8 +496,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   }
   if (threadIdx.x == kTmaWarp * 32) {
-    for (int i = 0; i < (OP == OP_AG && !p.pull_a ? 2 : p.W); ++i) tma_prefetch_map(&p.tm_a[i]);
-    for (int i = 0; i < (OP == OP_AG ? 1 : p.W); ++i) tma_prefetch_map(&p.tm_b[i]);
+    const int na = OP == OP_MOE ? 1 : (OP == OP_AG && !p.pull_a ? 2 : p.W);
+    const int nb = OP == OP_RS ? p.W : 1;
+    for (int i = 0; i < na; ++i) tma_prefetch_map(&p.tm_a[i]);
+    for (int i = 0; i < nb; ++i) tma_prefetch_map(&p.tm_b[i]);
   }
   tc_fence_before();
   if constexpr (CL > 1)
@@ -493,12 +514,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   const int ncl = gridDim.x / CL;           // clusters in the grid
 
   constexpr bool ag = OP == OP_AG;
-  const bool ag_move_only = ag && p.mode == MODE_MOVE_ONLY;
-  const bool rs_move_only = !ag && p.mode == MODE_MOVE_ONLY;
-  const int items_all = ag_move_only ? 0 : p.L * p.T;   // (element, tile) work items
+  constexpr bool rs = OP == OP_RS;
+  const bool ag_move_only = !rs && p.mode == MODE_MOVE_ONLY;   // AllGather / MoE: producer only
+  const bool rs_move_only = rs && p.mode == MODE_MOVE_ONLY;
+  int t_dyn = p.T;
+  bool moe_bad = false;
+  if constexpr (OP == OP_MOE) {
+    // the count of 128-row tiles is known only on the device (written by the layout kernel before
+    // this launch; never above the host's bound p.T); every one is cut into tiles_n N-tiles
+    moe_bad = p.moe_ntiles[1] != 0;
+    t_dyn = moe_bad ? 0 : min(p.moe_ntiles[0], p.T) * p.tiles_n;
+  }
+  const int items_all = ag_move_only ? 0 : p.L * t_dyn;   // (element, tile) work items
   const int items = items_all / CL;                       // items of one cluster-wide sequence
   const bool use_mma = !rs_move_only;  // RS move-only runs the chain on zero partials
-  const bool chain = p.L > 1 && !(!ag && p.mode == MODE_GEMM_ONLY);
+  const bool chain = p.L > 1 && !(rs && p.mode == MODE_GEMM_ONLY);
   const int grid = gridDim.x;
   uint32_t* trace = p.trace;
   const int per_cta = (items_all + grid - 1) / grid;
@@ -555,6 +585,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               fence_proxy_async_global();
             }
           }
+        } else if (OP == OP_MOE) {
+          map_a = &p.tm_a[0];
+          map_b = &p.tm_b[0];
+          if (p.wait_flags) {
+            // the 128-row chunks of the receive buffer holding this expert's rows of the tile; rows
+            // past the expert's end are loaded too but never stored, so their chunk is not awaited
+            if (p.perturb) __nanosleep(perturb_hash(p.perturb, it) & 4095u);
+            ++n_waits;
+            if (!wait_flags_all(p, w.m0 / kBM, (w.mend - 1) / kBM, abort_flag, &flag_ns)) break;
+            fence_proxy_async_global();
+          }
         } else {
           map_a = &p.tm_a[w.c];
           map_b = &p.tm_b[w.c];
@@ -606,7 +647,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
-            if constexpr (CL == 1) {
+            if constexpr (OP == OP_MOE) {
+  #pragma unroll
+              for (int j = 0; j < C::B_BOXES; ++j)
+                tma_load_3d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, w.e, keep);
+            } else if constexpr (CL == 1) {
   #pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
@@ -755,6 +801,59 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
       }
+    } else if (OP == OP_MOE && p.copy_active && !moe_bad) {
+      // AllToAll dispatch: the receive buffer is filled in 128-row chunks in row order; a piece is
+      // moe_rpp whole rows of a chunk, each row gathered from its source token (row -> s * T + t),
+      // in rounds of 16 vectors per thread; the last piece of a chunk releases the chunk's flag
+      const int ct = threadIdx.x - kCopyWarp0 * 32;
+      const uint64_t stream_pol = policy_evict_first();   // each token row is read topk times, far apart
+      constexpr int kVec = kCopyRoundBytes / (16 * kCopyThreads);
+      const int vpr = static_cast<int>(p.row_bytes / 16);   // 16-byte vectors per row
+      const int ntok = p.W * p.moe_T;
+      for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
+        const int ck = piece / p.ppc;
+        const int pc = piece - ck * p.ppc;
+        const int r0 = ck * kBM + pc * p.moe_rpp;
+        const int r1 = min(min(r0 + p.moe_rpp, (ck + 1) * kBM), p.M);
+        const int nvec = r1 > r0 ? (r1 - r0) * vpr : 0;
+        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
+        for (int v0 = 0; v0 < nvec; v0 += kVec * kCopyThreads) {
+          uint4 v[kVec];
+          uint8_t* dst[kVec];
+#pragma unroll
+          for (int j = 0; j < kVec; ++j) {
+            const int idx = v0 + j * kCopyThreads + ct;
+            dst[j] = nullptr;
+            if (idx < nvec) {
+              const int rr = idx / vpr;
+              const int col = idx - rr * vpr;
+              const int row = r0 + rr;
+              const int tok = p.moe_src[row];
+              if (tok >= 0 && tok < ntok) {
+                const int s = tok / p.moe_T;
+                const uint8_t* src = p.shard[s] + (long long)(tok - s * p.moe_T) * p.row_bytes + col * 16;
+                v[j] = ld_nc_v4_hint(src, stream_pol);
+                dst[j] = p.G + (long long)row * p.row_bytes + col * 16;
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kVec; ++j)
+            if (dst[j] != nullptr) st_v4(dst[j], v[j]);
+        }
+        named_bar_sync(2, kCopyThreads);
+        if (ct == 0) {
+          __threadfence();
+          const uint32_t old = atomicAdd(p.chunk_cnt + ck, 1u);
+          if (old == static_cast<uint32_t>(p.ppc - 1)) {
+            p.chunk_cnt[ck] = 0u;
+            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
+            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
+            __threadfence();
+            st_release_gpu(p.chunk_flags + ck, p.epoch);
+          }
+        }
+      }
     }
   } else {
     // =============================================================== epilogue
@@ -765,7 +864,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     const bool elected = threadIdx.x == kEpiWarp0 * 32;
     volatile uint32_t* decision = misc + 4;    // written before barrier 1, read after it
     volatile uint32_t* is_last = misc + 5;     // written between barriers 2 and 3, read after 3
-    const bool rs_gemm_only = !ag && p.mode == MODE_GEMM_ONLY;
+    const bool rs_gemm_only = rs && p.mode == MODE_GEMM_ONLY;
     const bool chained = chain && !p.reduce_last;   // running sum handed from element to element
     const bool slotted = chain && p.reduce_last;    // own partial slot; the last arriver folds
     uint64_t chain_ns = 0;
@@ -853,7 +952,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
           }
         }
-        if (direct_out) store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
+        if (direct_out) store_out_chunk<OP, FP8>(p, (OP == OP_MOE && row >= w.mend) ? p.M : row, w.n0 + col0, v, once);
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);

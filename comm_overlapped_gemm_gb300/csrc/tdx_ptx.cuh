@@ -91,6 +91,15 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
+// 3D tiled load (x innermost); used for a stack of matrices addressed by z (expert weights).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                            int x, int y, uint16_t cta_mask, uint64_t pol) {
   asm volatile(

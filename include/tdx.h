@@ -199,10 +199,59 @@ tdx_status tdx_gemm_ar(const void* const* A_parts, const void* const* B_parts, v
                        void* workspace, size_t workspace_bytes, int W, int M, int K, int N, tdx_dtype dtype,
                        const tdx_opts* opts, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Mixture-of-experts AllToAll dispatch + grouped GEMM.
+ * (Triton-distributed article, section "DITRON adds three levels of tiling": AllToAll is among the
+ * collectives broken into chunks and paired with compute tiles; the tokens routed to each expert of
+ * a mixture-of-experts model are known only at run time, so its device-level tiles are sized
+ * dynamically.)
+ *
+ * W ranks; rank s holds T tokens X[s] (T x H bf16 row-major) and their routing topk_idx[s]
+ * (T x topk int32 expert ids in [0, E)). Rank rho owns experts rho*E/W .. (rho+1)*E/W - 1. The
+ * dispatch sends every (s, t, j) row X[s][t] to expert topk_idx[s][t][j]; the receive side (one
+ * buffer for all ranks, in the workspace) groups the W*T*topk rows by expert, experts ascending,
+ * and inside an expert by source rank then token, ascending. Expert e's rows are multiplied by its
+ * weights B_experts[e] (H x F); Y keeps the dispatched row order:
+ *   Y[dest[s][t][j]] = round_bf16(X[s][t] @ B_experts[topk_idx[s][t][j]]).
+ * The layout (counts, offsets, row of every pair, GEMM tile table) is computed on the device; the
+ * dispatch copies the receive buffer in 128-row chunks, each released by a flag, while the GEMM
+ * tiles of the experts whose rows have arrived already run.
+ *  X              host array of W device pointers, each T x H bf16 (16-byte aligned).
+ *  topk_idx       host array of W device pointers, each T x topk int32. Ids outside [0, E) make the
+ *                 call do nothing further and record TDX_ERR_INVALID_ARG in the device status.
+ *  B_experts      device pointer, E x H x F bf16 (expert e's weights at e*H*F).
+ *  Y              device pointer, (W*T*topk) x F bf16, the dispatched order.
+ *  dest           device pointer, W x T x topk int32 (output): the row of Y of every (s, t, j).
+ *  expert_offsets optional device pointer, E + 1 int32 (output): expert e's rows are
+ *                 [expert_offsets[e], expert_offsets[e+1]).
+ *  workspace      caller-owned device memory of tdx_moe_workspace_size() bytes, 256-byte aligned,
+ *                 zeroed once by tdx_workspace_init; it holds the status word, chunk flags, the
+ *                 layout tables and the receive buffer ((W*T*topk) x H bf16).
+ *  H, F multiples of 8; 1 <= topk <= E <= 512; W <= 16; bf16 only (e4m3: TDX_ERR_UNSUPPORTED).
+ *  opts: epoch, timeout_ns, perturb_seed, trace, num_sms, block_n and mode (TDX_FUSED, TDX_GEMM_ONLY:
+ *  the receive buffer is assumed filled by an earlier call with the same routing, TDX_MOVE_ONLY:
+ *  dispatch only) apply; other cooperation options must keep their defaults. */
+tdx_status tdx_moe_workspace_size(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype,
+                                  const tdx_opts* opts, size_t* bytes);
+tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* topk_idx, const void* B_experts,
+                                 void* Y, int32_t* dest, int32_t* expert_offsets, void* workspace,
+                                 size_t workspace_bytes, int W, int T, int H, int F, int E, int topk,
+                                 tdx_dtype dtype, const tdx_opts* opts, void* stream);
+/* Plan of one MoE call (13 words to info): [0] tile width, [1] N-tiles, [2] tile-table capacity,
+ * [3] 128-row chunks of the receive buffer (one flag each), [4] dispatched rows W*T*topk, byte
+ * offsets in the workspace of [5] chunk flags (uint32 per chunk), [6] tile count + invalid-routing
+ * words, [7] expert offsets (int32 [E+1]), [8] source of every dispatched row (int32, s*T + t),
+ * [9] tile table (int32x4 {first row, end row of the expert, expert, 0}), [10] receive buffer,
+ * [11] total workspace bytes, [12] 128-byte K blocks. */
+tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype,
+                             const tdx_opts* opts, int64_t* info);
+
 /* Synchronise `stream`, then read the workspace's device status word into *out (TDX_OK, or the
  * first device-side error since tdx_workspace_init). If detail is not NULL it receives 8 words:
- * [0] status, [1] role that failed (1 flag wait, 2 pipeline wait, 3 chain wait, 4 producer),
- * [2] CTA index, [3] flag/barrier index, [4] value observed, [5] value expected, [6..7] reserved. */
+ * [0] status, [1] role that failed (1 flag wait, 2 pipeline wait, 3 chain wait, 4 producer,
+ * 5 MoE routing layout: [4] the first invalid expert id seen, [5] E), [2] CTA index, [3] flag/barrier
+ * index, [4] value observed, [5] value expected, [6..7] reserved. An invalid MoE routing is reported
+ * as TDX_ERR_INVALID_ARG here (the ids are only read on the device). */
 tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_status* out,
                                   uint32_t* detail);
 

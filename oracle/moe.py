@@ -40,32 +40,27 @@ def moe_layout(topk, E: int):
 
     Returns ``(counts, offsets, dest, src)``: ``counts[s, e]`` tokens of rank s routed to expert e;
     ``offsets[e]`` first dispatched row of expert e (``offsets[E]`` = total rows = W*T*k);
-    ``dest[s]`` (T x k) the dispatched row of every (s, t, j); ``src[row] = (s, t)``."""
+    ``dest[s]`` (T x k) the dispatched row of every (s, t, j); ``src[row] = (s, t)``.
+    Expert by expert, the rows are taken rank by rank; inside a rank, ``np.nonzero`` lists the
+    (t, j) hits of the expert in row-major order, i.e. token ascending."""
     W = len(topk)
-    counts = np.zeros((W, E), dtype=np.int64)
     for s in range(W):
-        T, k = topk[s].shape
-        for t in range(T):
-            for j in range(k):
-                e = int(topk[s][t, j])
-                if not 0 <= e < E:
-                    raise ValueError(f"expert id {e} out of range")
-                counts[s, e] += 1
+        bad = (topk[s] < 0) | (topk[s] >= E)
+        if bad.any():
+            raise ValueError(f"expert id {int(topk[s][bad][0])} out of range")
+    counts = np.array([[int((topk[s] == e).sum()) for e in range(E)] for s in range(W)], dtype=np.int64)
     offsets = np.zeros(E + 1, dtype=np.int64)
-    for e in range(E):
-        offsets[e + 1] = offsets[e] + counts[:, e].sum()
+    offsets[1:] = np.cumsum(counts.sum(axis=0))
     dest = [np.zeros(topk[s].shape, dtype=np.int64) for s in range(W)]
     src = [None] * int(offsets[E])
     for e in range(E):
         row = int(offsets[e])
         for s in range(W):
-            T, k = topk[s].shape
-            for t in range(T):
-                for j in range(k):
-                    if int(topk[s][t, j]) == e:
-                        dest[s][t, j] = row
-                        src[row] = (s, t)
-                        row += 1
+            tt, jj = np.nonzero(topk[s] == e)
+            dest[s][tt, jj] = np.arange(row, row + len(tt))
+            for i, t in enumerate(tt):
+                src[row + i] = (s, int(t))
+            row += len(tt)
     return counts, offsets, dest, src
 
 
@@ -95,14 +90,18 @@ def moe_dispatch_gemm(x, topk, b_experts, E: int, dtype: str = "bf16", scale_x=N
 def moe_dispatch_gemm_rows(x, topk, b_experts, E: int, rows, dtype: str = "bf16", scale_x=None, scale_b=None):
     """Rows ``rows`` (dispatched row indices) of :func:`moe_dispatch_gemm` only."""
     _, offsets, _, src = moe_layout(topk, E)
-    out = []
-    for r in rows:
-        s, t = src[int(r)]
-        e = row_expert(offsets, int(r))
-        sx = 1.0 if scale_x is None else float(scale_x[s])
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), b_experts.shape[2]), dtype=np.float64)
+    experts = np.array([row_expert(offsets, int(r)) for r in rows], dtype=np.int64)
+    for e in np.unique(experts):
+        sel = np.nonzero(experts == e)[0]
+        b = decode(b_experts[e], dtype)                   # decoded once per expert
         sb = 1.0 if scale_b is None else float(scale_b[e])
-        out.append((decode(x[s][t][None, :], dtype) @ decode(b_experts[e], dtype))[0] * (sx * sb))
-    return np.array(out, dtype=np.float64).reshape(len(rows), b_experts.shape[2])
+        for i in sel:
+            s, t = src[int(rows[i])]
+            sx = 1.0 if scale_x is None else float(scale_x[s])
+            out[i] = (decode(x[s][t][None, :], dtype) @ b)[0] * (sx * sb)
+    return out
 
 
 def moe_combine(Z: np.ndarray, dest, gates):

@@ -169,3 +169,36 @@ def sample_rows(M: int, chunk: int, extra_stride: int = 97) -> np.ndarray:
         rows.update({t0, min(t0 + 128, M) - 1, min(t0 + 77, M - 1)})
     rows.update(range(0, M, extra_stride))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+class MoECase:
+    """Device buffers of one AllToAll dispatch + grouped GEMM problem."""
+
+    def __init__(self, inp, opts=None, offsets=True):
+        wl = inp.wl
+        self.inp, self.wl = inp, wl
+        self.W, self.T, self.H, self.F, self.E, self.k = wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk
+        self.X = [dev_bits(a) for a in inp.a]
+        self.route = [torch.from_numpy(np.ascontiguousarray(r)).cuda() for r in inp.route]
+        self.B = dev_bits(inp.b[0])
+        rows = wl.M_total
+        self.Y = torch.full((rows, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        self.dest = torch.full((wl.W, wl.M, wl.topk), -7, dtype=torch.int32, device="cuda")
+        self.offsets = torch.full((wl.E + 1,), -7, dtype=torch.int32, device="cuda") if offsets else None
+        self.opts = opts
+        n = tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16, opts)
+        self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        tdx.check(tdx.tdx_workspace_init(self.ws), "init")
+
+    def run(self, opts=None):
+        o = opts if opts is not None else self.opts
+        return tdx.tdx_moe_dispatch_gemm(self.X, self.route, self.B, self.Y, self.dest, self.offsets, self.ws,
+                                         self.W, self.T, self.H, self.F, self.E, self.k, tdx.TDX_BF16, o)
+
+    def result_bits(self) -> np.ndarray:
+        torch.cuda.synchronize()
+        return host_bits(self.Y)
+
+    def plan(self, opts=None):
+        return tdx.tdx_moe_plan_info(self.W, self.T, self.H, self.F, self.E, self.k, tdx.TDX_BF16,
+                                     opts if opts is not None else self.opts)

@@ -199,3 +199,46 @@ def test_noalloc_rejects_copy_engine_producer_before_any_device_work(tdx):
 def test_noalloc_rejects_oversized_problem_before_any_device_work(tdx):
     rc = tdx.tdx_ag_gemm_noalloc([FAKE] * 8, FAKE, FAKE, 8, 1024, 8192, 3584, tdx.TDX_BF16, None, stream=0)
     assert rc == tdx.TDX_ERR_WORKSPACE
+
+
+def test_moe_validation_codes(tdx):
+    def ws_size(W=2, T=8, H=64, F=64, E=4, k=2, dtype=0, opts=None):
+        try:
+            tdx.tdx_moe_workspace_size(W, T, H, F, E, k, dtype, opts)
+            return tdx.TDX_OK
+        except tdx.TdxError as e:
+            return e.status
+
+    assert ws_size() == tdx.TDX_OK
+    assert ws_size(E=513) == tdx.TDX_ERR_UNSUPPORTED
+    assert ws_size(k=5) == tdx.TDX_ERR_INVALID_ARG          # topk > E
+    assert ws_size(k=0) == tdx.TDX_ERR_INVALID_ARG
+    assert ws_size(W=17) == tdx.TDX_ERR_INVALID_ARG
+    assert ws_size(dtype=1) == tdx.TDX_ERR_UNSUPPORTED
+    assert ws_size(opts=tdx.make_opts(cluster=3)) == tdx.TDX_ERR_UNSUPPORTED
+    assert ws_size(opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
+
+    def moe(X=None, R=None, B=FAKE, Y=FAKE, dest=FAKE, offs=0, W=2, T=8, H=64, F=64, E=4, k=2, opts=None,
+            wsb=1 << 30, ws=FAKE):
+        X = [FAKE] * W if X is None else X
+        R = [FAKE] * W if R is None else R
+        return tdx.tdx_moe_dispatch_gemm(X, R, B, Y, dest, offs, ws, W, T, H, F, E, k, tdx.TDX_BF16, opts,
+                                         stream=0, workspace_bytes=wsb)
+
+    assert moe(X=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert moe(R=[0, FAKE]) == tdx.TDX_ERR_INVALID_ARG
+    assert moe(dest=0) == tdx.TDX_ERR_INVALID_ARG
+    assert moe(X=[FAKE, FAKE + 8]) == tdx.TDX_ERR_ALIGNMENT
+    assert moe(dest=FAKE + 2) == tdx.TDX_ERR_ALIGNMENT
+    assert moe(H=60) == tdx.TDX_ERR_ALIGNMENT                # 120-byte rows
+    assert moe(wsb=100) == tdx.TDX_ERR_WORKSPACE
+    assert moe(opts=tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY)) == tdx.TDX_ERR_UNSUPPORTED
+    assert moe(opts=tdx.make_opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE)) == tdx.TDX_ERR_UNSUPPORTED
+
+
+def test_moe_plan(tdx):
+    # 262144 dispatched rows of 7168: 2048 chunks, tile table bound 2048 + 64, receive buffer 3.5 GiB
+    p = tdx.tdx_moe_plan_info(8, 4096, 7168, 2048, 64, 8, tdx.TDX_BF16)
+    assert p["total_rows"] == 262144 and p["n_chunks"] == 2048 and p["max_tiles"] == 2048 + 64
+    assert p["BN"] == 256 and p["tiles_n"] == 8 and p["num_kb"] == 112
+    assert p["total"] - p["off_R"] == 262144 * 7168 * 2

@@ -1,0 +1,163 @@
+"""AllToAll dispatch + grouped GEMM of a mixture-of-experts layer on the GPU through the C ABI,
+against the CPU oracle: the routing layout (row of every token slot, expert offsets) is compared
+exactly, the expert outputs bit-exactly on integer inputs and within the bf16 tolerance on random
+ones; the receive buffer, chunk flags and tile table left in the workspace are checked as well."""
+import numpy as np
+import pytest
+import torch
+
+import comm_overlapped_gemm_gb300 as tdx
+from oracle import moe as MO
+from oracle import reference as R
+import workloads as wls
+from gpu_util import MoECase, assert_bit_exact, assert_within_tol
+
+pytestmark = pytest.mark.gpu
+
+TMO = int(5e8)
+
+
+def opts(**kw):
+    return tdx.make_opts(timeout_ns=TMO, **kw)
+
+
+def status_ok(case):
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_OK, (tdx.tdx_status_string(st), detail)
+
+
+def check_layout(case, lay):
+    counts, offsets, dest, _ = lay
+    torch.cuda.synchronize()
+    got = case.dest.cpu().numpy()
+    for s in range(case.W):
+        assert np.array_equal(got[s], dest[s])
+    if case.offsets is not None:
+        assert np.array_equal(case.offsets.cpu().numpy(), offsets)
+
+
+SHAPES = [
+    dict(W=2, M=5, K=64, N=128, E=4, topk=2),          # a handful of rows, every tile partial
+    dict(W=3, M=70, K=200, N=136, E=6, topk=3),        # ragged K and N
+    dict(W=8, M=128, K=256, N=512, E=64, topk=8),      # 128 tokens per rank, 8 experts per rank
+    dict(W=1, M=300, K=128, N=256, E=3, topk=1),
+    dict(W=4, M=257, K=64, N=64, E=8, topk=2),         # experts with several tiles and a tail
+    dict(W=16, M=17, K=64, N=192, E=32, topk=4),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("integer", [True, False])
+def test_moe_small_shapes(shape, integer):
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    want, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
+    for bn in (0, 64, 256):
+        case = MoECase(inp, opts=opts(block_n=bn))
+        tdx.check(case.run(), f"moe {shape} bn={bn}")
+        status_ok(case)
+        check_layout(case, lay)
+        if integer:
+            assert_bit_exact(case.result_bits(), want, "bf16")
+        else:
+            assert_within_tol(R.decode_bf16(case.result_bits()), want, "bf16")
+
+
+def test_moe_workspace_bookkeeping():
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=4, M=100, K=256, N=256, E=8, topk=2)
+    inp = wls.make_inputs(wl, integer=True)
+    case = MoECase(inp, opts=opts(epoch=5))
+    tdx.check(case.run())
+    status_ok(case)
+    _, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
+    counts, offsets, dest, src = lay
+    pl = case.plan()
+    ws = case.ws
+    rows = pl["total_rows"]
+    # the receive buffer holds every dispatched token row, bit for bit
+    R_ = ws[pl["off_R"]:pl["off_R"] + rows * wl.K * 2].view(torch.int16).cpu().numpy().view(np.uint16)
+    R_ = R_.reshape(rows, wl.K)
+    for r in range(rows):
+        s, t = src[r]
+        assert np.array_equal(R_[r], inp.a[s][t])
+    # every chunk flag holds the epoch; the tile table lists each expert's 128-row tiles
+    fl = ws[pl["off_chunk_flags"]:pl["off_chunk_flags"] + 4 * pl["n_chunks"]].view(torch.int32).cpu().numpy()
+    assert np.array_equal(fl.astype(np.uint32), R.expected_flags(pl["n_chunks"], 5))
+    nt = ws[pl["off_ntiles"]:pl["off_ntiles"] + 8].view(torch.int32).cpu().numpy()
+    tiles = ws[pl["off_tiles"]:pl["off_tiles"] + 16 * int(nt[0])].view(torch.int32).cpu().numpy().reshape(-1, 4)
+    want_tiles = [(int(offsets[e]) + 128 * i, int(offsets[e + 1]), e, 0)
+                  for e in range(wl.E) for i in range((int(offsets[e + 1] - offsets[e]) + 127) // 128)]
+    assert nt[1] == 0 and [tuple(x) for x in tiles.tolist()] == want_tiles
+    srcw = ws[pl["off_src"]:pl["off_src"] + 4 * rows].view(torch.int32).cpu().numpy()
+    assert [tuple(divmod(int(v), wl.M)) for v in srcw] == src
+
+
+def test_moe_modes_and_epochs():
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=4, M=128, K=512, N=256, E=16, topk=4)
+    inp = wls.make_inputs(wl, integer=True)
+    want, _ = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
+    case = MoECase(inp, opts=opts())
+    # dispatch alone, then the grouped GEMM alone on the filled receive buffer
+    tdx.check(case.run(opts(mode=tdx.TDX_MOVE_ONLY, epoch=1)))
+    tdx.check(case.run(opts(mode=tdx.TDX_GEMM_ONLY, epoch=2)))
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), want, "bf16")
+    for ep in (3, 4):
+        case.Y.fill_(float("nan"))
+        tdx.check(case.run(opts(epoch=ep, perturb_seed=ep)))
+        status_ok(case)
+        assert_bit_exact(case.result_bits(), want, "bf16")
+
+
+def test_moe_invalid_expert_id_is_reported_not_run():
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=2, M=16, K=64, N=64, E=4, topk=2)
+    inp = wls.make_inputs(wl, integer=True)
+    inp.route[1] = inp.route[1].copy()
+    inp.route[1][3, 1] = 9
+    case = MoECase(inp, opts=opts())
+    tdx.check(case.run())
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_ERR_INVALID_ARG and detail[1] == 5 and detail[4] == 9
+    assert bool(torch.isnan(case.Y.float()).all())         # nothing was computed
+
+
+def test_moe_degenerate_sizes():
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=2, M=8, K=64, N=64, E=4, topk=2)
+    inp = wls.make_inputs(wl, integer=True)
+    _, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
+    case = MoECase(inp, opts=opts())
+    # H = 0: the layout is still produced and every expert output is zero
+    tdx.check(tdx.tdx_moe_dispatch_gemm(case.X, case.route, case.B, case.Y, case.dest, case.offsets, case.ws,
+                                        2, 8, 0, 64, 4, 2, tdx.TDX_BF16, opts()))
+    check_layout(case, lay)
+    assert int(torch.count_nonzero(case.Y)) == 0
+    # T = 0: no rows; the expert offsets are all zero
+    tdx.check(tdx.tdx_moe_dispatch_gemm(case.X, case.route, case.B, case.Y, case.dest, case.offsets, case.ws,
+                                        2, 0, 64, 64, 4, 2, tdx.TDX_BF16, opts()))
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(case.offsets)) == 0
+    status_ok(case)
+
+
+def test_moe_full_size_sampled_and_deterministic():
+    wl = wls.WORKLOADS["moe_w8"]
+    inp = wls.make_inputs(wl, integer=False)
+    case = MoECase(inp, opts=opts())
+    tdx.check(case.run())
+    status_ok(case)
+    counts, offsets, dest, src = MO.moe_layout(inp.route, wl.E)
+    check_layout(case, (counts, offsets, dest, src))
+    first = case.result_bits()
+    # first, second and last row of every expert, plus a stride
+    rows = set(range(0, wl.M_total, 4099))
+    for e in range(wl.E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            rows.update({a, min(a + 1, b - 1), b - 1, min(a + 127, b - 1), min(a + 128, b - 1)})
+    rows = np.array(sorted(rows))
+    want = MO.moe_dispatch_gemm_rows(inp.a, inp.route, inp.b[0], wl.E, rows)
+    assert_within_tol(R.decode_bf16(first[rows]), want, "bf16")
+    case.Y.fill_(float("nan"))
+    tdx.check(case.run(opts(perturb_seed=17)))
+    status_ok(case)
+    assert np.array_equal(case.result_bits(), first)
