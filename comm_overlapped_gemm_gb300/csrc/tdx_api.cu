@@ -850,20 +850,10 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   int grid = device_sms();
   if (grid <= 0) return TDX_ERR_CUDA;
   if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
-  {
-    // producer copy unit: about one piece per CTA, whole rows, at most 64 KiB (one row if larger)
-    const long long bytes_all = pl.total * kp.row_bytes;
-    long long pb = (bytes_all / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;
-    if (pb < kCopyRoundBytes) pb = kCopyRoundBytes;
-    if (pb > kMaxPieceBytes) pb = kMaxPieceBytes;
-    long long rpp = pb / kp.row_bytes;
-    if (rpp < 1) rpp = 1;
-    if (rpp > kBM) rpp = kBM;
-    kp.moe_rpp = static_cast<int>(rpp);
-    kp.piece_bytes = static_cast<int>(rpp * kp.row_bytes);
-  }
-  kp.ppc = (kBM + kp.moe_rpp - 1) / kp.moe_rpp;
-  kp.total_pieces = pl.n_chunks * kp.ppc;
+  // producer: one CTA copies a whole 128-row chunk and releases its flag
+  kp.moe_rpp = kBM;
+  kp.ppc = 1;
+  kp.total_pieces = pl.n_chunks;
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
   kp.copy_active = moving ? 1 : 0;
   kp.wait_flags = o.mode == TDX_FUSED ? 1 : 0;

@@ -59,6 +59,12 @@ namespace tdx {
 #ifndef TDX_SUM_POLICY
 #define TDX_SUM_POLICY 0
 #endif
+// MoE dispatch producer: rows of the chunk ahead of the bulk copies that the producer threads
+// prefetch into L2 (0 = none). Off: 16 and 48 rows ahead measured 3-5% slower on GB300 (the bulk
+// loads already keep three segments in flight per SM).
+#ifndef TDX_MOE_PREFETCH_ROWS
+#define TDX_MOE_PREFETCH_ROWS 0
+#endif
 // Drop dead running-sum / partial-slot lines from L2 after their last read (1) or leave them (0).
 // Measured neutral on GB300, so off: the workspace then keeps the last call's sums and partials.
 #ifndef TDX_DISCARD_DEAD
@@ -90,7 +96,13 @@ struct Cfg {
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
   static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+  // flags/decisions (64 B), MoE producer row sources (kBM ints) and staging barriers (8)
+  static constexpr int MISC_BYTES = 64 + kBM * 4 + 8 * 8;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
+  // MoE dispatch staging ring for bulk row copies: what the GEMM ring leaves of the 227 KiB, at
+  // most 32 KiB, in whole KiB (at least 4 KiB)
+  static constexpr int MOE_STG_RAW = 227 * 1024 - SMEM_BYTES - 128;
+  static constexpr int MOE_STG = (MOE_STG_RAW > 32 * 1024 ? 32 * 1024 : MOE_STG_RAW) / 1024 * 1024;
   static constexpr int COLS_PER_WARP = BN / 2;    // 8 epilogue warps = 4 lane quarters x 2 halves
   static constexpr int CHUNKS = COLS_PER_WARP / 32;
   // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B type (bits 7-9, 10-12: bf16 = 1,
@@ -459,6 +471,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   // misc[0] TMEM base, misc[1] abort flag, misc[2] TMA k-blocks issued, misc[3] MMA k-blocks
   // consumed, misc[4] epilogue go/stop decision, misc[5] epilogue "last arriver" decision
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  // MoE dispatch: staging barriers after the row-source table, staging ring 128-byte aligned after them
+  uint64_t* stg_bars = reinterpret_cast<uint64_t*>(misc + 16 + kBM);
+  uint8_t* stg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(stg_bars + 8) + 127) & ~static_cast<uintptr_t>(127));
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + C::STAGES);
@@ -479,6 +494,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       mbar_init(tempty0 + 8 * a, PM == 2 ? 2 : 1);   // PM 2: both CTAs' epilogues free the leader's
     }
     mbar_init(drain_bar, 1);
+    if constexpr (OP == OP_MOE)
+      for (int b = 0; b < 8; ++b) mbar_init(smem_u32(stg_bars + b), 1);
     misc[1] = 0;
     misc[2] = 0;
     misc[3] = 0;
@@ -802,57 +819,87 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
       }
     } else if (OP == OP_MOE && p.copy_active && !moe_bad) {
-      // AllToAll dispatch: the receive buffer is filled in 128-row chunks in row order; a piece is
-      // moe_rpp whole rows of a chunk, each row gathered from its source token (row -> s * T + t),
-      // in rounds of 16 vectors per thread; the last piece of a chunk releases the chunk's flag
+      // AllToAll dispatch: CTAs take whole 128-row chunks of the receive buffer in row order. The
+      // producer threads stage the chunk's row sources (row -> s * T + t) in shared memory and
+      // prefetch upcoming source rows into L2; one thread moves the rows with bulk copies through a
+      // ring of NB shared-memory segments (NB - 1 loads in flight, each segment stored back as soon
+      // as it lands), waits for its stores to complete and releases the chunk's flag.
       const int ct = threadIdx.x - kCopyWarp0 * 32;
-      const uint64_t stream_pol = policy_evict_first();   // each token row is read topk times, far apart
-      constexpr int kVec = kCopyRoundBytes / (16 * kCopyThreads);
-      const int vpr = static_cast<int>(p.row_bytes / 16);   // 16-byte vectors per row
+      int* psrc = reinterpret_cast<int*>(misc + 16);         // [kBM] row sources of the chunk
       const int ntok = p.W * p.moe_T;
-      for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
-        const int ck = piece / p.ppc;
-        const int pc = piece - ck * p.ppc;
-        const int r0 = ck * kBM + pc * p.moe_rpp;
-        const int r1 = min(min(r0 + p.moe_rpp, (ck + 1) * kBM), p.M);
-        const int nvec = r1 > r0 ? (r1 - r0) * vpr : 0;
-        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
-        for (int v0 = 0; v0 < nvec; v0 += kVec * kCopyThreads) {
-          uint4 v[kVec];
-          uint8_t* dst[kVec];
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) {
-            const int idx = v0 + j * kCopyThreads + ct;
-            dst[j] = nullptr;
-            if (idx < nvec) {
-              const int rr = idx / vpr;
-              const int col = idx - rr * vpr;
-              const int row = r0 + rr;
-              const int tok = p.moe_src[row];
-              if (tok >= 0 && tok < ntok) {
-                const int s = tok / p.moe_T;
-                const uint8_t* src = p.shard[s] + (long long)(tok - s * p.moe_T) * p.row_bytes + col * 16;
-                v[j] = ld_nc_v4_hint(src, stream_pol);
-                dst[j] = p.G + (long long)row * p.row_bytes + col * 16;
-              }
+      const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+      // segment: a whole row if it fits a quarter of the ring, else a 16-byte multiple of that
+      // quarter (at least four segments in the ring, three loads in flight)
+      constexpr uint32_t kStg = static_cast<uint32_t>(C::MOE_STG);
+      const uint32_t seg = rb <= kStg / 4 ? rb : (kStg / 4) / 16 * 16;
+      const int nb = min(8, static_cast<int>(kStg / seg));
+      const int spr = static_cast<int>((rb + seg - 1) / seg);   // segments per row
+      uint32_t gseg = 0;                                        // segments issued by this CTA so far
+      auto src_of = [&](int tok, uint32_t off) -> const uint8_t* {
+        const int s = tok / p.moe_T;
+        return p.shard[s] + (long long)(tok - s * p.moe_T) * p.row_bytes + off;
+      };
+      for (int ck = blockIdx.x; ck < p.n_chunks; ck += grid) {
+        const int r0 = ck * kBM;
+        const int nrows = min(kBM, p.M - r0);
+        for (int i = ct; i < nrows; i += kCopyThreads) psrc[i] = p.moe_src[r0 + i];
+        named_bar_sync(2, kCopyThreads);
+        if (TDX_MOE_PREFETCH_ROWS > 0) {
+          for (int i = ct; i < min(nrows, TDX_MOE_PREFETCH_ROWS); i += kCopyThreads) {
+            const int tok = psrc[i];
+            if (tok >= 0 && tok < ntok) prefetch_l2_bulk(src_of(tok, 0), rb);
+          }
+        }
+        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + ck) & 4095u);
+        if (ct == 0) {
+          const int nseg = nrows * spr;
+          auto issue = [&](int i) {
+            const int row = i / spr;
+            const uint32_t off = static_cast<uint32_t>(i - row * spr) * seg;
+            const uint32_t n = rb - off < seg ? rb - off : seg;
+            const uint32_t g = gseg + static_cast<uint32_t>(i);
+            const uint32_t b = g % static_cast<uint32_t>(nb);
+            const int tok = psrc[row];
+            const uint32_t bar = smem_u32(stg_bars + b);
+            if (tok >= 0 && tok < ntok) {
+              mbar_arrive_expect_tx(bar, n);
+              bulk_load_g2s(smem_u32(stg + b * seg), src_of(tok, off), n, bar);
+            } else {
+              mbar_arrive(bar);   // nothing to move for an invalid source; keep the phases in step
+            }
+            if (TDX_MOE_PREFETCH_ROWS > 0 && off == 0 && row + TDX_MOE_PREFETCH_ROWS < nrows) {
+              const int t2 = psrc[row + TDX_MOE_PREFETCH_ROWS];
+              if (t2 >= 0 && t2 < ntok) prefetch_l2_bulk(src_of(t2, 0), rb);
+            }
+          };
+          for (int i = 0; i < min(nb - 1, nseg); ++i) issue(i);
+          for (int i = 0; i < nseg; ++i) {
+            const int j = i + nb - 1;
+            if (j < nseg) {
+              bulk_wait_read_all();   // the buffer of segment j held segment i - 1, stored just before
+              issue(j);
+            }
+            const uint32_t g = gseg + static_cast<uint32_t>(i);
+            const uint32_t b = g % static_cast<uint32_t>(nb);
+            wait_mbar_drain(p, smem_u32(stg_bars + b), (g / static_cast<uint32_t>(nb)) & 1u);
+            const int row = i / spr;
+            const uint32_t off = static_cast<uint32_t>(i - row * spr) * seg;
+            const uint32_t n = rb - off < seg ? rb - off : seg;
+            const int tok = psrc[row];
+            if (tok >= 0 && tok < ntok) {
+              bulk_store_s2g(p.G + (long long)(r0 + row) * p.row_bytes + off, smem_u32(stg + b * seg), n);
+              bulk_commit();
             }
           }
-#pragma unroll
-          for (int j = 0; j < kVec; ++j)
-            if (dst[j] != nullptr) st_v4(dst[j], v[j]);
-        }
-        named_bar_sync(2, kCopyThreads);
-        if (ct == 0) {
+          gseg += static_cast<uint32_t>(nseg);
+          bulk_wait_all();            // the chunk's rows are written
+          fence_proxy_async_global();
+          const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
+          if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
           __threadfence();
-          const uint32_t old = atomicAdd(p.chunk_cnt + ck, 1u);
-          if (old == static_cast<uint32_t>(p.ppc - 1)) {
-            p.chunk_cnt[ck] = 0u;
-            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
-            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
-            __threadfence();
-            st_release_gpu(p.chunk_flags + ck, p.epoch);
-          }
+          st_release_gpu(p.chunk_flags + ck, p.epoch);
         }
+        named_bar_sync(2, kCopyThreads);   // psrc is rewritten for the next chunk
       }
     }
   } else {
@@ -1133,6 +1180,9 @@ template <int BN, bool FP8, int OP, int PM>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8, PM == 2>;
   constexpr int CL = PM == 0 ? 1 : 2;
+  // MoE adds the dispatch staging ring (128-byte aligned) after the GEMM's shared memory
+  constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
+  static_assert(OP != OP_MOE || (C::MOE_STG >= 4096 && kSmem <= 227 * 1024), "MoE staging ring budget");
   // the dynamic shared-memory limit is raised once per device for each instantiation
   static bool attr_done[64] = {};
   int dev = 0;
@@ -1140,14 +1190,14 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES);
+                             kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if constexpr (CL == 1) {
