@@ -365,6 +365,33 @@ def moe_case(tdx, torch, wl, dev):
     return call, status
 
 
+def combine_case(tdx, torch, wl, dev):
+    """Device buffers + a timed call for one MoE grouped GEMM + combine workload."""
+    import workloads as wls
+    inp = wls.make_inputs(wl)
+    Hd = torch.from_numpy(np.ascontiguousarray(inp.a[0]).view(np.int16)).to(dev)
+    route = [torch.from_numpy(np.ascontiguousarray(r)).to(dev) for r in inp.route]
+    gates = [torch.from_numpy(np.ascontiguousarray(g)).to(dev) for g in inp.gates]
+    B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(np.int16)).to(dev)
+    out = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    ws = torch.empty(tdx.tdx_moe_combine_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16),
+                     dtype=torch.uint8, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    state = {"epoch": 0}
+
+    def call(mode=0, epoch=None):
+        state["epoch"] += 1
+        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode)
+        tdx.check(tdx.tdx_moe_gemm_combine(Hd, route, B, gates, out, ws, wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk,
+                                           tdx.TDX_BF16, o))
+
+    def status():
+        st, d = tdx.tdx_read_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    return call, status
+
+
 def graph_time_us(torch, fn, reps: int = 50):
     """GPU time per call (us) of fn captured in a CUDA graph of `reps` back-to-back calls (no host
     submission cost inside the timed region); None if the call cannot be captured."""
@@ -492,6 +519,19 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     res["moe_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
                      "tflops": tf, "frac_of_peak": tf / peak_bf16, "dispatch_bytes": moved,
                      "dispatch_gbs_alone": moved / (m * 1e-3) / 1e9}
+    del call, status
+    # MoE grouped GEMM + combine: fused, GEMM alone (expert outputs only), combine alone
+    wl = W["moe_combine_w8"]
+    call, status = combine_case(tdx, torch, wl, dev)
+    for _ in range(3):
+        call()
+    f = time_mode(torch, call, reps)
+    g = time_mode(torch, lambda: call(mode=1), reps)
+    m = time_mode(torch, lambda: call(mode=2), reps)
+    status()
+    tf = wl.flops / (f * 1e-3) / 1e12
+    res["moe_combine_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m,
+                             "overlap_efficiency": max(g, m) / f, "tflops": tf, "frac_of_peak": tf / peak_bf16}
     del call, status
     wl = W["moe_w8_decode"]
     call, status = moe_case(tdx, torch, wl, dev)

@@ -24,7 +24,8 @@ OP_AG, OP_RS, OP_AR = 0, 1, 2
 EXPORTED = ["tdx_opts_default", "tdx_workspace_size", "tdx_workspace_init", "tdx_ag_gemm", "tdx_gemm_rs",
             "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info",
             "tdx_ag_gemm_noalloc", "tdx_gemm_ar", "tdx_moe_workspace_size", "tdx_moe_plan_info",
-            "tdx_moe_dispatch_gemm"]
+            "tdx_moe_dispatch_gemm", "tdx_moe_combine_workspace_size", "tdx_moe_combine_plan_info",
+            "tdx_moe_gemm_combine"]
 
 
 class tdx_opts(ctypes.Structure):
@@ -78,6 +79,9 @@ def _load():
         "tdx_moe_workspace_size": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(SZ)]),
         "tdx_moe_plan_info": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
         "tdx_moe_dispatch_gemm": (I, [PP, PP, P, P, P, P, P, SZ, I, I, I, I, I, I, I, OP, P]),
+        "tdx_moe_combine_workspace_size": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(SZ)]),
+        "tdx_moe_combine_plan_info": (I, [I, I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
+        "tdx_moe_gemm_combine": (I, [P, PP, P, PP, PP, P, SZ, I, I, I, I, I, I, I, OP, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -238,7 +242,7 @@ def check(status: int, what: str = "tdx") -> None:
 
 # ------------------------------------------------------------------ mixture-of-experts dispatch
 MOE_PLAN_KEYS = ["BN", "tiles_n", "max_tiles", "n_chunks", "total_rows", "off_chunk_flags", "off_ntiles",
-                 "off_offsets", "off_src", "off_tiles", "off_R", "total", "num_kb"]
+                 "off_offsets", "off_src", "off_tiles", "off_R", "total", "num_kb", "off_tokcnt", "off_dest"]
 
 
 def tdx_moe_workspace_size(W: int, T: int, H: int, F: int, E: int, topk: int, dtype: int, opts=None) -> int:
@@ -264,3 +268,27 @@ def tdx_moe_dispatch_gemm(X, topk_idx, B_experts, Y, dest, expert_offsets, works
     return int(_lib.tdx_moe_dispatch_gemm(_ptr_array(X), _ptr_array(topk_idx), _ptr(B_experts), _ptr(Y), _ptr(dest),
                                           _ptr(expert_offsets), _ptr(workspace), wsb, W, T, H, F, E, topk, dtype,
                                           _opts_ref(opts), _stream(stream)))
+
+
+def tdx_moe_combine_workspace_size(W: int, T: int, F: int, H: int, E: int, topk: int, dtype: int, opts=None) -> int:
+    out = ctypes.c_size_t(0)
+    st = _lib.tdx_moe_combine_workspace_size(W, T, F, H, E, topk, dtype, _opts_ref(opts), ctypes.byref(out))
+    if st != TDX_OK:
+        raise TdxError(st, "tdx_moe_combine_workspace_size")
+    return int(out.value)
+
+
+def tdx_moe_combine_plan_info(W: int, T: int, F: int, H: int, E: int, topk: int, dtype: int, opts=None) -> dict:
+    info = (ctypes.c_int64 * len(MOE_PLAN_KEYS))()
+    st = _lib.tdx_moe_combine_plan_info(W, T, F, H, E, topk, dtype, _opts_ref(opts), info)
+    if st != TDX_OK:
+        raise TdxError(st, "tdx_moe_combine_plan_info")
+    return {k: int(info[i]) for i, k in enumerate(MOE_PLAN_KEYS)}
+
+
+def tdx_moe_gemm_combine(Hd, topk_idx, B_experts, gates, out, workspace, W: int, T: int, F: int, H: int, E: int,
+                         topk: int, dtype: int, opts=None, stream=None, workspace_bytes: int | None = None) -> int:
+    wsb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    return int(_lib.tdx_moe_gemm_combine(_ptr(Hd), _ptr_array(topk_idx), _ptr(B_experts), _ptr_array(gates),
+                                         _ptr_array(out), _ptr(workspace), wsb, W, T, F, H, E, topk, dtype,
+                                         _opts_ref(opts), _stream(stream)))

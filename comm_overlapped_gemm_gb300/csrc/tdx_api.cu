@@ -662,21 +662,29 @@ uint32_t tdx_version(void) { return kVersion; }
 // ================================================================================================
 namespace {
 
+// Dispatch (combine = false): A = receive buffer (total x H, in the workspace), B = E x H x F, the
+// GEMM's N = F. Combine (combine = true): A = the caller's dispatched rows (total x H, here H is the
+// GEMM's K = the expert input width), B = E x H x F with F = the combined output width; the
+// workspace holds the expert outputs Z (total x F bf16), the slot table and per-(token, N-tile)
+// arrival counters instead of the receive buffer.
 struct MoePlan {
   int W = 0, T = 0, H = 0, F = 0, E = 0, k = 0, BN = 0, tiles_n = 0, num_kb = 0;
+  bool combine = false;
   long long total = 0;              // dispatched rows = W * T * k
   int n_chunks = 0, max_tiles = 0;  // 128-row chunks of the receive buffer; tile-table bound
-  size_t off_flags = 0, off_cnt = 0, off_ntiles = 0, ctrl_end = 0;
-  size_t off_offsets = 0, off_src = 0, off_tiles = 0, off_R = 0, bytes = 0;
+  size_t off_flags = 0, off_cnt = 0, off_ntiles = 0, off_tokcnt = 0, ctrl_end = 0;
+  size_t off_offsets = 0, off_src = 0, off_dest = 0, off_tiles = 0, off_R = 0, bytes = 0;
 };
 
-tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dtype, const tdx_opts& o, MoePlan* out) {
+tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dtype, const tdx_opts& o, MoePlan* out,
+                         bool combine = false) {
   if (W < 1 || W > kMaxW || T < 0 || H < 0 || F < 0 || E < 1 || k < 1 || k > E) return TDX_ERR_INVALID_ARG;
-  if (E > kMoeMaxExperts) return TDX_ERR_UNSUPPORTED;
+  if (E > kMoeMaxExperts || (combine && k > kMoeMaxTopk)) return TDX_ERR_UNSUPPORTED;
   if (dtype == TDX_FP8_E4M3) return TDX_ERR_UNSUPPORTED;
   if (dtype != TDX_BF16) return TDX_ERR_INVALID_ARG;
   if (o.split_k > 1 || o.cluster > 1 || o.bf16_partials != 0 || o.out_dtype != TDX_BF16) return TDX_ERR_UNSUPPORTED;
   MoePlan p;
+  p.combine = combine;
   p.W = W;
   p.T = T;
   p.H = H;
@@ -700,15 +708,19 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   off += static_cast<size_t>(p.n_chunks) * 4;
   p.off_ntiles = off;
   off += 8;
+  p.off_tokcnt = off;
+  if (combine) off += static_cast<size_t>(W) * T * p.tiles_n * 4;
   p.ctrl_end = off = align_up(off, 1024);
   p.off_offsets = off;
   off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
   p.off_src = off;
   off = align_up(off + static_cast<size_t>(p.total) * 4, 256);
+  p.off_dest = off;
+  if (combine) off = align_up(off + static_cast<size_t>(p.total) * 4, 256);
   p.off_tiles = off;
   off = align_up(off + static_cast<size_t>(p.max_tiles) * 16, 1024);
-  p.off_R = off;
-  off = align_up(off + static_cast<size_t>(p.total) * H * 2, 1024);
+  p.off_R = off;   // dispatch: receive buffer (total x H); combine: expert outputs Z (total x F)
+  off = align_up(off + static_cast<size_t>(p.total) * (combine ? F : H) * 2, 1024);
   p.bytes = off;
   *out = p;
   return TDX_OK;
@@ -752,10 +764,140 @@ tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dt
   MoePlan pl;
   tdx_status s = make_moe_plan(W, T, H, F, E, topk, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const int64_t v[13] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
+  const int64_t v[15] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
                          (int64_t)pl.off_ntiles, (int64_t)pl.off_offsets, (int64_t)pl.off_src, (int64_t)pl.off_tiles,
-                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb};
+                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb, 0, 0};
   std::memcpy(info, v, sizeof(v));
+  return TDX_OK;
+}
+
+tdx_status tdx_moe_combine_workspace_size(int W, int T, int F, int H, int E, int topk, tdx_dtype dtype,
+                                          const tdx_opts* opts, size_t* bytes) {
+  if (bytes == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, F, H, E, topk, dtype, o, &pl, true);
+  if (s != TDX_OK) return s;
+  *bytes = pl.bytes;
+  return TDX_OK;
+}
+
+tdx_status tdx_moe_combine_plan_info(int W, int T, int F, int H, int E, int topk, tdx_dtype dtype,
+                                     const tdx_opts* opts, int64_t* info) {
+  if (info == nullptr) return TDX_ERR_INVALID_ARG;
+  const tdx_opts o = opts ? *opts : defaults();
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, F, H, E, topk, dtype, o, &pl, true);
+  if (s != TDX_OK) return s;
+  const int64_t v[15] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
+                         (int64_t)pl.off_ntiles, (int64_t)pl.off_offsets, (int64_t)pl.off_src, (int64_t)pl.off_tiles,
+                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb, (int64_t)pl.off_tokcnt,
+                         (int64_t)pl.off_dest};
+  std::memcpy(info, v, sizeof(v));
+  return TDX_OK;
+}
+
+tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, const void* B_experts,
+                                const float* const* gates, void* const* out, void* workspace, size_t workspace_bytes,
+                                int W, int T, int F, int H, int E, int topk, tdx_dtype dtype, const tdx_opts* opts,
+                                void* stream) {
+  const tdx_opts o = opts ? *opts : defaults();
+  if (Hd == nullptr || topk_idx == nullptr || B_experts == nullptr || gates == nullptr || out == nullptr)
+    return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
+  for (int s = 0; s < W; ++s)
+    if (topk_idx[s] == nullptr || gates[s] == nullptr || out[s] == nullptr) return TDX_ERR_INVALID_ARG;
+  if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
+  if (o.mode == TDX_CONSUMER_ONLY || o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;
+  MoePlan pl;
+  tdx_status s = make_moe_plan(W, T, F, H, E, topk, dtype, o, &pl, true);
+  if (s != TDX_OK) return s;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(out[r]) || (reinterpret_cast<uintptr_t>(topk_idx[r]) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(gates[r]) & 3u) != 0)
+      return TDX_ERR_ALIGNMENT;
+  if (!aligned16(Hd) || !aligned16(B_experts)) return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(F) * 2) % 16 != 0 || (static_cast<long long>(H) * 2) % 16 != 0) return TDX_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.bytes)
+    return TDX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (pl.total == 0 || H == 0) return TDX_OK;
+  if (o.epoch == 0) {
+    s = fill_zero(ws + pl.off_flags, pl.ctrl_end - pl.off_flags, st);
+    if (s != TDX_OK) return s;
+  }
+  // 1. routing layout on the device (the same as the dispatch's)
+  static thread_local MoeLayoutParams lq;
+  std::memset(&lq, 0, sizeof(lq));
+  for (int r = 0; r < W; ++r) lq.topk[r] = topk_idx[r];
+  lq.dest = reinterpret_cast<int32_t*>(ws + pl.off_dest);
+  lq.src = reinterpret_cast<int32_t*>(ws + pl.off_src);
+  lq.offsets = reinterpret_cast<int32_t*>(ws + pl.off_offsets);
+  lq.user_offsets = nullptr;
+  lq.tiles = reinterpret_cast<int4*>(ws + pl.off_tiles);
+  lq.ntiles = reinterpret_cast<int32_t*>(ws + pl.off_ntiles);
+  lq.status = reinterpret_cast<uint32_t*>(ws);
+  lq.W = W;
+  lq.T = T;
+  lq.k = topk;
+  lq.E = E;
+  lq.max_tiles = pl.max_tiles;
+  if (launch_moe_layout(lq, st) != cudaSuccess) return TDX_ERR_CUDA;
+  if (F == 0) {
+    for (int r = 0; r < W; ++r) {
+      s = fill_zero(out[r], static_cast<size_t>(T) * H * 2, st);
+      if (s != TDX_OK) return s;
+    }
+    return TDX_OK;
+  }
+  // 2. fused grouped GEMM + combine
+  static thread_local KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.op = OP_MOE_COMBINE;
+  kp.mode = o.mode;
+  kp.W = W;
+  kp.M = static_cast<int>(pl.total);
+  kp.K = F;
+  kp.N = H;
+  kp.M_local = kp.M;
+  kp.tiles_m = pl.n_chunks;
+  kp.tiles_n = pl.tiles_n;
+  kp.T = pl.max_tiles;
+  kp.group_n = pl.tiles_n;
+  kp.rank_block = 1;
+  kp.L = 1;
+  kp.num_kb = pl.num_kb;
+  kp.status = reinterpret_cast<uint32_t*>(ws);
+  kp.trace = static_cast<uint32_t*>(o.trace);
+  kp.epoch = o.epoch == 0 ? 1u : o.epoch;
+  kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
+  kp.perturb = o.perturb_seed;
+  kp.row_bytes = static_cast<long long>(F) * 2;
+  kp.G = ws + pl.off_R;
+  for (int r = 0; r < W; ++r) {
+    kp.out[r] = static_cast<uint8_t*>(out[r]);
+    kp.moe_gates[r] = gates[r];
+  }
+  kp.moe_src = lq.src;
+  kp.moe_tiles = lq.tiles;
+  kp.moe_ntiles = lq.ntiles;
+  kp.moe_T = T;
+  kp.moe_k = topk;
+  kp.moe_dest = lq.dest;
+  kp.moe_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tokcnt);
+  kp.copy_active = 0;
+  kp.wait_flags = 0;
+  int grid = device_sms();
+  if (grid <= 0) return TDX_ERR_CUDA;
+  if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
+  if (!make_map(&kp.tm_a[0], Hd, false, pl.total, F, 64, kBM) || !make_map_3d(&kp.tm_b[0], B_experts, E, F, H, 64, 64))
+    return TDX_ERR_CUDA;
+  const cudaError_t e = launch_fused_moe_combine_bf16(pl.BN, kp, grid, st);
+  if (e != cudaSuccess) {
+    if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
+    return TDX_ERR_CUDA;
+  }
   return TDX_OK;
 }
 

@@ -45,9 +45,11 @@ constexpr int kRefSMs = 148;             // fixed SM count used only for the (ho
 // (per-slot barrier/commit overhead and a 64-byte-swizzled A operand cost more than the depth buys).
 constexpr int k_slice_bytes(int /*block_n*/) { return 128; }
 
-enum Op { OP_AG = 0, OP_RS = 1, OP_MOE = 3 };   // OP_MOE: AllToAll dispatch + grouped GEMM
+// OP_MOE: AllToAll dispatch + grouped GEMM; OP_MOE_COMBINE: grouped GEMM + AllToAll combine
+enum Op { OP_AG = 0, OP_RS = 1, OP_MOE = 3, OP_MOE_COMBINE = 4 };
 constexpr int kOpAllReduce = 2;          // API op code: GEMM+AllReduce (runs the OP_RS kernel)
 constexpr int kMoeMaxExperts = 512;      // layout kernel: per-expert tables live in shared memory
+constexpr int kMoeMaxTopk = 16;          // combine: a token's slots are held in registers
 enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUMER_ONLY = 3 };
 enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4, ROLE_LAYOUT = 5 };
 enum DevStatus { DEV_OK = 0, DEV_BAD_INPUT = 1, DEV_TIMEOUT = 6, DEV_STALE = 7 };
@@ -93,6 +95,10 @@ struct KParams {
   const int32_t* moe_ntiles;     // MoE: [0] tiles in the table, [1] nonzero if the routing was invalid
   int moe_T;                     // MoE: tokens per rank
   int moe_rpp;                   // MoE producer: dispatched rows per piece
+  int moe_k;                     // MoE combine: slots per token
+  const int32_t* moe_dest;       // MoE combine: W x T x k dispatched row of every token slot
+  const float* moe_gates[kMaxW]; // MoE combine: [W] T x k gate weights
+  uint32_t* moe_cnt;             // MoE combine: arrivals per (token, N-tile), reset by the last
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;
@@ -115,8 +121,10 @@ int fused_max_grid_bf16(int op, int pm, int sms);
 int fused_max_grid_fp8(int op, int pm, int sms);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
-// MoE: the fused dispatch + grouped GEMM kernel (bf16, single CTAs).
+// MoE: the fused dispatch + grouped GEMM kernel and the fused grouped GEMM + combine kernel
+// (bf16, single CTAs).
 cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_moe_combine_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
 
 // MoE routing layout: from every rank's top-k expert ids, the dispatched row of every (rank, token,
 // slot), the source of every dispatched row, the expert row offsets and the GEMM tile table.

@@ -134,7 +134,7 @@ struct Item {
 template <int OP, int CL>
 __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, int crank) {
   Item r;
-  if constexpr (OP == OP_MOE) {
+  if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
     // MoE: the tile table lists each expert's 128-row tiles in dispatched-row order (experts
     // ascending), which is the order the producers fill the receive buffer in; N-tiles innermost
     const int t = it / p.tiles_n;
@@ -447,11 +447,80 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
     orow = p.out[0] + (size_t)row * p.N * 2;
   } else if constexpr (OP == OP_MOE) {
     orow = p.out[0] + (size_t)row * p.N * 2;    // rows past the tile's expert arrive as row >= M
+  } else if constexpr (OP == OP_MOE_COMBINE) {
+    orow = p.G + (size_t)row * p.N * 2;         // expert outputs, dispatched order (bf16)
   } else {
     const int j = row / p.M_local;
     orow = p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2;
   }
   store_row_chunk(orow, p, col, v, pol);
+}
+
+// MoE combine of one token over columns [col0, col0 + ncols), one warp: lane l takes the 8
+// columns col0 + 8l .. col0 + 8l + 7 and keeps the k expert-output loads of its slots in flight
+// together. out_s[t] = sum_j g[s][t][j] * Z[dest[s][t][j]] in slot order j = 0..k-1 (fp32 fused
+// multiply-adds), rounded once to bf16. The expert-output rows were written by other CTAs: read
+// through L2.
+static __device__ __noinline__ void moe_combine_warp(const KParams& p, int tok, int col0, int ncols, int lane) {
+  const int s = tok / p.moe_T;
+  const int t = tok - s * p.moe_T;
+  const int k = p.moe_k;
+  const int c = col0 + 8 * lane;
+  if (8 * lane >= ncols || c >= p.N) return;
+  const uint64_t once = policy_evict_first();
+  const bool full = c + 8 <= p.N;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  // slots in groups of 8: a group's loads are in flight together, the sum keeps slot order
+#pragma unroll 1
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 zr[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      if (j < k) {
+        const uint8_t* zp = p.G + (size_t)p.moe_dest[(size_t)tok * k + j] * p.N * 2 + (size_t)c * 2;
+        if (full) {
+          zr[jj] = ld_cg_v4_hint(zp, once);
+        } else {
+          uint16_t hv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hv[i] = c + i < p.N ? reinterpret_cast<const uint16_t*>(zp)[i] : 0;
+          zr[jj] = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16),
+                              hv[4] | (uint32_t(hv[5]) << 16), hv[6] | (uint32_t(hv[7]) << 16));
+        }
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      if (j < k) {
+        const float g = p.moe_gates[s][(size_t)t * k + j];
+        float z[8];
+        unpack_bf16x8(zr[jj], z);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, z[i], acc[i]);
+      }
+    }
+  }
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[s] + (size_t)t * p.N * 2) + c;
+  if (full) {
+    uint4 pk;
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
+    pk.x = *reinterpret_cast<uint32_t*>(&b0);
+    pk.y = *reinterpret_cast<uint32_t*>(&b1);
+    pk.z = *reinterpret_cast<uint32_t*>(&b2);
+    pk.w = *reinterpret_cast<uint32_t*>(&b3);
+    st_v4(o, pk);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c + i < p.N) o[i] = __float2bfloat16_rn(acc[i]);
+  }
 }
 
 // PM (pair mode): 0 = single CTAs; 1 = CTA pairs sharing the B slice by TMA multicast, each CTA
@@ -513,7 +582,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   }
   if (threadIdx.x == kTmaWarp * 32) {
-    const int na = OP == OP_MOE ? 1 : (OP == OP_AG && !p.pull_a ? 2 : p.W);
+    const int na = (OP == OP_MOE || OP == OP_MOE_COMBINE) ? 1 : (OP == OP_AG && !p.pull_a ? 2 : p.W);
     const int nb = OP == OP_RS ? p.W : 1;
     for (int i = 0; i < na; ++i) tma_prefetch_map(&p.tm_a[i]);
     for (int i = 0; i < nb; ++i) tma_prefetch_map(&p.tm_b[i]);
@@ -536,7 +605,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   const bool rs_move_only = rs && p.mode == MODE_MOVE_ONLY;
   int t_dyn = p.T;
   bool moe_bad = false;
-  if constexpr (OP == OP_MOE) {
+  if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
     // the count of 128-row tiles is known only on the device (written by the layout kernel before
     // this launch; never above the host's bound p.T); every one is cut into tiles_n N-tiles
     moe_bad = p.moe_ntiles[1] != 0;
@@ -602,7 +671,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               fence_proxy_async_global();
             }
           }
-        } else if (OP == OP_MOE) {
+        } else if (OP == OP_MOE || OP == OP_MOE_COMBINE) {
           map_a = &p.tm_a[0];
           map_b = &p.tm_b[0];
           if (p.wait_flags) {
@@ -664,7 +733,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
-            if constexpr (OP == OP_MOE) {
+            if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
   #pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_3d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
@@ -999,7 +1068,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               st_f4_hint(sp + j * kBM * 4, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), pol);
           }
         }
-        if (direct_out) store_out_chunk<OP, FP8>(p, (OP == OP_MOE && row >= w.mend) ? p.M : row, w.n0 + col0, v, once);
+        if (direct_out)
+          store_out_chunk<OP, FP8>(p, ((OP == OP_MOE || OP == OP_MOE_COMBINE) && row >= w.mend) ? p.M : row,
+                                   w.n0 + col0, v, once);
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
@@ -1034,6 +1105,36 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             __threadfence();
           }
           *is_last = last ? 1u : 0u;
+        }
+      }
+      if constexpr (OP == OP_MOE_COMBINE) {
+        if (p.mode == MODE_FUSED) {
+          // count the stored expert-output rows of every token, per N-tile; tokens whose k rows are
+          // now all stored are listed, and the epilogue warps fold them (one token per warp task)
+          volatile int* task_n = reinterpret_cast<volatile int*>(misc + 6);
+          int* tasks = reinterpret_cast<int*>(misc + 16);   // [kBM] tokens to combine
+          const int et = threadIdx.x - kEpiWarp0 * 32;
+          if (et == 0) *task_n = 0;
+          named_bar_sync(1, kEpiThreads);
+          if (h == 0 && row < w.mend) {
+            const int tok = p.moe_src[row];
+            if (tok >= 0) {
+              if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x40000u + row) & 1023u);
+              __threadfence();
+              const size_t ci = (size_t)tok * p.tiles_n + w.n0 / BN;
+              const uint32_t old = atomicAdd(p.moe_cnt + ci, 1u);
+              if (old == static_cast<uint32_t>(p.moe_k - 1)) {
+                p.moe_cnt[ci] = 0u;
+                tasks[atomicAdd(const_cast<int*>(task_n), 1)] = tok;
+              }
+            }
+          }
+          named_bar_sync(1, kEpiThreads);
+          const int nt_tasks = *task_n;
+          if (nt_tasks > 0) {
+            __threadfence();
+            for (int i = e; i < nt_tasks; i += kNumEpiWarps) moe_combine_warp(p, tasks[i], w.n0, BN, lane);
+          }
         }
       }
       if (slotted) {
@@ -1135,6 +1236,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               for (int l = et; l < (int)(sbytes / 128); l += kEpiThreads)
                 discard_l2_line(reinterpret_cast<uint8_t*>(p.sbuf) + ((size_t)c * p.T + w.tile) * sbytes + (size_t)l * 128);
           }
+        }
+      }
+    }
+    if constexpr (OP == OP_MOE_COMBINE) {
+      if (p.mode == MODE_MOVE_ONLY && !moe_bad) {
+        // the combine alone (expert outputs already in place): one (token, N-tile) per warp task
+        const long long units = (long long)p.W * p.moe_T * p.tiles_n;
+        for (long long u = (long long)blockIdx.x * kNumEpiWarps + e; u < units; u += (long long)grid * kNumEpiWarps) {
+          const int tok = static_cast<int>(u / p.tiles_n);
+          moe_combine_warp(p, tok, static_cast<int>(u - (long long)tok * p.tiles_n) * BN, BN, lane);
         }
       }
     }

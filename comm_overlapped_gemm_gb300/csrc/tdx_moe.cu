@@ -193,4 +193,13 @@ cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaS
   }
 }
 
+cudaError_t launch_fused_moe_combine_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream) {
+  switch (block_n) {
+    case 64: return launch_fused_t<64, false, OP_MOE_COMBINE, 0>(p, grid, stream);
+    case 128: return launch_fused_t<128, false, OP_MOE_COMBINE, 0>(p, grid, stream);
+    case 256: return launch_fused_t<256, false, OP_MOE_COMBINE, 0>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace tdx

@@ -237,14 +237,49 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
                                  void* Y, int32_t* dest, int32_t* expert_offsets, void* workspace,
                                  size_t workspace_bytes, int W, int T, int H, int F, int E, int topk,
                                  tdx_dtype dtype, const tdx_opts* opts, void* stream);
-/* Plan of one MoE call (13 words to info): [0] tile width, [1] N-tiles, [2] tile-table capacity,
- * [3] 128-row chunks of the receive buffer (one flag each), [4] dispatched rows W*T*topk, byte
+/* Plan of one MoE call (15 words to info): [0] tile width, [1] N-tiles, [2] tile-table capacity,
+ * [3] 128-row chunks of the dispatched rows (one flag each), [4] dispatched rows W*T*topk, byte
  * offsets in the workspace of [5] chunk flags (uint32 per chunk), [6] tile count + invalid-routing
  * words, [7] expert offsets (int32 [E+1]), [8] source of every dispatched row (int32, s*T + t),
- * [9] tile table (int32x4 {first row, end row of the expert, expert, 0}), [10] receive buffer,
- * [11] total workspace bytes, [12] 128-byte K blocks. */
+ * [9] tile table (int32x4 {first row, end row of the expert, expert, 0}), [10] receive buffer
+ * (dispatch) / expert outputs Z (combine, (W*T*topk) x H bf16 in dispatched order), [11] total
+ * workspace bytes, [12] 128-byte K blocks, [13] per-(token, N-tile) arrival counters (combine; 0
+ * for the dispatch), [14] dispatched row of every token slot (combine, int32 W x T x topk; 0). */
 tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype,
                              const tdx_opts* opts, int64_t* info);
+
+/* ---------------------------------------------------------------------------------------------
+ * Mixture-of-experts grouped GEMM + AllToAll combine (the reverse of the dispatch above; same
+ * article section: AllToAll is chunked and paired with compute tiles).
+ *
+ * Hd holds the dispatched rows ((W*T*topk) x F bf16) in the order tdx_moe_dispatch_gemm lays out
+ * for the same routing topk_idx (grouped by expert, then source rank, then token). Expert e's rows
+ * are multiplied by B_experts[e] (F x H) into expert outputs Z, rounded once to bf16 (the type a
+ * rank sends back), kept in the workspace in dispatched order; then every token is combined on its
+ * source rank with its gates:
+ *   out[s][t] = round_bf16( sum_{j=0}^{topk-1} gates[s][t][j] * Z[row of (s, t, j)] ),
+ * the sum in slot order j (fp32 fused multiply-adds). A token's combine runs as soon as the tiles
+ * holding all its rows are stored (an arrival counter per (token, N-tile); the last arriver folds),
+ * so the combine overlaps the GEMM and the result does not depend on timing.
+ *  Hd         device pointer, (W*T*topk) x F bf16 (16-byte aligned).
+ *  topk_idx   host array of W device pointers, each T x topk int32 expert ids in [0, E).
+ *  B_experts  device pointer, E x F x H bf16.
+ *  gates      host array of W device pointers, each T x topk fp32.
+ *  out        host array of W device pointers, each T x H bf16 (output).
+ *  workspace  tdx_moe_combine_workspace_size() bytes, 256-byte aligned, zeroed once by
+ *             tdx_workspace_init (layout tables, counters, Z).
+ *  F, H multiples of 8; topk <= 16; 1 <= topk <= E <= 512; bf16 only. opts.mode: TDX_FUSED,
+ *  TDX_GEMM_ONLY (Z only, no combine), TDX_MOVE_ONLY (combine only, from the Z of an earlier
+ *  call with the same routing). */
+tdx_status tdx_moe_combine_workspace_size(int W, int T, int F, int H, int E, int topk, tdx_dtype dtype,
+                                          const tdx_opts* opts, size_t* bytes);
+tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, const void* B_experts,
+                                const float* const* gates, void* const* out, void* workspace,
+                                size_t workspace_bytes, int W, int T, int F, int H, int E, int topk,
+                                tdx_dtype dtype, const tdx_opts* opts, void* stream);
+/* Plan of one combine call: the 15 words of tdx_moe_plan_info, [10] = Z, [13] and [14] set. */
+tdx_status tdx_moe_combine_plan_info(int W, int T, int F, int H, int E, int topk, tdx_dtype dtype,
+                                     const tdx_opts* opts, int64_t* info);
 
 /* Synchronise `stream`, then read the workspace's device status word into *out (TDX_OK, or the
  * first device-side error since tdx_workspace_init). If detail is not NULL it receives 8 words:

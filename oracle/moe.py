@@ -118,19 +118,51 @@ def moe_combine(Z: np.ndarray, dest, gates):
     return outs
 
 
+def moe_grouped_gemm(h, topk, b_experts, E: int, dtype: str = "bf16", rows=None):
+    """Grouped GEMM over rows already in the dispatched order, unrounded fp64: row r of expert e
+    (``offsets[e] <= r < offsets[e+1]`` for the layout of ``topk``) gives ``h[r] @ B_e``. All rows,
+    or only ``rows`` when given."""
+    _, offsets, _, _ = moe_layout(topk, E)
+    H = b_experts.shape[2]
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        out = np.zeros((len(rows), H), dtype=np.float64)
+        for e in np.unique([row_expert(offsets, int(r)) for r in rows]):
+            sel = [i for i, r in enumerate(rows) if row_expert(offsets, int(r)) == e]
+            out[sel] = decode(h[rows[sel]], dtype) @ decode(b_experts[e], dtype)
+        return out
+    Z = np.zeros((h.shape[0], H), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r0 < r1:
+            Z[r0:r1] = decode(h[r0:r1], dtype) @ decode(b_experts[e], dtype)
+    return Z
+
+
+def moe_gemm_combine_rows(h, topk, b_experts, gates, E: int, tokens, dtype: str = "bf16", z_dtype: str = "bf16"):
+    """Combined outputs of the (rank, token) pairs in ``tokens`` only: ``out_s[t]`` of
+    :func:`moe_gemm_combine` for each pair, as an array (len(tokens) x H)."""
+    _, _, dest, _ = moe_layout(topk, E)
+    rows = sorted({int(dest[s][t, j]) for (s, t) in tokens for j in range(dest[s].shape[1])})
+    Zr = moe_grouped_gemm(h, topk, b_experts, E, dtype, rows=rows)
+    if z_dtype == "bf16":
+        Zr = decode_bf16(round_bf16_rne(Zr))
+    at = {r: i for i, r in enumerate(rows)}
+    out = np.zeros((len(tokens), b_experts.shape[2]), dtype=np.float64)
+    for i, (s, t) in enumerate(tokens):
+        for j in range(dest[s].shape[1]):
+            out[i] += float(gates[s][t, j]) * Zr[at[int(dest[s][t, j])]]
+    return out
+
+
 def moe_gemm_combine(h, topk, b_experts, gates, E: int, dtype: str = "bf16", z_dtype: str = "fp32"):
     """Grouped GEMM + AllToAll combine, unrounded fp64. ``h`` is the dispatched activations
     (W*T*k x F, bf16 bits, the rows in the dispatch layout of ``topk``), ``b_experts`` E x F x H.
     Row r of expert e gives ``Z[r] = h[r] @ B_e``; with ``z_dtype="bf16"`` each Z row is rounded to
     bf16 first (the type a rank would send back), else it enters the sum exactly. Returns the W
     combined outputs (T x H) of :func:`moe_combine`."""
-    _, offsets, dest, _ = moe_layout(topk, E)
-    H = b_experts.shape[2]
-    Z = np.zeros((h.shape[0], H), dtype=np.float64)
-    for e in range(E):
-        r0, r1 = int(offsets[e]), int(offsets[e + 1])
-        if r0 < r1:
-            Z[r0:r1] = decode(h[r0:r1], dtype) @ decode(b_experts[e], dtype)
+    _, _, dest, _ = moe_layout(topk, E)
+    Z = moe_grouped_gemm(h, topk, b_experts, E, dtype)
     if z_dtype == "bf16":
         Z = decode_bf16(round_bf16_rne(Z))
     elif z_dtype != "fp32":

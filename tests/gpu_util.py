@@ -202,3 +202,42 @@ class MoECase:
     def plan(self, opts=None):
         return tdx.tdx_moe_plan_info(self.W, self.T, self.H, self.F, self.E, self.k, tdx.TDX_BF16,
                                      opts if opts is not None else self.opts)
+
+
+class CombineCase:
+    """Device buffers of one grouped GEMM + AllToAll combine problem (workload op "moe_combine":
+    M tokens per rank, K = expert input width F, N = hidden width H)."""
+
+    def __init__(self, inp, opts=None):
+        wl = inp.wl
+        self.inp, self.wl = inp, wl
+        self.W, self.T, self.F, self.H, self.E, self.k = wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk
+        self.Hd = dev_bits(inp.a[0])
+        self.route = [torch.from_numpy(np.ascontiguousarray(r)).cuda() for r in inp.route]
+        self.gates = [torch.from_numpy(np.ascontiguousarray(g)).cuda() for g in inp.gates]
+        self.B = dev_bits(inp.b[0])
+        self.out = [torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(wl.W)]
+        self.opts = opts
+        n = tdx.tdx_moe_combine_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16, opts)
+        self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        tdx.check(tdx.tdx_workspace_init(self.ws), "init")
+
+    def run(self, opts=None):
+        o = opts if opts is not None else self.opts
+        return tdx.tdx_moe_gemm_combine(self.Hd, self.route, self.B, self.gates, self.out, self.ws, self.W, self.T,
+                                        self.F, self.H, self.E, self.k, tdx.TDX_BF16, o)
+
+    def result_bits(self) -> np.ndarray:
+        torch.cuda.synchronize()
+        return np.stack([host_bits(o) for o in self.out])
+
+    def plan(self, opts=None):
+        return tdx.tdx_moe_combine_plan_info(self.W, self.T, self.F, self.H, self.E, self.k, tdx.TDX_BF16,
+                                             opts if opts is not None else self.opts)
+
+    def z_bits(self) -> np.ndarray:
+        pl = self.plan()
+        rows = pl["total_rows"]
+        torch.cuda.synchronize()
+        z = self.ws[pl["off_R"]:pl["off_R"] + rows * self.H * 2].view(torch.int16).cpu().numpy().view(np.uint16)
+        return z.reshape(rows, self.H)

@@ -253,3 +253,27 @@ def test_planted_dispatch_mistakes_are_caught(mut, golden):
     except AssertionError:
         caught += 1
     assert caught > 0
+
+
+def test_grouped_gemm_rows_and_combine_rows_match_full():
+    rng = np.random.default_rng(21)
+    W, T, E, k, F, H = 2, 5, 4, 2, 6, 5
+    topk = random_routing(rng, W, T, E, k)
+    h = rand_bf16_bits(rng, (W * T * k, F), False)
+    b = np.stack([rand_bf16_bits(rng, (F, H), False) for _ in range(E)])
+    gates = [rng.uniform(0, 1, size=(T, k)).astype(np.float32) for _ in range(W)]
+    Z = MO.moe_grouped_gemm(h, topk, b, E)
+    rows = [0, 3, 7, 19]
+    assert np.array_equal(MO.moe_grouped_gemm(h, topk, b, E, rows=rows), Z[rows])
+    _, offsets, _, _ = MO.moe_layout(topk, E)
+    for r in rows:                                   # brute force: h[r] @ B_e in exact rationals
+        e = MO.row_expert(offsets, r)
+        for n in range(H):
+            exact = sum((bf16_bits_to_fraction(int(h[r, f])) * bf16_bits_to_fraction(int(b[e, f, n]))
+                         for f in range(F)), Fraction(0))
+            assert abs(Fraction(Z[r, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 70)
+    full = MO.moe_gemm_combine(h, topk, b, gates, E, z_dtype="bf16")
+    toks = [(0, 0), (1, 4), (0, 3)]
+    got = MO.moe_gemm_combine_rows(h, topk, b, gates, E, toks)
+    for i, (s, t) in enumerate(toks):
+        assert np.array_equal(got[i], full[s][t])
