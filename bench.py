@@ -774,6 +774,28 @@ def run_case(args):
     return 0
 
 
+def run_moe_case(args):
+    """One MoE op on a given shape (profiling helper): --case moe|moe_combine --shape W,T,K,N,E,topk
+    (moe: K = hidden, N = expert width; moe_combine: K = expert width, N = hidden) --mode."""
+    import torch
+    import comm_overlapped_gemm_gb300 as tdx
+    import workloads as wls
+    W, T, K, N, E, k = (int(x) for x in args.shape.split(","))
+    name = "moe_w8" if args.case == "moe" else "moe_combine_w8"
+    wl = wls.with_shape(wls.WORKLOADS[name], W=W, M=T, K=K, N=N, E=E, topk=k)
+    dev = torch.device("cuda", 0)
+    call, status = (moe_case if args.case == "moe" else combine_case)(tdx, torch, wl, dev)
+    mode = {"fused": 0, "gemm": 1, "move": 2}[args.mode]
+    for _ in range(args.warmup + args.steps):
+        call(mode=mode)
+    torch.cuda.synchronize()
+    status()
+    ms = time_mode(torch, lambda: call(mode=mode), 5)
+    print(json.dumps({"case": args.case, "shape": [W, T, K, N, E, k], "mode": args.mode, "ms": ms,
+                      "tflops": wl.flops / (ms * 1e-3) / 1e12}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -782,7 +804,8 @@ def main():
     ap.add_argument("--impl", default="tdx", choices=["tdx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra configurations")
-    ap.add_argument("--case", choices=["ag", "rs"], default=None)
+    ap.add_argument("--case", choices=["ag", "rs", "moe", "moe_combine"], default=None)
+    ap.add_argument("--mode", choices=["fused", "gemm", "move"], default="fused", help="--case moe* only")
     ap.add_argument("--shape", default="8,1024,8192,3584")
     ap.add_argument("--opts", default="", help="--case only: tdx_opts fields, e.g. block_n=256,split_k=4")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
@@ -794,6 +817,8 @@ def main():
         return 0
     if args.impl == "reference":
         return run_reference(args)
+    if args.case in ("moe", "moe_combine"):
+        return run_moe_case(args)
     if args.case is not None:
         return run_case(args)
     return run_gpu(args)

@@ -242,3 +242,37 @@ def test_moe_plan(tdx):
     assert p["total_rows"] == 262144 and p["n_chunks"] == 2048 and p["max_tiles"] == 2048 + 64
     assert p["BN"] == 256 and p["tiles_n"] == 8 and p["num_kb"] == 112
     assert p["total"] - p["off_R"] == 262144 * 7168 * 2
+
+
+def test_moe_combine_validation_codes(tdx):
+    def ws_size(W=2, T=8, F=64, H=64, E=4, k=2, dtype=0):
+        try:
+            tdx.tdx_moe_combine_workspace_size(W, T, F, H, E, k, dtype)
+            return tdx.TDX_OK
+        except tdx.TdxError as e:
+            return e.status
+
+    assert ws_size() == tdx.TDX_OK
+    assert ws_size(E=32, k=17) == tdx.TDX_ERR_UNSUPPORTED      # more than 16 slots per token
+    assert ws_size(k=5) == tdx.TDX_ERR_INVALID_ARG
+    assert ws_size(dtype=1) == tdx.TDX_ERR_UNSUPPORTED
+
+    def comb(Hd=FAKE, R=None, B=FAKE, G=None, O=None, W=2, T=8, F=64, H=64, E=4, k=2, opts=None, wsb=1 << 30):
+        R = [FAKE] * W if R is None else R
+        G = [FAKE] * W if G is None else G
+        O = [FAKE] * W if O is None else O
+        return tdx.tdx_moe_gemm_combine(Hd, R, B, G, O, FAKE, W, T, F, H, E, k, tdx.TDX_BF16, opts, stream=0,
+                                        workspace_bytes=wsb)
+
+    assert comb(Hd=0) == tdx.TDX_ERR_INVALID_ARG
+    assert comb(G=[FAKE, 0]) == tdx.TDX_ERR_INVALID_ARG
+    assert comb(O=[0, FAKE]) == tdx.TDX_ERR_INVALID_ARG
+    assert comb(O=[FAKE, FAKE + 8]) == tdx.TDX_ERR_ALIGNMENT
+    assert comb(G=[FAKE + 2, FAKE]) == tdx.TDX_ERR_ALIGNMENT
+    assert comb(F=60) == tdx.TDX_ERR_ALIGNMENT
+    assert comb(wsb=64) == tdx.TDX_ERR_WORKSPACE
+    assert comb(opts=tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY)) == tdx.TDX_ERR_UNSUPPORTED
+    # the plan keeps per-(token, N-tile) counters and the slot table
+    p = tdx.tdx_moe_combine_plan_info(8, 4096, 2048, 7168, 64, 8, tdx.TDX_BF16)
+    assert p["tiles_n"] == 28 and p["off_tokcnt"] > 0 and p["off_dest"] > p["off_src"]
+    assert p["total"] - p["off_R"] == 262144 * 7168 * 2
