@@ -992,10 +992,16 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   int grid = device_sms();
   if (grid <= 0) return TDX_ERR_CUDA;
   if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
-  // producer: one CTA copies a whole 128-row chunk and releases its flag
-  kp.moe_rpp = kBM;
-  kp.ppc = 1;
-  kp.total_pieces = pl.n_chunks;
+  // producer: a CTA copies a whole 128-row chunk and releases its flag; with fewer chunks than CTAs
+  // a chunk is cut into ppc pieces (at most 16) so that every CTA moves rows
+  {
+    int ppc = (grid + pl.n_chunks - 1) / pl.n_chunks;
+    if (ppc < 1) ppc = 1;
+    if (ppc > 16) ppc = 16;
+    kp.ppc = ppc;
+    kp.moe_rpp = (kBM + ppc - 1) / ppc;
+    kp.total_pieces = pl.n_chunks * ppc;
+  }
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
   kp.copy_active = moving ? 1 : 0;
   kp.wait_flags = o.mode == TDX_FUSED ? 1 : 0;

@@ -888,11 +888,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
       }
     } else if (OP == OP_MOE && p.copy_active && !moe_bad) {
-      // AllToAll dispatch: CTAs take whole 128-row chunks of the receive buffer in row order. The
-      // producer threads stage the chunk's row sources (row -> s * T + t) in shared memory and
-      // prefetch upcoming source rows into L2; one thread moves the rows with bulk copies through a
-      // ring of NB shared-memory segments (NB - 1 loads in flight, each segment stored back as soon
-      // as it lands), waits for its stores to complete and releases the chunk's flag.
+      // AllToAll dispatch: CTAs take pieces of the receive buffer's 128-row chunks in row order (a
+      // whole chunk, or 1/ppc of it when there are fewer chunks than CTAs). The producer threads
+      // stage the piece's row sources (row -> s * T + t) in shared memory; one thread moves the rows
+      // with bulk copies through a ring of NB shared-memory segments (NB - 1 loads in flight, each
+      // segment stored back as soon as it lands) and waits for its stores to complete; the chunk's
+      // flag is released by its last piece (a per-chunk counter when ppc > 1).
       const int ct = threadIdx.x - kCopyWarp0 * 32;
       int* psrc = reinterpret_cast<int*>(misc + 16);         // [kBM] row sources of the chunk
       const int ntok = p.W * p.moe_T;
@@ -908,9 +909,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         const int s = tok / p.moe_T;
         return p.shard[s] + (long long)(tok - s * p.moe_T) * p.row_bytes + off;
       };
-      for (int ck = blockIdx.x; ck < p.n_chunks; ck += grid) {
-        const int r0 = ck * kBM;
-        const int nrows = min(kBM, p.M - r0);
+      for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
+        const int ck = piece / p.ppc;
+        const int pc = piece - ck * p.ppc;
+        const int r0 = ck * kBM + pc * p.moe_rpp;
+        const int nrows = max(0, min(min(p.moe_rpp, kBM - pc * p.moe_rpp), p.M - r0));
         for (int i = ct; i < nrows; i += kCopyThreads) psrc[i] = p.moe_src[r0 + i];
         named_bar_sync(2, kCopyThreads);
         if (TDX_MOE_PREFETCH_ROWS > 0) {
@@ -919,7 +922,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             if (tok >= 0 && tok < ntok) prefetch_l2_bulk(src_of(tok, 0), rb);
           }
         }
-        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + ck) & 4095u);
+        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
         if (ct == 0) {
           const int nseg = nrows * spr;
           auto issue = [&](int i) {
@@ -961,12 +964,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
           gseg += static_cast<uint32_t>(nseg);
-          bulk_wait_all();            // the chunk's rows are written
+          bulk_wait_all();            // the piece's rows are written
           fence_proxy_async_global();
-          const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
-          if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
-          __threadfence();
-          st_release_gpu(p.chunk_flags + ck, p.epoch);
+          bool release = true;
+          if (p.ppc > 1) {
+            __threadfence();
+            const uint32_t old = atomicAdd(p.chunk_cnt + ck, 1u);
+            release = old == static_cast<uint32_t>(p.ppc - 1);
+            if (release) p.chunk_cnt[ck] = 0u;
+          }
+          if (release) {
+            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
+            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
+            __threadfence();
+            st_release_gpu(p.chunk_flags + ck, p.epoch);
+          }
         }
         named_bar_sync(2, kCopyThreads);   // psrc is rewritten for the next chunk
       }
