@@ -242,7 +242,8 @@ def check(status: int, what: str = "tdx") -> None:
 
 # ------------------------------------------------------------------ mixture-of-experts dispatch
 MOE_PLAN_KEYS = ["BN", "tiles_n", "max_tiles", "n_chunks", "total_rows", "off_chunk_flags", "off_ntiles",
-                 "off_offsets", "off_src", "off_tiles", "off_R", "total", "num_kb", "off_tokcnt", "off_dest"]
+                 "off_offsets", "off_src", "off_tiles", "off_R", "total", "num_kb", "off_tokcnt", "off_dest",
+                 "cluster"]
 
 
 def tdx_moe_workspace_size(W: int, T: int, H: int, F: int, E: int, topk: int, dtype: int, opts=None) -> int:

@@ -672,6 +672,7 @@ struct MoePlan {
   bool combine = false;
   long long total = 0;              // dispatched rows = W * T * k
   int n_chunks = 0, max_tiles = 0;  // 128-row chunks of the receive buffer; tile-table bound
+  int PM = 0;                       // 0 single CTAs, 2 2-SM pairs on two tiles of one expert
   size_t off_flags = 0, off_cnt = 0, off_ntiles = 0, off_tokcnt = 0, ctrl_end = 0;
   size_t off_offsets = 0, off_src = 0, off_dest = 0, off_tiles = 0, off_R = 0, bytes = 0;
 };
@@ -682,7 +683,9 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   if (E > kMoeMaxExperts || (combine && k > kMoeMaxTopk)) return TDX_ERR_UNSUPPORTED;
   if (dtype == TDX_FP8_E4M3) return TDX_ERR_UNSUPPORTED;
   if (dtype != TDX_BF16) return TDX_ERR_INVALID_ARG;
-  if (o.split_k > 1 || o.cluster > 1 || o.bf16_partials != 0 || o.out_dtype != TDX_BF16) return TDX_ERR_UNSUPPORTED;
+  if (o.split_k > 1 || o.cluster == 2 || o.cluster < 0 || o.cluster > 3 || o.bf16_partials != 0 ||
+      o.out_dtype != TDX_BF16)
+    return TDX_ERR_UNSUPPORTED;
   MoePlan p;
   p.combine = combine;
   p.W = W;
@@ -700,7 +703,13 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   p.tiles_n = (F + bn - 1) / bn;
   p.num_kb = static_cast<int>((static_cast<long long>(H) * 2 + 127) / 128);
   p.n_chunks = static_cast<int>((p.total + kBM - 1) / kBM);
-  p.max_tiles = p.n_chunks + E;     // every expert adds at most one partial tile
+  // 2-SM pairs (M = 256 per MMA, two tiles of one expert) when the experts average at least 8 tiles:
+  // the tile table then pads every expert to an even tile count (at most one empty tile each)
+  if (o.cluster == 3 || (o.cluster == 0 && bn == 256 && p.total >= 8LL * kBM * E)) {
+    if (bn != 256) return TDX_ERR_UNSUPPORTED;
+    p.PM = 2;
+  }
+  p.max_tiles = p.n_chunks + (p.PM == 2 ? 2 : 1) * E;   // a partial tile (and a pad) per expert
   size_t off = kHeaderBytes;
   p.off_flags = off;
   off += static_cast<size_t>(p.n_chunks) * 4;
@@ -764,9 +773,9 @@ tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dt
   MoePlan pl;
   tdx_status s = make_moe_plan(W, T, H, F, E, topk, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const int64_t v[15] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
+  const int64_t v[16] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
                          (int64_t)pl.off_ntiles, (int64_t)pl.off_offsets, (int64_t)pl.off_src, (int64_t)pl.off_tiles,
-                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb, 0, 0};
+                         (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb, 0, 0, pl.PM == 2 ? 3 : 1};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }
@@ -789,10 +798,10 @@ tdx_status tdx_moe_combine_plan_info(int W, int T, int F, int H, int E, int topk
   MoePlan pl;
   tdx_status s = make_moe_plan(W, T, F, H, E, topk, dtype, o, &pl, true);
   if (s != TDX_OK) return s;
-  const int64_t v[15] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
+  const int64_t v[16] = {pl.BN, pl.tiles_n, pl.max_tiles, pl.n_chunks, pl.total, (int64_t)pl.off_flags,
                          (int64_t)pl.off_ntiles, (int64_t)pl.off_offsets, (int64_t)pl.off_src, (int64_t)pl.off_tiles,
                          (int64_t)pl.off_R, (int64_t)pl.bytes, pl.num_kb, (int64_t)pl.off_tokcnt,
-                         (int64_t)pl.off_dest};
+                         (int64_t)pl.off_dest, pl.PM == 2 ? 3 : 1};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }
@@ -843,6 +852,7 @@ tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, 
   lq.k = topk;
   lq.E = E;
   lq.max_tiles = pl.max_tiles;
+  lq.pair = pl.PM == 2 ? 1 : 0;
   if (launch_moe_layout(lq, st) != cudaSuccess) return TDX_ERR_CUDA;
   if (F == 0) {
     for (int r = 0; r < W; ++r) {
@@ -888,12 +898,14 @@ tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, 
   kp.moe_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tokcnt);
   kp.copy_active = 0;
   kp.wait_flags = 0;
-  int grid = device_sms();
+  int grid = fused_max_grid_moe(true, pl.PM, device_sms());
   if (grid <= 0) return TDX_ERR_CUDA;
   if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
+  grid -= grid % (pl.PM == 2 ? 2 : 1);
+  if (grid <= 0) return TDX_ERR_INVALID_ARG;
   if (!make_map(&kp.tm_a[0], Hd, false, pl.total, F, 64, kBM) || !make_map_3d(&kp.tm_b[0], B_experts, E, F, H, 64, 64))
     return TDX_ERR_CUDA;
-  const cudaError_t e = launch_fused_moe_combine_bf16(pl.BN, kp, grid, st);
+  const cudaError_t e = launch_fused_moe_combine_bf16(pl.BN, pl.PM, kp, grid, st);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;
@@ -950,6 +962,7 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   lq.k = topk;
   lq.E = E;
   lq.max_tiles = pl.max_tiles;
+  lq.pair = pl.PM == 2 ? 1 : 0;
   if (launch_moe_layout(lq, st) != cudaSuccess) return TDX_ERR_CUDA;
   if (F == 0) return TDX_OK;
   if (H == 0) return fill_zero(Y, static_cast<size_t>(pl.total) * F * 2, st);
@@ -989,9 +1002,11 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   kp.moe_tiles = lq.tiles;
   kp.moe_ntiles = lq.ntiles;
   kp.moe_T = T;
-  int grid = device_sms();
+  int grid = fused_max_grid_moe(false, pl.PM, device_sms());
   if (grid <= 0) return TDX_ERR_CUDA;
   if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
+  grid -= grid % (pl.PM == 2 ? 2 : 1);
+  if (grid <= 0) return TDX_ERR_INVALID_ARG;
   // producer: a CTA copies a whole 128-row chunk and releases its flag; with fewer chunks than CTAs
   // a chunk is cut into ppc pieces (at most 16) so that every CTA moves rows
   {
@@ -1008,7 +1023,7 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   if (!make_map(&kp.tm_a[0], kp.G, false, pl.total, H, 64, kBM) ||
       !make_map_3d(&kp.tm_b[0], B_experts, E, H, F, 64, 64))
     return TDX_ERR_CUDA;
-  const cudaError_t e = launch_fused_moe_bf16(pl.BN, kp, grid, st);
+  const cudaError_t e = launch_fused_moe_bf16(pl.BN, pl.PM, kp, grid, st);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;

@@ -123,8 +123,10 @@ cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
 // MoE: the fused dispatch + grouped GEMM kernel and the fused grouped GEMM + combine kernel
 // (bf16, single CTAs).
-cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_fused_moe_combine_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream);
+// pm: 0 single CTAs, 2 2-SM pairs (tile width 256).
+cudaError_t launch_fused_moe_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
+int fused_max_grid_moe(bool combine, int pm, int sms);
 
 // MoE routing layout: from every rank's top-k expert ids, the dispatched row of every (rank, token,
 // slot), the source of every dispatched row, the expert row offsets and the GEMM tile table.
@@ -138,6 +140,7 @@ struct MoeLayoutParams {
   int32_t* ntiles;               // [0] tiles, [1] invalid routing (output)
   uint32_t* status;              // workspace status words
   int W, T, k, E, max_tiles;
+  int pair;                      // pad every expert's tile count to even (CTA pairs)
 };
 cudaError_t launch_moe_layout(const MoeLayoutParams& q, cudaStream_t stream);
 

@@ -136,15 +136,17 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it, int BN, in
   Item r;
   if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
     // MoE: the tile table lists each expert's 128-row tiles in dispatched-row order (experts
-    // ascending), which is the order the producers fill the receive buffer in; N-tiles innermost
-    const int t = it / p.tiles_n;
-    const int4 ti = p.moe_tiles[t];
+    // ascending), which is the order the producers fill the receive buffer in; N-tiles innermost.
+    // With CTA pairs an item is a pair of consecutive tiles of one expert (the table pads every
+    // expert to an even count) and the CTA of cluster rank r takes tile 2*pair + r.
+    const int tp = it / p.tiles_n;
+    const int4 ti = p.moe_tiles[tp * CL + crank];
     r.c = 0;
     r.tile = it;
     r.m0 = ti.x;
     r.mend = ti.y;
     r.e = ti.z;
-    r.n0 = (it - t * p.tiles_n) * BN;
+    r.n0 = (it - tp * p.tiles_n) * BN;
     return r;
   }
   r.mend = 0;
@@ -727,9 +729,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             const uint32_t fbl = mapa_shared(fb, 0);
             tma_load_2d_pair_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fbl, kb * C::BK, arow, keep);
 #pragma unroll
-            for (int jj = 0; jj < C::B_BOXES_CTA; ++jj)
-              tma_load_2d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
-                                    w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep);
+            for (int jj = 0; jj < C::B_BOXES_CTA; ++jj) {
+              if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE)
+                tma_load_3d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
+                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, w.e, keep);
+              else
+                tma_load_2d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
+                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep);
+            }
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
@@ -1348,17 +1355,18 @@ int max_grid_t(int sms) {
     return sms;
   } else {
     using C = Cfg<BN, FP8, PM == 2>;
+    constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
     static int cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
     if (cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+                             kSmem) != cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * sms, 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.dynamicSmemBytes = kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;

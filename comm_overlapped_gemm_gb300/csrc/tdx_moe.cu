@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) tdx_moe_layout_kernel(const
   }
   if (s == 0) {
     // expert offsets and the tile table: expert e's rows [off_e, off_e + n_e) in 128-row tiles
-    const int tc = (n_e + kBM - 1) / kBM;
+    int tc = (n_e + kBM - 1) / kBM;
+    if (q.pair) tc = (tc + 1) & ~1;   // CTA pairs: an even count per expert (a padded tile stores nothing)
     const int toff = block_exclusive_scan(tc, warp_sums, &ntiles);
     if (tid < E) {
       q.offsets[tid] = off_e;
@@ -184,7 +185,8 @@ cudaError_t launch_moe_layout(const MoeLayoutParams& q, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_moe_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
+  if (pm == 2) return block_n == 256 ? launch_fused_t<256, false, OP_MOE, 2>(p, grid, stream) : cudaErrorInvalidValue;
   switch (block_n) {
     case 64: return launch_fused_t<64, false, OP_MOE, 0>(p, grid, stream);
     case 128: return launch_fused_t<128, false, OP_MOE, 0>(p, grid, stream);
@@ -193,13 +195,20 @@ cudaError_t launch_fused_moe_bf16(int block_n, const KParams& p, int grid, cudaS
   }
 }
 
-cudaError_t launch_fused_moe_combine_bf16(int block_n, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
+  if (pm == 2)
+    return block_n == 256 ? launch_fused_t<256, false, OP_MOE_COMBINE, 2>(p, grid, stream) : cudaErrorInvalidValue;
   switch (block_n) {
     case 64: return launch_fused_t<64, false, OP_MOE_COMBINE, 0>(p, grid, stream);
     case 128: return launch_fused_t<128, false, OP_MOE_COMBINE, 0>(p, grid, stream);
     case 256: return launch_fused_t<256, false, OP_MOE_COMBINE, 0>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int fused_max_grid_moe(bool combine, int pm, int sms) {
+  if (pm != 2) return sms;
+  return combine ? max_grid_t<256, false, OP_MOE_COMBINE, 2>(sms) : max_grid_t<256, false, OP_MOE, 2>(sms);
 }
 
 }  // namespace tdx

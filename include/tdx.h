@@ -237,14 +237,18 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
                                  void* Y, int32_t* dest, int32_t* expert_offsets, void* workspace,
                                  size_t workspace_bytes, int W, int T, int H, int F, int E, int topk,
                                  tdx_dtype dtype, const tdx_opts* opts, void* stream);
-/* Plan of one MoE call (15 words to info): [0] tile width, [1] N-tiles, [2] tile-table capacity,
+/* Plan of one MoE call (16 words to info): [0] tile width, [1] N-tiles, [2] tile-table capacity,
  * [3] 128-row chunks of the dispatched rows (one flag each), [4] dispatched rows W*T*topk, byte
  * offsets in the workspace of [5] chunk flags (uint32 per chunk), [6] tile count + invalid-routing
  * words, [7] expert offsets (int32 [E+1]), [8] source of every dispatched row (int32, s*T + t),
  * [9] tile table (int32x4 {first row, end row of the expert, expert, 0}), [10] receive buffer
  * (dispatch) / expert outputs Z (combine, (W*T*topk) x H bf16 in dispatched order), [11] total
  * workspace bytes, [12] 128-byte K blocks, [13] per-(token, N-tile) arrival counters (combine; 0
- * for the dispatch), [14] dispatched row of every token slot (combine, int32 W x T x topk; 0). */
+ * for the dispatch), [14] dispatched row of every token slot (combine, int32 W x T x topk; 0),
+ * [15] CTA cooperation in use: 1 single CTAs, 3 2-SM pairs on two 128-row tiles of one expert
+ * (chosen by default for tile width 256 when the experts average at least 8 tiles; the tile table
+ * then pads every expert to an even count with an empty tile). opts.cluster: 0 library choice,
+ * 1 single, 3 pairs (2: TDX_ERR_UNSUPPORTED). */
 tdx_status tdx_moe_plan_info(int W, int T, int H, int F, int E, int topk, tdx_dtype dtype,
                              const tdx_opts* opts, int64_t* info);
 
@@ -277,7 +281,7 @@ tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, 
                                 const float* const* gates, void* const* out, void* workspace,
                                 size_t workspace_bytes, int W, int T, int F, int H, int E, int topk,
                                 tdx_dtype dtype, const tdx_opts* opts, void* stream);
-/* Plan of one combine call: the 15 words of tdx_moe_plan_info, [10] = Z, [13] and [14] set. */
+/* Plan of one combine call: the 16 words of tdx_moe_plan_info, [10] = Z, [13] and [14] set. */
 tdx_status tdx_moe_combine_plan_info(int W, int T, int F, int H, int E, int topk, tdx_dtype dtype,
                                      const tdx_opts* opts, int64_t* info);
 

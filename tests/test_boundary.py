@@ -237,9 +237,17 @@ def test_moe_validation_codes(tdx):
 
 
 def test_moe_plan(tdx):
-    # 262144 dispatched rows of 7168: 2048 chunks, tile table bound 2048 + 64, receive buffer 3.5 GiB
+    # 262144 dispatched rows of 7168: 2048 chunks; 2-SM pairs (4096 rows per expert on average), so
+    # the tile table holds a partial and a padding tile per expert: 2048 + 2 * 64; receive buffer 3.5 GiB
     p = tdx.tdx_moe_plan_info(8, 4096, 7168, 2048, 64, 8, tdx.TDX_BF16)
-    assert p["total_rows"] == 262144 and p["n_chunks"] == 2048 and p["max_tiles"] == 2048 + 64
+    assert p["total_rows"] == 262144 and p["n_chunks"] == 2048 and p["max_tiles"] == 2048 + 128
+    assert p["cluster"] == 3
+    # 128 tokens per rank: 128 rows per expert on average, single CTAs
+    q = tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16)
+    assert q["cluster"] == 1 and q["max_tiles"] == 64 + 64
+    assert tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(cluster=3))["cluster"] == 3
+    with pytest.raises(tdx.TdxError):
+        tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(cluster=3, block_n=128))
     assert p["BN"] == 256 and p["tiles_n"] == 8 and p["num_kb"] == 112
     assert p["total"] - p["off_R"] == 262144 * 7168 * 2
 

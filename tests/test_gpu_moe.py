@@ -52,9 +52,9 @@ def test_moe_small_shapes(shape, integer):
     wl = wls.with_shape(wls.WORKLOADS["moe_w8"], **shape)
     inp = wls.make_inputs(wl, integer=integer)
     want, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
-    for bn in (0, 64, 256):
-        case = MoECase(inp, opts=opts(block_n=bn))
-        tdx.check(case.run(), f"moe {shape} bn={bn}")
+    for bn, cl in ((0, 0), (64, 0), (256, 1), (256, 3)):
+        case = MoECase(inp, opts=opts(block_n=bn, cluster=cl))
+        tdx.check(case.run(), f"moe {shape} bn={bn} cluster={cl}")
         status_ok(case)
         check_layout(case, lay)
         if integer:
@@ -161,3 +161,16 @@ def test_moe_full_size_sampled_and_deterministic():
     tdx.check(case.run(opts(perturb_seed=17)))
     status_ok(case)
     assert np.array_equal(case.result_bits(), first)
+
+
+def test_moe_pairs_match_single_ctas_bitwise():
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=4, M=300, K=512, N=512, E=8, topk=2)
+    inp = wls.make_inputs(wl, integer=False)
+    bits = []
+    for cl in (1, 3):
+        case = MoECase(inp, opts=opts(block_n=256, cluster=cl, perturb_seed=3))
+        assert case.plan()["cluster"] == cl
+        tdx.check(case.run())
+        status_ok(case)
+        bits.append(case.result_bits())
+    assert np.array_equal(bits[0], bits[1])

@@ -49,9 +49,9 @@ def test_combine_small_shapes(shape, integer):
     inp = wls.make_inputs(wl, integer=integer)
     want = oracle_out(inp)
     Z = MO.moe_grouped_gemm(inp.a[0], inp.route, inp.b[0], wl.E)
-    for bn in (0, 64, 256):
-        case = CombineCase(inp, opts=opts(block_n=bn))
-        tdx.check(case.run(), f"combine {shape} bn={bn}")
+    for bn, cl in ((0, 0), (64, 0), (256, 1), (256, 3)):
+        case = CombineCase(inp, opts=opts(block_n=bn, cluster=cl))
+        tdx.check(case.run(), f"combine {shape} bn={bn} cluster={cl}")
         status_ok(case)
         got = case.result_bits()
         if integer:
