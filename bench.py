@@ -342,21 +342,24 @@ def moe_case(tdx, torch, wl, dev):
     """Device buffers + a timed call for one MoE dispatch + grouped GEMM workload."""
     import workloads as wls
     inp = wls.make_inputs(wl)
-    X = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev) for a in inp.a]
+    view = np.int16 if wl.dtype == "bf16" else np.uint8
+    dt = tdx.TDX_BF16 if wl.dtype == "bf16" else tdx.TDX_FP8_E4M3
+    kw = {} if wl.dtype == "bf16" else dict(scale_a=inp.scale_a, scale_b=inp.scale_b)
+    X = [torch.from_numpy(np.ascontiguousarray(a).view(view)).to(dev) for a in inp.a]
     route = [torch.from_numpy(np.ascontiguousarray(r)).to(dev) for r in inp.route]
-    B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(np.int16)).to(dev)
+    B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(view)).to(dev)
     Y = torch.empty((wl.M_total, wl.N), dtype=torch.bfloat16, device=dev)
     dest = torch.empty((wl.W, wl.M, wl.topk), dtype=torch.int32, device=dev)
-    ws = torch.empty(tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16),
+    ws = torch.empty(tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, dt),
                      dtype=torch.uint8, device=dev)
     tdx.check(tdx.tdx_workspace_init(ws))
     state = {"epoch": 0}
 
     def call(mode=0, epoch=None):
         state["epoch"] += 1
-        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode)
+        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode, **kw)
         tdx.check(tdx.tdx_moe_dispatch_gemm(X, route, B, Y, dest, None, ws, wl.W, wl.M, wl.K, wl.N, wl.E,
-                                            wl.topk, tdx.TDX_BF16, o))
+                                            wl.topk, dt, o))
 
     def status():
         st, d = tdx.tdx_read_device_status(ws)
@@ -519,6 +522,32 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     res["moe_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
                      "tflops": tf, "frac_of_peak": tf / peak_bf16, "dispatch_bytes": moved,
                      "dispatch_gbs_alone": moved / (m * 1e-3) / 1e9}
+    del call, status
+    # the same in e4m3 (tokens and expert weights quantised per tensor; dispatch moves half the bytes)
+    wl = W["moe_fp8_w8"]
+    call, status = moe_case(tdx, torch, wl, dev)
+    for _ in range(3):
+        call()
+    f = time_mode(torch, call, reps)
+    m = time_mode(torch, lambda: call(mode=2), reps)
+    g = time_mode(torch, lambda: call(mode=1), reps)
+    status()
+    tf = wl.flops / (f * 1e-3) / 1e12
+    res["moe_fp8_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
+                         "tflops": tf, "peak_fp8_tflops": 2 * peak_bf16, "frac_of_peak": tf / (2 * peak_bf16)}
+    del call, status
+    wl = W["moe_fp8_w8_decode"]
+    call, status = moe_case(tdx, torch, wl, dev)
+    for _ in range(5):
+        call()
+    f = time_mode(torch, call, reps)
+    m = time_mode(torch, lambda: call(mode=2), reps)
+    gus = graph_time_us(torch, lambda: call(epoch=0))
+    status()
+    byt = wl.E * wl.K * wl.N + 2 * wl.M_total * wl.K + wl.M_total * wl.N * 2   # weights, dispatch r+w, Y
+    t_us = gus or 1e3 * f
+    res["moe_fp8_w8_decode"] = {"us_call": 1e3 * f, "us_gpu_graph": gus, "us_dispatch_alone": 1e3 * m,
+                                "algorithmic_bytes": byt, "hbm_frac": byt / (t_us * 1e-6) / 1e9 / hbm_gbs}
     del call, status
     # MoE grouped GEMM + combine: fused, GEMM alone (expert outputs only), combine alone
     wl = W["moe_combine_w8"]

@@ -673,6 +673,7 @@ struct MoePlan {
   long long total = 0;              // dispatched rows = W * T * k
   int n_chunks = 0, max_tiles = 0;  // 128-row chunks of the receive buffer; tile-table bound
   int PM = 0;                       // 0 single CTAs, 2 2-SM pairs on two tiles of one expert
+  int elt = 2;                      // bytes per input element (bf16 2, e4m3 1)
   size_t off_flags = 0, off_cnt = 0, off_ntiles = 0, off_tokcnt = 0, ctrl_end = 0;
   size_t off_offsets = 0, off_src = 0, off_dest = 0, off_tiles = 0, off_R = 0, bytes = 0;
 };
@@ -681,13 +682,15 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
                          bool combine = false) {
   if (W < 1 || W > kMaxW || T < 0 || H < 0 || F < 0 || E < 1 || k < 1 || k > E) return TDX_ERR_INVALID_ARG;
   if (E > kMoeMaxExperts || (combine && k > kMoeMaxTopk)) return TDX_ERR_UNSUPPORTED;
-  if (dtype == TDX_FP8_E4M3) return TDX_ERR_UNSUPPORTED;
-  if (dtype != TDX_BF16) return TDX_ERR_INVALID_ARG;
+  if (dtype != TDX_BF16 && dtype != TDX_FP8_E4M3) return TDX_ERR_INVALID_ARG;
+  const bool fp8 = dtype == TDX_FP8_E4M3;
+  if (fp8 && combine) return TDX_ERR_UNSUPPORTED;
   if (o.split_k > 1 || o.cluster == 2 || o.cluster < 0 || o.cluster > 3 || o.bf16_partials != 0 ||
       o.out_dtype != TDX_BF16)
     return TDX_ERR_UNSUPPORTED;
   MoePlan p;
   p.combine = combine;
+  p.elt = fp8 ? 1 : 2;
   p.W = W;
   p.T = T;
   p.H = H;
@@ -698,10 +701,11 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   if (p.total > (1ll << 30)) return TDX_ERR_INVALID_ARG;
   int bn = o.block_n;
   if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return TDX_ERR_UNSUPPORTED;
-  if (bn == 0) bn = F > 128 ? 256 : (F > 64 ? 128 : 64);
+  if (fp8 && bn == 64) return TDX_ERR_UNSUPPORTED;   // e4m3 B boxes are 128 columns wide
+  if (bn == 0) bn = F > 128 ? 256 : ((F > 64 || fp8) ? 128 : 64);
   p.BN = bn;
   p.tiles_n = (F + bn - 1) / bn;
-  p.num_kb = static_cast<int>((static_cast<long long>(H) * 2 + 127) / 128);
+  p.num_kb = static_cast<int>((static_cast<long long>(H) * p.elt + 127) / 128);
   p.n_chunks = static_cast<int>((p.total + kBM - 1) / kBM);
   // 2-SM pairs (M = 256 per MMA, two tiles of one expert) when the experts average at least 8 tiles:
   // the tile table then pads every expert to an even tile count (at most one empty tile each)
@@ -729,7 +733,8 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   p.off_tiles = off;
   off = align_up(off + static_cast<size_t>(p.max_tiles) * 16, 1024);
   p.off_R = off;   // dispatch: receive buffer (total x H); combine: expert outputs Z (total x F)
-  off = align_up(off + static_cast<size_t>(p.total) * (combine ? F : H) * 2, 1024);
+  off = align_up(off + static_cast<size_t>(p.total) * (combine ? static_cast<size_t>(F) * 2 : static_cast<size_t>(H) * p.elt),
+                 1024);
   p.bytes = off;
   *out = p;
   return TDX_OK;
@@ -738,14 +743,16 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
 // 3D map over a stack of `depth` row-major (rows x cols) bf16 matrices; box = box_cols x box_rows x 1,
 // 128-byte swizzle (the same shared-memory image as the 2D box of one matrix).
 bool make_map_3d(CUtensorMap* m, const void* base, long long depth, long long rows, long long cols, int box_cols,
-                 int box_rows) {
+                 int box_rows, bool fp8 = false) {
   EncodeTiledFn enc = get_encode();
   if (enc == nullptr) return false;
+  const int elt = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(depth)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(rows * cols) * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * elt, static_cast<cuuint64_t>(rows * cols) * elt};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                   dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -933,7 +940,10 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   if (!aligned16(B_experts) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(dest) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
     return TDX_ERR_ALIGNMENT;
-  if ((static_cast<long long>(H) * 2) % 16 != 0 || (static_cast<long long>(F) * 2) % 16 != 0) return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(H) * pl.elt) % 16 != 0 || (static_cast<long long>(F) * pl.elt) % 16 != 0 ||
+      (static_cast<long long>(F) * 2) % 16 != 0)
+    return TDX_ERR_ALIGNMENT;
+  const bool fp8 = pl.elt == 1;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.bytes)
     return TDX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -991,18 +1001,22 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   kp.epoch = epoch;
   kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
   kp.perturb = o.perturb_seed;
-  kp.row_bytes = static_cast<long long>(H) * 2;
+  kp.row_bytes = static_cast<long long>(H) * pl.elt;
   kp.chunk_rows = kBM;
   kp.n_chunks = pl.n_chunks;
   kp.chunk_bytes = kBM * kp.row_bytes;
   kp.G = ws + pl.off_R;
   kp.out[0] = static_cast<uint8_t*>(Y);
-  for (int r = 0; r < W; ++r) kp.shard[r] = static_cast<const uint8_t*>(X[r]);
+  for (int r = 0; r < W; ++r) {
+    kp.shard[r] = static_cast<const uint8_t*>(X[r]);
+    kp.row_scale[r] = (fp8 && o.scale_a) ? o.scale_a[r] : 1.0f;
+  }
+  for (int e = 0; e < E; ++e) kp.moe_bscale[e] = (fp8 && o.scale_b) ? o.scale_b[e] : 1.0f;
   kp.moe_src = lq.src;
   kp.moe_tiles = lq.tiles;
   kp.moe_ntiles = lq.ntiles;
   kp.moe_T = T;
-  int grid = fused_max_grid_moe(false, pl.PM, device_sms());
+  int grid = fused_max_grid_moe(false, pl.PM, device_sms(), fp8);
   if (grid <= 0) return TDX_ERR_CUDA;
   if (o.num_sms > 0 && o.num_sms < grid) grid = o.num_sms;
   grid -= grid % (pl.PM == 2 ? 2 : 1);
@@ -1020,10 +1034,13 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
   kp.copy_active = moving ? 1 : 0;
   kp.wait_flags = o.mode == TDX_FUSED ? 1 : 0;
-  if (!make_map(&kp.tm_a[0], kp.G, false, pl.total, H, 64, kBM) ||
-      !make_map_3d(&kp.tm_b[0], B_experts, E, H, F, 64, 64))
+  // A: 128-byte K slices of 128 rows; B: 128-byte N rows, one K slice deep, one expert
+  const int box = 128 / pl.elt;
+  if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.total, H, box, kBM) ||
+      !make_map_3d(&kp.tm_b[0], B_experts, E, H, F, box, box, fp8))
     return TDX_ERR_CUDA;
-  const cudaError_t e = launch_fused_moe_bf16(pl.BN, pl.PM, kp, grid, st);
+  const cudaError_t e = fp8 ? launch_fused_moe_fp8(pl.BN, pl.PM, kp, grid, st)
+                            : launch_fused_moe_bf16(pl.BN, pl.PM, kp, grid, st);
   if (e != cudaSuccess) {
     if (std::getenv("TDX_VERBOSE")) std::fprintf(stderr, "tdx: launch failed: %s\n", cudaGetErrorString(e));
     return TDX_ERR_CUDA;

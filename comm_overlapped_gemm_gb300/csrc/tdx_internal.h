@@ -99,6 +99,7 @@ struct KParams {
   const int32_t* moe_dest;       // MoE combine: W x T x k dispatched row of every token slot
   const float* moe_gates[kMaxW]; // MoE combine: [W] T x k gate weights
   uint32_t* moe_cnt;             // MoE combine: arrivals per (token, N-tile), reset by the last
+  float moe_bscale[kMoeMaxExperts];   // MoE e4m3: per-expert weight scale (row_scale: per source rank)
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t perturb;
@@ -126,7 +127,8 @@ cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 // pm: 0 single CTAs, 2 2-SM pairs (tile width 256).
 cudaError_t launch_fused_moe_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
-int fused_max_grid_moe(bool combine, int pm, int sms);
+cudaError_t launch_fused_moe_fp8(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
+int fused_max_grid_moe(bool combine, int pm, int sms, bool fp8 = false);
 
 // MoE routing layout: from every rank's top-k expert ids, the dispatched row of every (rank, token,
 // slot), the source of every dispatched row, the expert row offsets and the GEMM tile table.

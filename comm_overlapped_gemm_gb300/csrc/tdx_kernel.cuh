@@ -1033,6 +1033,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 
       const int row = w.m0 + row_in_tile;
       const size_t slot = slotted ? (size_t)w.c * p.T + w.tile : (size_t)w.tile;
+      float moe_row_scale = 1.0f;
+      if constexpr (FP8 && OP == OP_MOE) {
+        if (row < w.mend) {
+          const int tok = p.moe_src[row];
+          if (tok >= 0 && tok < p.W * p.moe_T) moe_row_scale = p.row_scale[tok / p.moe_T] * p.moe_bscale[w.e];
+        }
+      }
       float* sb = p.sbuf + slot * (kBM * BN);
 #pragma unroll 1
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
@@ -1049,6 +1056,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if constexpr (FP8 && OP == OP_RS) {
             // rank r's partial enters the fold dequantised: scale_a[r] * scale_b[r]
             const float s = p.elem_scale[w.c];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= s;
+          }
+          if constexpr (FP8 && OP == OP_MOE) {
+            // dequantised by the token's source-rank scale and the expert's scale
+            const float s = moe_row_scale;
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= s;
           }

@@ -1,5 +1,6 @@
-// Mixture-of-experts AllToAll dispatch + grouped GEMM: the routing-layout kernel and the bf16
-// instantiations of the fused kernel for OP_MOE.
+// Mixture-of-experts AllToAll dispatch + grouped GEMM and grouped GEMM + AllToAll combine: the
+// routing-layout kernel and the instantiations of the fused kernel for OP_MOE (bf16, e4m3) and
+// OP_MOE_COMBINE (bf16).
 //
 // The Triton-distributed article (cronfeed.work), section "DITRON adds three levels of tiling",
 // lists AllToAll among the collectives split into chunks and paired with compute tiles, and notes
@@ -206,8 +207,18 @@ cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p,
   }
 }
 
-int fused_max_grid_moe(bool combine, int pm, int sms) {
+cudaError_t launch_fused_moe_fp8(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
+  if (pm == 2) return block_n == 256 ? launch_fused_t<256, true, OP_MOE, 2>(p, grid, stream) : cudaErrorInvalidValue;
+  switch (block_n) {
+    case 128: return launch_fused_t<128, true, OP_MOE, 0>(p, grid, stream);
+    case 256: return launch_fused_t<256, true, OP_MOE, 0>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int fused_max_grid_moe(bool combine, int pm, int sms, bool fp8) {
   if (pm != 2) return sms;
+  if (fp8) return max_grid_t<256, true, OP_MOE, 2>(sms);
   return combine ? max_grid_t<256, false, OP_MOE_COMBINE, 2>(sms) : max_grid_t<256, false, OP_MOE, 2>(sms);
 }
 

@@ -178,6 +178,7 @@ class MoECase:
         wl = inp.wl
         self.inp, self.wl = inp, wl
         self.W, self.T, self.H, self.F, self.E, self.k = wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk
+        self.dt = dtype_code(wl.dtype)
         self.X = [dev_bits(a) for a in inp.a]
         self.route = [torch.from_numpy(np.ascontiguousarray(r)).cuda() for r in inp.route]
         self.B = dev_bits(inp.b[0])
@@ -186,21 +187,21 @@ class MoECase:
         self.dest = torch.full((wl.W, wl.M, wl.topk), -7, dtype=torch.int32, device="cuda")
         self.offsets = torch.full((wl.E + 1,), -7, dtype=torch.int32, device="cuda") if offsets else None
         self.opts = opts
-        n = tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16, opts)
+        n = tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, self.dt, opts)
         self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
         tdx.check(tdx.tdx_workspace_init(self.ws), "init")
 
     def run(self, opts=None):
         o = opts if opts is not None else self.opts
         return tdx.tdx_moe_dispatch_gemm(self.X, self.route, self.B, self.Y, self.dest, self.offsets, self.ws,
-                                         self.W, self.T, self.H, self.F, self.E, self.k, tdx.TDX_BF16, o)
+                                         self.W, self.T, self.H, self.F, self.E, self.k, self.dt, o)
 
     def result_bits(self) -> np.ndarray:
         torch.cuda.synchronize()
         return host_bits(self.Y)
 
     def plan(self, opts=None):
-        return tdx.tdx_moe_plan_info(self.W, self.T, self.H, self.F, self.E, self.k, tdx.TDX_BF16,
+        return tdx.tdx_moe_plan_info(self.W, self.T, self.H, self.F, self.E, self.k, self.dt,
                                      opts if opts is not None else self.opts)
 
 

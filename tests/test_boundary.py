@@ -214,7 +214,9 @@ def test_moe_validation_codes(tdx):
     assert ws_size(k=5) == tdx.TDX_ERR_INVALID_ARG          # topk > E
     assert ws_size(k=0) == tdx.TDX_ERR_INVALID_ARG
     assert ws_size(W=17) == tdx.TDX_ERR_INVALID_ARG
-    assert ws_size(dtype=1) == tdx.TDX_ERR_UNSUPPORTED
+    assert ws_size(dtype=1) == tdx.TDX_OK                       # e4m3 dispatch
+    assert ws_size(dtype=1, opts=tdx.make_opts(block_n=64)) == tdx.TDX_ERR_UNSUPPORTED
+    assert ws_size(dtype=2) == tdx.TDX_ERR_INVALID_ARG
     assert ws_size(opts=tdx.make_opts(cluster=3)) == tdx.TDX_ERR_UNSUPPORTED
     assert ws_size(opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
 
@@ -231,6 +233,8 @@ def test_moe_validation_codes(tdx):
     assert moe(X=[FAKE, FAKE + 8]) == tdx.TDX_ERR_ALIGNMENT
     assert moe(dest=FAKE + 2) == tdx.TDX_ERR_ALIGNMENT
     assert moe(H=60) == tdx.TDX_ERR_ALIGNMENT                # 120-byte rows
+    assert tdx.tdx_moe_dispatch_gemm([FAKE] * 2, [FAKE] * 2, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 72, 64, 4, 2,
+                                     tdx.TDX_FP8_E4M3, None, stream=0, workspace_bytes=1 << 30) == tdx.TDX_ERR_ALIGNMENT
     assert moe(wsb=100) == tdx.TDX_ERR_WORKSPACE
     assert moe(opts=tdx.make_opts(mode=tdx.TDX_CONSUMER_ONLY)) == tdx.TDX_ERR_UNSUPPORTED
     assert moe(opts=tdx.make_opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE)) == tdx.TDX_ERR_UNSUPPORTED

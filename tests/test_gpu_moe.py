@@ -174,3 +174,38 @@ def test_moe_pairs_match_single_ctas_bitwise():
         status_ok(case)
         bits.append(case.result_bits())
     assert np.array_equal(bits[0], bits[1])
+
+
+@pytest.mark.parametrize("shape", [dict(W=2, M=5, K=128, N=128, E=4, topk=2),
+                                   dict(W=8, M=128, K=512, N=512, E=64, topk=8),
+                                   dict(W=4, M=300, K=256, N=384, E=8, topk=2)])
+@pytest.mark.parametrize("integer", [True, False])
+def test_moe_e4m3(shape, integer):
+    wl = wls.with_shape(wls.WORKLOADS["moe_fp8_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    want, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E, "e4m3", inp.scale_a, inp.scale_b)
+    for bn, cl in ((0, 0), (256, 1), (256, 3)):
+        case = MoECase(inp, opts=opts(block_n=bn, cluster=cl, scale_a=inp.scale_a, scale_b=inp.scale_b))
+        tdx.check(case.run(), f"moe e4m3 {shape} bn={bn} cluster={cl}")
+        status_ok(case)
+        check_layout(case, lay)
+        if integer:
+            assert_bit_exact(case.result_bits(), want, "bf16")
+        else:
+            assert_within_tol(R.decode_bf16(case.result_bits()), want, "e4m3")
+
+
+def test_moe_e4m3_full_size_sampled():
+    wl = wls.WORKLOADS["moe_fp8_w8"]
+    inp = wls.make_inputs(wl, integer=False)
+    case = MoECase(inp, opts=opts(scale_a=inp.scale_a, scale_b=inp.scale_b))
+    tdx.check(case.run())
+    status_ok(case)
+    _, offsets, _, _ = MO.moe_layout(inp.route, wl.E)
+    rows = set(range(0, wl.M_total, 8191))
+    for e in range(0, wl.E, 7):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        rows.update({a, b - 1, min(a + 128, b - 1)})
+    rows = np.array(sorted(rows))
+    want = MO.moe_dispatch_gemm_rows(inp.a, inp.route, inp.b[0], wl.E, rows, "e4m3", inp.scale_a, inp.scale_b)
+    assert_within_tol(R.decode_bf16(case.result_bits()[rows]), want, "e4m3")

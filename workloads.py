@@ -94,6 +94,12 @@ WORKLOADS = {
                                out_dtype="bf16", chunk_rows=128, E=64, topk=8,
                                note="W=8, 262144 dispatched rows of 2048, expert weights 2048x7168, combined "
                                     "back to 4096x7168 per rank with top-8 gates"),
+    "moe_fp8_w8": Workload("moe_fp8_w8", 11, "moe", W=8, M=4096, K=7168, N=2048, dtype="e4m3", out_dtype="bf16",
+                           chunk_rows=128, E=64, topk=8, b_dist=("normal", 1.0),
+                           note="moe_w8 in e4m3: tokens and expert weights quantised per tensor (per rank, per expert)"),
+    "moe_fp8_w8_decode": Workload("moe_fp8_w8_decode", 12, "moe", W=8, M=128, K=7168, N=2048, dtype="e4m3",
+                                  out_dtype="bf16", chunk_rows=128, E=64, topk=8, b_dist=("normal", 1.0),
+                                  note="128 e4m3 tokens per rank (the AllToAll size the pages quote), top-8 of 64"),
     "ag_small": Workload("ag_small", 4, "ag", W=8, M=16, K=8192, N=1024, dtype="bf16",
                          out_dtype="bf16", chunk_rows=16,
                          note="small-M latency: shard 16x8192, B 8192x1024, chunk 16"),
