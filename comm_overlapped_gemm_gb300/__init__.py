@@ -181,7 +181,7 @@ def tdx_workspace_init(workspace, nbytes: int | None = None, stream=None) -> int
 
 PLAN_KEYS = ["BN", "L", "tiles_m", "tiles_n", "T", "num_kb", "chunk_rows", "n_chunks", "off_chunk_flags",
              "off_chunk_cnt", "off_chain_flags", "off_G", "off_S", "total", "reduce_mode", "off_tile_cnt",
-             "cluster", "group_n", "rank_block", "pull_a", "partial_bytes"]
+             "cluster", "group_n", "rank_block", "pull_a", "partial_bytes", "coop_fold"]
 
 
 def tdx_plan_info(op: int, W: int, M_local_or_M: int, K: int, N: int, dtype: int, opts=None) -> dict:

@@ -58,11 +58,14 @@ struct Plan {
   int group_n = 1;
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
   int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
-  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, ctrl_end = 0;
+  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, off_tile_done = 0, ctrl_end = 0;
+  int coop = 0;          // slotted fold shared by the L elements of a tile (see make_plan)
   size_t off_G = 0, off_S = 0, total = 0;
 };
 
 bool valid_bn(int bn, bool fp8) { return fp8 ? (bn == 128 || bn == 256) : (bn == 64 || bn == 128 || bn == 256); }
+
+int device_sms();
 
 tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const tdx_opts& o, Plan* pl) {
   const bool allreduce = op == kOpAllReduce;
@@ -161,6 +164,16 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   }
   // slotted ReduceScatter may take a rank-inner order (blocks of one position) instead
   if (op == OP_RS && p.reduce_last && kSlottedRankInner) p.rank_block = 1;
+  // cooperative fold (slotted, single CTAs, fp32 partials): every element of a tile waits for the
+  // tile's L partials and folds 1/L of it, instead of the last arriver folding all of it. The wait
+  // is safe only when a tile's elements are processed in the same wave of the persistent grid; it is
+  // used when all work items fit one wave (a rank-inner order with the grid a multiple of L would
+  // also qualify, but that order measured slower on the multi-wave small-M ReduceScatter).
+  if (p.reduce_last && p.PM == 0 && !p.bf16_partials && L > 1) {
+    int sms = device_sms();
+    if (o.num_sms > 0 && (sms == 0 || o.num_sms < sms)) sms = o.num_sms;
+    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) p.coop = 1;
+  }
   // workspace layout
   size_t off = kHeaderBytes;
   const size_t n_chunk_words = op == OP_AG ? static_cast<size_t>(W) * p.n_chunks : 0;
@@ -171,6 +184,8 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.off_chain_flags = off;
   off += static_cast<size_t>(L > 1 && !p.reduce_last ? L - 1 : 0) * p.T * 4;
   p.off_tile_cnt = off;
+  off += static_cast<size_t>(p.reduce_last ? p.T : 0) * 4;
+  p.off_tile_done = off;   // cooperative fold: elements done folding per tile (reset by the last)
   off += static_cast<size_t>(p.reduce_last ? p.T : 0) * 4;
   off = align_up(off, 1024);
   p.ctrl_end = off;
@@ -306,6 +321,8 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.chain_flags = reinterpret_cast<uint32_t*>(ws + pl.off_chain_flags);
   kp.sbuf = pl.L > 1 ? reinterpret_cast<float*>(ws + pl.off_S) : nullptr;
   kp.tile_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tile_cnt);
+  kp.tile_done = reinterpret_cast<uint32_t*>(ws + pl.off_tile_done);
+  kp.coop_fold = pl.coop;
   kp.reduce_last = pl.reduce_last;
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;
@@ -560,11 +577,11 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
   Plan pl;
   tdx_status s = make_plan(op, W, M_local_or_M, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const int64_t v[21] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
+  const int64_t v[22] = {pl.BN, pl.L, pl.tiles_m, pl.tiles_n, pl.T, pl.num_kb, pl.chunk_rows, pl.n_chunks,
                          (int64_t)pl.off_chunk_flags, (int64_t)pl.off_chunk_cnt, (int64_t)pl.off_chain_flags,
                          (int64_t)pl.off_G, (int64_t)pl.off_S, (int64_t)pl.total,
                          pl.L > 1 ? (pl.reduce_last ? 2 : 1) : 0, (int64_t)pl.off_tile_cnt, pl.PM + 1, pl.group_n, pl.rank_block, pl.pull_a,
-                         pl.bf16_partials ? 2 : 4};
+                         pl.bf16_partials ? 2 : 4, pl.coop};
   std::memcpy(info, v, sizeof(v));
   return TDX_OK;
 }

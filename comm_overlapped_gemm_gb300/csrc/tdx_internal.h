@@ -70,6 +70,8 @@ struct KParams {
   uint32_t* chain_flags;         // [(L-1) * T]: running sum of chain elements 0..c done for tile
   float* sbuf;                   // chained: [T][kBM*BN] running sum; slotted: [L][T][kBM*BN] partials
   uint32_t* tile_cnt;            // slotted: partials stored per tile (reset by the last arriver)
+  uint32_t* tile_done;           // cooperative fold: elements that folded their share (reset by the last)
+  int coop_fold;                 // slotted: the L elements of a tile fold 1/L each after all arrived
   int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
   float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r

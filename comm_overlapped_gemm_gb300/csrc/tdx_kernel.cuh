@@ -458,6 +458,76 @@ __device__ __forceinline__ void store_out_chunk(const KParams& p, int row, int c
   store_row_chunk(orow, p, col, v, pol);
 }
 
+// Bounded acquire-wait until *ctr >= target (cooperative fold: all L partials of a tile stored).
+static __device__ __noinline__ bool wait_count(const KParams& p, const uint32_t* ctr, uint32_t target,
+                                               volatile int* abort_flag, uint32_t idx) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    __nanosleep(64);
+    if ((it & 15u) == 15u) {
+      if (*abort_flag) return false;
+      if (ld_relaxed_gpu(p.status) != 0u) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        report_error(p, DEV_TIMEOUT, ROLE_CHAIN, idx, ld_relaxed_gpu(ctr), target);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Round 4 consecutive fp32 values (row, col..col+3) once to the output type and store them, like
+// store_out_chunk (AllGather: C with the e4m3 row scale; ReduceScatter: output shard; AllReduce:
+// every rank's output). Rows >= M and columns >= N are skipped.
+template <int OP, bool FP8>
+__device__ __forceinline__ void store_out_4(const KParams& p, int row, int col, float4 v) {
+  if (row >= p.M) return;
+  float a[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (OP == OP_AG) {
+    if constexpr (FP8) {
+      const float s = p.row_scale[row / p.M_local];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] *= s;
+    }
+    if (p.out_fp32) {
+      float* o = reinterpret_cast<float*>(p.out[0] + (size_t)row * p.N * 4) + col;
+      if (col + 4 <= p.N) {
+        st_f4(o, make_float4(a[0], a[1], a[2], a[3]));
+      } else {
+        for (int i = 0; i < 4; ++i)
+          if (col + i < p.N) o[i] = a[i];
+      }
+      return;
+    }
+  }
+  __nv_bfloat162 b0 = __floats2bfloat162_rn(a[0], a[1]);
+  __nv_bfloat162 b1 = __floats2bfloat162_rn(a[2], a[3]);
+  const uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
+  auto put = [&](uint8_t* orow) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(orow) + col;
+    if (col + 4 <= p.N) {
+      *reinterpret_cast<uint2*>(o) = pk;
+    } else {
+      for (int i = 0; i < 4; ++i)
+        if (col + i < p.N) o[i] = __float2bfloat16_rn(a[i]);
+    }
+  };
+  if constexpr (OP == OP_AG) {
+    put(p.out[0] + (size_t)row * p.N * 2);
+  } else {
+    if (p.allreduce) {
+      for (int r = 0; r < p.W; ++r) put(p.out[r] + (size_t)row * p.N * 2);
+    } else {
+      const int j = row / p.M_local;
+      put(p.out[j] + (size_t)(row - j * p.M_local) * p.N * 2);
+    }
+  }
+}
+
 // MoE combine of one token over columns [col0, col0 + ncols), one warp: lane l takes the 8
 // columns col0 + 8l .. col0 + 8l + 7 and keeps the k expert-output loads of its slots in flight
 // together. out_s[t] = sum_j g[s][t][j] * Z[dest[s][t][j]] in slot order j = 0..k-1 (fp32 fused
@@ -1128,15 +1198,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
         if (slotted) {
           // count this tile's stored partials; the element that completes the count folds them
+          // (cooperative fold: every element waits for the count, then folds its share)
           if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x30000u + it) & 4095u);
           __threadfence();
           const uint32_t old = atomicAdd(p.tile_cnt + w.tile, 1u);
-          const bool last = old == static_cast<uint32_t>(p.L - 1);
-          if (last) {
-            p.tile_cnt[w.tile] = 0u;
-            __threadfence();
+          if (p.coop_fold) {
+            const bool ok = wait_count(p, p.tile_cnt + w.tile, static_cast<uint32_t>(p.L), abort_flag,
+                                       static_cast<uint32_t>(w.tile));
+            if (ok) fence_acq_rel_gpu();
+            *is_last = ok ? 1u : 0u;
+          } else {
+            const bool last = old == static_cast<uint32_t>(p.L - 1);
+            if (last) {
+              p.tile_cnt[w.tile] = 0u;
+              __threadfence();
+            }
+            *is_last = last ? 1u : 0u;
           }
-          *is_last = last ? 1u : 0u;
         }
       }
       if constexpr (OP == OP_MOE_COMBINE) {
@@ -1169,7 +1247,42 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
       }
-      if (slotted) {
+      if (slotted && p.coop_fold) {
+        // cooperative fold: this element folds float4 block [c*per, (c+1)*per) of the tile's slot
+        // layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), all L
+        // slots in order 0..L-1, and the element that completes the tile's done count resets both
+        // counters for the next call
+        named_bar_sync(1, kEpiThreads);
+        if (*is_last) {
+          const int et = threadIdx.x - kEpiWarp0 * 32;
+          constexpr int N4 = kBM * BN / 4;
+          const int per = (N4 + p.L - 1) / p.L;
+          const int f0 = w.c * per;
+          const int f1 = min(N4, f0 + per);
+          const size_t slot_f4 = (size_t)p.T * N4;
+          const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)w.tile * N4;
+          for (int f = f0 + et; f < f1; f += kEpiThreads) {
+            float4 acc = ld_cg_f4_hint(base + f, once);
+            for (int c = 1; c < p.L; ++c) {
+              const float4 sv = ld_cg_f4_hint(base + (size_t)c * slot_f4 + f, once);
+              acc.x = acc.x + sv.x;
+              acc.y = acc.y + sv.y;
+              acc.z = acc.z + sv.z;
+              acc.w = acc.w + sv.w;
+            }
+            store_out_4<OP, FP8>(p, w.m0 + (f & 127), w.n0 + 32 * (f >> 10) + 4 * ((f >> 7) & 7), acc);
+          }
+          named_bar_sync(1, kEpiThreads);
+          if (elected) {
+            const uint32_t done = atomicAdd(p.tile_done + w.tile, 1u);
+            if (done == static_cast<uint32_t>(p.L - 1)) {
+              p.tile_cnt[w.tile] = 0u;
+              p.tile_done[w.tile] = 0u;
+              __threadfence();
+            }
+          }
+        }
+      } else if (slotted) {
         named_bar_sync(1, kEpiThreads);
         if (*is_last) {
           // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ..., two slots' loads in

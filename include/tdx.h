@@ -295,7 +295,7 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
                                   uint32_t* detail);
 
 /* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
- * uses. Writes 21 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
+ * uses. Writes 22 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
  * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] K blocks (64 bytes of K for BN = 256, else 128), [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
@@ -308,7 +308,10 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
  * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
  * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
- * 2 bf16 partials). */
+ * 2 bf16 partials), [21] 1 if the slotted fold is cooperative (every element of a tile waits for the
+ * tile's L partials and folds 1/L of it; chosen for single CTAs and fp32 partials when every work
+ * item fits one wave of the persistent grid, which depends on the device's SM count and
+ * opts.num_sms), else 0. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -357,3 +357,27 @@ def test_ag_small_shards_pull_and_flag_paths_agree():
         n = wl.W * plan["n_chunks"]
         f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
         assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 4))
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_split_k_cooperative_fold(integer):
+    # one wave of split-K work items: every element of a tile folds 1/L of it after all L arrived
+    wl = wls.with_shape(wls.WORKLOADS["ag_small"], W=8, M=16, K=4096, N=512)
+    inp = wls.make_inputs(wl, integer=integer)
+    o = tdx.make_opts(timeout_ns=int(5e8), chunk_rows=16, split_k=8)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 16, 4096, 512, tdx.TDX_BF16, o)
+    assert plan["L"] == 8 and plan["reduce_mode"] == 2
+    case = AGCase(inp, opts=o)
+    tdx.check(case.run())
+    st, detail = tdx.tdx_read_device_status(case.ws)
+    assert st == tdx.TDX_OK, detail
+    assert tdx.tdx_plan_info(tdx.OP_AG, 8, 16, 4096, 512, tdx.TDX_BF16, o)["coop_fold"] == 1
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+    # counters are back to zero: a second call with the next epoch gives the same bits
+    first = case.result_bits()
+    case.C.fill_(float("nan"))
+    tdx.check(case.run(tdx.make_opts(timeout_ns=int(5e8), chunk_rows=16, split_k=8, epoch=2, perturb_seed=5)))
+    assert np.array_equal(case.result_bits(), first)
