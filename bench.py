@@ -425,22 +425,12 @@ def graph_time_us(torch, fn, reps: int = 50):
 
 
 def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
-    """The other configurations, timed alone (median of CUDA-event times, warm): the AllGather
-    with the copy-engine producer, e4m3 AllGather and ReduceScatter, GEMM+AllReduce, and the
-    small-M latency cases."""
+    """The other configurations, timed alone (median of CUDA-event times, warm): e4m3 AllGather
+    and ReduceScatter, GEMM+AllReduce, bf16 partials, the MoE dispatch and combine, and the small-M
+    latency cases."""
     import workloads as wls
     W = wls.WORKLOADS
     res = {}
-    call, status = ag_case(tdx, torch, W["ag_w8"], dev)
-    for _ in range(3):
-        call(producer=1)
-    f = time_mode(torch, lambda: call(producer=1), reps)
-    g = time_mode(torch, lambda: call(mode=1), reps)
-    m = time_mode(torch, lambda: call(mode=2, producer=1), reps)
-    status()
-    res["ag_w8_copy_engine"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m,
-                                "overlap_efficiency": max(g, m) / f, "tflops": W["ag_w8"].flops / (f * 1e-3) / 1e12}
-    del call, status
     call, status = ag_case(tdx, torch, W["ag_fp8_w8"], dev)
     for _ in range(3):
         call()

@@ -59,7 +59,8 @@ struct Plan {
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
   int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, off_tile_done = 0, ctrl_end = 0;
-  int coop = 0;          // slotted fold shared by the L elements of a tile (see make_plan)
+  int coop = 0;          // slotted fold: 0 last arriver, 1 cooperative, 2 deferred tasks (make_plan)
+  int fold_parts = 1;    // deferred fold: parts per tile
   size_t off_G = 0, off_S = 0, total = 0;
 };
 
@@ -169,10 +170,19 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   // is safe only when a tile's elements are processed in the same wave of the persistent grid; it is
   // used when all work items fit one wave (a rank-inner order with the grid a multiple of L would
   // also qualify, but that order measured slower on the multi-wave small-M ReduceScatter).
+  // With more work than one wave, the fold is deferred instead: CTAs that have finished their items
+  // take fold tasks (a tile's part) and wait for that tile's partials, which spreads the folds of
+  // the last tiles over every SM rather than leaving them to the last arrivers.
   if (p.reduce_last && p.PM == 0 && !p.bf16_partials && L > 1) {
     int sms = device_sms();
     if (o.num_sms > 0 && (sms == 0 || o.num_sms < sms)) sms = o.num_sms;
-    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) p.coop = 1;
+    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) {
+      p.coop = 1;
+    } else if (sms > 0) {
+      p.coop = 2;
+      int q = (2 * sms + p.T - 1) / (p.T > 0 ? p.T : 1);
+      p.fold_parts = q < 1 ? 1 : (q > 16 ? 16 : q);
+    }
   }
   // workspace layout
   size_t off = kHeaderBytes;
@@ -239,44 +249,6 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long l
   return r == CUDA_SUCCESS;
 }
 
-// Copy-engine producer: one side stream and a fork/join event pair per device, created on first
-// use and kept for the life of the process; cuStreamWriteValue32 through the driver entry point.
-typedef CUresult (*StreamWriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
-
-struct CeState {
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-
-StreamWriteValue32Fn get_write_value32() {
-  static StreamWriteValue32Fn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<StreamWriteValue32Fn>(ptr);
-  });
-  return fn;
-}
-
-bool ce_state(CeState** out) {
-  static std::mutex mu;
-  static CeState states[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  std::lock_guard<std::mutex> lock(mu);
-  CeState& s = states[dev];
-  if (s.side == nullptr) {
-    if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess) return false;
-    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return false;
-    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return false;
-  }
-  *out = &s;
-  return true;
-}
-
 int device_sms() {
   static int cache[64] = {};
   int dev = 0;
@@ -323,6 +295,7 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.tile_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tile_cnt);
   kp.tile_done = reinterpret_cast<uint32_t*>(ws + pl.off_tile_done);
   kp.coop_fold = pl.coop;
+  kp.fold_parts = pl.fold_parts;
   kp.reduce_last = pl.reduce_last;
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;
@@ -382,6 +355,9 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   if (o.out_dtype != TDX_BF16 && o.out_dtype != TDX_FP32) return TDX_ERR_INVALID_ARG;
   if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
   if (o.producer != TDX_PRODUCER_SM && o.producer != TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_INVALID_ARG;
+  // The copy-engine producer is not offered: the consumer kernel would wait on copies issued
+  // outside it, which need not run while the kernel holds every SM.
+  if (o.producer == TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_UNSUPPORTED;
   Plan pl;
   tdx_status s = make_plan(OP_AG, W, M_local, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
@@ -429,9 +405,8 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   }
   kp.ppc = static_cast<int>((kp.chunk_bytes + kp.piece_bytes - 1) / kp.piece_bytes);
   kp.total_pieces = W * pl.n_chunks * kp.ppc;
-  const bool ce = o.producer == TDX_PRODUCER_COPY_ENGINE;
   const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
-  kp.copy_active = (moving && !ce) ? 1 : 0;
+  kp.copy_active = moving ? 1 : 0;
   kp.pull_a = pl.pull_a;
   kp.wait_flags = (!pl.pull_a && (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY)) ? 1 : 0;
   // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
@@ -450,35 +425,7 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
     s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
     if (s != TDX_OK) return s;
   }
-  if (!(ce && moving)) return launch(pl, kp, fp8, grid, st);
-
-  // Copy-engine producer: the side stream starts after everything already on `st`, copies the
-  // chunks in release order (peers self+1, ..., self+W-1, then self) and writes each chunk's flag
-  // once its copy is done (the default write orders it after the preceding copy); the consumer
-  // kernel runs on `st` meanwhile, and `st` joins the side stream before returning.
-  CeState* ce_st = nullptr;
-  StreamWriteValue32Fn wv = get_write_value32();
-  if (!ce_state(&ce_st) || wv == nullptr) return TDX_ERR_CUDA;
-  if (cudaEventRecord(ce_st->fork, st) != cudaSuccess || cudaStreamWaitEvent(ce_st->side, ce_st->fork, 0) != cudaSuccess)
-    return TDX_ERR_CUDA;
-  for (int rr = 0; rr < W; ++rr) {
-    const int rank = (o.self_rank + 1 + rr) % W;
-    for (int ck = 0; ck < pl.n_chunks; ++ck) {
-      const uint8_t* src = static_cast<const uint8_t*>(shards[rank]) + static_cast<size_t>(ck) * kp.chunk_bytes;
-      uint8_t* dst = kp.G + (static_cast<size_t>(rank) * M_local + static_cast<size_t>(ck) * pl.chunk_rows) * kp.row_bytes;
-      if (cudaMemcpyAsync(dst, src, kp.chunk_bytes, cudaMemcpyDeviceToDevice, ce_st->side) != cudaSuccess)
-        return TDX_ERR_CUDA;
-      uint32_t* flag = kp.chunk_flags + rank * pl.n_chunks + ck;
-      if (wv(reinterpret_cast<CUstream>(ce_st->side), reinterpret_cast<CUdeviceptr>(flag), kp.epoch, 0) != CUDA_SUCCESS)
-        return TDX_ERR_CUDA;
-    }
-  }
-  if (cudaEventRecord(ce_st->join, ce_st->side) != cudaSuccess) return TDX_ERR_CUDA;
-  if (o.mode == TDX_FUSED) {
-    s = launch(pl, kp, fp8, grid, st);
-    if (s != TDX_OK) return s;
-  }
-  return cudaStreamWaitEvent(st, ce_st->join, 0) == cudaSuccess ? TDX_OK : TDX_ERR_CUDA;
+  return launch(pl, kp, fp8, grid, st);
 }
 
 }  // extern "C"
@@ -623,7 +570,7 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
                                void* stream) {
   tdx_opts o = opts ? *opts : defaults();
   o.epoch = 0;   // the shared scratch is cleared by every call
-  if (o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;   // the copy-engine producer creates a stream
+  if (o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;
   size_t need = 0;
   tdx_status s = tdx_workspace_size(OP_AG, W, M_local, K, N, dtype, &o, &need);
   if (s != TDX_OK) return s;

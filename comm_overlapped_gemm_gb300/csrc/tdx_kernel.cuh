@@ -528,6 +528,46 @@ __device__ __forceinline__ void store_out_4(const KParams& p, int row, int col, 
   }
 }
 
+// Fold part `part` of `nparts` of tile `tile`: float4 blocks [part*per, (part+1)*per) of the slot
+// layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), every one of
+// the L slots added in order 0..L-1, rounded once and stored. Called by all epilogue threads.
+template <int OP, bool FP8, int BN>
+__device__ __forceinline__ void fold_part(const KParams& p, int tile, int part, int nparts, int et, uint64_t pol) {
+  constexpr int N4 = kBM * BN / 4;
+  const int per = (N4 + nparts - 1) / nparts;
+  const int f0 = part * per;
+  const int f1 = min(N4, f0 + per);
+  const size_t slot_f4 = (size_t)p.T * N4;
+  const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)tile * N4;
+  const int m0 = (tile / p.tiles_n) * kBM;
+  const int n0 = (tile % p.tiles_n) * BN;
+  for (int f = f0 + et; f < f1; f += kEpiThreads) {
+    // slots in groups of 8: a group's loads are all in flight before the in-order adds
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+    for (int c0 = 0; c0 < p.L; c0 += 8) {
+      float4 sv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c0 + c < p.L) sv[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4 + f, pol);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (c0 + c < p.L) {
+          if (c0 + c == 0) {
+            acc = sv[c];
+          } else {
+            acc.x = acc.x + sv[c].x;
+            acc.y = acc.y + sv[c].y;
+            acc.z = acc.z + sv[c].z;
+            acc.w = acc.w + sv[c].w;
+          }
+        }
+      }
+    }
+    store_out_4<OP, FP8>(p, m0 + (f & 127), n0 + 32 * (f >> 10) + 4 * ((f >> 7) & 7), acc);
+  }
+}
+
 // MoE combine of one token over columns [col0, col0 + ncols), one warp: lane l takes the 8
 // columns col0 + 8l .. col0 + 8l + 7 and keeps the k expert-output loads of its slots in flight
 // together. out_s[t] = sum_j g[s][t][j] * Z[dest[s][t][j]] in slot order j = 0..k-1 (fp32 fused
@@ -1202,7 +1242,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x30000u + it) & 4095u);
           __threadfence();
           const uint32_t old = atomicAdd(p.tile_cnt + w.tile, 1u);
-          if (p.coop_fold) {
+          if (p.coop_fold == 2) {
+            *is_last = 0u;   // deferred fold: the tile is folded by the fold tasks after the items
+          } else if (p.coop_fold) {
             const bool ok = wait_count(p, p.tile_cnt + w.tile, static_cast<uint32_t>(p.L), abort_flag,
                                        static_cast<uint32_t>(w.tile));
             if (ok) fence_acq_rel_gpu();
@@ -1247,31 +1289,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
       }
-      if (slotted && p.coop_fold) {
+      if (slotted && p.coop_fold == 2) {
+        // deferred fold: nothing more for this item
+      } else if (slotted && p.coop_fold) {
         // cooperative fold: this element folds float4 block [c*per, (c+1)*per) of the tile's slot
         // layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), all L
         // slots in order 0..L-1, and the element that completes the tile's done count resets both
         // counters for the next call
         named_bar_sync(1, kEpiThreads);
         if (*is_last) {
-          const int et = threadIdx.x - kEpiWarp0 * 32;
-          constexpr int N4 = kBM * BN / 4;
-          const int per = (N4 + p.L - 1) / p.L;
-          const int f0 = w.c * per;
-          const int f1 = min(N4, f0 + per);
-          const size_t slot_f4 = (size_t)p.T * N4;
-          const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)w.tile * N4;
-          for (int f = f0 + et; f < f1; f += kEpiThreads) {
-            float4 acc = ld_cg_f4_hint(base + f, once);
-            for (int c = 1; c < p.L; ++c) {
-              const float4 sv = ld_cg_f4_hint(base + (size_t)c * slot_f4 + f, once);
-              acc.x = acc.x + sv.x;
-              acc.y = acc.y + sv.y;
-              acc.z = acc.z + sv.z;
-              acc.w = acc.w + sv.w;
-            }
-            store_out_4<OP, FP8>(p, w.m0 + (f & 127), w.n0 + 32 * (f >> 10) + 4 * ((f >> 7) & 7), acc);
-          }
+          fold_part<OP, FP8, BN>(p, w.tile, w.c, p.L, threadIdx.x - kEpiWarp0 * 32, once);
           named_bar_sync(1, kEpiThreads);
           if (elected) {
             const uint32_t done = atomicAdd(p.tile_done + w.tile, 1u);
@@ -1380,6 +1407,36 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             for (int c = 0; c < p.L; ++c)
               for (int l = et; l < (int)(sbytes / 128); l += kEpiThreads)
                 discard_l2_line(reinterpret_cast<uint8_t*>(p.sbuf) + ((size_t)c * p.T + w.tile) * sbytes + (size_t)l * 128);
+          }
+        }
+      }
+    }
+    if (chain && p.reduce_last && p.coop_fold == 2 && !*abort_flag) {
+      // deferred fold: once its own items are done, a CTA takes fold tasks (tile, part) in tile
+      // order, waits (bounded) until the tile's L partials are stored, and folds that part. The
+      // items never wait on fold tasks, so the waits end. The task that completes a tile's done
+      // count resets its counters for the next call.
+      const int et = threadIdx.x - kEpiWarp0 * 32;
+      const int Q = p.fold_parts;
+      const int ntask = p.T * Q;
+      for (int task = blockIdx.x; task < ntask; task += grid) {
+        const int tile = task / Q;
+        if (elected) {
+          const bool ok = wait_count(p, p.tile_cnt + tile, static_cast<uint32_t>(p.L), abort_flag,
+                                     static_cast<uint32_t>(tile));
+          if (ok) fence_acq_rel_gpu();
+          *decision = ok ? 1u : 0u;
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (*decision == 0u) break;
+        fold_part<OP, FP8, BN>(p, tile, task - tile * Q, Q, et, once);
+        named_bar_sync(1, kEpiThreads);
+        if (elected) {
+          const uint32_t done = atomicAdd(p.tile_done + tile, 1u);
+          if (done == static_cast<uint32_t>(Q - 1)) {
+            p.tile_cnt[tile] = 0u;
+            p.tile_done[tile] = 0u;
+            __threadfence();
           }
         }
       }

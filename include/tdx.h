@@ -62,9 +62,8 @@ typedef enum {
 
 typedef enum {
   TDX_PRODUCER_SM = 0,          /* chunk copies by producer warps of the persistent kernel */
-  TDX_PRODUCER_COPY_ENGINE = 1  /* chunk copies by cudaMemcpyAsync on a library-owned side stream (created
-                                   once per device), each followed by a stream write of its flag; the
-                                   caller's stream waits for the side stream before the call returns */
+  TDX_PRODUCER_COPY_ENGINE = 1  /* not offered (TDX_ERR_UNSUPPORTED): copies issued outside the kernel
+                                   that its consumers wait on need not run while it holds every SM */
 } tdx_producer;
 
 /* Per-call options. Pass NULL for all defaults; tdx_opts_default fills the same values. */
@@ -308,10 +307,11 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
  * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
  * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
- * 2 bf16 partials), [21] 1 if the slotted fold is cooperative (every element of a tile waits for the
- * tile's L partials and folds 1/L of it; chosen for single CTAs and fp32 partials when every work
- * item fits one wave of the persistent grid, which depends on the device's SM count and
- * opts.num_sms), else 0. */
+ * 2 bf16 partials), [21] how the slotted fold is shared (single CTAs, fp32 partials; depends on the
+ * device's SM count and opts.num_sms): 1 cooperative (every work item fits one wave of the
+ * persistent grid: each element of a tile waits for the tile's L partials and folds 1/L of it),
+ * 2 deferred (more than one wave: CTAs that finished their items take fold tasks, parts of tiles,
+ * each waiting for its tile's partials), 0 the last arriver folds the tile. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 

@@ -190,6 +190,12 @@ def test_trace_size(tdx):
     assert tdx.tdx_trace_size(0, 10) == 0
 
 
+def test_copy_engine_producer_is_not_offered(tdx):
+    rc = tdx.tdx_ag_gemm([FAKE] * 2, FAKE, FAKE, FAKE, 2, 64, 128, 256, tdx.TDX_BF16,
+                         tdx.make_opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE), stream=0, workspace_bytes=1 << 30)
+    assert rc == tdx.TDX_ERR_UNSUPPORTED
+
+
 def test_noalloc_rejects_copy_engine_producer_before_any_device_work(tdx):
     o = tdx.make_opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE)
     rc = tdx.tdx_ag_gemm_noalloc([FAKE] * 2, FAKE, FAKE, 2, 64, 128, 256, tdx.TDX_BF16, o, stream=0)

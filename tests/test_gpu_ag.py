@@ -228,43 +228,6 @@ def test_ag_stale_epoch_is_reported():
     assert detail[4] == 10 and detail[5] == 5
 
 
-@pytest.mark.parametrize("shape", [dict(W=4, M=256, K=512, N=768, chunk_rows=64),
-                                   dict(W=2, M=64, K=128, N=256, chunk_rows=32)])
-def test_ag_copy_engine_producer(shape):
-    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], **shape)
-    inp = wls.make_inputs(wl, integer=True)
-    o = opts(chunk_rows=shape["chunk_rows"], producer=tdx.TDX_PRODUCER_COPY_ENGINE)
-    case = AGCase(inp, opts=o)
-    want = R.round_out(case.oracle(), "bf16")
-    for e in (0, 3, 4):
-        case.C.fill_(float("nan"))
-        tdx.check(case.run(opts(chunk_rows=shape["chunk_rows"], producer=tdx.TDX_PRODUCER_COPY_ENGINE, epoch=e)))
-        status_ok(case)
-        assert np.array_equal(case.result_bits(), want)
-    plan = tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o)
-    assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
-    n = wl.W * plan["n_chunks"]
-    f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
-    assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 4))
-    # move-only through the copy engine
-    case.ws[plan["off_G"]:plan["off_G"] + wl.W * wl.M * wl.K * 2].zero_()
-    tdx.check(case.run(opts(chunk_rows=shape["chunk_rows"], producer=tdx.TDX_PRODUCER_COPY_ENGINE,
-                            mode=tdx.TDX_MOVE_ONLY)))
-    torch.cuda.synchronize()
-    assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
-    status_ok(case)
-
-
-def test_ag_full_size_copy_engine_sampled():
-    wl = wls.WORKLOADS["ag_w8"]
-    inp = wls.make_inputs(wl, integer=False)
-    case = AGCase(inp, opts=opts(producer=tdx.TDX_PRODUCER_COPY_ENGINE))
-    tdx.check(case.run())
-    status_ok(case)
-    rows = sample_rows(wl.W * wl.M, wl.chunk_rows)
-    assert_within_tol(R.decode_bf16(case.result_bits()[rows]), case.oracle(rows), "bf16")
-
-
 def test_ag_split_k_chained_and_slotted_identical():
     wl = wls.WORKLOADS["ag_small"]
     inp = wls.make_inputs(wl, integer=False)
