@@ -59,8 +59,7 @@ struct Plan {
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
   int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
   size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, off_tile_done = 0, ctrl_end = 0;
-  int coop = 0;          // slotted fold: 0 last arriver, 1 cooperative, 2 deferred tasks (make_plan)
-  int fold_parts = 1;    // deferred fold: parts per tile
+  int coop = 0;          // slotted fold: 0 last arriver, 1 cooperative (see make_plan)
   size_t off_G = 0, off_S = 0, total = 0;
 };
 
@@ -170,19 +169,14 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   // is safe only when a tile's elements are processed in the same wave of the persistent grid; it is
   // used when all work items fit one wave (a rank-inner order with the grid a multiple of L would
   // also qualify, but that order measured slower on the multi-wave small-M ReduceScatter).
-  // With more work than one wave, the fold is deferred instead: CTAs that have finished their items
-  // take fold tasks (a tile's part) and wait for that tile's partials, which spreads the folds of
-  // the last tiles over every SM rather than leaving them to the last arrivers.
+  // (Spreading the folds of a multi-wave schedule over the CTAs that finished their items, as
+  // deferred fold tasks, measured slower on the small-M ReduceScatter than the last arriver: with
+  // the rank-outer order the tiles complete only at the end, while the last arriver's slots are
+  // still in L2.)
   if (p.reduce_last && p.PM == 0 && !p.bf16_partials && L > 1) {
     int sms = device_sms();
     if (o.num_sms > 0 && (sms == 0 || o.num_sms < sms)) sms = o.num_sms;
-    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) {
-      p.coop = 1;
-    } else if (sms > 0) {
-      p.coop = 2;
-      int q = (2 * sms + p.T - 1) / (p.T > 0 ? p.T : 1);
-      p.fold_parts = q < 1 ? 1 : (q > 16 ? 16 : q);
-    }
+    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) p.coop = 1;
   }
   // workspace layout
   size_t off = kHeaderBytes;
@@ -295,7 +289,6 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.tile_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tile_cnt);
   kp.tile_done = reinterpret_cast<uint32_t*>(ws + pl.off_tile_done);
   kp.coop_fold = pl.coop;
-  kp.fold_parts = pl.fold_parts;
   kp.reduce_last = pl.reduce_last;
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;

@@ -71,9 +71,8 @@ struct KParams {
   float* sbuf;                   // chained: [T][kBM*BN] running sum; slotted: [L][T][kBM*BN] partials
   uint32_t* tile_cnt;            // slotted: partials stored per tile (reset by the last arriver)
   uint32_t* tile_done;           // cooperative fold: elements that folded their share (reset by the last)
-  int coop_fold;                 // slotted fold: 0 last arriver, 1 the L elements of a tile fold 1/L
-                                 // each after all arrived, 2 deferred fold tasks after the items
-  int fold_parts;                // deferred fold: parts per tile
+  int coop_fold;                 // slotted fold: 0 the last arriver folds the tile, 1 the L elements
+                                 // of a tile fold 1/L each after all arrived (one wave of work)
   int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
   float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r

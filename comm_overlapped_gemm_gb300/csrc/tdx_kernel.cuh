@@ -1242,9 +1242,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x30000u + it) & 4095u);
           __threadfence();
           const uint32_t old = atomicAdd(p.tile_cnt + w.tile, 1u);
-          if (p.coop_fold == 2) {
-            *is_last = 0u;   // deferred fold: the tile is folded by the fold tasks after the items
-          } else if (p.coop_fold) {
+          if (p.coop_fold) {
             const bool ok = wait_count(p, p.tile_cnt + w.tile, static_cast<uint32_t>(p.L), abort_flag,
                                        static_cast<uint32_t>(w.tile));
             if (ok) fence_acq_rel_gpu();
@@ -1289,9 +1287,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
       }
-      if (slotted && p.coop_fold == 2) {
-        // deferred fold: nothing more for this item
-      } else if (slotted && p.coop_fold) {
+      if (slotted && p.coop_fold) {
         // cooperative fold: this element folds float4 block [c*per, (c+1)*per) of the tile's slot
         // layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), all L
         // slots in order 0..L-1, and the element that completes the tile's done count resets both
@@ -1407,36 +1403,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             for (int c = 0; c < p.L; ++c)
               for (int l = et; l < (int)(sbytes / 128); l += kEpiThreads)
                 discard_l2_line(reinterpret_cast<uint8_t*>(p.sbuf) + ((size_t)c * p.T + w.tile) * sbytes + (size_t)l * 128);
-          }
-        }
-      }
-    }
-    if (chain && p.reduce_last && p.coop_fold == 2 && !*abort_flag) {
-      // deferred fold: once its own items are done, a CTA takes fold tasks (tile, part) in tile
-      // order, waits (bounded) until the tile's L partials are stored, and folds that part. The
-      // items never wait on fold tasks, so the waits end. The task that completes a tile's done
-      // count resets its counters for the next call.
-      const int et = threadIdx.x - kEpiWarp0 * 32;
-      const int Q = p.fold_parts;
-      const int ntask = p.T * Q;
-      for (int task = blockIdx.x; task < ntask; task += grid) {
-        const int tile = task / Q;
-        if (elected) {
-          const bool ok = wait_count(p, p.tile_cnt + tile, static_cast<uint32_t>(p.L), abort_flag,
-                                     static_cast<uint32_t>(tile));
-          if (ok) fence_acq_rel_gpu();
-          *decision = ok ? 1u : 0u;
-        }
-        named_bar_sync(1, kEpiThreads);
-        if (*decision == 0u) break;
-        fold_part<OP, FP8, BN>(p, tile, task - tile * Q, Q, et, once);
-        named_bar_sync(1, kEpiThreads);
-        if (elected) {
-          const uint32_t done = atomicAdd(p.tile_done + tile, 1u);
-          if (done == static_cast<uint32_t>(Q - 1)) {
-            p.tile_cnt[tile] = 0u;
-            p.tile_done[tile] = 0u;
-            __threadfence();
           }
         }
       }

@@ -307,11 +307,10 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
  * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
  * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
- * 2 bf16 partials), [21] how the slotted fold is shared (single CTAs, fp32 partials; depends on the
- * device's SM count and opts.num_sms): 1 cooperative (every work item fits one wave of the
- * persistent grid: each element of a tile waits for the tile's L partials and folds 1/L of it),
- * 2 deferred (more than one wave: CTAs that finished their items take fold tasks, parts of tiles,
- * each waiting for its tile's partials), 0 the last arriver folds the tile. */
+ * 2 bf16 partials), [21] 1 if the slotted fold is cooperative (single CTAs, fp32 partials, every
+ * work item in one wave of the persistent grid, which depends on the device's SM count and
+ * opts.num_sms: each element of a tile waits for the tile's L partials and folds 1/L of it), 0 if
+ * the last arriver folds the tile. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 
