@@ -199,7 +199,7 @@ def tdx_ag_gemm(shards, B, C, workspace, W: int, M_local: int, K: int, N: int, d
                                 dtype, _opts_ref(opts), _stream(stream)))
 
 
-TDX_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+TDX_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 def tdx_ag_gemm_noalloc(shards, B, C, W: int, M_local: int, K: int, N: int, dtype: int, opts=None,

@@ -154,8 +154,8 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
                        int W, int M, int K, int N, tdx_dtype dtype,
                        const tdx_opts* opts, void* stream);
 
-/* Size of the library's built-in scratch array used by tdx_ag_gemm_noalloc: 8 MiB per device. */
-#define TDX_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+/* Size of the library's built-in scratch array used by tdx_ag_gemm_noalloc: 16 MiB per device. */
+#define TDX_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /* AllGather+GEMM for callers that cannot allocate device memory themselves: for example code that
  * runs inside a host framework which owns every device allocation and exposes no allocator to it
