@@ -121,8 +121,10 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   } else {
     if (bn == 0) {
       bn = N > 128 ? 256 : ((N > 64 || fp8) ? 128 : 64);
-      // few output tiles: narrower tiles spread the ranks' partial reductions over more CTAs
-      if (bn == 256 && static_cast<long long>(p.tiles_m) * ((N + 255) / 256) < 2 * kRefSMs) bn = 128;
+      // few output tiles: narrower tiles spread the ranks' partial reductions over more CTAs; not for
+      // one or two M-tiles, where the run is bound by streaming B_r and 256-wide rows read it best
+      // (small-M: 45.8 vs 49.0 us)
+      if (bn == 256 && p.tiles_m > 2 && static_cast<long long>(p.tiles_m) * ((N + 255) / 256) < 2 * kRefSMs) bn = 128;
     }
     L = W;
   }
