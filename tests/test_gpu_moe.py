@@ -209,3 +209,34 @@ def test_moe_e4m3_full_size_sampled():
     rows = np.array(sorted(rows))
     want = MO.moe_dispatch_gemm_rows(inp.a, inp.route, inp.b[0], wl.E, rows, "e4m3", inp.scale_a, inp.scale_b)
     assert_within_tol(R.decode_bf16(case.result_bits()[rows]), want, "e4m3")
+
+
+def _skewed(inp, experts):
+    """Every token of every rank routed to the same `experts` (one slot each)."""
+    for s in range(len(inp.route)):
+        r = np.empty_like(inp.route[s])
+        r[:] = np.asarray(experts, dtype=np.int32)[None, :]
+        inp.route[s] = r
+    return inp
+
+
+@pytest.mark.parametrize("case_name", ["mostly_empty", "skewed"])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_moe_empty_and_skewed_experts(case_name, dtype):
+    base = "moe_w8" if dtype == "bf16" else "moe_fp8_w8"
+    if case_name == "mostly_empty":
+        wl = wls.with_shape(wls.WORKLOADS[base], W=2, M=3, K=128, N=256, E=64, topk=2)   # 12 rows, 64 experts
+        inp = wls.make_inputs(wl, integer=True)
+    else:
+        wl = wls.with_shape(wls.WORKLOADS[base], W=4, M=660, K=128, N=256, E=8, topk=2)  # all to experts 1 and 6: 21 tiles each
+        inp = _skewed(wls.make_inputs(wl, integer=True), [6, 1])
+    sa = inp.scale_a if dtype == "e4m3" else None
+    sb = inp.scale_b if dtype == "e4m3" else None
+    want, lay = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E, dtype, sa, sb)
+    kw = dict(scale_a=sa, scale_b=sb) if dtype == "e4m3" else {}
+    for bn, cl in ((0, 0), (256, 3)):
+        case = MoECase(inp, opts=opts(block_n=bn, cluster=cl, **kw))
+        tdx.check(case.run())
+        status_ok(case)
+        check_layout(case, lay)
+        assert_bit_exact(case.result_bits(), want, "bf16")

@@ -113,3 +113,23 @@ def test_combine_full_size_sampled():
     want = MO.moe_gemm_combine_rows(inp.a[0], inp.route, inp.b[0], inp.gates, wl.E, toks)
     sel = np.stack([got[s][t] for (s, t) in toks])
     assert_within_tol(R.decode_bf16(sel), want, "bf16")
+
+
+@pytest.mark.parametrize("case_name", ["mostly_empty", "skewed"])
+def test_combine_empty_and_skewed_experts(case_name):
+    if case_name == "mostly_empty":
+        wl = wls.with_shape(wls.WORKLOADS["moe_combine_w8"], W=2, M=3, K=128, N=256, E=64, topk=2)
+        inp = wls.make_inputs(wl, integer=True)
+    else:
+        wl = wls.with_shape(wls.WORKLOADS["moe_combine_w8"], W=4, M=660, K=128, N=256, E=8, topk=2)
+        inp = wls.make_inputs(wl, integer=True)
+        for s in range(wl.W):
+            r = np.empty_like(inp.route[s])
+            r[:] = np.array([6, 1], dtype=np.int32)[None, :]
+            inp.route[s] = r
+    want = oracle_out(inp)
+    for bn, cl in ((0, 0), (256, 3)):
+        case = CombineCase(inp, opts=opts(block_n=bn, cluster=cl))
+        tdx.check(case.run())
+        status_ok(case)
+        assert_bit_exact(case.result_bits().reshape(-1, wl.N), want.reshape(-1, wl.N), "bf16")
