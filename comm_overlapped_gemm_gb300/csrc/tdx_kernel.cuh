@@ -71,10 +71,15 @@ namespace tdx {
 #define TDX_DISCARD_DEAD 0
 #endif
 
+// Largest MoE dispatch staging ring (KiB).
+#ifndef TDX_MOE_STG_MAX_KB
+#define TDX_MOE_STG_MAX_KB 32
+#endif
+
 // PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
 // 256 x BN tile with one instruction stream issued by the leader; each CTA stages its own 128 rows
 // of A and its half (BN/2 columns) of the B slice, and holds its 128 x BN accumulator in TMEM.
-template <int BN, bool FP8, bool PAIR_MMA = false>
+template <int BN, bool FP8, bool PAIR_MMA = false, int RING_KB = 216>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
   // K bytes per ring slot (k_slice_bytes): A rows in a slot are KB bytes long; B keeps 128-byte MN
@@ -92,7 +97,7 @@ struct Cfg {
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_BOXES_CTA * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (216 * 1024) / STAGE_BYTES;   // ring budget: 216 KiB
+  static constexpr int STAGES_RAW = (RING_KB * 1024) / STAGE_BYTES;   // ring budget (216 KiB by default)
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
   static constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -102,7 +107,7 @@ struct Cfg {
   // MoE dispatch staging ring for bulk row copies: what the GEMM ring leaves of the 227 KiB, at
   // most 32 KiB, in whole KiB (at least 4 KiB)
   static constexpr int MOE_STG_RAW = 227 * 1024 - SMEM_BYTES - 128;
-  static constexpr int MOE_STG = (MOE_STG_RAW > 32 * 1024 ? 32 * 1024 : MOE_STG_RAW) / 1024 * 1024;
+  static constexpr int MOE_STG = (MOE_STG_RAW > TDX_MOE_STG_MAX_KB * 1024 ? TDX_MOE_STG_MAX_KB * 1024 : MOE_STG_RAW) / 1024 * 1024;
   static constexpr int COLS_PER_WARP = BN / 2;    // 8 epilogue warps = 4 lane quarters x 2 halves
   static constexpr int CHUNKS = COLS_PER_WARP / 32;
   // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B type (bits 7-9, 10-12: bf16 = 1,
@@ -117,6 +122,12 @@ struct Cfg {
   static_assert(CHUNKS >= 1, "at least one 32-column chunk per epilogue warp");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
+
+// GEMM ring budget per op: the MoE dispatch may give part of it to its staging ring.
+#ifndef TDX_MOE_RING_KB
+#define TDX_MOE_RING_KB 216
+#endif
+constexpr int ring_kb(int op) { return op == OP_MOE ? TDX_MOE_RING_KB : 216; }
 
 struct Item {
   int c;      // chain element (RS rank, or AG K split)
@@ -641,7 +652,7 @@ template <int BN, bool FP8, int OP, int PM>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
   constexpr int CL = PM == 0 ? 1 : 2;      // CTAs per cluster
   static_assert(PM == 0 || Cfg<BN, FP8>::B_BOXES % 2 == 0, "pairs split B into two halves");
-  using C = Cfg<BN, FP8, PM == 2>;
+  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1457,7 +1468,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 
 template <int BN, bool FP8, int OP, int PM>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, FP8, PM == 2>;
+  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
   constexpr int CL = PM == 0 ? 1 : 2;
   // MoE adds the dispatch staging ring (128-byte aligned) after the GEMM's shared memory
   constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
@@ -1503,7 +1514,7 @@ int max_grid_t(int sms) {
   if constexpr (CL == 1) {
     return sms;
   } else {
-    using C = Cfg<BN, FP8, PM == 2>;
+    using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
     constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
     static int cache[64] = {};
     int dev = 0;
