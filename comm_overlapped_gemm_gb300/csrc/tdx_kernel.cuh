@@ -71,6 +71,16 @@ namespace tdx {
 #define TDX_DISCARD_DEAD 0
 #endif
 
+// MoE dispatch bulk copies: L2 policy of the token-row loads and of the receive-buffer stores
+// (-1 = no hint, else as TDX_OPERAND_POLICY: 0 evict_first, 1 evict_last, 2 evict_normal). Token
+// rows evict-first (each is re-read only by its other slots, far apart) and receive-buffer rows
+// evict-last (the GEMM reads them next): fused dispatch + GEMM 5.54 -> 5.33 ms on GB300.
+#ifndef TDX_MOE_LOAD_POLICY
+#define TDX_MOE_LOAD_POLICY 0
+#endif
+#ifndef TDX_MOE_STORE_POLICY
+#define TDX_MOE_STORE_POLICY 1
+#endif
 // Largest MoE dispatch staging ring (KiB).
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
@@ -1063,7 +1073,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             const uint32_t bar = smem_u32(stg_bars + b);
             if (tok >= 0 && tok < ntok) {
               mbar_arrive_expect_tx(bar, n);
-              bulk_load_g2s(smem_u32(stg + b * seg), src_of(tok, off), n, bar);
+              if constexpr (TDX_MOE_LOAD_POLICY >= 0)
+                bulk_load_g2s_hint(smem_u32(stg + b * seg), src_of(tok, off), n, bar, policy_of(TDX_MOE_LOAD_POLICY));
+              else
+                bulk_load_g2s(smem_u32(stg + b * seg), src_of(tok, off), n, bar);
             } else {
               mbar_arrive(bar);   // nothing to move for an invalid source; keep the phases in step
             }
@@ -1087,7 +1100,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             const uint32_t n = rb - off < seg ? rb - off : seg;
             const int tok = psrc[row];
             if (tok >= 0 && tok < ntok) {
-              bulk_store_s2g(p.G + (long long)(r0 + row) * p.row_bytes + off, smem_u32(stg + b * seg), n);
+              if constexpr (TDX_MOE_STORE_POLICY >= 0)
+                bulk_store_s2g_hint(p.G + (long long)(r0 + row) * p.row_bytes + off, smem_u32(stg + b * seg), n,
+                                    policy_of(TDX_MOE_STORE_POLICY));
+              else
+                bulk_store_s2g(p.G + (long long)(r0 + row) * p.row_bytes + off, smem_u32(stg + b * seg), n);
               bulk_commit();
             }
           }
