@@ -81,6 +81,10 @@ namespace tdx {
 #ifndef TDX_MOE_STORE_POLICY
 #define TDX_MOE_STORE_POLICY 1
 #endif
+// MoE combine: L2 policy of the expert-output stores (read back by the combine): as above.
+#ifndef TDX_COMBINE_Z_POLICY
+#define TDX_COMBINE_Z_POLICY 1
+#endif
 // Largest MoE dispatch staging ring (KiB).
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
@@ -1143,6 +1147,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     uint64_t chain_ns = 0;
     const uint64_t once = policy_of(TDX_SUM_POLICY);   // running sums and outputs
     const uint64_t keep_slot = policy_evict_last();     // slotted partials, folded soon after
+    const uint64_t z_pol = policy_of(TDX_COMBINE_Z_POLICY);   // MoE expert outputs, combined soon after
     int local = 0;
     for (int it = cid; it < items; it += ncl, ++local) {
       const Item w = decode_item<OP, CL>(p, it, BN, crank);
@@ -1240,7 +1245,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
         if (direct_out)
           store_out_chunk<OP, FP8>(p, ((OP == OP_MOE || OP == OP_MOE_COMBINE) && row >= w.mend) ? p.M : row,
-                                   w.n0 + col0, v, once);
+                                   w.n0 + col0, v, OP == OP_MOE_COMBINE ? z_pol : once);
       }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
