@@ -85,6 +85,11 @@ namespace tdx {
 #ifndef TDX_COMBINE_Z_POLICY
 #define TDX_COMBINE_Z_POLICY 1
 #endif
+// AllGather producer: 1 = TMA bulk copies through the staging ring (one thread per CTA), 0 =
+// register rounds of the two producer warps.
+#ifndef TDX_AG_BULK
+#define TDX_AG_BULK 1
+#endif
 // Largest MoE dispatch staging ring (KiB).
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
@@ -142,6 +147,10 @@ struct Cfg {
 #define TDX_MOE_RING_KB 216
 #endif
 constexpr int ring_kb(int op) { return op == OP_MOE ? TDX_MOE_RING_KB : 216; }
+// Ops whose producer moves data with bulk copies through a shared-memory staging ring.
+constexpr bool uses_staging(int op) { return op == OP_MOE || (op == OP_AG && TDX_AG_BULK != 0); }
+
+
 
 struct Item {
   int c;      // chain element (RS rank, or AG K split)
@@ -299,6 +308,43 @@ static __device__ __noinline__ bool wait_mbar_drain(const KParams& p, uint32_t b
       return false;
     }
   }
+}
+
+// Copy `n` bytes (16-byte aligned addresses, n a multiple of 16) from src to dst with bulk copies
+// through the staging ring: segments of `seg` bytes in `nb` ring buffers, nb - 1 loads in flight,
+// each segment stored back as soon as it lands; returns once every store has completed and is
+// ordered before later generic accesses. `g` counts the CTA's segments (ring barrier phases). One
+// thread.
+static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* stg, uint64_t* bars, uint32_t seg, int nb,
+                                                     uint32_t& g, const uint8_t* src, uint8_t* dst, uint32_t n,
+                                                     uint64_t lpol, uint64_t spol) {
+  const int nseg = static_cast<int>((n + seg - 1) / seg);
+  auto issue = [&](int i) {
+    const uint32_t off = static_cast<uint32_t>(i) * seg;
+    const uint32_t m = n - off < seg ? n - off : seg;
+    const uint32_t b = (g + static_cast<uint32_t>(i)) % static_cast<uint32_t>(nb);
+    const uint32_t bar = smem_u32(bars + b);
+    mbar_arrive_expect_tx(bar, m);
+    bulk_load_g2s_hint(smem_u32(stg + b * seg), src + off, m, bar, lpol);
+  };
+  for (int i = 0; i < min(nb - 1, nseg); ++i) issue(i);
+  for (int i = 0; i < nseg; ++i) {
+    const int j = i + nb - 1;
+    if (j < nseg) {
+      bulk_wait_read_all();
+      issue(j);
+    }
+    const uint32_t gi = g + static_cast<uint32_t>(i);
+    const uint32_t b = gi % static_cast<uint32_t>(nb);
+    wait_mbar_drain(p, smem_u32(bars + b), (gi / static_cast<uint32_t>(nb)) & 1u);
+    const uint32_t off = static_cast<uint32_t>(i) * seg;
+    const uint32_t m = n - off < seg ? n - off : seg;
+    bulk_store_s2g_hint(dst + off, smem_u32(stg + b * seg), m, spol);
+    bulk_commit();
+  }
+  g += static_cast<uint32_t>(nseg);
+  bulk_wait_all();
+  fence_proxy_async_global();
 }
 
 // Bounded acquire-wait until *flag == epoch. A value above the epoch is a stale flag. Also gives
@@ -700,7 +746,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       mbar_init(tempty0 + 8 * a, PM == 2 ? 2 : 1);   // PM 2: both CTAs' epilogues free the leader's
     }
     mbar_init(drain_bar, 1);
-    if constexpr (OP == OP_MOE)
+    if constexpr (uses_staging(OP))
       for (int b = 0; b < 8; ++b) mbar_init(smem_u32(stg_bars + b), 1);
     misc[1] = 0;
     misc[2] = 0;
@@ -982,7 +1028,44 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
     // =============================================================== AllGather producer
-    if (ag && p.copy_active) {
+    if (ag && p.copy_active && uses_staging(OP)) {
+      // One thread moves the CTA's pieces with bulk copies through the staging ring; the piece that
+      // completes a chunk's count releases the chunk's flag.
+      const int ct = threadIdx.x - kCopyWarp0 * 32;
+      if (ct == 0) {
+        constexpr uint32_t kStg = static_cast<uint32_t>(C::MOE_STG);
+        const uint32_t seg = (kStg / 4) / 16 * 16;
+        const int nb = min(8, static_cast<int>(kStg / seg));
+        const uint64_t lpol = policy_evict_first();   // each shard byte is read once
+        const uint64_t spol = policy_evict_last();    // the GEMM reads the gathered rows next
+        uint32_t gseg = 0;
+        for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
+          const int q = piece / p.ppc;
+          const int pc = piece - q * p.ppc;
+          const int rr = q / p.n_chunks;
+          const int rank = (p.self_rank + 1 + rr) % p.W;
+          const int ck = q - rr * p.n_chunks;
+          const long long off = (long long)pc * p.piece_bytes;
+          const long long rem = p.chunk_bytes - off;
+          const int n = rem < p.piece_bytes ? static_cast<int>(rem) : p.piece_bytes;
+          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
+          if (n > 0)
+            bulk_copy_contig(p, stg, stg_bars, seg, nb, gseg, p.shard[rank] + (long long)ck * p.chunk_bytes + off,
+                             p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off,
+                             static_cast<uint32_t>(n), lpol, spol);
+          const int fi = rank * p.n_chunks + ck;
+          __threadfence();
+          const uint32_t old = atomicAdd(p.chunk_cnt + fi, 1u);
+          if (old == static_cast<uint32_t>(p.ppc - 1)) {
+            p.chunk_cnt[fi] = 0u;
+            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
+            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
+            __threadfence();
+            st_release_gpu(p.chunk_flags + fi, p.epoch);
+          }
+        }
+      }
+    } else if (ag && p.copy_active) {
       // A piece (p.piece_bytes, a multiple of 16 KiB) is copied in rounds of 16 KiB: each of the
       // 64 producer threads keeps 16 vector loads in flight, stores them, and the next round
       // starts at once; the synchronisation that releases a chunk (barrier, fence, counter
@@ -1493,8 +1576,8 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
   constexpr int CL = PM == 0 ? 1 : 2;
   // MoE adds the dispatch staging ring (128-byte aligned) after the GEMM's shared memory
-  constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
-  static_assert(OP != OP_MOE || (C::MOE_STG >= 4096 && kSmem <= 227 * 1024), "MoE staging ring budget");
+  constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
+  static_assert(!uses_staging(OP) || (C::MOE_STG >= 4096 && kSmem <= 227 * 1024), "staging ring budget");
   // the dynamic shared-memory limit is raised once per device for each instantiation
   static bool attr_done[64] = {};
   int dev = 0;
@@ -1537,7 +1620,7 @@ int max_grid_t(int sms) {
     return sms;
   } else {
     using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
-    constexpr int kSmem = C::SMEM_BYTES + (OP == OP_MOE ? 128 + C::MOE_STG : 0);
+    constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
     static int cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
