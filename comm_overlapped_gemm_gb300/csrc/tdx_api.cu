@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/tdx.h: argument validation, tiling choice, workspace
-// carving (status word, chunk flags, gathered buffer, running-sum buffer), TMA tensor maps and the
-// launch of the persistent fused kernel. No arithmetic of the operations happens here.
+// carving (status word, chunk flags, gathered buffer, running-sum / partial-slot buffer, MoE layout
+// tables and receive buffer), TMA tensor maps and the launches of the persistent fused kernel and
+// of the MoE routing-layout kernel. No arithmetic of the operations happens here.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -13,7 +14,7 @@ using namespace tdx;
 
 namespace {
 
-constexpr uint32_t kVersion = (1u << 16) | 0u;
+constexpr uint32_t kVersion = (1u << 16) | 1u;   // 1.1: AllReduce, bf16 partials, MoE dispatch and combine
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -392,7 +393,7 @@ tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* 
   kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
   const int grid = grid_for(o, pl, fp8, 0);
   if (grid <= 0) return TDX_ERR_CUDA;
-  // producer copy unit: about one piece per CTA, in 16 KiB rounds, at most 64 KiB per release
+  // producer copy unit: about one piece per CTA, a multiple of 16 KiB, at most 64 KiB per release
   {
     const long long total = static_cast<long long>(W) * pl.n_chunks * kp.chunk_bytes;
     long long pb = (total / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;

@@ -1,15 +1,19 @@
-// The persistent fused kernel: AllGather chunk producer + flag-gated tcgen05/TMEM GEMM, and
-// GEMM + rank-ordered ReduceScatter, in one launch per call.
+// The persistent fused kernel: AllGather chunk producer + flag-gated tcgen05/TMEM GEMM, GEMM +
+// rank-ordered ReduceScatter / AllReduce, and the mixture-of-experts AllToAll dispatch + grouped
+// GEMM and grouped GEMM + combine, in one launch per call.
 //
 // Roles (one CTA per SM, 12 warps):
-//   warp 0  lane 0  TMA issuer. For an AllGather tile it first acquire-waits the flags of every
-//                   chunk the tile's rows fall in (unless the rows are the local shard), then
-//                   streams 128-byte K slices of A and B into an S-stage shared-memory ring.
+//   warp 0  lane 0  TMA issuer. For an AllGather (or MoE dispatch) tile it first acquire-waits the
+//                   flags of every chunk the tile's rows fall in (unless the rows are the local
+//                   shard), then streams 128-byte K slices of A and B into an S-stage ring.
 //   warp 1  lane 0  MMA issuer: tcgen05.mma (bf16: kind::f16, e4m3: kind::f8f6f4) into one of two
 //                   TMEM accumulators of 128 x BN fp32; tcgen05.commit frees ring slots and
 //                   hands finished accumulators to the epilogue. Warp 1 allocates TMEM.
-//   warps 2-3       AllGather producer: copies 16 KiB pieces of shard chunks into the gathered
-//                   buffer; the last piece of a chunk releases the chunk's flag (= epoch).
+//   warps 2-3       producer: one thread moves pieces of shard chunks (AllGather) or gathered
+//                   token rows (MoE dispatch) into the gathered / receive buffer with TMA bulk
+//                   copies through a shared-memory staging ring; the piece that completes a chunk
+//                   releases the chunk's flag (= epoch). (Build switch TDX_AG_BULK=0: the two
+//                   warps copy AllGather pieces in register rounds.)
 //   warps 4-11      epilogue: TMEM -> registers; either the output tile (rounded once) or, along
 //                   a chain (RS ranks or AG K-splits) of L elements, the fixed-order fp32 sum
 //                   ((P_0 + P_1) + P_2) + ... of the elements' partial tiles, in one of two ways:
@@ -18,9 +22,12 @@
 //                   last element rounds and stores the output (large problems: the elements of a
 //                   tile run far apart in time, one running-sum buffer). "slotted": every element
 //                   stores its partial in its own slot and bumps the tile's arrival counter; the
-//                   element that completes the count folds the slots in order 0..L-1 (small
-//                   problems: the elements of a tile run concurrently, nothing waits). Either way
-//                   the order is fixed, so results are bit-identical run to run.
+//                   element that completes the count folds the slots in order 0..L-1, or, when
+//                   all the work fits one wave, every element folds 1/L of the tile once all L
+//                   arrived (small problems: the elements of a tile run concurrently). Either way
+//                   the order is fixed, so results are bit-identical run to run. For the MoE
+//                   combine the epilogue also counts each token's stored expert-output rows and
+//                   folds the tokens it completes with their gates.
 //
 // The chunk/flag pipeline follows the Triton-distributed article (cronfeed.work), section "The
 // first move was to expose the overlap" (chunks, compute on arrived chunks while others move,
