@@ -22,7 +22,14 @@ constexpr int kCopyThreads = kNumCopyWarps * 32;
 constexpr int kCopyRoundBytes = 16384;   // producer: bytes in flight per CTA per round
 constexpr int kMaxPieceBytes = 65536;    // producer: largest copy unit released at once
 constexpr int kMaxSplitK = 16;
-constexpr int kRsGroupN = 8;             // RS raster: N-tiles per group
+// RS raster: N-tiles per group (a rank's tiles are taken group by group, M-tiles, then the group's
+// N-tiles), so that a wave reads few columns of B_r while A_r is streamed once per group. Step
+// throughput on GB300 (W=8 AG + RS) by group size 4 / 8 / 16 / 32: 1516 / 1538 / 1561 / 1513
+// TFLOP/s.
+#ifndef TDX_RS_GROUP_N
+#define TDX_RS_GROUP_N 16
+#endif
+constexpr int kRsGroupN = TDX_RS_GROUP_N;
 // RS order: tiles per rank block (divided by the CTAs per cluster to count positions); a block is
 // processed for every rank before the next, so a tile's running sum is re-read by the next rank
 // about one block later. Default: one block of every tile (rank-outer order), which measured

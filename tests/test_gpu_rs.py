@@ -229,13 +229,14 @@ def test_rs_pairs_parity_trace_and_identity(rm, cluster):
 
 
 def test_rs_grouped_raster_trace():
-    # 10 N-tiles of 128: groups of 8 and 2 within each rank
-    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=2, M=256, K=128, N=1280)
+    # 20 N-tiles of 128: a full group and a partial one within each rank
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=2, M=256, K=128, N=2560)
     inp = wls.make_inputs(wl, integer=True)
     grid = 6
     o = opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1)
-    plan = tdx.tdx_plan_info(tdx.OP_RS, 2, 256, 128, 1280, tdx.TDX_BF16, o)
-    assert plan["group_n"] == 8 and plan["tiles_n"] == 10
+    plan = tdx.tdx_plan_info(tdx.OP_RS, 2, 256, 128, 2560, tdx.TDX_BF16, o)
+    gn = plan["group_n"]
+    assert plan["tiles_n"] == 20 and 1 < gn < 20 and 20 % gn != 0
     items = plan["L"] * plan["T"]
     trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
     case = RSCase(inp, opts=opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1, trace=trace))
@@ -243,7 +244,7 @@ def test_rs_grouped_raster_trace():
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(2, 256, 1280, 128, 128, group_n=8, rank_block=plan["rank_block"])
+    sched = R.rs_item_schedule(2, 256, 2560, 128, 128, group_n=gn, rank_block=plan["rank_block"])
     per = (items + grid - 1) // grid
     for b in range(grid):
         for k, it in enumerate(range(b, items, grid)):
