@@ -658,6 +658,27 @@ def run_gpu(args):
     t_rs_m = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_MOVE_ONLY)), reps)
     st.status()
 
+    # stall-on-flag: one traced fused AllGather call; the kernel's trace holds, per CTA, the TMA
+    # issuer's total time spent waiting for chunk flags and the number of tiles that waited
+    wa = st.wa
+    plan_ag = tdx.tdx_plan_info(tdx.OP_AG, wa.W, wa.M, wa.K, wa.N, tdx.TDX_BF16, tdx.make_opts(chunk_rows=wa.chunk_rows))
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    items_ag = plan_ag["L"] * plan_ag["T"]
+    # the layout depends on the grid actually launched (at most one CTA per SM): size for any of them
+    trace = torch.zeros(max(tdx.tdx_trace_size(g, items_ag) // 4 for g in range(2, n_sm + 1)), dtype=torch.int32,
+                        device=dev)
+    saved = st.extra
+    st.extra = dict(saved, trace=trace)
+    tdx.check(st.ag())
+    st.extra = saved
+    torch.cuda.synchronize()
+    st.status()
+    tr = trace.cpu().numpy().view(np.uint32)
+    g_ag = int(tr[0])
+    per_cta = tr[4:4 + 4 * g_ag].reshape(g_ag, 4).astype(np.float64)
+    flag_wait = {"mean_us": float(per_cta[:, 0].mean() / 1e3), "max_us": float(per_cta[:, 0].max() / 1e3),
+                 "tiles_that_waited_per_cta": float(per_cta[:, 1].mean())}
+
     # end to end through the same C-ABI calls with pinned host buffers, double-buffered: step i+1's
     # inputs go host -> device on four copy streams (several copy engines) while step i computes on
     # the other device buffer set; every step's results come back to pinned host memory
@@ -749,7 +770,8 @@ def run_gpu(args):
         "ag_gemm": {"tflops": fl_ag / (ms_ag * 1e-3) / 1e12, "ms": ms_ag, "ms_fused": t_ag_f,
                     "ms_gemm_only": t_ag_g, "ms_move_only": t_ag_m,
                     "overlap_efficiency": max(t_ag_g, t_ag_m) / t_ag_f,
-                    "frac_of_peak": fl_ag / (ms_ag * 1e-3) / 1e12 / peak_tf},
+                    "frac_of_peak": fl_ag / (ms_ag * 1e-3) / 1e12 / peak_tf,
+                    "stall_on_flag": flag_wait},
         "gemm_rs": {"tflops": achieved, "ms": ms_rs, "ms_fused": t_rs_f, "ms_gemm_only": t_rs_g,
                     "ms_move_only": t_rs_m, "overlap_efficiency": max(t_rs_g, t_rs_m) / t_rs_f,
                     "frac_of_peak": achieved / peak_tf},
