@@ -97,6 +97,10 @@ namespace tdx {
 #ifndef TDX_AG_BULK
 #define TDX_AG_BULK 1
 #endif
+// AllGather bulk producer: L2 policy of the gathered-buffer stores (as TDX_OPERAND_POLICY).
+#ifndef TDX_AG_STORE_POLICY
+#define TDX_AG_STORE_POLICY 1
+#endif
 // Largest MoE dispatch staging ring (KiB).
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
@@ -1044,7 +1048,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         const uint32_t seg = (kStg / 4) / 16 * 16;
         const int nb = min(8, static_cast<int>(kStg / seg));
         const uint64_t lpol = policy_evict_first();   // each shard byte is read once
-        const uint64_t spol = policy_evict_last();    // the GEMM reads the gathered rows next
+        const uint64_t spol = policy_of(TDX_AG_STORE_POLICY);   // the GEMM reads the gathered rows next
         uint32_t gseg = 0;
         for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
           const int q = piece / p.ppc;
