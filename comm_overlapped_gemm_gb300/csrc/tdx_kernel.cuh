@@ -650,70 +650,141 @@ __device__ __forceinline__ void fold_part(const KParams& p, int tile, int part, 
   }
 }
 
-// MoE combine of one token over columns [col0, col0 + ncols), one warp: lane l takes the 8
-// columns col0 + 8l .. col0 + 8l + 7 and keeps the k expert-output loads of its slots in flight
-// together. out_s[t] = sum_j g[s][t][j] * Z[dest[s][t][j]] in slot order j = 0..k-1 (fp32 fused
-// multiply-adds), rounded once to bf16. The expert-output rows were written by other CTAs: read
-// through L2.
-static __device__ __noinline__ void moe_combine_warp(const KParams& p, int tok, int col0, int ncols, int lane) {
-  const int s = tok / p.moe_T;
-  const int t = tok - s * p.moe_T;
+// MoE combine, one warp: `count` units taken first, first + stride, ...; a unit is one token of the
+// shared task list `tasks` at columns [col0, col0 + BN), or, without a list, the (token, N-tile)
+// pair of index idx = token * tiles_n + N-tile. Units go two at a time (half h of the warp holds
+// the k destination rows and gates of unit h, lane 16h + j for slot j), so the 2k expert-output
+// loads of a lane (8 columns each, col0 + 8*lane) are in flight together, and the next pair's rows
+// and gates are loaded while the current pair's outputs are. out_s[t] = sum_j g[s][t][j] *
+// Z[dest[s][t][j]] in slot order j = 0..k-1 (fp32 fused multiply-adds), rounded once to bf16. The
+// expert-output rows were written by other CTAs: read through L2.
+__device__ __forceinline__ void moe_unit(const KParams& p, const int* tasks, long long idx, int col0, int BN, int& tok,
+                                         int& c0) {
+  if (tasks != nullptr) {
+    tok = tasks[idx];
+    c0 = col0;
+  } else {
+    tok = static_cast<int>(idx / p.tiles_n);
+    c0 = static_cast<int>(idx - (long long)tok * p.tiles_n) * BN;
+  }
+}
+
+static __device__ __forceinline__ void moe_combine_units(const KParams& p, const int* tasks, long long first,
+                                                         long long stride, long long count, int col0, int BN,
+                                                         int lane) {
   const int k = p.moe_k;
-  const int c = col0 + 8 * lane;
-  if (8 * lane >= ncols || c >= p.N) return;
+  const int half = lane >> 4;
+  const int slot = lane & 15;
   const uint64_t once = policy_evict_first();
-  const bool full = c + 8 <= p.N;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  // slots in groups of 8: a group's loads are in flight together, the sum keeps slot order
+  // this lane's (destination row, gate) for unit 2q + half
+  auto meta = [&](long long q, int& d, float& g) {
+    d = 0;
+    g = 0.0f;
+    const long long u = 2 * q + half;
+    if (u < count && slot < k) {
+      int tok, c0;
+      moe_unit(p, tasks, first + u * stride, col0, BN, tok, c0);
+      const int s = tok / p.moe_T;
+      d = p.moe_dest[(size_t)tok * k + slot];
+      g = p.moe_gates[s][(size_t)(tok - s * p.moe_T) * k + slot];
+    }
+  };
+  const long long npairs = (count + 1) / 2;
+  int cd;
+  float cg;
+  meta(0, cd, cg);
 #pragma unroll 1
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    uint4 zr[8];
+  for (long long q = 0; q < npairs; ++q) {
+    int nd = 0;
+    float ng = 0.0f;
+    if (q + 1 < npairs) meta(q + 1, nd, ng);
+    int tok[2], c[2];
+    bool live[2], full[2];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = j0 + jj;
-      if (j < k) {
-        const uint8_t* zp = p.G + (size_t)p.moe_dest[(size_t)tok * k + j] * p.N * 2 + (size_t)c * 2;
-        if (full) {
-          zr[jj] = ld_cg_v4_hint(zp, once);
-        } else {
-          uint16_t hv[8];
+    for (int h = 0; h < 2; ++h) {
+      const long long u = 2 * q + h;
+      live[h] = u < count;
+      tok[h] = 0;
+      c[h] = 0;
+      if (live[h]) {
+        int c0;
+        moe_unit(p, tasks, first + u * stride, col0, BN, tok[h], c0);
+        c[h] = c0 + 8 * lane;
+        live[h] = 8 * lane < BN && c[h] < p.N;
+      }
+      full[h] = c[h] + 8 <= p.N;
+    }
+    float acc[2][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) hv[i] = c + i < p.N ? reinterpret_cast<const uint16_t*>(zp)[i] : 0;
-          zr[jj] = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16),
-                              hv[4] | (uint32_t(hv[5]) << 16), hv[6] | (uint32_t(hv[7]) << 16));
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
+    // slots in groups of 8 per unit: a group's loads of both units are in flight together, the sum
+    // keeps slot order
+#pragma unroll 1
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 zr[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const int d = __shfl_sync(0xFFFFFFFFu, cd, 16 * h + (j & 15));
+          zr[h][jj] = make_uint4(0u, 0u, 0u, 0u);
+          if (j < k && live[h]) {
+            const uint8_t* zp = p.G + (size_t)d * p.N * 2 + (size_t)c[h] * 2;
+            if (full[h]) {
+              zr[h][jj] = ld_cg_v4_hint(zp, once);
+            } else {
+              uint16_t hv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hv[i] = c[h] + i < p.N ? reinterpret_cast<const uint16_t*>(zp)[i] : 0;
+              zr[h][jj] = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16),
+                                     hv[4] | (uint32_t(hv[5]) << 16), hv[6] | (uint32_t(hv[7]) << 16));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const float g = __shfl_sync(0xFFFFFFFFu, cg, 16 * h + (j & 15));
+          if (j < k) {
+            float z[8];
+            unpack_bf16x8(zr[h][jj], z);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(g, z[i], acc[h][i]);
+          }
         }
       }
     }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = j0 + jj;
-      if (j < k) {
-        const float g = p.moe_gates[s][(size_t)t * k + j];
-        float z[8];
-        unpack_bf16x8(zr[jj], z);
+    for (int h = 0; h < 2; ++h) {
+      if (!live[h]) continue;
+      const int s = tok[h] / p.moe_T;
+      const int t = tok[h] - s * p.moe_T;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[s] + (size_t)t * p.N * 2) + c[h];
+      if (full[h]) {
+        uint4 pk;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[h][0], acc[h][1]);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[h][2], acc[h][3]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[h][4], acc[h][5]);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[h][6], acc[h][7]);
+        pk.x = *reinterpret_cast<uint32_t*>(&b0);
+        pk.y = *reinterpret_cast<uint32_t*>(&b1);
+        pk.z = *reinterpret_cast<uint32_t*>(&b2);
+        pk.w = *reinterpret_cast<uint32_t*>(&b3);
+        st_v4(o, pk);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, z[i], acc[i]);
+        for (int i = 0; i < 8; ++i)
+          if (c[h] + i < p.N) o[i] = __float2bfloat16_rn(acc[h][i]);
       }
     }
-  }
-  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[s] + (size_t)t * p.N * 2) + c;
-  if (full) {
-    uint4 pk;
-    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
-    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
-    __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
-    pk.x = *reinterpret_cast<uint32_t*>(&b0);
-    pk.y = *reinterpret_cast<uint32_t*>(&b1);
-    pk.z = *reinterpret_cast<uint32_t*>(&b2);
-    pk.w = *reinterpret_cast<uint32_t*>(&b3);
-    st_v4(o, pk);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c + i < p.N) o[i] = __float2bfloat16_rn(acc[i]);
+    cd = nd;
+    cg = ng;
   }
 }
 
@@ -1410,7 +1481,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           const int nt_tasks = *task_n;
           if (nt_tasks > 0) {
             __threadfence();
-            for (int i = e; i < nt_tasks; i += kNumEpiWarps) moe_combine_warp(p, tasks[i], w.n0, BN, lane);
+            if (e < nt_tasks)
+              moe_combine_units(p, tasks, e, kNumEpiWarps, (nt_tasks - e + kNumEpiWarps - 1) / kNumEpiWarps, w.n0, BN,
+                                lane);
           }
         }
       }
@@ -1538,10 +1611,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       if (p.mode == MODE_MOVE_ONLY && !moe_bad) {
         // the combine alone (expert outputs already in place): one (token, N-tile) per warp task
         const long long units = (long long)p.W * p.moe_T * p.tiles_n;
-        for (long long u = (long long)blockIdx.x * kNumEpiWarps + e; u < units; u += (long long)grid * kNumEpiWarps) {
-          const int tok = static_cast<int>(u / p.tiles_n);
-          moe_combine_warp(p, tok, static_cast<int>(u - (long long)tok * p.tiles_n) * BN, BN, lane);
-        }
+        const long long first = (long long)blockIdx.x * kNumEpiWarps + e;
+        const long long stride = (long long)grid * kNumEpiWarps;
+        if (first < units) moe_combine_units(p, nullptr, first, stride, (units - first + stride - 1) / stride, 0, BN, lane);
       }
     }
     if (elected && trace != nullptr) {
