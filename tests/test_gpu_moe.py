@@ -43,6 +43,7 @@ SHAPES = [
     dict(W=1, M=300, K=128, N=256, E=3, topk=1),
     dict(W=4, M=257, K=64, N=64, E=8, topk=2),         # experts with several tiles and a tail
     dict(W=16, M=17, K=64, N=192, E=32, topk=4),
+    dict(W=4, M=33, K=128, N=256, E=16, topk=16),      # the most slots a token may have: every expert
 ]
 
 

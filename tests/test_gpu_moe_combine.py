@@ -39,6 +39,8 @@ SHAPES = [
     dict(W=1, M=300, K=128, N=256, E=3, topk=1),
     dict(W=4, M=257, K=64, N=64, E=8, topk=2),
     dict(W=16, M=17, K=64, N=192, E=32, topk=4),
+    dict(W=2, M=40, K=64, N=136, E=20, topk=12),       # two slot groups, the second partial
+    dict(W=4, M=33, K=128, N=256, E=16, topk=16),      # the most slots a token may have: every expert
 ]
 
 
@@ -133,3 +135,24 @@ def test_combine_empty_and_skewed_experts(case_name):
         tdx.check(case.run())
         status_ok(case)
         assert_bit_exact(case.result_bits().reshape(-1, wl.N), want.reshape(-1, wl.N), "bf16")
+
+
+@pytest.mark.parametrize("topk", [5, 16])
+def test_combine_alone_matches_fused(topk):
+    """The combine alone (expert outputs already in place) walks (token, N-tile) units two at a
+    time across the grid, the fused combine walks each tile's task list: both give the fused bits,
+    also for an odd unit count per warp and for a token's slots in two groups of loads."""
+    wl = wls.with_shape(wls.WORKLOADS["moe_combine_w8"], W=3, M=37, K=64, N=328, E=18, topk=topk)
+    inp = wls.make_inputs(wl, integer=False)
+    for bn in (0, 64):
+        case = CombineCase(inp, opts=opts(block_n=bn))
+        tdx.check(case.run(opts(block_n=bn, epoch=1)))
+        status_ok(case)
+        fused = case.result_bits()
+        assert_within_tol(R.decode_bf16(fused.reshape(-1, wl.N)), oracle_out(inp).reshape(-1, wl.N), "bf16")
+        for o in case.out:
+            o.fill_(float("nan"))
+        tdx.check(case.run(opts(block_n=bn, mode=tdx.TDX_GEMM_ONLY, epoch=2)))
+        tdx.check(case.run(opts(block_n=bn, mode=tdx.TDX_MOVE_ONLY, epoch=3)))
+        status_ok(case)
+        assert np.array_equal(case.result_bits(), fused), f"topk={topk} bn={bn}"
