@@ -53,15 +53,43 @@ FUSED_KERNEL_SOURCES = ["tdx_api.cu", "tdx_internal.h", "tdx_kernel.cuh", "tdx_k
                         "tdx_kernel_fp8.cu", "tdx_ptx.cuh"]
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and whitespace runs collapsed to one space
+    (string and character literals kept as written), so that editing a comment or the layout does
+    not change what identifies the code."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the sources of the fused GEMM kernel and its host launch code (identifies the
-    kernel an ncu capture measured)."""
+    """sha256 over the code (comments and layout excluded) of the fused GEMM kernel and its host
+    launch code: identifies the kernel an ncu capture measured."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "comm_overlapped_gemm_gb300", "csrc")
     for name in FUSED_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()
 
 

@@ -1458,7 +1458,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       if constexpr (OP == OP_MOE_COMBINE) {
         if (p.mode == MODE_FUSED) {
           // count the stored expert-output rows of every token, per N-tile; tokens whose k rows are
-          // now all stored are listed, and the epilogue warps fold them (one token per warp task)
+          // now all stored are listed, and the epilogue warps fold them (two tokens per warp iteration)
           volatile int* task_n = reinterpret_cast<volatile int*>(misc + 6);
           int* tasks = reinterpret_cast<int*>(misc + 16);   // [kBM] tokens to combine
           const int et = threadIdx.x - kEpiWarp0 * 32;

@@ -1,0 +1,50 @@
+"""Host logic of bench.py that needs no GPU: the code hash that ties a committed ncu traffic
+capture to the kernel sources it measured, and the shape of that capture's record."""
+import json
+import os
+import shutil
+
+import bench
+
+
+def test_code_tokens_drops_comments_and_layout():
+    src = "int a = 1;   // note\n/* block\n comment */ float b =\n\t2.0f; // end"
+    assert bench.code_tokens(src) == "int a = 1; float b = 2.0f;"
+
+
+def test_code_tokens_keeps_literals():
+    src = 'asm("mov.u32 %0, 1; // not a comment /* nor this */" : "=r"(x)); char q = \'"\'; char e = \'\\\'\';'
+    out = bench.code_tokens(src)
+    assert '"mov.u32 %0, 1; // not a comment /* nor this */"' in out
+    assert "'\"'" in out and "'\\''" in out
+
+
+def _copy_sources(tmp_path):
+    dst = tmp_path / "comm_overlapped_gemm_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    src = os.path.join(bench.ROOT, "comm_overlapped_gemm_gb300", "csrc")
+    for name in bench.FUSED_KERNEL_SOURCES:
+        shutil.copy(os.path.join(src, name), dst / name)
+    return dst
+
+
+def test_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    dst = _copy_sources(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_source_hash()
+    f = dst / "tdx_kernel.cuh"
+    text = f.read_text()
+    f.write_text(text + "\n// a comment added at the end\n/* and a block */\n")
+    assert bench.kernel_source_hash() == base
+    f.write_text(text + "\nstatic constexpr int kUnused = 1;\n")
+    assert bench.kernel_source_hash() != base
+
+
+def test_traffic_record_is_consistent():
+    path = os.path.join(bench.ROOT, "profiles", "tdx_fused_rs_w8_traffic.json")
+    with open(path) as fh:
+        d = json.load(fh)
+    assert d["dram_bytes_per_launch"] == d["dram_bytes_read"] + d["dram_bytes_written"]
+    assert d["algorithmic_bytes_per_launch"] > 0
+    assert "--clock-control none" in d["command"]
+    assert len(d["kernel_source_sha256"]) == 64
