@@ -2,6 +2,7 @@
 // carving (status word, chunk flags, gathered buffer, running-sum / partial-slot buffer, MoE layout
 // tables and receive buffer), TMA tensor maps and the launches of the persistent fused kernel and
 // of the MoE routing-layout kernel. No arithmetic of the operations happens here.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -249,13 +250,16 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, long long rows, long l
 }
 
 int device_sms() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];   // per device; calls may come from several host threads
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -41,6 +41,7 @@
 // the kernel returns. Nothing traps.
 #pragma once
 
+#include <atomic>
 #include <cuda_bf16.h>
 
 #include "tdx_internal.h"
@@ -1661,16 +1662,17 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   // MoE adds the dispatch staging ring (128-byte aligned) after the GEMM's shared memory
   constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
   static_assert(!uses_staging(OP) || (C::MOE_STG >= 4096 && kSmem <= 227 * 1024), "staging ring budget");
-  // the dynamic shared-memory limit is raised once per device for each instantiation
-  static bool attr_done[64] = {};
+  // the dynamic shared-memory limit is raised once per device for each instantiation (setting it
+  // twice from two host threads is harmless; the flag only saves the call)
+  static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -1704,10 +1706,13 @@ int max_grid_t(int sms) {
   } else {
     using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
     constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
-    static int cache[64] = {};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 64) {
+      const int c = cache[dev].load(std::memory_order_relaxed);
+      if (c > 0) return c;
+    }
     if (cudaFuncSetAttribute(tdx_fused_kernel<BN, FP8, OP, PM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem) != cudaSuccess)
       return 0;
@@ -1725,7 +1730,7 @@ int max_grid_t(int sms) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, tdx_fused_kernel<BN, FP8, OP, PM>, &cfg) != cudaSuccess) return 0;
     const int g = n * CL;
-    if (dev >= 0 && dev < 64) cache[dev] = g;
+    if (dev >= 0 && dev < 64) cache[dev].store(g, std::memory_order_relaxed);
     return g;
   }
 }

@@ -173,14 +173,14 @@ size_t layout_smem_bytes(int W, int E) { return static_cast<size_t>(W * E + 32 *
 cudaError_t launch_moe_layout(const MoeLayoutParams& q, cudaStream_t stream) {
   if (q.W < 1 || q.W > kMaxW || q.E < 1 || q.E > kMoeMaxExperts) return cudaErrorInvalidValue;
   const size_t smem = layout_smem_bytes(q.W, q.E);
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];   // per device; calls may come from several host threads
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (!(dev >= 0 && dev < 64 && attr_done[dev])) {
+  if (!(dev >= 0 && dev < 64 && attr_done[dev].load(std::memory_order_relaxed))) {
     const cudaError_t e = cudaFuncSetAttribute(tdx_moe_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(layout_smem_bytes(kMaxW, kMoeMaxExperts)));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
   }
   tdx_moe_layout_kernel<<<q.W, kLayoutThreads, smem, stream>>>(q);
   return cudaGetLastError();
