@@ -185,6 +185,38 @@ def test_bf16_partials_plan(tdx):
         tdx.tdx_workspace_size(tdx.OP_AG, 2, 64, 128, 256, tdx.TDX_BF16, tdx.make_opts(bf16_partials=1))
 
 
+PLANS = [
+    # (name, op, W, M_local or M, K, N, chunk_rows, expected plan words)
+    ("AG W=8", "OP_AG", 8, 1024, 8192, 3584, 0,
+     dict(BN=256, L=1, cluster=3, tiles_m=64, tiles_n=14, n_chunks=8, chunk_rows=128, pull_a=0)),
+    ("RS W=8", "OP_RS", 8, 8192, 3584, 8192, 0,
+     dict(BN=256, L=8, cluster=3, reduce_mode=1, group_n=16, tiles_m=64, tiles_n=32, coop_fold=0)),
+    ("small-M AG", "OP_AG", 8, 16, 8192, 1024, 16,
+     dict(BN=128, L=16, cluster=1, reduce_mode=2, pull_a=1, coop_fold=1, T=8, n_chunks=1)),
+    ("small-M RS", "OP_RS", 8, 128, 1024, 8192, 0,
+     dict(BN=256, L=8, cluster=1, reduce_mode=2, coop_fold=0, T=32)),
+    ("RS, 8 M-tiles", "OP_RS", 8, 1024, 1024, 8192, 0,
+     dict(BN=128, L=8, cluster=1, reduce_mode=1, T=512)),
+    ("AG, N=64, 2-row shards", "OP_AG", 8, 2, 8192, 64, 0,
+     dict(BN=64, L=16, cluster=1, reduce_mode=2, pull_a=0)),
+    ("tiny AG", "OP_AG", 2, 64, 128, 256, 32,
+     dict(BN=128, L=2, cluster=1, reduce_mode=2, pull_a=1, n_chunks=2)),
+]
+
+
+@pytest.mark.parametrize("case", PLANS, ids=[c[0] for c in PLANS])
+def test_planner_choices_for_the_workloads(tdx, case):
+    """Tile width, K splits, CTA cooperation and reduction chosen for the measured workloads and a
+    few neighbours (a 152-SM device): 2-SM pairs with a chained running sum for the large RS,
+    128-wide tiles over 16 K splits that read the shards in place and fold cooperatively for the
+    small-M AllGather, 256-wide tiles with a last-arriver fold for the small-M ReduceScatter."""
+    _, op, W, M, K, N, cr, want = case
+    p = tdx.tdx_plan_info(getattr(tdx, op), W, M, K, N, tdx.TDX_BF16, tdx.make_opts(chunk_rows=cr, num_sms=152))
+    got = {k: p[k] for k in want}
+    assert got == want
+    assert p["T"] == p["tiles_m"] * p["tiles_n"]
+
+
 def test_trace_size(tdx):
     assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 4 * 3)
     assert tdx.tdx_trace_size(0, 10) == 0
