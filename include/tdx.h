@@ -71,8 +71,10 @@ typedef struct tdx_opts {
   int self_rank;             /* AG: rank whose shard is local; arrival order self, self+1, ... (default 0) */
   int chunk_rows;            /* AG: rows per chunk and per flag; must divide M_local (default min(128, M_local)) */
   tdx_dtype out_dtype;       /* AG: TDX_BF16 (default) or TDX_FP32. RS: TDX_BF16 only */
-  const float* scale_a;      /* host array [W]: per-shard (AG) / per-A_r (RS) e4m3 dequantisation scales (NULL = 1) */
-  const float* scale_b;      /* host array: AG [1] B's scale; RS [W] the B_r scales; e4m3 only (NULL = 1) */
+  const float* scale_a;      /* host array [W]: per-shard (AG) / per-A_r (RS) / per source rank (MoE)
+                                e4m3 dequantisation scales (NULL = 1) */
+  const float* scale_b;      /* host array: AG [1] B's scale; RS [W] the B_r scales; MoE [E] the
+                                experts' scales; e4m3 only (NULL = 1) */
   tdx_mode mode;             /* default TDX_FUSED */
   tdx_producer producer;     /* default TDX_PRODUCER_SM */
   uint32_t epoch;            /* 0: the library clears the flags on `stream` and uses epoch 1.
@@ -205,28 +207,33 @@ tdx_status tdx_gemm_ar(const void* const* A_parts, const void* const* B_parts, v
  * a mixture-of-experts model are known only at run time, so its device-level tiles are sized
  * dynamically.)
  *
- * W ranks; rank s holds T tokens X[s] (T x H bf16 row-major) and their routing topk_idx[s]
+ * W ranks; rank s holds T tokens X[s] (T x H of `dtype`, row-major) and their routing topk_idx[s]
  * (T x topk int32 expert ids in [0, E)). Rank rho owns experts rho*E/W .. (rho+1)*E/W - 1. The
  * dispatch sends every (s, t, j) row X[s][t] to expert topk_idx[s][t][j]; the receive side (one
  * buffer for all ranks, in the workspace) groups the W*T*topk rows by expert, experts ascending,
  * and inside an expert by source rank then token, ascending. Expert e's rows are multiplied by its
  * weights B_experts[e] (H x F); Y keeps the dispatched row order:
- *   Y[dest[s][t][j]] = round_bf16(X[s][t] @ B_experts[topk_idx[s][t][j]]).
+ *   Y[dest[s][t][j]] = round_bf16(X[s][t] @ B_experts[topk_idx[s][t][j]]),
+ * for e4m3 inputs multiplied first by scale_a[s] * scale_b[e] (fp32, in the epilogue).
  * The layout (counts, offsets, row of every pair, GEMM tile table) is computed on the device; the
  * dispatch copies the receive buffer in 128-row chunks, each released by a flag, while the GEMM
  * tiles of the experts whose rows have arrived already run.
- *  X              host array of W device pointers, each T x H bf16 (16-byte aligned).
+ *  X              host array of W device pointers, each T x H of `dtype` (16-byte aligned).
  *  topk_idx       host array of W device pointers, each T x topk int32. Ids outside [0, E) make the
  *                 call do nothing further and record TDX_ERR_INVALID_ARG in the device status.
- *  B_experts      device pointer, E x H x F bf16 (expert e's weights at e*H*F).
- *  Y              device pointer, (W*T*topk) x F bf16, the dispatched order.
+ *  B_experts      device pointer, E x H x F of `dtype` (expert e's weights at e*H*F).
+ *  Y              device pointer, (W*T*topk) x F bf16 (for either input type), the dispatched order.
  *  dest           device pointer, W x T x topk int32 (output): the row of Y of every (s, t, j).
  *  expert_offsets optional device pointer, E + 1 int32 (output): expert e's rows are
  *                 [expert_offsets[e], expert_offsets[e+1]).
  *  workspace      caller-owned device memory of tdx_moe_workspace_size() bytes, 256-byte aligned,
  *                 zeroed once by tdx_workspace_init; it holds the status word, chunk flags, the
- *                 layout tables and the receive buffer ((W*T*topk) x H bf16).
- *  H, F multiples of 8; 1 <= topk <= E <= 512; W <= 16; bf16 only (e4m3: TDX_ERR_UNSUPPORTED).
+ *                 layout tables and the receive buffer ((W*T*topk) x H of `dtype`).
+ *  dtype          TDX_BF16, or TDX_FP8_E4M3 with per-tensor scales: opts->scale_a host array [W]
+ *                 (one per source rank's tokens), opts->scale_b host array [E] (one per expert's
+ *                 weights); NULL = 1. e4m3 needs tile width 128 or 256.
+ *  H and F rows of 16-byte multiples (bf16: multiples of 8; e4m3: H and F multiples of 16);
+ *  1 <= topk <= E <= 512; W <= 16.
  *  opts: epoch, timeout_ns, perturb_seed, trace, num_sms, block_n and mode (TDX_FUSED, TDX_GEMM_ONLY:
  *  the receive buffer is assumed filled by an earlier call with the same routing, TDX_MOVE_ONLY:
  *  dispatch only) apply; other cooperation options must keep their defaults. */
@@ -295,13 +302,15 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
 
 /* Introspection for tests and tools: the tiling and workspace layout a call with these arguments
  * uses. Writes 22 words to info: [0] tile width BN, [1] chain length L (RS: W; AG: K splits),
- * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] K blocks (64 bytes of K for BN = 256, else 128), [6] chunk rows, [7] chunks per rank,
+ * [2] M-tiles, [3] N-tiles, [4] tiles T, [5] K blocks (128 bytes of K each, one ring slot),
+ * [6] chunk rows, [7] chunks per rank,
  * byte offsets in the workspace of [8] chunk flags (uint32 [W * chunks], index rank*chunks + c),
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
  * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters,
- * [16] CTA cooperation in use (1 single, 2 multicast pair, 3 2-SM pair), [17] ReduceScatter raster: N-tiles per group (within a rank the
- * tiles are taken group by group, M-tiles, then the group's N-tiles), [18] ReduceScatter rank block:
+ * [16] CTA cooperation in use (1 single, 2 multicast pair, 3 2-SM pair), [17] ReduceScatter
+ * raster: N-tiles per group (within a rank the tiles are taken group by group, M-tiles, then the
+ * group's N-tiles), [18] ReduceScatter rank block:
  * that many positions of a rank's tile order are processed for ranks 0..W-1 before the next block
  * (positions count tiles, or tile pairs when [16] >= 2), [19] 1 if AllGather tiles read A straight
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
