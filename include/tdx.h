@@ -1,5 +1,7 @@
 /*
- * tdx.h -- C ABI of the tile-pipelined AllGather+GEMM and GEMM+ReduceScatter library (sm_103a).
+ * tdx.h -- C ABI of the tile-pipelined collective+GEMM library (sm_103a): AllGather+GEMM,
+ * GEMM+ReduceScatter, GEMM+AllReduce and the mixture-of-experts AllToAll dispatch + grouped GEMM
+ * and grouped GEMM + combine.
  *
  * What the operations are. The Triton-distributed article on cronfeed.work ("Triton-distributed
  * is turning communication into compiler territory"), section "The first move was to expose the
@@ -8,11 +10,12 @@
  * operation GEMM-plus-ReduceScatter; communication and computation thread blocks of one kernel
  * are coordinated through symmetric memory and signals. Section "DITRON adds three levels of
  * tiling" adds that collectives such as AllGather and ReduceScatter are broken into chunks, paired
- * with compute tiles, and synchronised. This library implements those two kernels for one GPU:
- * the W ranks are logical, i.e. W shard buffers (and, for ReduceScatter, W partial products) in
- * one device's memory; the "network" is a chunk producer that copies shard chunks into a
- * symmetric gathered buffer and releases one flag per chunk, and the GEMM tiles acquire those
- * flags before they read a chunk.
+ * with compute tiles, and synchronised (AllToAll and AllReduce among them; the AllToAll entry
+ * points are further down). This library implements these kernels for one GPU: the W ranks are
+ * logical, i.e. W shard buffers (W partial products for ReduceScatter / AllReduce, W token sets
+ * for the AllToAll) in one device's memory; the "network" is a chunk producer that copies shard
+ * chunks into a symmetric gathered buffer and releases one flag per chunk, and the GEMM tiles
+ * acquire those flags before they read a chunk.
  *
  * Conventions for every entry point:
  *  - Ownership: every tensor and the workspace are device memory owned by the caller. The library
