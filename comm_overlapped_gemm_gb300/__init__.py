@@ -1,4 +1,6 @@
-"""Python binding of libtdx (tile-pipelined AllGather+GEMM and GEMM+ReduceScatter on sm_103a).
+"""Python binding of libtdx (tile-pipelined collective+GEMM kernels on sm_103a: AllGather+GEMM,
+GEMM+ReduceScatter, GEMM+AllReduce, mixture-of-experts AllToAll dispatch + grouped GEMM and grouped
+GEMM + combine).
 
 Argument marshalling only: every function below converts its arguments (torch tensors or raw
 device pointers) into the plain pointers and sizes of the C ABI in ``include/tdx.h`` and calls the
