@@ -48,3 +48,26 @@ def test_traffic_record_is_consistent():
     assert d["algorithmic_bytes_per_launch"] > 0
     assert "--clock-control none" in d["command"]
     assert len(d["kernel_source_sha256"]) == 64
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the CPU oracle on a bounded sample of the same workload and
+    prints one JSON line with the main arm's metric, unit and direction, a `cpu_baseline` that
+    describes the run and a zero-copy `e2e`."""
+    import subprocess
+    import sys
+    res = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                         cwd=bench.ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == bench.WORKLOAD
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
