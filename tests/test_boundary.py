@@ -46,6 +46,28 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/tdx.h compiles as C99 on its own (no C++, CUDA or torch types in the ABI), and a C
+    program that calls every entry point links against the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_tdx.c"
+    calls = "\n".join(f"  (void)&{n};" for n in declared_functions())
+    src.write_text('#include "tdx.h"\nint main(void) {\n' + calls + "\n  return 0;\n}\n")
+    inc = os.path.join(ROOT, "include")
+    res = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", inc, "-c", str(src),
+                          "-o", str(tmp_path / "use_tdx.o")], capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    lib = _load_build_module().LIB
+    if os.path.exists(lib):
+        res = subprocess.run([cc, str(tmp_path / "use_tdx.o"), lib, "-o", str(tmp_path / "use_tdx")],
+                             capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
+
+
 def test_library_exports_every_declared_symbol(tdx):
     lib = ctypes.CDLL(tdx.LIB_PATH)
     for name in declared_functions():
