@@ -191,7 +191,9 @@ def test_combine_with_identity_experts_sums_gates():
         assert np.array_equal(out[s], want)
 
 
-def test_combine_brute_force_and_z_rounding():
+def check_combine_brute(combine):
+    """``combine(h, topk, b, gates, E, z_dtype)`` against exact rational arithmetic on a tiny case,
+    with the expert outputs entering exactly (fp32 reading) or rounded once to bf16 first."""
     rng = np.random.default_rng(12)
     W, T, E, k, F, H = 2, 3, 3, 2, 4, 3
     topk = random_routing(rng, W, T, E, k)
@@ -199,7 +201,7 @@ def test_combine_brute_force_and_z_rounding():
     b = np.stack([rand_bf16_bits(rng, (F, H), False) for _ in range(E)])
     gates = [rng.uniform(0, 1, size=(T, k)).astype(np.float32) for _ in range(W)]
     _, offsets, dest, _ = MO.moe_layout(topk, E)
-    outs = {z: MO.moe_gemm_combine(h, topk, b, gates, E, z_dtype=z) for z in ("fp32", "bf16")}
+    outs = {z: combine(h, topk, b, gates, E, z) for z in ("fp32", "bf16")}
     for s in range(W):
         for t in range(T):
             for n in range(H):
@@ -216,6 +218,10 @@ def test_combine_brute_force_and_z_rounding():
                     exact_rz += g * zr
                 assert abs(Fraction(outs["fp32"][s][t, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 48) + Fraction(1, 2 ** 60)
                 assert abs(Fraction(outs["bf16"][s][t, n]) - exact_rz) <= abs(exact_rz) * Fraction(1, 2 ** 48) + Fraction(1, 2 ** 60)
+
+
+def test_combine_brute_force_and_z_rounding():
+    check_combine_brute(lambda h, topk, b, gates, E, z: MO.moe_gemm_combine(h, topk, b, gates, E, z_dtype=z))
 
 
 # ------------------------------------------------------------------ planted mistakes
@@ -253,6 +259,36 @@ def test_planted_dispatch_mistakes_are_caught(mut, golden):
     except AssertionError:
         caught += 1
     assert caught > 0
+
+
+def _cmut_rotated_gates(h, topk, b, gates, E, z):
+    # slot j weighted by the gate of slot j+1
+    return MO.moe_gemm_combine(h, topk, b, [np.roll(g, -1, axis=1) for g in gates], E, z_dtype=z)
+
+
+def _cmut_unrounded_z(h, topk, b, gates, E, z):
+    # expert outputs never rounded to bf16
+    return MO.moe_gemm_combine(h, topk, b, gates, E, z_dtype="fp32")
+
+
+def _cmut_wrong_experts(h, topk, b, gates, E, z):
+    return MO.moe_gemm_combine(h, topk, b[::-1].copy(), gates, E, z_dtype=z)
+
+
+def _cmut_first_slot_row(h, topk, b, gates, E, z):
+    # every slot reads the expert output of slot 0
+    _, _, dest, _ = MO.moe_layout(topk, E)
+    Z = MO.moe_grouped_gemm(h, topk, b, E)
+    if z == "bf16":
+        Z = R.decode_bf16(R.round_bf16_rne(Z))
+    bad = [np.repeat(d[:, :1], d.shape[1], axis=1) for d in dest]
+    return MO.moe_combine(Z, bad, gates)
+
+
+@pytest.mark.parametrize("mut", [_cmut_rotated_gates, _cmut_unrounded_z, _cmut_wrong_experts, _cmut_first_slot_row])
+def test_planted_combine_mistakes_are_caught(mut):
+    with pytest.raises(AssertionError):
+        check_combine_brute(mut)
 
 
 def test_grouped_gemm_rows_and_combine_rows_match_full():
