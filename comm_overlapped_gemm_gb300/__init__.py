@@ -73,7 +73,7 @@ def _load():
         "tdx_gemm_rs": (I, [PP, PP, PP, P, SZ, I, I, I, I, I, OP, P]),
         "tdx_gemm_ar": (I, [PP, PP, PP, P, SZ, I, I, I, I, I, OP, P]),
         "tdx_read_device_status": (I, [P, P, ctypes.POINTER(I), ctypes.POINTER(U32)]),
-        "tdx_trace_size": (SZ, [I, I]),
+        "tdx_trace_size": (SZ, [I, I, I]),
         "tdx_status_string": (ctypes.c_char_p, [I]),
         "tdx_version": (U32, []),
         "tdx_plan_info": (I, [I, I, I, I, I, I, OP, ctypes.POINTER(ctypes.c_int64)]),
@@ -164,8 +164,8 @@ def tdx_version() -> int:
     return int(_lib.tdx_version())
 
 
-def tdx_trace_size(grid: int, items: int) -> int:
-    return int(_lib.tdx_trace_size(grid, items))
+def tdx_trace_size(grid: int, items: int, chunks: int = 0) -> int:
+    return int(_lib.tdx_trace_size(grid, items, chunks))
 
 
 def tdx_workspace_size(op: int, W: int, M_local_or_M: int, K: int, N: int, dtype: int, opts=None) -> int:

@@ -56,7 +56,7 @@ struct Plan {
   int chunk_rows = 0, n_chunks = 0;
   int reduce_last = 0;
   int CL = 1;            // CTAs per cluster (1 or 2)
-  int PM = 0;            // pair mode: 0 single, 1 B multicast, 2 two-SM MMA
+  int PM = 0;            // pair mode: 0 single CTAs, 2 two-SM MMA pairs
   int group_n = 1;
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
   int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
@@ -136,13 +136,15 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.tiles_n = (N + bn - 1) / bn;
   p.T = p.tiles_m * p.tiles_n;
   p.group_n = op == OP_RS ? (p.tiles_n < kRsGroupN ? (p.tiles_n > 0 ? p.tiles_n : 1) : kRsGroupN) : p.tiles_n;
-  // CTA pairs on vertically adjacent 128 x 256 tiles: large problems with 256-wide tiles and an
-  // even M-tile count; by default the 2-SM MMA pair (mode 3), else on request the multicast pair (2)
+  // CTA pairs on vertically adjacent 128 x 256 tiles running one 2-SM MMA stream (cooperation mode
+  // 3): large problems with 256-wide tiles and an even M-tile count. Mode 2 (pairs sharing B through
+  // multicast loads) is not offered: every CTA loads only into its own shared memory.
   if (o.cluster < 0 || o.cluster > 3) return TDX_ERR_INVALID_ARG;
+  if (o.cluster == 2) return TDX_ERR_UNSUPPORTED;
   const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
-  if (o.cluster >= 2) {
-    if (!pair_ok || (op == OP_RS && fp8 && o.cluster == 2)) return TDX_ERR_UNSUPPORTED;
-    p.PM = o.cluster - 1;
+  if (o.cluster == 3) {
+    if (!pair_ok) return TDX_ERR_UNSUPPORTED;
+    p.PM = 2;
   } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs) {
     p.PM = 2;
   }
@@ -320,6 +322,94 @@ int grid_for(const tdx_opts& o, const Plan& pl, bool fp8, int items_or_zero) {
   return g;
 }
 
+// Every host-side check of an AllGather+GEMM call that does not involve the workspace (arguments,
+// options, tiling, alignment); fills the plan. Launches nothing.
+tdx_status ag_check(const void* const* shards, const void* B, const void* C, int W, int M_local, int K, int N,
+                    tdx_dtype dtype, const tdx_opts& o, Plan* pl) {
+  if (shards == nullptr || B == nullptr || C == nullptr) return TDX_ERR_INVALID_ARG;
+  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
+  for (int r = 0; r < W; ++r)
+    if (shards[r] == nullptr) return TDX_ERR_INVALID_ARG;
+  if (o.self_rank < 0 || o.self_rank >= W) return TDX_ERR_INVALID_ARG;
+  if (o.out_dtype != TDX_BF16 && o.out_dtype != TDX_FP32) return TDX_ERR_INVALID_ARG;
+  if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
+  if (o.producer != TDX_PRODUCER_SM && o.producer != TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_INVALID_ARG;
+  // The copy-engine producer is not offered: the consumer kernel would wait on copies issued
+  // outside it, which need not run while the kernel holds every SM.
+  if (o.producer == TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_UNSUPPORTED;
+  tdx_status s = make_plan(OP_AG, W, M_local, K, N, dtype, o, pl);
+  if (s != TDX_OK) return s;
+  const int out_elt = o.out_dtype == TDX_FP32 ? 4 : 2;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(shards[r])) return TDX_ERR_ALIGNMENT;
+  if (!aligned16(B) || !aligned16(C)) return TDX_ERR_ALIGNMENT;
+  if ((static_cast<long long>(K) * pl->elt) % 16 != 0 || (static_cast<long long>(N) * pl->elt) % 16 != 0 ||
+      (static_cast<long long>(N) * out_elt) % 16 != 0)
+    return TDX_ERR_ALIGNMENT;
+  return TDX_OK;
+}
+
+// The launches of a checked AllGather+GEMM call on a workspace of at least pl.total bytes.
+tdx_status ag_run(const void* const* shards, const void* B, void* C, uint8_t* ws, const Plan& pl, const tdx_opts& o,
+                  cudaStream_t st) {
+  const int W = pl.W, M_local = pl.M_local, K = pl.K;
+  const bool fp8 = pl.elt == 1;
+  const int out_elt = o.out_dtype == TDX_FP32 ? 4 : 2;
+  if (M_local == 0 || pl.N == 0) return TDX_OK;
+  if (K == 0) return fill_zero(C, static_cast<size_t>(pl.M) * pl.N * out_elt, st);
+  static thread_local KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(kp, pl, o, ws);
+  kp.op = OP_AG;
+  kp.self_rank = o.self_rank;
+  kp.chunk_rows = pl.chunk_rows;
+  kp.n_chunks = pl.n_chunks;
+  kp.out_fp32 = o.out_dtype == TDX_FP32;
+  kp.G = ws + pl.off_G;
+  kp.out[0] = static_cast<uint8_t*>(C);
+  for (int r = 0; r < W; ++r) {
+    kp.shard[r] = static_cast<const uint8_t*>(shards[r]);
+    const float sa = (fp8 && o.scale_a) ? o.scale_a[r] : 1.0f;
+    const float sb = (fp8 && o.scale_b) ? o.scale_b[0] : 1.0f;
+    kp.row_scale[r] = sa * sb;
+  }
+  kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
+  kp.trace_chunks = W * pl.n_chunks;
+  const int grid = grid_for(o, pl, fp8, 0);
+  if (grid <= 0) return TDX_ERR_CUDA;
+  // producer copy unit: about one piece per CTA, a multiple of 16 KiB, at most 64 KiB per release
+  {
+    const long long total = static_cast<long long>(W) * pl.n_chunks * kp.chunk_bytes;
+    long long pb = (total / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;
+    if (pb < kCopyRoundBytes) pb = kCopyRoundBytes;
+    if (pb > kMaxPieceBytes) pb = kMaxPieceBytes;
+    kp.piece_bytes = static_cast<int>(pb);
+  }
+  kp.ppc = static_cast<int>((kp.chunk_bytes + kp.piece_bytes - 1) / kp.piece_bytes);
+  kp.total_pieces = W * pl.n_chunks * kp.ppc;
+  const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
+  kp.copy_active = moving ? 1 : 0;
+  kp.pull_a = pl.pull_a;
+  kp.wait_flags = (!pl.pull_a && (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY)) ? 1 : 0;
+  // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
+  const int ks = k_slice_bytes(pl.BN);
+  const int a_box = ks / pl.elt, b_box_n = 128 / pl.elt, b_box_k = ks / pl.elt;
+  if (pl.pull_a) {
+    // one map per shard, a box of the whole shard's M_local rows
+    for (int r = 0; r < W; ++r)
+      if (!make_map(&kp.tm_a[r], shards[r], fp8, M_local, K, a_box, M_local, ks)) return TDX_ERR_CUDA;
+  } else if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, a_box, kBM, ks) ||
+             !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, a_box, kBM, ks)) {
+    return TDX_ERR_CUDA;
+  }
+  if (!make_map(&kp.tm_b[0], B, fp8, K, pl.N, b_box_n, b_box_k)) return TDX_ERR_CUDA;
+  if (o.epoch == 0) {
+    const tdx_status s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
+    if (s != TDX_OK) return s;
+  }
+  return launch(pl, kp, fp8, grid, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -349,85 +439,12 @@ tdx_status tdx_workspace_init(void* workspace, size_t bytes, void* stream) {
 tdx_status tdx_ag_gemm(const void* const* shards, const void* B, void* C, void* workspace, size_t workspace_bytes,
                        int W, int M_local, int K, int N, tdx_dtype dtype, const tdx_opts* opts, void* stream) {
   const tdx_opts o = opts ? *opts : defaults();
-  if (shards == nullptr || B == nullptr || C == nullptr) return TDX_ERR_INVALID_ARG;
-  if (W < 1 || W > kMaxW) return TDX_ERR_INVALID_ARG;
-  for (int r = 0; r < W; ++r)
-    if (shards[r] == nullptr) return TDX_ERR_INVALID_ARG;
-  if (o.self_rank < 0 || o.self_rank >= W) return TDX_ERR_INVALID_ARG;
-  if (o.out_dtype != TDX_BF16 && o.out_dtype != TDX_FP32) return TDX_ERR_INVALID_ARG;
-  if (o.mode < TDX_FUSED || o.mode > TDX_CONSUMER_ONLY) return TDX_ERR_INVALID_ARG;
-  if (o.producer != TDX_PRODUCER_SM && o.producer != TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_INVALID_ARG;
-  // The copy-engine producer is not offered: the consumer kernel would wait on copies issued
-  // outside it, which need not run while the kernel holds every SM.
-  if (o.producer == TDX_PRODUCER_COPY_ENGINE) return TDX_ERR_UNSUPPORTED;
   Plan pl;
-  tdx_status s = make_plan(OP_AG, W, M_local, K, N, dtype, o, &pl);
+  tdx_status s = ag_check(shards, B, C, W, M_local, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  const bool fp8 = dtype == TDX_FP8_E4M3;
-  const int out_elt = o.out_dtype == TDX_FP32 ? 4 : 2;
-  for (int r = 0; r < W; ++r)
-    if (!aligned16(shards[r])) return TDX_ERR_ALIGNMENT;
-  if (!aligned16(B) || !aligned16(C)) return TDX_ERR_ALIGNMENT;
-  if ((static_cast<long long>(K) * pl.elt) % 16 != 0 || (static_cast<long long>(N) * pl.elt) % 16 != 0 ||
-      (static_cast<long long>(N) * out_elt) % 16 != 0)
-    return TDX_ERR_ALIGNMENT;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < pl.total)
     return TDX_ERR_WORKSPACE;
-  if (M_local == 0 || N == 0) return TDX_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0) return fill_zero(C, static_cast<size_t>(pl.M) * N * out_elt, st);
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  static thread_local KParams kp;
-  std::memset(&kp, 0, sizeof(kp));
-  fill_common(kp, pl, o, ws);
-  kp.op = OP_AG;
-  kp.self_rank = o.self_rank;
-  kp.chunk_rows = pl.chunk_rows;
-  kp.n_chunks = pl.n_chunks;
-  kp.out_fp32 = o.out_dtype == TDX_FP32;
-  kp.G = ws + pl.off_G;
-  kp.out[0] = static_cast<uint8_t*>(C);
-  for (int r = 0; r < W; ++r) {
-    kp.shard[r] = static_cast<const uint8_t*>(shards[r]);
-    const float sa = (fp8 && o.scale_a) ? o.scale_a[r] : 1.0f;
-    const float sb = (fp8 && o.scale_b) ? o.scale_b[0] : 1.0f;
-    kp.row_scale[r] = sa * sb;
-  }
-  kp.chunk_bytes = static_cast<long long>(pl.chunk_rows) * kp.row_bytes;
-  const int grid = grid_for(o, pl, fp8, 0);
-  if (grid <= 0) return TDX_ERR_CUDA;
-  // producer copy unit: about one piece per CTA, a multiple of 16 KiB, at most 64 KiB per release
-  {
-    const long long total = static_cast<long long>(W) * pl.n_chunks * kp.chunk_bytes;
-    long long pb = (total / grid + kCopyRoundBytes - 1) / kCopyRoundBytes * kCopyRoundBytes;
-    if (pb < kCopyRoundBytes) pb = kCopyRoundBytes;
-    if (pb > kMaxPieceBytes) pb = kMaxPieceBytes;
-    kp.piece_bytes = static_cast<int>(pb);
-  }
-  kp.ppc = static_cast<int>((kp.chunk_bytes + kp.piece_bytes - 1) / kp.piece_bytes);
-  kp.total_pieces = W * pl.n_chunks * kp.ppc;
-  const bool moving = o.mode == TDX_FUSED || o.mode == TDX_MOVE_ONLY;
-  kp.copy_active = moving ? 1 : 0;
-  kp.pull_a = pl.pull_a;
-  kp.wait_flags = (!pl.pull_a && (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY)) ? 1 : 0;
-  // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
-  const int ks = k_slice_bytes(pl.BN);
-  const int a_box = ks / pl.elt, b_box_n = 128 / pl.elt, b_box_k = ks / pl.elt;
-  if (pl.pull_a) {
-    // one map per shard, a box of the whole shard's M_local rows
-    for (int r = 0; r < W; ++r)
-      if (!make_map(&kp.tm_a[r], shards[r], fp8, M_local, K, a_box, M_local, ks)) return TDX_ERR_CUDA;
-  } else if (!make_map(&kp.tm_a[0], kp.G, fp8, pl.M, K, a_box, kBM, ks) ||
-             !make_map(&kp.tm_a[1], shards[o.self_rank], fp8, M_local, K, a_box, kBM, ks)) {
-    return TDX_ERR_CUDA;
-  }
-  if (!make_map(&kp.tm_b[0], B, fp8, K, N, b_box_n, b_box_k)) return TDX_ERR_CUDA;
-  if (o.epoch == 0) {
-    s = fill_zero(ws + pl.off_chunk_flags, pl.ctrl_end - pl.off_chunk_flags, st);
-    if (s != TDX_OK) return s;
-  }
-  return launch(pl, kp, fp8, grid, st);
+  return ag_run(shards, B, C, static_cast<uint8_t*>(workspace), pl, o, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -540,8 +557,10 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
 // ------------------------------------------------------------------------------------------------
 // Allocation-free AllGather+GEMM: the workspace is this file-scope device array, shared by every
 // call on a device. Host code never dereferences or passes the symbol itself (on the host it is
-// only a stand-in); the device address is looked up with cudaGetSymbolAddress, once per device,
-// with that device current, and cached.
+// only a stand-in); its device address is looked up with cudaGetSymbolAddress, with the device
+// current, at the first call on that device and cached together with the unique ID of the CUDA
+// context it belongs to. A call made in another context (the device's context was re-created, for
+// example after cudaDeviceReset) looks the address up again, so a stale address is never used.
 static __device__ __align__(256) uint8_t g_tdx_noalloc_scratch[TDX_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -549,15 +568,46 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique ID of the calling thread's current CUDA context (IDs are never reused within a process).
+tdx_status current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_cur == nullptr || get_id == nullptr) return TDX_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return TDX_ERR_CUDA;
+  return get_id(ctx, id) == CUDA_SUCCESS ? TDX_OK : TDX_ERR_CUDA;
+}
 
 tdx_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TDX_ERR_CUDA;
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx) == TDX_OK;   // false before the runtime made one current
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (!have_ctx || g_noalloc_ptr[dev] == nullptr || g_noalloc_ctx[dev] != ctx) {
+    // set-up: the lookup also makes the device's primary context current if none was
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_tdx_noalloc_scratch) != cudaSuccess || p == nullptr) return TDX_ERR_CUDA;
+    if (current_context_id(&ctx) != TDX_OK) return TDX_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return TDX_OK;
@@ -573,13 +623,14 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
   tdx_opts o = opts ? *opts : defaults();
   o.epoch = 0;   // the shared scratch is cleared by every call
   if (o.producer != TDX_PRODUCER_SM) return TDX_ERR_UNSUPPORTED;
-  size_t need = 0;
-  tdx_status s = tdx_workspace_size(OP_AG, W, M_local, K, N, dtype, &o, &need);
+  // every check comes before the first launch: a rejected call enqueues nothing on the shared array
+  Plan pl;
+  tdx_status s = ag_check(shards, B, C, W, M_local, K, N, dtype, o, &pl);
   if (s != TDX_OK) return s;
-  if (need > TDX_NOALLOC_SCRATCH_BYTES) {
+  if (pl.total > TDX_NOALLOC_SCRATCH_BYTES) {
     if (std::getenv("TDX_VERBOSE"))
       std::fprintf(stderr, "tdx_ag_gemm_noalloc: problem needs %zu bytes of scratch, the built-in scratch holds %u\n",
-                   need, TDX_NOALLOC_SCRATCH_BYTES);
+                   pl.total, TDX_NOALLOC_SCRATCH_BYTES);
     return TDX_ERR_WORKSPACE;
   }
   if (device_status != nullptr && !aligned16(device_status)) return TDX_ERR_ALIGNMENT;
@@ -590,7 +641,7 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
   // status word and details start at zero for this call (flags are cleared by the epoch-0 path)
   s = fill_zero(scratch, kStatusWords * sizeof(uint32_t), st);
   if (s != TDX_OK) return s;
-  s = tdx_ag_gemm(shards, B, C, scratch, TDX_NOALLOC_SCRATCH_BYTES, W, M_local, K, N, dtype, &o, stream);
+  s = ag_run(shards, B, C, static_cast<uint8_t*>(scratch), pl, o, st);
   if (s != TDX_OK) return s;
   if (device_status != nullptr &&
       cudaMemcpyAsync(device_status, scratch, kStatusWords * sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) !=
@@ -599,10 +650,11 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
   return TDX_OK;
 }
 
-size_t tdx_trace_size(int grid, int items) {
-  if (grid <= 0 || items < 0) return 0;
+size_t tdx_trace_size(int grid, int items, int chunks) {
+  if (grid <= 0 || items < 0 || chunks < 0) return 0;
   const size_t per_cta = (static_cast<size_t>(items) + grid - 1) / grid;
-  return 4 * (4 + 4 * static_cast<size_t>(grid) + static_cast<size_t>(grid) * per_cta);
+  return 4 * (4 + 4 * static_cast<size_t>(grid) + 1 + static_cast<size_t>(chunks) +
+              static_cast<size_t>(grid) * per_cta);
 }
 
 const char* tdx_status_string(tdx_status s) {
@@ -970,6 +1022,7 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   kp.row_bytes = static_cast<long long>(H) * pl.elt;
   kp.chunk_rows = kBM;
   kp.n_chunks = pl.n_chunks;
+  kp.trace_chunks = pl.n_chunks;
   kp.chunk_bytes = kBM * kp.row_bytes;
   kp.G = ws + pl.off_R;
   kp.out[0] = static_cast<uint8_t*>(Y);

@@ -82,6 +82,7 @@ struct KParams {
                                  // of a tile fold 1/L each after all arrived (one wave of work)
   int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
+  int trace_chunks;              // chunk flags this call releases (size of the trace's producer section)
   float row_scale[kMaxW];        // AG e4m3: scale_a[r] * scale_b for rows of rank r
   float elem_scale[kMaxW];       // RS e4m3: scale_a[r] * scale_b[r] for rank r's partial
   int op, mode;
@@ -124,7 +125,7 @@ struct KParams {
 int fused_smem_bytes(int block_n, bool fp8);
 
 // Launch the persistent fused kernel for (op, block_n, pair mode pm) on `grid` CTAs. pm: 0 single
-// CTAs, 1 CTA pairs sharing B by multicast, 2 CTA pairs running one 2-SM MMA stream.
+// CTAs, 2 CTA pairs running one 2-SM MMA stream.
 cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 // Largest grid whose CTAs are resident together (pairs: twice the 2-CTA clusters that fit).

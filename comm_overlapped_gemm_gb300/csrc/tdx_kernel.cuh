@@ -289,6 +289,15 @@ __device__ __forceinline__ uint32_t perturb_hash(uint32_t seed, uint32_t x) {
   return h;
 }
 
+// Producer trace: the k-th chunk flag released by this call (by any CTA) is recorded as its flag
+// index in word 1 + k of the trace's producer section; word 0 of the section counts the releases and
+// must be zero when the call starts.
+__device__ __forceinline__ void trace_release(const KParams& p, int grid, uint32_t fi) {
+  uint32_t* rel = p.trace + 4 + 4 * grid;
+  const uint32_t k = atomicAdd(rel, 1u);
+  if (k < static_cast<uint32_t>(p.trace_chunks)) rel[1 + k] = fi;
+}
+
 // Bounded wait on an mbarrier phase. Gives up (false) when the CTA abort flag is raised or after
 // 2 * p.timeout_ns; a timeout is recorded as DEV_TIMEOUT / ROLE_PIPE. Pipeline stages only wait on
 // one another, so a stuck pipeline is normally caused by a flag wait upstream; the doubled bound
@@ -789,10 +798,12 @@ static __device__ __forceinline__ void moe_combine_units(const KParams& p, const
   }
 }
 
-// PM (pair mode): 0 = single CTAs; 1 = CTA pairs sharing the B slice by TMA multicast, each CTA
-// running its own 128-row MMA; 2 = CTA pairs running one 2-SM (cta_group::2) MMA stream.
+// PM (pair mode): 0 = single CTAs; 2 = CTA pairs running one 2-SM (cta_group::2) MMA stream. Every
+// CTA loads only into its own shared memory (no multicast loads), so the same code serves buffers
+// that live in another GPU's memory.
 template <int BN, bool FP8, int OP, int PM>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
+  static_assert(PM == 0 || PM == 2, "pair modes: 0 single CTAs, 2 two-SM MMA pairs");
   constexpr int CL = PM == 0 ? 1 : 2;      // CTAs per cluster
   static_assert(PM == 0 || Cfg<BN, FP8>::B_BOXES % 2 == 0, "pairs split B into two halves");
   using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
@@ -822,7 +833,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, PM == 1 ? 2 : 1);   // PM 1: freed once both CTAs' MMAs used it
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -855,7 +866,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   }
   tc_fence_before();
   if constexpr (CL > 1)
-    cluster_sync_all();   // the peer's barriers are initialised before any multicast targets them
+    cluster_sync_all();   // the peer's barriers are initialised before its loads or commits target them
   else
     __syncthreads();
   tc_fence_after();
@@ -1005,26 +1016,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
             if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_3d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
                                  w.n0 + j * C::B_BOX_N, kb * C::BK, w.e, keep);
-            } else if constexpr (CL == 1) {
-  #pragma unroll
+            } else {
+#pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
                                  w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
-            } else {
-              // both CTAs of the pair compute the same N-tile: each loads its half of the B slice
-              // into the slot of both CTAs (multicast); the slot's barrier in each CTA expects the
-              // whole stage (own A + both halves of B)
-  #pragma unroll
-              for (int jj = 0; jj < C::B_BOXES / 2; ++jj) {
-                const int j = crank * (C::B_BOXES / 2) + jj;
-                tma_load_2d_multicast_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b,
-                                           fb, w.n0 + j * C::B_BOX_N, kb * C::BK, static_cast<uint16_t>(0x3),
-                                           keep);
-              }
             }
           }
         issued_slice:
@@ -1085,10 +1085,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
           if constexpr (PM == 0)
             tc_commit(empty0 + 8 * stage);
-          else if constexpr (PM == 1)
-            tc_commit_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));   // free it in both CTAs
           else
-            tc_commit_pair_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));
+            tc_commit_pair_multicast(empty0 + 8 * stage, static_cast<uint16_t>(0x3));   // free it in both CTAs
           ++consumed;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1145,6 +1143,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
             __threadfence();
             st_release_gpu(p.chunk_flags + fi, p.epoch);
+            if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
           }
         }
       }
@@ -1192,6 +1191,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
             __threadfence();
             st_release_gpu(p.chunk_flags + fi, p.epoch);
+            if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
           }
         }
       }
@@ -1293,6 +1293,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
             __threadfence();
             st_release_gpu(p.chunk_flags + ck, p.epoch);
+            if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(ck));
           }
         }
         named_bar_sync(2, kCopyThreads);   // psrc is rewritten for the next chunk
@@ -1320,8 +1321,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const bool read_s = chained && w.c > 0;
-      const bool write_s = (chained && w.c < p.L - 1) || slotted || rs_gemm_only;
-      const bool direct_out = (!chain && !rs_gemm_only) || (chained && w.c == p.L - 1);
+      const bool write_s = (chained && w.c < p.L - 1) || slotted;
+      // ReduceScatter GEMM-only: every rank's partial is computed and read out of TMEM, but only the
+      // last rank's tile is stored (rounded, into the output): the GEMM without partial traffic
+      const bool direct_out = (!chain && (!rs_gemm_only || w.c == p.L - 1)) || (chained && w.c == p.L - 1);
       if (elected) {
         bool ok = true;
         if (use_mma) ok = wait_mbar(p, tfull0 + 8 * acc, aph, abort_flag, 400 + acc);
@@ -1333,7 +1336,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         if (*abort_flag) ok = false;
         *decision = ok ? 1u : 0u;
         if (trace != nullptr && ok)
-          trace[4 + 4 * grid + blockIdx.x * per_cta + local] =
+          trace[4 + 4 * grid + 1 + p.trace_chunks + blockIdx.x * per_cta + local] =
               (static_cast<uint32_t>(w.c) << 24) | static_cast<uint32_t>(w.tile);
       }
       named_bar_sync(1, kEpiThreads);
@@ -1643,7 +1646,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   }
   tc_fence_before();
   if constexpr (CL > 1)
-    cluster_sync_all();   // no CTA leaves while its peer may still multicast into it or arrive on it
+    cluster_sync_all();   // no CTA leaves while its peer may still load into it or arrive on it
   else
     __syncthreads();
   if (warp == kMmaWarp) {

@@ -5,10 +5,7 @@ namespace tdx {
 
 cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
   if (pm != 0) {
-    if (block_n != 256) return cudaErrorInvalidValue;
-    if (pm == 1)
-      return op == OP_AG ? launch_fused_t<256, false, OP_AG, 1>(p, grid, stream)
-                         : launch_fused_t<256, false, OP_RS, 1>(p, grid, stream);
+    if (block_n != 256 || pm != 2) return cudaErrorInvalidValue;
     return op == OP_AG ? launch_fused_t<256, false, OP_AG, 2>(p, grid, stream)
                        : launch_fused_t<256, false, OP_RS, 2>(p, grid, stream);
   }
@@ -30,7 +27,7 @@ cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int
 
 int fused_max_grid_bf16(int op, int pm, int sms) {
   if (pm == 0) return sms;
-  if (pm == 1) return op == OP_AG ? max_grid_t<256, false, OP_AG, 1>(sms) : max_grid_t<256, false, OP_RS, 1>(sms);
+  if (pm != 2) return 0;
   return op == OP_AG ? max_grid_t<256, false, OP_AG, 2>(sms) : max_grid_t<256, false, OP_RS, 2>(sms);
 }
 

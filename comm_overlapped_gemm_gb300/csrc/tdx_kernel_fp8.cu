@@ -7,11 +7,9 @@ namespace tdx {
 
 cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
   if (pm != 0) {
-    if (block_n != 256) return cudaErrorInvalidValue;
-    if (op == OP_AG)
-      return pm == 1 ? launch_fused_t<256, true, OP_AG, 1>(p, grid, stream)
-                     : launch_fused_t<256, true, OP_AG, 2>(p, grid, stream);
-    return pm == 2 ? launch_fused_t<256, true, OP_RS, 2>(p, grid, stream) : cudaErrorInvalidValue;
+    if (block_n != 256 || pm != 2) return cudaErrorInvalidValue;
+    return op == OP_AG ? launch_fused_t<256, true, OP_AG, 2>(p, grid, stream)
+                       : launch_fused_t<256, true, OP_RS, 2>(p, grid, stream);
   }
   if (op == OP_AG) {
     switch (block_n) {
@@ -29,8 +27,8 @@ cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int 
 
 int fused_max_grid_fp8(int op, int pm, int sms) {
   if (pm == 0) return sms;
-  if (op == OP_AG) return pm == 1 ? max_grid_t<256, true, OP_AG, 1>(sms) : max_grid_t<256, true, OP_AG, 2>(sms);
-  return pm == 2 ? max_grid_t<256, true, OP_RS, 2>(sms) : 0;
+  if (pm != 2) return 0;
+  return op == OP_AG ? max_grid_t<256, true, OP_AG, 2>(sms) : max_grid_t<256, true, OP_RS, 2>(sms);
 }
 
 }  // namespace tdx

@@ -100,15 +100,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                           int x, int y, uint16_t cta_mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(pol)
-      : "memory");
-}
-
 // Bring a box into L2 ahead of its load (no shared memory, no barrier).
 // Untiled bulk copies (TMA engine): global -> shared counted on an mbarrier, shared -> global in
 // bulk groups. Addresses 16-byte aligned, sizes multiples of 16.
@@ -150,17 +141,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
                "r"(x), "r"(y)
                : "memory");
-}
-
-// Multicast form: the box is written at the same shared-memory offset in every CTA of the cluster
-// named in cta_mask, and each destination CTA's barrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                      int x, int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
 }
 
 // Pair (2-SM) form: the box lands in this CTA's shared memory and its bytes are counted on the
@@ -324,13 +304,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-// Same, arriving on the barrier at `bar`'s offset in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
 // CTA-pair (cta_group::2) forms: the allocation is made collectively by one warp in each CTA of
 // the pair (same address in both); the MMA is issued by one thread of the pair's leader and works
 // on both CTAs' shared memory and Tensor Memory; commits track it and can signal both CTAs.
@@ -348,6 +321,8 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
+// Commit of a pair's MMAs that arrives on the barrier at `bar`'s offset in each CTA of the pair named in
+// cta_mask (an mbarrier arrive, not a data transfer).
 __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

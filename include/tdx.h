@@ -57,7 +57,9 @@ typedef enum { TDX_BF16 = 0, TDX_FP8_E4M3 = 1, TDX_FP32 = 2 } tdx_dtype;
 typedef enum {
   TDX_FUSED = 0,          /* producer and consumer overlapped in one persistent kernel (default) */
   TDX_GEMM_ONLY = 1,      /* AG: GEMM on an already gathered buffer, no flag waits, no copies.
-                             RS: every rank's fp32 partial tile stored, no rank chain, no output */
+                             RS: every rank's partial tile computed and read out of Tensor Memory,
+                             no partial buffer, no rank chain; only rank W-1's partial is stored,
+                             rounded to bf16, into the output (the GEMM alone, for measurements) */
   TDX_MOVE_ONLY = 2,      /* AG: chunk copies and flag releases only. RS: the rank-order
                              read-add-write chain over the running-sum buffer with zero partials */
   TDX_CONSUMER_ONLY = 3   /* AG: consumers wait on flags that no producer releases (fault tests) */
@@ -95,11 +97,11 @@ typedef struct tdx_opts {
                                 partial; the last to arrive folds them in order 0..L-1). Both give
                                 the same bits. */
   int cluster;               /* how CTAs cooperate on the GEMM: 0 = library choice, 1 = single CTAs,
-                                2 = pairs of CTAs on vertically adjacent 128 x 256 tiles sharing the B
-                                slice (each loads half of it into both CTAs' shared memory),
                                 3 = pairs running one 2-SM MMA stream on a 256 x 256 tile (each CTA
-                                stages its 128 rows of A and half of B). 2 and 3 need tile width 256
-                                and an even number of 128-row M-tiles. */
+                                stages its 128 rows of A and half of B in its own shared memory;
+                                needs tile width 256 and an even number of 128-row M-tiles).
+                                2 (pairs sharing B through multicast loads) is not offered:
+                                TDX_ERR_UNSUPPORTED. */
   int bf16_partials;         /* ReduceScatter / AllReduce: 0 (default) = each rank's partial enters
                                 the fold in fp32; 1 = each partial is rounded once to bf16 (RNE, the
                                 type a rank would send) before the fp32 fold, which halves the
@@ -177,7 +179,12 @@ tdx_status tdx_gemm_rs(const void* const* A_parts, const void* const* B_parts,
  *    TDX_NOALLOC_SCRATCH_BYTES are rejected with TDX_ERR_WORKSPACE before anything is launched
  *    (the small-M and tiny AllGather shapes fit; W=8 x 1024 x 8192 bf16 does not).
  *  - First call on a device: it looks up the device address of the scratch array (with that
- *    device current) and caches it; make this first call before any stream capture.
+ *    device current) and caches it with the ID of the current CUDA context; make this first call
+ *    before any stream capture. The cached address belongs to that context: after the device's
+ *    context is destroyed and re-created (for example by cudaDeviceReset), the next call looks the
+ *    address up again, and that call too should come before any stream capture.
+ *  - Every argument is checked before anything is enqueued: a call that returns an error has
+ *    launched nothing and left the scratch array untouched.
  *  - Shared state: every call on a device uses the same array, which keeps the previous call's
  *    contents. Each call clears, on `stream`, the status word and the flags that must start at
  *    zero (opts->epoch is ignored; epoch 1 is used). Calls that overlap on the GPU (different
@@ -311,7 +318,7 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * [9] chunk piece counters, [10] chain flags (uint32 [(L-1) * T], index c*T + tile), [11] gathered
  * buffer G, [12] fp32 running-sum / partial-slot buffer, [13] total workspace bytes, [14] reduce
  * mode in use (1 chained, 2 slotted, 0 none), [15] offset of the per-tile arrival counters,
- * [16] CTA cooperation in use (1 single, 2 multicast pair, 3 2-SM pair), [17] ReduceScatter
+ * [16] CTA cooperation in use (1 single, 3 2-SM pair), [17] ReduceScatter
  * raster: N-tiles per group (within a rank the tiles are taken group by group, M-tiles, then the
  * group's N-tiles), [18] ReduceScatter rank block:
  * that many positions of a rank's tile order are processed for ranks 0..W-1 before the next block
@@ -326,12 +333,20 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 
-/* Bytes of the optional trace buffer for a call on `grid` CTAs taking `items` work items:
- * words [0..3] = {grid, items, chain length, tiles}; then per CTA 4 statistics words {ns spent
- * waiting on chunk flags, number of flag waits, ns spent waiting on rank-chain flags, items taken};
- * then per CTA, in order, the work items it took, one word each: (chain element << 24) | tile id,
- * tile id = m_tile * N-tiles + n_tile. CTA b takes items b, b + grid, b + 2*grid, ... */
-size_t tdx_trace_size(int grid, int items);
+/* Bytes of the optional trace buffer (opts->trace) for a call on `grid` CTAs taking `items` work
+ * items and releasing `chunks` chunk flags (AllGather: W * chunks per rank; MoE dispatch: the 128-row
+ * chunks of the dispatched rows; 0 otherwise). Layout, in 32-bit words:
+ *  [0..3]  {grid, items, chain length, tiles};
+ *  then per CTA 4 statistics words {ns spent waiting on chunk flags, number of flag waits, ns spent
+ *          waiting on rank-chain flags, items taken};
+ *  then the producer section: one count of released chunks, then `chunks` words: word k holds the
+ *          flag index (AllGather: rank * chunks per rank + chunk) of the k-th chunk released by the
+ *          call, whichever CTA released it. The count must be zero when the call starts (pass a
+ *          zero-filled buffer); every other word is written by the kernel;
+ *  then per CTA, in order, the work items it took, one word each: (chain element << 24) | tile id,
+ *          tile id = m_tile * N-tiles + n_tile. CTA b takes items b, b + grid, b + 2*grid, ... (CTA
+ *          pairs: pair b/2 takes items b/2, b/2 + grid/2, ...). */
+size_t tdx_trace_size(int grid, int items, int chunks);
 
 /* Static description of a status code. Never NULL. */
 const char* tdx_status_string(tdx_status s);

@@ -16,5 +16,5 @@ hand-worked fixture and library routines (torch's bf16 and e4m3 casts).
 from .reference import (  # noqa: F401
     decode_bf16, decode_e4m3, round_bf16_rne, round_fp32_rne,
     ag_gemm, ag_gemm_rows, gemm_rs, gemm_rs_rows, gemm_ar, round_out,
-    ag_chunk_release_order, ag_tile_schedule, rs_item_schedule, expected_flags,
+    ag_chunk_release_order, ag_arrival_rank_order, ag_consumer_order_ok, rs_fold_order, expected_flags,
 )

@@ -219,7 +219,14 @@ def gemm_rs_rows(a_parts, b_parts, rows, dtype: str = "bf16", scale_a=None, scal
 
 
 # ----------------------------------------------------------------------------------------------
-# Bookkeeping: flags and the rank-swizzled schedules
+# Bookkeeping: flags, arrival order and reduction order
+#
+# What the method fixes about order (Triton-distributed article, section "The first move was to
+# expose the overlap": compute on one chunk while another is still moving; section "DITRON adds
+# three levels of tiling": collectives broken into chunks paired with compute tiles, synchronised by
+# signals) is stated here at the level of ranks and chunks only. How a kernel cuts the output into
+# tiles, and in which raster it walks the tiles that one rank owns, is its own choice and is not
+# part of the definition: the checks below take the consumed work as row ranges of the output.
 # ----------------------------------------------------------------------------------------------
 
 
@@ -233,46 +240,26 @@ def ag_chunk_release_order(W: int, M_local: int, chunk: int, self_rank: int = 0)
     return [(r, c) for r in ranks for c in range(n_chunks)]
 
 
-def ag_tile_schedule(W: int, M_local: int, N: int, BM: int, BN: int, self_rank: int = 0, group: int = 1):
-    """Order in which the consumer GEMM takes output tiles: M-tiles grouped by the rank that owns
-    the tile's first row, in arrival order self, self+1, ..., self+W-1 (mod W); M-tiles ascending
-    within a rank; N-tiles innermost. Returns (m_tile, n_tile) pairs.
-
-    With ``group`` > 1, ``group`` consecutive M-tiles are taken together (one per CTA of a cluster):
-    the groups follow the same rule keyed by the rank owning the group's first row, and the list
-    holds (m_group, n_tile) pairs; the CTA of cluster rank r takes M-tile ``group*m_group + r``."""
-    M = W * M_local
-    tiles_m = (M + BM - 1) // BM
-    tiles_n = (N + BN - 1) // BN
-    n_groups = tiles_m // group
-    key = lambda mg: (((mg * group * BM) // M_local - self_rank) % W, mg)
-    return [(mg, nt) for mg in sorted(range(n_groups), key=key) for nt in range(tiles_n)]
+def ag_arrival_rank_order(W: int, self_rank: int = 0):
+    """Order in which the AllGather's consumer takes the ranks' rows: its own shard first (local,
+    no wait), then the peers in the order their chunks arrive, self+1, self+2, ... (mod W)."""
+    return [(self_rank + i) % W for i in range(W)]
 
 
-def rs_item_schedule(W: int, M: int, N: int, BM: int, BN: int, group: int = 1, group_n=None, rank_block=None):
-    """Order of GEMM+ReduceScatter work items. Within a rank, the tile order ("positions") takes the
-    N-tiles in groups of ``group_n`` (default: one group of all N-tiles; the last group may be
-    narrower): group by group, M-tiles ascending, the group's N-tiles innermost. Ranks are
-    interleaved in blocks of ``rank_block`` positions (default: one block of all positions, i.e.
-    rank-outer): for each block, ranks 0..W-1 (the reduction order), the block's positions in
-    order. Item (r, t) adds rank r's partial tile to the running sum of ranks 0..r-1. Returns
-    (rank, m_tile, n_tile) triples; with ``group`` > 1 the middle entry is the M-tile group (see
-    :func:`ag_tile_schedule`)."""
-    tiles_m = (M + BM - 1) // BM
-    tiles_n = (N + BN - 1) // BN
-    gn = tiles_n if group_n is None else max(1, min(group_n, tiles_n))
-    order = []
-    for n0 in range(0, tiles_n, gn):
-        for mg in range(tiles_m // group):
-            for nt in range(n0, min(n0 + gn, tiles_n)):
-                order.append((mg, nt))
-    P = len(order) if rank_block is None else max(1, min(rank_block, len(order)))
-    out = []
-    for b0 in range(0, len(order), P):
-        for r in range(W):
-            for pos in range(b0, min(b0 + P, len(order))):
-                out.append((r,) + order[pos])
-    return out
+def ag_consumer_order_ok(row_starts, W: int, M_local: int, self_rank: int = 0) -> bool:
+    """True if a sequence of consumed output row blocks (the first row of each block, in the order
+    the consumer took them) visits the ranks in :func:`ag_arrival_rank_order`: the rank that owns a
+    block's first row never moves back to an earlier position of that order."""
+    pos = {r: i for i, r in enumerate(ag_arrival_rank_order(W, self_rank))}
+    seq = [pos[int(r0) // M_local] for r0 in row_starts]
+    return all(b >= a for a, b in zip(seq, seq[1:]))
+
+
+def rs_fold_order(W: int):
+    """Order in which the ranks' partial products enter the ReduceScatter's sum of one output tile:
+    ranks 0, 1, ..., W-1, a left fold ((P_0 + P_1) + P_2) + ..., the same for every tile and
+    independent of timing and of which rank is local."""
+    return list(range(W))
 
 
 def expected_flags(n: int, epoch: int) -> np.ndarray:

@@ -242,3 +242,59 @@ class CombineCase:
         torch.cuda.synchronize()
         z = self.ws[pl["off_R"]:pl["off_R"] + rows * self.H * 2].view(torch.int16).cpu().numpy().view(np.uint16)
         return z.reshape(rows, self.H)
+
+
+# ------------------------------------------------------------------ trace decoding (tdx_trace_size)
+def trace_items(tr: np.ndarray, grid: int, chunks: int, cl: int = 1) -> dict:
+    """Work items a traced call took: {(item index in the cluster-wide sequence, CTA rank in its
+    pair): (chain element, tile id)}. CTA b of a grid of pairs (cl = 2) is CTA b % 2 of pair b // 2,
+    and pair q takes items q, q + grid/2, ...; single CTAs (cl = 1) take b, b + grid, ..."""
+    items = int(tr[1])
+    per = (items + grid - 1) // grid
+    base = 4 + 4 * grid + 1 + chunks
+    ncl = grid // cl
+    out = {}
+    for b in range(grid):
+        cid, crank = divmod(b, cl)
+        mine = list(range(cid, items // cl, ncl))
+        assert int(tr[4 + 4 * b + 3]) == len(mine), (b, int(tr[4 + 4 * b + 3]), len(mine))
+        for k, it in enumerate(mine):
+            w = int(tr[base + b * per + k])
+            out[(it, crank)] = (w >> 24, w & 0xFFFFFF)
+    return out
+
+
+def trace_releases(tr: np.ndarray, grid: int, chunks: int) -> list:
+    """Flag indices of the chunks a traced call released, in release order."""
+    base = 4 + 4 * grid
+    n = int(tr[base])
+    assert n == chunks, (n, chunks)
+    return [int(x) for x in tr[base + 1:base + 1 + n]]
+
+
+def check_each_item_once(taken: dict, L: int, T: int):
+    got = sorted(taken.values())
+    assert got == [(c, t) for c in range(L) for t in range(T)], "some (element, tile) missing or repeated"
+
+
+def check_ag_consumer_order(taken: dict, L: int, tiles_n: int, W: int, M_local: int, self_rank: int):
+    """For every K split c, the first rows of the tiles taken, in item order, visit the ranks in the
+    oracle's arrival order (own shard first, then self+1, self+2, ...)."""
+    for c in range(L):
+        seq = sorted((it, crank, t) for (it, crank), (cc, t) in taken.items() if cc == c)
+        rows, last = [], None
+        for it, _, t in seq:
+            if it != last:     # the two CTAs of a pair share an item: its first row is the lower tile's
+                rows.append(min((tt // tiles_n) * 128 for i2, _, tt in seq if i2 == it))
+                last = it
+        assert R.ag_consumer_order_ok(rows, W, M_local, self_rank), rows[:16]
+
+
+def check_rs_fold_order(taken: dict, W: int, T: int):
+    """For every output tile, the ranks' items come in the oracle's fold order 0, 1, ..., W-1."""
+    by_tile = {}
+    for (it, _), (r, t) in taken.items():
+        by_tile.setdefault(t, []).append((it, r))
+    assert len(by_tile) == T
+    for t, lst in by_tile.items():
+        assert [r for _, r in sorted(lst)] == R.rs_fold_order(W), (t, sorted(lst))

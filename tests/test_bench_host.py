@@ -71,3 +71,21 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_peak_follows_the_length_of_the_timed_region():
+    pk = {"bf16_tflops": 1915.0, "bf16_tflops_sustained": 1713.0}
+    v, src = bench.bf16_peak(pk, "measured", 0.05)
+    assert v == 1915.0 and "burst" in src
+    v, src = bench.bf16_peak(pk, "measured", 4.0)
+    assert v == 1713.0 and "sustained" in src
+    v, _ = bench.bf16_peak({"bf16_tflops": 1900.0}, "fallback", 4.0)
+    assert v == 1900.0
+
+
+def test_clock_samples_stay_out_of_the_repository(monkeypatch, tmp_path):
+    monkeypatch.setenv("TDX_CLOCKS_DIR", str(tmp_path))
+    c = bench.ClockSampler(0)
+    assert c.path.startswith(str(tmp_path))
+    monkeypatch.delenv("TDX_CLOCKS_DIR")
+    assert not bench.ClockSampler(0).path.startswith(bench.ROOT)

@@ -156,6 +156,8 @@ def test_ag_validation_codes(tdx):
     assert _ag(tdx, opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
     assert _ag(tdx, opts=tdx.make_opts(cluster=4)) == tdx.TDX_ERR_INVALID_ARG
     assert _ag(tdx, opts=tdx.make_opts(cluster=3, block_n=128)) == tdx.TDX_ERR_UNSUPPORTED
+    # pairs sharing B through multicast loads are not offered
+    assert _ag(tdx, M_local=256, opts=tdx.make_opts(cluster=2, block_n=256)) == tdx.TDX_ERR_UNSUPPORTED
     assert _ag(tdx, dtype=1, opts=tdx.make_opts(block_n=64)) == tdx.TDX_ERR_UNSUPPORTED
     # empty problems launch nothing and succeed
     assert _ag(tdx, M_local=0) == tdx.TDX_OK
@@ -172,6 +174,7 @@ def test_rs_validation_codes(tdx):
     assert rs(O=[0, FAKE]) == tdx.TDX_ERR_INVALID_ARG
     assert rs(M=129) == tdx.TDX_ERR_INVALID_ARG
     assert rs(dtype=1, M=256, opts=tdx.make_opts(cluster=2, block_n=256)) == tdx.TDX_ERR_UNSUPPORTED
+    assert rs(M=256, opts=tdx.make_opts(cluster=2, block_n=256)) == tdx.TDX_ERR_UNSUPPORTED
     assert rs(dtype=1, K=120) == tdx.TDX_ERR_ALIGNMENT      # 120-byte e4m3 rows
     assert rs(opts=tdx.make_opts(out_dtype=2)) == tdx.TDX_ERR_UNSUPPORTED
     assert rs(B=[FAKE, FAKE + 2]) == tdx.TDX_ERR_ALIGNMENT
@@ -240,8 +243,11 @@ def test_planner_choices_for_the_workloads(tdx, case):
 
 
 def test_trace_size(tdx):
-    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 4 * 3)
+    # header, 4 statistics words per CTA, the producer's release count and sequence, items per CTA
+    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 1 + 4 * 3)
+    assert tdx.tdx_trace_size(4, 10, 64) == 4 * (4 + 16 + 1 + 64 + 4 * 3)
     assert tdx.tdx_trace_size(0, 10) == 0
+    assert tdx.tdx_trace_size(4, 10, -1) == 0
 
 
 def test_copy_engine_producer_is_not_offered(tdx):
@@ -259,6 +265,33 @@ def test_noalloc_rejects_copy_engine_producer_before_any_device_work(tdx):
 def test_noalloc_rejects_oversized_problem_before_any_device_work(tdx):
     rc = tdx.tdx_ag_gemm_noalloc([FAKE] * 8, FAKE, FAKE, 8, 1024, 8192, 3584, tdx.TDX_BF16, None, stream=0)
     assert rc == tdx.TDX_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("bad", ["B", "shard", "C", "K", "self_rank", "out_dtype", "null_shard", "status"])
+def test_noalloc_checks_every_argument_before_any_device_work(tdx, bad):
+    # No GPU here: a call that reached the scratch set-up or a launch would fail with
+    # TDX_ERR_CUDA, so the specific code proves the argument was rejected before anything was
+    # enqueued on the shared scratch array.
+    shards, B, C, K, o, status = [FAKE] * 2, FAKE, FAKE, 128, None, None
+    want = tdx.TDX_ERR_ALIGNMENT
+    if bad == "B":
+        B = FAKE + 8
+    elif bad == "shard":
+        shards = [FAKE, FAKE + 4]
+    elif bad == "C":
+        C = FAKE + 2
+    elif bad == "K":
+        K = 100                                    # 200-byte rows
+    elif bad == "self_rank":
+        o, want = tdx.make_opts(self_rank=5), tdx.TDX_ERR_INVALID_ARG
+    elif bad == "out_dtype":
+        o, want = tdx.make_opts(out_dtype=tdx.TDX_FP8_E4M3), tdx.TDX_ERR_INVALID_ARG
+    elif bad == "null_shard":
+        shards, want = [FAKE, 0], tdx.TDX_ERR_INVALID_ARG
+    elif bad == "status":
+        status = FAKE + 4
+    rc = tdx.tdx_ag_gemm_noalloc(shards, B, C, 2, 64, K, 256, tdx.TDX_BF16, o, device_status=status, stream=0)
+    assert rc == want, tdx.tdx_status_string(rc)
 
 
 def test_moe_validation_codes(tdx):

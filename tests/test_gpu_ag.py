@@ -11,7 +11,8 @@ import torch
 import comm_overlapped_gemm_gb300 as tdx
 from oracle import reference as R
 import workloads as wls
-from gpu_util import AGCase, assert_bit_exact, assert_within_tol, sample_rows, host_bits
+from gpu_util import (AGCase, assert_bit_exact, assert_within_tol, check_ag_consumer_order,
+                      check_each_item_once, host_bits, sample_rows, trace_items, trace_releases)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,16 +65,17 @@ def test_ag_tiny_random_within_tolerance():
 
 @pytest.mark.parametrize("name", ["ag_w8", "ag_fp8_w8"])
 @pytest.mark.parametrize("integer", [True, False])
-def test_ag_full_size_sampled(name, integer):
+def test_ag_full_size_full_output(name, integer):
+    # the headline shapes, every element of C against the full fp64 oracle
     wl = wls.WORKLOADS[name]
     inp = wls.make_inputs(wl, integer=integer)
     o = opts(scale_a=inp.scale_a, scale_b=inp.scale_b[0]) if wl.dtype == "e4m3" else opts()
     case = AGCase(inp, opts=o)
     tdx.check(case.run(), name)
     status_ok(case)
-    rows = sample_rows(wl.W * wl.M, wl.chunk_rows)
-    got_bits = case.result_bits()[rows]
-    want = case.oracle(rows)
+    got_bits = case.result_bits()
+    want = case.oracle()
+    assert want.shape == got_bits.shape == (wl.W * wl.M, wl.N)
     if integer:
         assert_bit_exact(got_bits, want, "bf16")
     else:
@@ -126,30 +128,33 @@ def test_ag_fp8_ragged_and_scales():
 
 
 @pytest.mark.parametrize("self_rank", [0, 3, 7])
-def test_ag_self_rank_and_trace_follow_the_oracle_schedule(self_rank):
+@pytest.mark.parametrize("grid", [1, 16])
+def test_ag_trace_follows_the_oracle_orders(self_rank, grid):
+    """Bookkeeping against what the method fixes: every (split, tile) is computed exactly once, the
+    consumer takes the ranks' rows in the arrival order self, self+1, ... (in whatever raster inside
+    a rank), and the producer releases every chunk exactly once; with one CTA (a single producer
+    thread) the release sequence is exactly the oracle's release order."""
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=512, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
-    grid = 16
     o = opts(self_rank=self_rank, num_sms=grid)
     plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 512, 512, tdx.TDX_BF16, o)
     items = plan["L"] * plan["T"]
-    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    o = opts(self_rank=self_rank, num_sms=grid, trace=trace)
-    case = AGCase(inp, opts=o)
+    chunks = 8 * plan["n_chunks"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items, chunks) // 4, dtype=torch.int32, device="cuda")
+    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
     tr = trace.cpu().numpy().astype(np.uint32)
     assert list(tr[:4]) == [grid, items, plan["L"], plan["T"]]
-    sched = R.ag_tile_schedule(8, 256, 512, 128, plan["BN"], self_rank)
-    per = (items + grid - 1) // grid
-    for b in range(grid):
-        mine = list(range(b, items, grid))
-        assert tr[4 + 4 * b + 3] == len(mine)
-        for k, it in enumerate(mine):
-            c, pos = divmod(it, plan["T"])
-            mt, nt = sched[pos]
-            assert tr[4 + 4 * grid + b * per + k] == (c << 24) | (mt * plan["tiles_n"] + nt)
+    taken = trace_items(tr, grid, chunks)
+    check_each_item_once(taken, plan["L"], plan["T"])
+    check_ag_consumer_order(taken, plan["L"], plan["tiles_n"], 8, 256, self_rank)
+    rel = trace_releases(tr, grid, chunks)
+    want = [r * plan["n_chunks"] + c for r, c in R.ag_chunk_release_order(8, 256, 128, self_rank)]
+    assert sorted(rel) == list(range(chunks))
+    if grid == 1:
+        assert rel == want
 
 
 def test_ag_modes_and_epochs():
@@ -240,33 +245,30 @@ def test_ag_split_k_chained_and_slotted_identical():
     assert np.array_equal(bits[0], bits[1])
 
 
-@pytest.mark.parametrize("cluster", [2, 3])
 @pytest.mark.parametrize("self_rank", [0, 5])
-def test_ag_pairs_parity_and_trace(self_rank, cluster):
+def test_ag_pairs_parity_and_trace(self_rank):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=1024, N=768, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)
     grid = 16
-    o = opts(self_rank=self_rank, num_sms=grid, cluster=cluster, block_n=256)
+    o = opts(self_rank=self_rank, num_sms=grid, cluster=3, block_n=256)
     plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 1024, 768, tdx.TDX_BF16, o)
-    assert plan["cluster"] == cluster and plan["BN"] == 256
+    assert plan["cluster"] == 3 and plan["BN"] == 256
     items = plan["L"] * plan["T"]
-    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
-    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=cluster, block_n=256, trace=trace))
+    chunks = 8 * plan["n_chunks"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items, chunks) // 4, dtype=torch.int32, device="cuda")
+    case = AGCase(inp, opts=opts(self_rank=self_rank, num_sms=grid, cluster=3, block_n=256, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.ag_tile_schedule(8, 256, 768, 128, 256, self_rank, group=2)
-    per = (items + grid - 1) // grid
-    ncl = grid // 2
-    for b in range(grid):
-        cid, crank = divmod(b, 2)
-        mine = list(range(cid, items // 2, ncl))
-        assert tr[4 + 4 * b + 3] == len(mine)
-        for k, it in enumerate(mine):
-            c, pos = divmod(it, len(sched))
-            mg, nt = sched[pos]
-            assert tr[4 + 4 * grid + b * per + k] == (c << 24) | ((2 * mg + crank) * plan["tiles_n"] + nt)
+    taken = trace_items(tr, grid, chunks, cl=2)
+    check_each_item_once(taken, plan["L"], plan["T"])
+    # the two CTAs of a pair take vertically adjacent tiles of the same N-tile
+    for it in {k[0] for k in taken}:
+        (c0, t0), (c1, t1) = taken[(it, 0)], taken[(it, 1)]
+        assert c0 == c1 and t1 == t0 + plan["tiles_n"]
+    check_ag_consumer_order(taken, plan["L"], plan["tiles_n"], 8, 256, self_rank)
+    assert sorted(trace_releases(tr, grid, chunks)) == list(range(chunks))
 
 
 @pytest.mark.parametrize("name", ["ag_w8", "ag_fp8_w8"])
@@ -274,7 +276,7 @@ def test_ag_pairs_and_singles_give_identical_bits(name):
     wl = wls.with_shape(wls.WORKLOADS[name], W=4, M=256, K=1024, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=False)
     bits = []
-    for cl in (1, 2, 3):
+    for cl in (1, 3):
         kw = dict(cluster=cl, block_n=256)
         if wl.dtype == "e4m3":
             kw.update(scale_a=inp.scale_a, scale_b=inp.scale_b[0])
@@ -284,10 +286,9 @@ def test_ag_pairs_and_singles_give_identical_bits(name):
         bits.append(case.result_bits())
         assert_within_tol(case.result(), case.oracle(), wl.dtype)
     assert np.array_equal(bits[0], bits[1])
-    assert np.array_equal(bits[0], bits[2])
 
 
-@pytest.mark.parametrize("cluster", [2, 3])
+@pytest.mark.parametrize("cluster", [3])
 def test_ag_pairs_timeout_recovers(cluster):
     wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=256, N=512, chunk_rows=128)
     inp = wls.make_inputs(wl, integer=True)

@@ -70,7 +70,7 @@ def test_ar_matches_reducescatter_shards_bitwise():
 
 
 @pytest.mark.parametrize("variant", [dict(cluster=3, block_n=256, reduce_mode=1),
-                                     dict(cluster=2, block_n=256, reduce_mode=2)])
+                                     dict(cluster=3, block_n=256, reduce_mode=2)])
 def test_ar_pairs(variant):
     wl = wls.with_shape(wls.WORKLOADS["ar_w8"], W=4, M=512, K=512, N=512)
     inp = wls.make_inputs(wl, integer=True)

@@ -7,7 +7,8 @@ import torch
 import comm_overlapped_gemm_gb300 as tdx
 from oracle import reference as R
 import workloads as wls
-from gpu_util import RSCase, assert_bit_exact, assert_within_tol, sample_rows
+from gpu_util import (RSCase, assert_bit_exact, assert_within_tol, check_each_item_once, check_rs_fold_order,
+                      sample_rows, trace_items)
 
 pytestmark = pytest.mark.gpu
 
@@ -45,15 +46,16 @@ def test_rs_small_shapes(shape, integer):
 
 
 @pytest.mark.parametrize("integer", [True, False])
-def test_rs_full_size_sampled(integer):
+def test_rs_full_size_full_output(integer):
+    # the headline shape, every element of the W output shards against the full fp64 oracle
     wl = wls.WORKLOADS["rs_w8"]
     inp = wls.make_inputs(wl, integer=integer)
     case = RSCase(inp, opts=opts())
     tdx.check(case.run())
     status_ok(case)
-    rows = sample_rows(wl.M, wl.M // wl.W)
-    got = case.result_bits()[rows]
-    want = case.oracle(rows)
+    got = case.result_bits()
+    want = case.oracle()
+    assert want.shape == got.shape == (wl.M, wl.N)
     if integer:
         assert_bit_exact(got, want, "bf16")
     else:
@@ -90,7 +92,7 @@ def test_rs_chain_flags_trace_and_order():
     plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, o)
     assert plan["reduce_mode"] == 1
     items = plan["L"] * plan["T"]
-    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items, 0) // 4, dtype=torch.int32, device="cuda")
     case = RSCase(inp, opts=opts(num_sms=grid, trace=trace, epoch=3, reduce_mode=1))
     tdx.check(case.run())
     status_ok(case)
@@ -99,12 +101,9 @@ def test_rs_chain_flags_trace_and_order():
     f = case.ws[plan["off_chain_flags"]:plan["off_chain_flags"] + 4 * n].view(torch.int32).cpu().numpy()
     assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 3))
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(4, 512, 512, 128, plan["BN"], group_n=plan["group_n"], rank_block=plan["rank_block"])
-    per = (items + grid - 1) // grid
-    for b in range(grid):
-        for k, it in enumerate(range(b, items, grid)):
-            r, mt, nt = sched[it]
-            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)
+    taken = trace_items(tr, grid, 0)
+    check_each_item_once(taken, plan["L"], plan["T"])
+    check_rs_fold_order(taken, 4, plan["T"])
     # the running sum of ranks 0..W-2 left in the workspace is the left fold of the partials:
     # with fp32 partials it matches the oracle's fp64 sum of ranks 0..W-2 to fp32 accuracy
     S = case.ws[plan["off_S"]:plan["off_S"] + 4 * plan["T"] * 128 * plan["BN"]].view(torch.float32).cpu().numpy()
@@ -119,12 +118,18 @@ def test_rs_chain_flags_trace_and_order():
         assert np.max(np.abs(T - want)) <= 1e-5 * np.max(np.abs(want))
 
 
-def test_rs_modes_run():
+@pytest.mark.parametrize("variant", [dict(), dict(reduce_mode=2), dict(cluster=3, block_n=256)])
+def test_rs_modes_run(variant):
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
     inp = wls.make_inputs(wl, integer=True)
-    case = RSCase(inp, opts=opts())
-    for mode in (tdx.TDX_GEMM_ONLY, tdx.TDX_MOVE_ONLY, tdx.TDX_FUSED):
-        tdx.check(case.run(opts(mode=mode)))
+    case = RSCase(inp, opts=opts(**variant))
+    # GEMM alone: every rank's partial computed, only rank W-1's stored into the output
+    tdx.check(case.run(opts(mode=tdx.TDX_GEMM_ONLY, **variant)))
+    status_ok(case)
+    last = np.concatenate(R.gemm_rs(inp.a[3:], inp.b[3:], "bf16"))
+    assert_bit_exact(case.result_bits(), last, "bf16")
+    for mode in (tdx.TDX_MOVE_ONLY, tdx.TDX_FUSED):
+        tdx.check(case.run(opts(mode=mode, **variant)))
         status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
 
@@ -198,7 +203,7 @@ def test_rs_full_size_slotted_matches_chained():
     assert np.array_equal(bits[0], bits[1])
 
 
-@pytest.mark.parametrize("cluster", [2, 3])
+@pytest.mark.parametrize("cluster", [3])
 @pytest.mark.parametrize("rm", [1, 2])
 def test_rs_pairs_parity_trace_and_identity(rm, cluster):
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=512, N=512)
@@ -208,48 +213,40 @@ def test_rs_pairs_parity_trace_and_identity(rm, cluster):
     plan = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 512, 512, tdx.TDX_BF16, o)
     assert plan["cluster"] == cluster
     items = plan["L"] * plan["T"]
-    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items, 0) // 4, dtype=torch.int32, device="cuda")
     case = RSCase(inp, opts=opts(num_sms=grid, cluster=cluster, block_n=256, reduce_mode=rm, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_within_tol(case.result(), case.oracle(), "bf16")
     paired = case.result_bits()
     tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(4, 512, 512, 128, 256, group=2, group_n=plan["group_n"], rank_block=plan["rank_block"])
-    per = (items + grid - 1) // grid
-    for b in range(grid):
-        cid, crank = divmod(b, 2)
-        for k, it in enumerate(range(cid, items // 2, grid // 2)):
-            r, mg, nt = sched[it]
-            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | ((2 * mg + crank) * plan["tiles_n"] + nt)
+    taken = trace_items(tr, grid, 0, cl=2)
+    check_each_item_once(taken, plan["L"], plan["T"])
+    check_rs_fold_order(taken, 4, plan["T"])
     single = RSCase(inp, opts=opts(cluster=1, block_n=256, reduce_mode=rm))
     tdx.check(single.run())
     status_ok(single)
     assert np.array_equal(single.result_bits(), paired)
 
 
-def test_rs_grouped_raster_trace():
-    # 20 N-tiles of 128: a full group and a partial one within each rank
+def test_rs_many_n_tiles_trace():
+    # 20 N-tiles of 128 per rank: whatever raster the kernel takes inside a rank, every (rank, tile)
+    # is computed once and every tile's ranks come in the fold order 0..W-1
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=2, M=256, K=128, N=2560)
     inp = wls.make_inputs(wl, integer=True)
     grid = 6
     o = opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1)
     plan = tdx.tdx_plan_info(tdx.OP_RS, 2, 256, 128, 2560, tdx.TDX_BF16, o)
-    gn = plan["group_n"]
-    assert plan["tiles_n"] == 20 and 1 < gn < 20 and 20 % gn != 0
+    assert plan["tiles_n"] == 20
     items = plan["L"] * plan["T"]
-    trace = torch.zeros(tdx.tdx_trace_size(grid, items) // 4, dtype=torch.int32, device="cuda")
+    trace = torch.zeros(tdx.tdx_trace_size(grid, items, 0) // 4, dtype=torch.int32, device="cuda")
     case = RSCase(inp, opts=opts(num_sms=grid, block_n=128, reduce_mode=1, cluster=1, trace=trace))
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
-    tr = trace.cpu().numpy().astype(np.uint32)
-    sched = R.rs_item_schedule(2, 256, 2560, 128, 128, group_n=gn, rank_block=plan["rank_block"])
-    per = (items + grid - 1) // grid
-    for b in range(grid):
-        for k, it in enumerate(range(b, items, grid)):
-            r, mt, nt = sched[it]
-            assert tr[4 + 4 * grid + b * per + k] == (r << 24) | (mt * plan["tiles_n"] + nt)
+    taken = trace_items(trace.cpu().numpy().astype(np.uint32), grid, 0)
+    check_each_item_once(taken, plan["L"], plan["T"])
+    check_rs_fold_order(taken, 2, plan["T"])
 
 
 @pytest.mark.parametrize("variant", [dict(), dict(reduce_mode=1), dict(reduce_mode=2, block_n=256),
@@ -268,15 +265,20 @@ def test_rs_e4m3(variant, integer):
         assert_within_tol(case.result(), case.oracle(), "e4m3")
 
 
-def test_rs_e4m3_full_size_sampled_and_deterministic():
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_e4m3_full_size_full_output_and_deterministic(integer):
     wl = wls.WORKLOADS["rs_fp8_w8"]
-    inp = wls.make_inputs(wl, integer=False)
+    inp = wls.make_inputs(wl, integer=integer)
     case = RSCase(inp, opts=opts(scale_a=inp.scale_a, scale_b=inp.scale_b))
     tdx.check(case.run())
     status_ok(case)
-    rows = sample_rows(wl.M, wl.M // wl.W)
     first = case.result_bits()
-    assert_within_tol(R.decode_bf16(first[rows]), case.oracle(rows), "e4m3")
+    want = case.oracle()
+    assert want.shape == first.shape == (wl.M, wl.N)
+    if integer:
+        assert_bit_exact(first, want, "bf16")
+    else:
+        assert_within_tol(R.decode_bf16(first), want, "e4m3")
     tdx.check(case.run(opts(scale_a=inp.scale_a, scale_b=inp.scale_b, perturb_seed=3)))
     assert np.array_equal(case.result_bits(), first)
 

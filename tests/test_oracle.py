@@ -491,24 +491,77 @@ def test_integer_mode_is_exact_at_config_magnitudes():
 
 # ------------------------------------------------------------------ bookkeeping definitions
 
-def test_schedules_are_permutations_in_arrival_order():
-    W, M_local, chunk = 8, 1024, 128
-    order = R.ag_chunk_release_order(W, M_local, chunk, self_rank=3)
-    assert sorted(order) == [(r, c) for r in range(W) for c in range(M_local // chunk)]
-    assert [r for r, _ in order[:M_local // chunk]] == [4] * (M_local // chunk)
-    assert order[-1] == (3, M_local // chunk - 1)
-    sched = R.ag_tile_schedule(W, M_local, 3584, 128, 256, self_rank=3)
-    assert sorted(sched) == [(m, n) for m in range(64) for n in range(14)]
-    assert sched[0] == (24, 0) and sched[13] == (24, 13) and sched[14] == (25, 0)
-    assert sched[8 * 14] == (32, 0)
-    rs = R.rs_item_schedule(8, 8192, 8192, 128, 256)
-    assert len(rs) == 8 * 64 * 32 and rs[0] == (0, 0, 0) and rs[2048] == (1, 0, 0)
+def _check_release_order(order, W, M_local, chunk, self_rank):
+    """What the pages fix about the producer's order, as invariants: every chunk exactly once,
+    ranks in ring order from self+1 with the local shard last, chunks ascending within a rank."""
+    n = M_local // chunk
+    assert sorted(order) == [(r, c) for r in range(W) for c in range(n)]
+    ranks = [order[i * n][0] for i in range(W)]
+    assert ranks[-1] == self_rank
+    assert all((b - a) % W == 1 for a, b in zip(ranks, ranks[1:]))
+    for i in range(W):
+        assert [c for _, c in order[i * n:(i + 1) * n]] == list(range(n))
+        assert len({r for r, _ in order[i * n:(i + 1) * n]}) == 1
+
+
+@pytest.mark.parametrize("W,M_local,chunk,self_rank", [(8, 1024, 128, 3), (8, 16, 16, 0), (2, 64, 32, 1),
+                                                       (5, 96, 32, 4), (1, 128, 64, 0)])
+def test_chunk_release_order_invariants(W, M_local, chunk, self_rank):
+    _check_release_order(R.ag_chunk_release_order(W, M_local, chunk, self_rank), W, M_local, chunk, self_rank)
+
+
+def test_arrival_order_matches_release_order():
+    # the consumer takes the ranks in the order their rows become available: its own shard first
+    # (read in place), then the peers in the producer's release order
+    for W in (1, 2, 5, 8, 16):
+        for s in range(W):
+            arr = R.ag_arrival_rank_order(W, s)
+            assert sorted(arr) == list(range(W)) and arr[0] == s
+            rel = R.ag_chunk_release_order(W, 4 * W, 4, s)
+            peers = [r for i, (r, c) in enumerate(rel) if c == 0 and r != s]
+            assert arr[1:] == peers
+
+
+def test_consumer_order_check():
+    W, M_local = 4, 256
+    # any raster inside a rank is accepted: rows of rank 2 (self) in any order, then 3, 0, 1
+    ok = [600, 512, 700, 768, 1000, 0, 100, 300]
+    assert R.ag_consumer_order_ok(ok, W, M_local, self_rank=2)
+    # going back to an earlier rank, or starting with a peer, is rejected
+    assert not R.ag_consumer_order_ok([512, 768, 600], W, M_local, self_rank=2)
+    assert not R.ag_consumer_order_ok([0, 512], W, M_local, self_rank=2)
+    # a block whose first row is in rank 0 counts as rank 0's (the tiny config: one 128-row tile
+    # covers both 64-row shards)
+    assert R.ag_consumer_order_ok([0], 2, 64, self_rank=1)
+    assert R.ag_consumer_order_ok([], 8, 1024, self_rank=5)
+
+
+def test_fold_order_and_flags():
+    for W in (1, 2, 8, 16):
+        f = R.rs_fold_order(W)
+        assert f == sorted(f) and f[0] == 0 and len(set(f)) == W == len(f)
+    # the fold order decides the fp32 bits: the left fold of these partials in rank order differs
+    # from the reverse order, so a fixed order is what makes the result identical run to run
+    p = np.array([2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)], dtype=np.float32)
+    fwd = np.float32(0)
+    for r in R.rs_fold_order(4):
+        fwd = np.float32(fwd + p[r])
+    rev = np.float32(0)
+    for r in reversed(R.rs_fold_order(4)):
+        rev = np.float32(rev + p[r])
+    assert fwd != rev
     assert np.array_equal(R.expected_flags(3, 7), np.array([7, 7, 7], dtype=np.uint32))
 
 
-def test_tiny_schedule_tile_spans_ranks():
-    # tiny config: one 128-row M-tile covers both 64-row shards
-    assert R.ag_tile_schedule(2, 64, 256, 128, 256, self_rank=1) == [(0, 0)]
+def test_planted_order_mistakes_are_caught():
+    W, M_local, chunk, s = 8, 256, 128, 3
+    good = R.ag_chunk_release_order(W, M_local, chunk, s)
+    self_first = [(s, c) for c in range(2)] + [x for x in good if x[0] != s]
+    reversed_ring = sorted(good, key=lambda rc: ((s - rc[0]) % W == 0, (s - rc[0]) % W, rc[1]))
+    chunks_descending = [(r, 1 - c) for r, c in good]
+    for bad in (self_first, reversed_ring, chunks_descending):
+        with pytest.raises(AssertionError):
+            _check_release_order(bad, W, M_local, chunk, s)
 
 
 # ------------------------------------------------------------------ planted mistakes
@@ -590,39 +643,6 @@ def test_planted_format_mistakes_are_caught():
 
 
 def test_oracle_package_exports():
-    for name in ["ag_gemm", "gemm_rs", "gemm_ar", "round_out", "ag_tile_schedule", "rs_item_schedule"]:
+    for name in ["ag_gemm", "gemm_rs", "gemm_ar", "round_out", "ag_chunk_release_order", "ag_arrival_rank_order",
+                 "ag_consumer_order_ok", "rs_fold_order"]:
         assert hasattr(oracle, name)
-
-
-def test_grouped_schedules():
-    # groups of 2 M-tiles: a permutation of all groups, keyed by the owner of the group's first row
-    g = R.ag_tile_schedule(8, 1024, 3584, 128, 256, self_rank=3, group=2)
-    assert sorted(g) == [(m, n) for m in range(32) for n in range(14)]
-    assert g[0] == (12, 0) and g[14] == (13, 0) and g[4 * 14] == (16, 0)
-    assert R.ag_tile_schedule(8, 1024, 3584, 128, 256, 5, group=1) == R.ag_tile_schedule(8, 1024, 3584, 128, 256, 5)
-    # the tiles taken by the two CTAs of a cluster cover the ungrouped schedule's tile set
-    tiles = sorted((2 * mg + r, nt) for mg, nt in g for r in range(2))
-    assert tiles == sorted(R.ag_tile_schedule(8, 1024, 3584, 128, 256, 3))
-    rs = R.rs_item_schedule(8, 8192, 8192, 128, 256, group=2)
-    assert len(rs) == 8 * 32 * 32 and rs[1024] == (1, 0, 0)
-
-
-def test_rs_schedule_n_groups():
-    s = R.rs_item_schedule(2, 256, 2560, 128, 256, group_n=4)    # 2 M-tiles, 10 N-tiles: groups 4, 4, 2
-    assert sorted(s) == sorted(R.rs_item_schedule(2, 256, 2560, 128, 256))
-    assert s[:9] == [(0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 0, 3), (0, 1, 0), (0, 1, 1), (0, 1, 2), (0, 1, 3), (0, 0, 4)]
-    assert s[16:20] == [(0, 0, 8), (0, 0, 9), (0, 1, 8), (0, 1, 9)] and s[20] == (1, 0, 0)
-    assert R.rs_item_schedule(3, 512, 512, 128, 256, group_n=8) == R.rs_item_schedule(3, 512, 512, 128, 256)
-
-
-def test_rs_schedule_rank_blocks():
-    # 2 ranks, 3 M-tiles x 2 N-tiles = 6 positions per rank, blocks of 4: positions 0-3 for ranks
-    # 0 and 1, then positions 4-5 for ranks 0 and 1
-    s = R.rs_item_schedule(2, 384, 512, 128, 256, rank_block=4)
-    order = [(m, n) for m in range(3) for n in range(2)]
-    want = [(r,) + order[p] for r in range(2) for p in range(4)] + [(r,) + order[p] for r in range(2) for p in range(4, 6)]
-    assert s == want
-    assert sorted(s) == sorted(R.rs_item_schedule(2, 384, 512, 128, 256))
-    # the running sum of a tile is always handed to the next rank later in the order
-    idx = {it: i for i, it in enumerate(R.rs_item_schedule(8, 8192, 8192, 128, 256, group=2, group_n=8, rank_block=148))}
-    assert all(idx[(r, m, n)] > idx[(r - 1, m, n)] for (r, m, n) in idx if r > 0)

@@ -11,8 +11,9 @@ This file is collected last on purpose, so that a run that stops at the first fa
 run every other test. It must pass both alone in a fresh process and after the other tests: the
 scratch array keeps the previous call's contents, and every call must clear what has to start at
 zero. Each case below checks the output of two calls in a row against the output of the existing
-tdx_ag_gemm entry point (with its own caller-owned workspace) on the same inputs, within the
-tolerance the parity tests use.
+tdx_ag_gemm entry point (with its own caller-owned workspace) on the same inputs: bit for bit on
+integer inputs (where both must equal the oracle's single rounding of the exact sum), otherwise
+within the tolerance the parity tests use.
 """
 import numpy as np
 import pytest
@@ -38,7 +39,7 @@ def _close(got_bits: np.ndarray, ref_bits: np.ndarray, out_dtype: str, dtype: st
 
 
 @pytest.mark.parametrize("name,integer", [("ag_small", False), ("ag_small", True), ("ag_tiny", False),
-                                          ("ag_fp8_small", False)])
+                                          ("ag_tiny", True), ("ag_fp8_small", False)])
 def test_noalloc_matches_existing_entry_point_twice(name, integer):
     if name == "ag_fp8_small":
         wl = wls.with_shape(wls.WORKLOADS["ag_fp8_w8"], W=4, M=64, K=1024, N=512, chunk_rows=64)
@@ -71,7 +72,11 @@ def test_noalloc_matches_existing_entry_point_twice(name, integer):
         torch.cuda.synchronize()
         assert int(status[0]) == tdx.TDX_OK, status.tolist()
         got = C.view(torch.int16).cpu().numpy().view(np.uint16) if out_dtype == "bf16" else C.cpu().numpy()
-        _close(got, ref, out_dtype, wl.dtype)
+        if integer:
+            assert np.array_equal(got, ref)
+            assert np.array_equal(got, R.round_out(ref_case.oracle(), out_dtype))
+        else:
+            _close(got, ref, out_dtype, wl.dtype)
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
