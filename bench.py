@@ -315,6 +315,24 @@ class Step:
                 raise RuntimeError(f"device status {self.tdx.tdx_status_string(st)} {detail}")
 
 
+def time_interleaved(torch, fns: dict, reps: int) -> dict:
+    """Median per-call CUDA-event time (ms) of each fn in `fns`, the calls taken in turn (a, b, c,
+    a, b, c, ...), so that every variant runs under the same clock and power state; a variant timed
+    in a block of its own would see the power cap ramp in differently."""
+    s = torch.cuda.current_stream()
+    ts = {k: [] for k in fns}
+    for _ in range(reps):
+        for k, fn in fns.items():
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            e1.synchronize()
+            ts[k].append(e0.elapsed_time(e1))
+    return {k: statistics.median(v) for k, v in ts.items()}
+
+
 def time_mode(torch, fn, reps: int):
     """Median of per-call CUDA-event times of fn() on the current stream (ms)."""
     s = torch.cuda.current_stream()
@@ -356,6 +374,7 @@ def ag_case(tdx, torch, wl, dev, integer=False):
         st, d = tdx.tdx_read_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    status.reset = lambda: tdx.check(tdx.tdx_workspace_init(ws))
     return call, status
 
 
@@ -380,6 +399,7 @@ def rs_case(tdx, torch, wl, dev, **kw):
         st, d = tdx.tdx_read_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    status.reset = lambda: tdx.check(tdx.tdx_workspace_init(ws))
     return call, status
 
 
@@ -410,6 +430,7 @@ def moe_case(tdx, torch, wl, dev):
         st, d = tdx.tdx_read_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    status.reset = lambda: tdx.check(tdx.tdx_workspace_init(ws))
     return call, status
 
 
@@ -437,13 +458,18 @@ def combine_case(tdx, torch, wl, dev):
         st, d = tdx.tdx_read_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {tdx.tdx_status_string(st)} {d}")
+    status.reset = lambda: tdx.check(tdx.tdx_workspace_init(ws))
     return call, status
 
 
-def graph_time_us(torch, fn, reps: int = 50):
+def graph_time_us(torch, fn, reps: int = 50, reset=None):
     """GPU time per call (us) of fn captured in a CUDA graph of `reps` back-to-back calls (no host
-    submission cost inside the timed region); None if the call cannot be captured."""
+    submission cost inside the timed region); None if the call cannot be captured. fn makes its
+    call with device-kept epochs (nothing cleared between calls); `reset` re-initialises the
+    workspace first, since the eager calls before used host epochs."""
     try:
+        if reset is not None:
+            reset()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -577,7 +603,7 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
         call()
     f = time_mode(torch, call, reps)
     m = time_mode(torch, lambda: call(mode=2), reps)
-    gus = graph_time_us(torch, lambda: call(epoch=0))
+    gus = graph_time_us(torch, lambda: call(epoch=tdx.TDX_EPOCH_DEVICE), reset=status.reset)
     status()
     byt = wl.E * wl.K * wl.N + 2 * wl.M_total * wl.K + wl.M_total * wl.N * 2   # weights, dispatch r+w, Y
     t_us = gus or 1e3 * f
@@ -602,7 +628,7 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     for _ in range(5):
         call()
     f = time_mode(torch, call, reps)
-    gus = graph_time_us(torch, lambda: call(epoch=0))
+    gus = graph_time_us(torch, lambda: call(epoch=tdx.TDX_EPOCH_DEVICE), reset=status.reset)
     status()
     byt = wl.E * wl.K * wl.N * 2 + 2 * wl.M_total * wl.K * 2 + wl.M_total * wl.N * 2   # weights, dispatch r+w, Y
     t_us = gus or 1e3 * f
@@ -614,7 +640,7 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     for _ in range(5):
         call()
     f = time_mode(torch, call, reps)
-    gus = graph_time_us(torch, lambda: call(epoch=0))   # epoch 0: flags cleared inside the graph
+    gus = graph_time_us(torch, lambda: call(epoch=tdx.TDX_EPOCH_DEVICE), reset=status.reset)
     status()
     wl = W["ag_small"]
     byt = wl.W * wl.M * wl.K * 2 * 2 + wl.K * wl.N * 2 + wl.W * wl.M * wl.N * 2   # move r+w, B, C
@@ -626,7 +652,7 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     for _ in range(5):
         call()
     f = time_mode(torch, call, reps)
-    gus = graph_time_us(torch, lambda: call(epoch=0))
+    gus = graph_time_us(torch, lambda: call(epoch=tdx.TDX_EPOCH_DEVICE), reset=status.reset)
     status()
     wl = W["rs_small"]
     byt = wl.W * (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 2
@@ -695,12 +721,15 @@ def run_gpu(args):
 
     # overlap efficiency: fused vs GEMM-alone and movement-alone of the same kernel
     reps = max(5, min(20, args.steps))
-    t_ag_f = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_FUSED)), reps)
-    t_ag_g = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_GEMM_ONLY)), reps)
-    t_ag_m = time_mode(torch, lambda: tdx.check(st.ag(tdx.TDX_MOVE_ONLY)), reps)
-    t_rs_f = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_FUSED)), reps)
-    t_rs_g = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_GEMM_ONLY)), reps)
-    t_rs_m = time_mode(torch, lambda: tdx.check(st.rs(tdx.TDX_MOVE_ONLY)), reps)
+    with ClockSampler(local) as clk_modes:
+        t = time_interleaved(torch, {"f": lambda: tdx.check(st.ag(tdx.TDX_FUSED)),
+                                     "g": lambda: tdx.check(st.ag(tdx.TDX_GEMM_ONLY)),
+                                     "m": lambda: tdx.check(st.ag(tdx.TDX_MOVE_ONLY))}, 2 * reps)
+        t_ag_f, t_ag_g, t_ag_m = t["f"], t["g"], t["m"]
+        t = time_interleaved(torch, {"f": lambda: tdx.check(st.rs(tdx.TDX_FUSED)),
+                                     "g": lambda: tdx.check(st.rs(tdx.TDX_GEMM_ONLY)),
+                                     "m": lambda: tdx.check(st.rs(tdx.TDX_MOVE_ONLY))}, reps)
+        t_rs_f, t_rs_g, t_rs_m = t["f"], t["g"], t["m"]
     st.status()
 
     # stall-on-flag: one traced fused AllGather call; the kernel's trace holds, per CTA, the TMA
@@ -722,7 +751,7 @@ def run_gpu(args):
     st.status()
     tr = trace.cpu().numpy().view(np.uint32)
     g_ag = int(tr[0])
-    per_cta = tr[4:4 + 4 * g_ag].reshape(g_ag, 4).astype(np.float64)
+    per_cta = tr[4:4 + 8 * g_ag].reshape(g_ag, 8).astype(np.float64)
     flag_wait = {"mean_us": float(per_cta[:, 0].mean() / 1e3), "max_us": float(per_cta[:, 0].max() / 1e3),
                  "tiles_that_waited_per_cta": float(per_cta[:, 1].mean())}
 
@@ -841,7 +870,9 @@ def run_gpu(args):
                        "stall_on_flag_us_per_cta": {"mean": flag_wait["mean_us"], "max": flag_wait["max_us"]}}
     line["gemm_rs"] = {"tflops": achieved, "ms": ms_rs, "frac_of_peak": achieved / peak_tf,
                        "ms_fused": t_rs_f, "ms_gemm_only": t_rs_g, "ms_move_only": t_rs_m,
-                       "overlap_efficiency": max(t_rs_g, t_rs_m) / t_rs_f}
+                       "overlap_efficiency": max(t_rs_g, t_rs_m) / t_rs_f,
+                       "modes_timed": "interleaved fused / GEMM alone / movement alone, median",
+                       "modes_clocks": clk_modes.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -874,12 +905,38 @@ def run_case(args):
     st.status()
     ms = time_mode(torch, lambda: tdx.check(fn()), 5)
     fl = inp.wl.flops
-    gus = graph_time_us(torch, lambda: fn(epoch=0))
+    gus_clear = graph_time_us(torch, lambda: fn(epoch=0))
+    ws = st.ws_ag if args.case == "ag" else st.ws_rs
+    gus = graph_time_us(torch, lambda: fn(epoch=tdx.TDX_EPOCH_DEVICE),
+                        reset=lambda: tdx.check(tdx.tdx_workspace_init(ws)))
     plan = tdx.tdx_plan_info(tdx.OP_AG if args.case == "ag" else tdx.OP_RS, W, M, K, N, tdx.TDX_BF16,
                              tdx.make_opts(chunk_rows=min(128, M), **extra) if args.case == "ag" else tdx.make_opts(**extra))
+    # one traced call: per-CTA phase stamps (median / max over CTAs, us from the first CTA's entry)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    items = plan["L"] * plan["T"]
+    chunks = W * plan["n_chunks"] if args.case == "ag" else 0
+    trace = torch.zeros(max(tdx.tdx_trace_size(g, items, chunks) // 4 for g in range(1, n_sm + 1)),
+                        dtype=torch.int32, device=dev)
+    tdx.check(tdx.tdx_workspace_init(ws))
+    saved = st.extra
+    st.extra = dict(saved, trace=trace)
+    tdx.check(fn(epoch=0))
+    st.extra = saved
+    torch.cuda.synchronize()
+    st.status()
+    tr = trace.cpu().numpy().view(np.uint32)
+    g = int(tr[0])
+    stv = tr[4:4 + 8 * g].reshape(g, 8).astype(np.int64)
+    t0 = stv[:, 4].min()
+    rel = lambda col: ((stv[:, col] - t0) % (1 << 32)) / 1e3
+    phases = {}
+    for name, col in (("entry", 4), ("first_load", 5), ("mma_done", 6), ("epilogue_done", 7)):
+        v = rel(col) if col != 6 else rel(col)[stv[:, 6] != 0]
+        phases[name] = [round(float(np.median(v)), 2), round(float(np.max(v)), 2)] if len(v) else None
     print(json.dumps({"case": args.case, "shape": [W, M, K, N], "opts": extra, "ms": ms, "us_gpu_graph": gus,
-                      "tflops": fl / (ms * 1e-3) / 1e12,
-                      "plan": {k: plan[k] for k in ("BN", "L", "T", "reduce_mode", "cluster")}}))
+                      "us_gpu_graph_clearing": gus_clear, "tflops": fl / (ms * 1e-3) / 1e12,
+                      "phases_us_median_max": phases,
+                      "plan": {k: plan[k] for k in ("BN", "L", "T", "reduce_mode", "cluster", "coop_fold")}}))
     return 0
 
 

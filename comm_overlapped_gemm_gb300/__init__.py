@@ -22,6 +22,7 @@ TDX_BF16, TDX_FP8_E4M3, TDX_FP32 = 0, 1, 2
 TDX_FUSED, TDX_GEMM_ONLY, TDX_MOVE_ONLY, TDX_CONSUMER_ONLY = 0, 1, 2, 3
 TDX_PRODUCER_SM, TDX_PRODUCER_COPY_ENGINE = 0, 1
 OP_AG, OP_RS, OP_AR = 0, 1, 2
+TDX_EPOCH_DEVICE = 0xFFFFFFFF
 
 EXPORTED = ["tdx_opts_default", "tdx_workspace_size", "tdx_workspace_init", "tdx_ag_gemm", "tdx_gemm_rs",
             "tdx_read_device_status", "tdx_trace_size", "tdx_status_string", "tdx_version", "tdx_plan_info",

@@ -60,8 +60,9 @@ struct Plan {
   int group_n = 1;
   int rank_block = 1;    // RS: positions (in tile groups) per rank block
   int pull_a = 0;        // AG: tiles of whole small shards read A straight from the shards
-  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, off_tile_done = 0, ctrl_end = 0;
-  int coop = 0;          // slotted fold: 0 last arriver, 1 cooperative (see make_plan)
+  size_t off_chunk_flags = 0, off_chunk_cnt = 0, off_chain_flags = 0, off_tile_cnt = 0, off_tile_done = 0;
+  size_t off_grid_bar = 0, ctrl_end = 0;
+  int coop = 0;          // slotted fold: 0 last arriver, 1 per-tile cooperative, 2 grid-wide (see make_plan)
   size_t off_G = 0, off_S = 0, total = 0;
 };
 
@@ -141,11 +142,15 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   // multicast loads) is not offered: every CTA loads only into its own shared memory.
   if (o.cluster < 0 || o.cluster > 3) return TDX_ERR_INVALID_ARG;
   if (o.cluster == 2) return TDX_ERR_UNSUPPORTED;
+  if (o.reduce_mode < 0 || o.reduce_mode > 3) return TDX_ERR_INVALID_ARG;
+  // the grid-wide fold runs on single CTAs
+  if (o.reduce_mode == 3 && o.cluster == 3 && L > 1) return TDX_ERR_UNSUPPORTED;
   const bool pair_ok = bn == 256 && p.tiles_m % 2 == 0 && p.tiles_m > 0;
   if (o.cluster == 3) {
     if (!pair_ok) return TDX_ERR_UNSUPPORTED;
     p.PM = 2;
-  } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs) {
+  } else if (o.cluster == 0 && pair_ok && static_cast<long long>(L) * p.T >= 4 * kRefSMs &&
+             !(o.reduce_mode == 3 && L > 1)) {
     p.PM = 2;
   }
   p.CL = p.PM == 0 ? 1 : 2;
@@ -159,15 +164,15 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   p.pull_a = (op == OP_AG && p.PM == 0 && Mx > 0 && Mx < kBM && kBM % Mx == 0 && Mx % 8 == 0) ? 1 : 0;
   // reduction of the L chain elements: slotted when a tile's elements run concurrently (K splits;
   // ReduceScatter with fewer than two waves of tiles per rank), else chained through one buffer
-  if (o.reduce_mode < 0 || o.reduce_mode > 2) return TDX_ERR_INVALID_ARG;
   if (o.bf16_partials < 0 || o.bf16_partials > 1) return TDX_ERR_INVALID_ARG;
   // bf16 partials: a rank's partial is rounded before the fold, which the slotted reduction does
-  // (a chained running sum would be rounded at every hand-over instead)
-  if (o.bf16_partials && (op != OP_RS || o.reduce_mode == 1)) return TDX_ERR_UNSUPPORTED;
+  // (a chained running sum would be rounded at every hand-over instead); the grid-wide fold reads
+  // fp32 slots only
+  if (o.bf16_partials && (op != OP_RS || o.reduce_mode == 1 || o.reduce_mode == 3)) return TDX_ERR_UNSUPPORTED;
   p.bf16_partials = o.bf16_partials;
   if (L > 1) {
     if (o.reduce_mode == 1) p.reduce_last = 0;
-    else if (o.reduce_mode == 2 || p.bf16_partials) p.reduce_last = 1;
+    else if (o.reduce_mode >= 2 || p.bf16_partials) p.reduce_last = 1;
     else p.reduce_last = (op == OP_AG || p.T < 2 * kRefSMs) ? 1 : 0;
   }
   // slotted ReduceScatter may take a rank-inner order (blocks of one position) instead
@@ -181,10 +186,16 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   // deferred fold tasks, measured slower on the small-M ReduceScatter than the last arriver: with
   // the rank-outer order the tiles complete only at the end, while the last arriver's slots are
   // still in L2.)
+  // Grid-wide fold (coop 2): when the work takes several waves but there are fewer tiles than CTAs,
+  // the last arrivers of the few tiles would fold them alone at the end while the other CTAs idle.
+  // Instead every CTA, once it has stored all its partials, arrives at a grid barrier (all CTAs are
+  // resident: a cooperative launch), and then folds 1/grid of every tile's (row, 32-column) units.
   if (p.reduce_last && p.PM == 0 && !p.bf16_partials && L > 1) {
     int sms = device_sms();
     if (o.num_sms > 0 && (sms == 0 || o.num_sms < sms)) sms = o.num_sms;
-    if (sms > 0 && static_cast<long long>(L) * p.T <= sms) p.coop = 1;
+    if (o.reduce_mode == 3) p.coop = 2;
+    else if (sms > 0 && static_cast<long long>(L) * p.T <= sms) p.coop = 1;
+    else if (sms > 0 && p.T < sms) p.coop = 2;
   }
   // workspace layout
   size_t off = kHeaderBytes;
@@ -199,6 +210,8 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
   off += static_cast<size_t>(p.reduce_last ? p.T : 0) * 4;
   p.off_tile_done = off;   // cooperative fold: elements done folding per tile (reset by the last)
   off += static_cast<size_t>(p.reduce_last ? p.T : 0) * 4;
+  p.off_grid_bar = off;    // grid-wide fold: CTAs arrived, CTAs departed (reset by the last to depart)
+  off += p.reduce_last ? 8 : 0;
   off = align_up(off, 1024);
   p.ctrl_end = off;
   if (op == OP_AG) {
@@ -299,10 +312,12 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.sbuf = pl.L > 1 ? reinterpret_cast<float*>(ws + pl.off_S) : nullptr;
   kp.tile_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_tile_cnt);
   kp.tile_done = reinterpret_cast<uint32_t*>(ws + pl.off_tile_done);
+  kp.grid_bar = reinterpret_cast<uint32_t*>(ws + pl.off_grid_bar);
   kp.coop_fold = pl.coop;
   kp.reduce_last = pl.reduce_last;
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;
+  kp.dev_epoch = o.epoch == TDX_EPOCH_DEVICE ? reinterpret_cast<uint32_t*>(ws) + kDevEpochWord : nullptr;
   kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
   kp.perturb = o.perturb_seed;
   kp.mode = o.mode;
@@ -653,7 +668,7 @@ tdx_status tdx_ag_gemm_noalloc(const void* const* shards, const void* B, void* C
 size_t tdx_trace_size(int grid, int items, int chunks) {
   if (grid <= 0 || items < 0 || chunks < 0) return 0;
   const size_t per_cta = (static_cast<size_t>(items) + grid - 1) / grid;
-  return 4 * (4 + 4 * static_cast<size_t>(grid) + 1 + static_cast<size_t>(chunks) +
+  return 4 * (4 + kTraceStatWords * static_cast<size_t>(grid) + 1 + static_cast<size_t>(chunks) +
               static_cast<size_t>(grid) * per_cta);
 }
 
@@ -906,6 +921,7 @@ tdx_status tdx_moe_gemm_combine(const void* Hd, const int32_t* const* topk_idx, 
   kp.status = reinterpret_cast<uint32_t*>(ws);
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = o.epoch == 0 ? 1u : o.epoch;
+  kp.dev_epoch = o.epoch == TDX_EPOCH_DEVICE ? reinterpret_cast<uint32_t*>(ws) + kDevEpochWord : nullptr;
   kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
   kp.perturb = o.perturb_seed;
   kp.row_bytes = static_cast<long long>(F) * 2;
@@ -1017,6 +1033,7 @@ tdx_status tdx_moe_dispatch_gemm(const void* const* X, const int32_t* const* top
   kp.chunk_cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   kp.trace = static_cast<uint32_t*>(o.trace);
   kp.epoch = epoch;
+  kp.dev_epoch = o.epoch == TDX_EPOCH_DEVICE ? reinterpret_cast<uint32_t*>(ws) + kDevEpochWord : nullptr;
   kp.timeout_ns = o.timeout_ns == 0 ? 2000000000ull : o.timeout_ns;
   kp.perturb = o.perturb_seed;
   kp.row_bytes = static_cast<long long>(H) * pl.elt;

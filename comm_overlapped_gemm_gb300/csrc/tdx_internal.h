@@ -61,9 +61,13 @@ enum Mode { MODE_FUSED = 0, MODE_GEMM_ONLY = 1, MODE_MOVE_ONLY = 2, MODE_CONSUME
 enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4, ROLE_LAYOUT = 5 };
 enum DevStatus { DEV_OK = 0, DEV_BAD_INPUT = 1, DEV_TIMEOUT = 6, DEV_STALE = 7 };
 
-// Word offsets in the workspace header (first 4 KiB).
+// Word offsets in the workspace header (first 4 KiB): the status word and its details, then the
+// device-kept epoch (the last completed call's epoch) and the count of CTAs that finished this call.
 constexpr size_t kHeaderBytes = 4096;
 constexpr int kStatusWords = 8;
+constexpr int kDevEpochWord = 16;
+// Trace: statistics words per CTA (see tdx_trace_size in include/tdx.h).
+constexpr int kTraceStatWords = 8;
 
 struct KParams {
   CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard (pull mode: shard r). RS: A_r
@@ -78,8 +82,10 @@ struct KParams {
   float* sbuf;                   // chained: [T][kBM*BN] running sum; slotted: [L][T][kBM*BN] partials
   uint32_t* tile_cnt;            // slotted: partials stored per tile (reset by the last arriver)
   uint32_t* tile_done;           // cooperative fold: elements that folded their share (reset by the last)
+  uint32_t* grid_bar;            // grid-wide fold: [0] CTAs arrived, [1] CTAs departed (reset by the last)
   int coop_fold;                 // slotted fold: 0 the last arriver folds the tile, 1 the L elements
-                                 // of a tile fold 1/L each after all arrived (one wave of work)
+                                 // of a tile fold 1/L each after all arrived (one wave of work),
+                                 // 2 every CTA folds 1/grid of all tiles after a grid barrier
   int reduce_last;               // 1 = slotted (last arriver folds), 0 = chained running sum
   uint32_t* trace;               // optional
   int trace_chunks;              // chunk flags this call releases (size of the trace's producer section)
@@ -111,7 +117,8 @@ struct KParams {
   const float* moe_gates[kMaxW]; // MoE combine: [W] T x k gate weights
   uint32_t* moe_cnt;             // MoE combine: arrivals per (token, N-tile), reset by the last
   float moe_bscale[kMoeMaxExperts];   // MoE e4m3: per-expert weight scale (row_scale: per source rank)
-  uint32_t epoch;
+  uint32_t epoch;                // this call's epoch (unused when dev_epoch is set)
+  uint32_t* dev_epoch;           // device-kept epochs: [0] last completed call's epoch, [1] CTAs done
   uint64_t timeout_ns;
   uint32_t perturb;
   int piece_bytes;               // producer copy unit (multiple of kCopyRoundBytes)

@@ -293,7 +293,7 @@ __device__ __forceinline__ uint32_t perturb_hash(uint32_t seed, uint32_t x) {
 // index in word 1 + k of the trace's producer section; word 0 of the section counts the releases and
 // must be zero when the call starts.
 __device__ __forceinline__ void trace_release(const KParams& p, int grid, uint32_t fi) {
-  uint32_t* rel = p.trace + 4 + 4 * grid;
+  uint32_t* rel = p.trace + 4 + kTraceStatWords * grid;
   const uint32_t k = atomicAdd(rel, 1u);
   if (k < static_cast<uint32_t>(p.trace_chunks)) rel[1 + k] = fi;
 }
@@ -370,20 +370,20 @@ static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* 
 
 // Bounded acquire-wait until *flag == epoch. A value above the epoch is a stale flag. Also gives
 // up when any CTA has already recorded an error (status word != 0) or this CTA aborted.
-static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* flag, uint32_t role,
+static __device__ __noinline__ bool wait_flag(const KParams& p, uint32_t epoch, const uint32_t* flag, uint32_t role,
                                        uint32_t idx, volatile int* abort_flag, uint64_t* waited_ns) {
   uint32_t v = ld_acquire_gpu(flag);
-  if (v == p.epoch) return true;
+  if (v == epoch) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (v > p.epoch) {
-      report_error(p, DEV_STALE, role, idx, v, p.epoch);
+    if (v > epoch) {
+      report_error(p, DEV_STALE, role, idx, v, epoch);
       *abort_flag = 1;
       return false;
     }
     __nanosleep(32);
     v = ld_acquire_gpu(flag);
-    if (v == p.epoch) {
+    if (v == epoch) {
       *waited_ns += globaltimer_ns() - t0;
       return true;
     }
@@ -394,7 +394,7 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
         return false;
       }
       if (globaltimer_ns() - t0 > p.timeout_ns) {
-        report_error(p, DEV_TIMEOUT, role, idx, v, p.epoch);
+        report_error(p, DEV_TIMEOUT, role, idx, v, epoch);
         *abort_flag = 1;
         return false;
       }
@@ -406,8 +406,8 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const uint32_t* 
 // independent relaxed loads (one round trip for all of them, not one per flag), then a single
 // acquire fence orders the data reads after them. Stale values and timeouts are reported like
 // wait_flag's, for the first chunk not yet released.
-static __device__ __noinline__ bool wait_flags_all(const KParams& p, int gc0, int gc1, volatile int* abort_flag,
-                                                   uint64_t* waited_ns) {
+static __device__ __noinline__ bool wait_flags_all(const KParams& p, uint32_t epoch, int gc0, int gc1,
+                                                   volatile int* abort_flag, uint64_t* waited_ns) {
   constexpr int kBatch = 16;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
@@ -416,15 +416,15 @@ static __device__ __noinline__ bool wait_flags_all(const KParams& p, int gc0, in
     for (int b = gc0; b <= gc1 && pending < 0; b += kBatch) {
       uint32_t v[kBatch];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) v[j] = (b + j <= gc1) ? ld_relaxed_gpu(p.chunk_flags + b + j) : p.epoch;
+      for (int j = 0; j < kBatch; ++j) v[j] = (b + j <= gc1) ? ld_relaxed_gpu(p.chunk_flags + b + j) : epoch;
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        if (v[j] > p.epoch) {
-          report_error(p, DEV_STALE, ROLE_FLAG, b + j, v[j], p.epoch);
+        if (v[j] > epoch) {
+          report_error(p, DEV_STALE, ROLE_FLAG, b + j, v[j], epoch);
           *abort_flag = 1;
           return false;
         }
-        if (pending < 0 && v[j] != p.epoch) {
+        if (pending < 0 && v[j] != epoch) {
           pending = b + j;
           seen = v[j];
         }
@@ -444,7 +444,7 @@ static __device__ __noinline__ bool wait_flags_all(const KParams& p, int gc0, in
         return false;
       }
       if (globaltimer_ns() - t0 > p.timeout_ns) {
-        report_error(p, DEV_TIMEOUT, ROLE_FLAG, pending, seen, p.epoch);
+        report_error(p, DEV_TIMEOUT, ROLE_FLAG, pending, seen, epoch);
         *abort_flag = 1;
         return false;
       }
@@ -660,6 +660,57 @@ __device__ __forceinline__ void fold_part(const KParams& p, int tile, int part, 
   }
 }
 
+// Fixed-order fold ((P_0 + P_1) + P_2) + ... of the L fp32 partial slots of one unit of tile `tile`:
+// row i of the tile, columns col0..col0+31 (col0 a multiple of 32), two slots' loads in flight at a
+// time; rounded once and stored. A warp's 32 lanes take 32 consecutive rows, so every load of the
+// slot layout is 512 contiguous bytes.
+template <int OP, bool FP8, int BN>
+__device__ __forceinline__ void fold_unit_fp32(const KParams& p, int tile, int col0, int i, uint64_t pol) {
+  const size_t off = ((size_t)(col0 >> 5) * 8 * kBM + i) * 4;
+  const size_t slot = (size_t)p.T * (kBM * BN);
+  const float* s0p = p.sbuf + (size_t)tile * (kBM * BN) + off;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 s = ld_cg_f4_hint(s0p + j * kBM * 4, pol);
+    v[4 * j + 0] = s.x;
+    v[4 * j + 1] = s.y;
+    v[4 * j + 2] = s.z;
+    v[4 * j + 3] = s.w;
+  }
+  int c = 1;
+#pragma unroll 1
+  for (; c + 1 < p.L; c += 2) {
+    const float* sp0 = s0p + (size_t)c * slot;
+    const float* sp1 = sp0 + slot;
+    float4 a0[8], a1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      a0[j] = ld_cg_f4_hint(sp0 + j * kBM * 4, pol);
+      a1[j] = ld_cg_f4_hint(sp1 + j * kBM * 4, pol);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[4 * j + 0] = (v[4 * j + 0] + a0[j].x) + a1[j].x;
+      v[4 * j + 1] = (v[4 * j + 1] + a0[j].y) + a1[j].y;
+      v[4 * j + 2] = (v[4 * j + 2] + a0[j].z) + a1[j].z;
+      v[4 * j + 3] = (v[4 * j + 3] + a0[j].w) + a1[j].w;
+    }
+  }
+  if (c < p.L) {
+    const float* sp = s0p + (size_t)c * slot;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a = ld_cg_f4_hint(sp + j * kBM * 4, pol);
+      v[4 * j + 0] = v[4 * j + 0] + a.x;
+      v[4 * j + 1] = v[4 * j + 1] + a.y;
+      v[4 * j + 2] = v[4 * j + 2] + a.z;
+      v[4 * j + 3] = v[4 * j + 3] + a.w;
+    }
+  }
+  store_out_chunk<OP, FP8>(p, (tile / p.tiles_n) * kBM + i, (tile % p.tiles_n) * BN + col0, v, pol);
+}
+
 // MoE combine, one warp: `count` units taken first, first + stride, ...; a unit is one token of the
 // shared task list `tasks` at columns [col0, col0 + BN), or, without a list, the (token, N-tile)
 // pair of index idx = token * tiles_n + N-tile. Units go two at a time (half h of the warp holds
@@ -815,7 +866,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] TMA k-blocks issued, misc[3] MMA k-blocks
-  // consumed, misc[4] epilogue go/stop decision, misc[5] epilogue "last arriver" decision
+  // consumed, misc[4] epilogue go/stop decision, misc[5] epilogue "last arriver" decision, misc[6]
+  // MoE combine task count, misc[7] this call's epoch
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   // MoE dispatch: staging barriers after the row-source table, staging ring 128-byte aligned after them
   uint64_t* stg_bars = reinterpret_cast<uint64_t*>(misc + 16 + kBM);
@@ -829,8 +881,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t t_entry = globaltimer_ns();
 
   if (threadIdx.x == 0) {
+    // device-kept epochs: the workspace holds the last completed call's epoch (every CTA reads it
+    // before any CTA of this call can have finished, so all agree)
+    misc[7] = p.dev_epoch != nullptr ? ld_relaxed_gpu(p.dev_epoch) + 1u : p.epoch;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -871,6 +927,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
+  const uint32_t epoch = misc[7];
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const bool leader = crank == 0;           // PM 2: the CTA that issues the pair's MMAs
   const int cid = blockIdx.x / CL;          // cluster index
@@ -912,6 +969,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       const uint64_t keep = policy_of(TDX_OPERAND_POLICY);   // operand tiles are re-read by other tiles
       uint64_t flag_ns = 0;
       uint32_t n_waits = 0;
+      uint64_t t_first = 0;
       bool stop = false;
       for (int it = cid; it < items && !stop; it += ncl) {
         if (*abort_flag) break;
@@ -944,7 +1002,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               const int gc0 = w.m0 / p.chunk_rows;
               const int gc1 = last_row / p.chunk_rows;
               ++n_waits;
-              if (!wait_flags_all(p, gc0, gc1, abort_flag, &flag_ns)) break;
+              if (!wait_flags_all(p, epoch, gc0, gc1, abort_flag, &flag_ns)) break;
               fence_proxy_async_global();
             }
           }
@@ -956,7 +1014,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             // past the expert's end are loaded too but never stored, so their chunk is not awaited
             if (p.perturb) __nanosleep(perturb_hash(p.perturb, it) & 4095u);
             ++n_waits;
-            if (!wait_flags_all(p, w.m0 / kBM, (w.mend - 1) / kBM, abort_flag, &flag_ns)) break;
+            if (!wait_flags_all(p, epoch, w.m0 / kBM, (w.mend - 1) / kBM, abort_flag, &flag_ns)) break;
             fence_proxy_async_global();
           }
         } else {
@@ -1028,6 +1086,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
         issued_slice:
+          if (issued == 0) t_first = globaltimer_ns();
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1037,9 +1096,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       }
       misc[2] = issued;
       if (trace != nullptr) {
-        uint32_t* st = trace + 4 + 4 * blockIdx.x;
+        uint32_t* st = trace + 4 + kTraceStatWords * blockIdx.x;
         st[0] = static_cast<uint32_t>(flag_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : flag_ns);
         st[1] = n_waits;
+        st[4] = static_cast<uint32_t>(t_entry);
+        st[5] = static_cast<uint32_t>(t_first);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -1106,6 +1167,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         tc_commit(drain_bar);
       wait_mbar_drain(p, drain_bar, 0);
       misc[3] = consumed;
+      if (trace != nullptr) trace[4 + kTraceStatWords * blockIdx.x + 6] = static_cast<uint32_t>(globaltimer_ns());
     }
   } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
     // =============================================================== AllGather producer
@@ -1140,9 +1202,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if (old == static_cast<uint32_t>(p.ppc - 1)) {
             p.chunk_cnt[fi] = 0u;
             const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
-            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
+            if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, epoch);
             __threadfence();
-            st_release_gpu(p.chunk_flags + fi, p.epoch);
+            st_release_gpu(p.chunk_flags + fi, epoch);
             if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
           }
         }
@@ -1188,9 +1250,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if (old == static_cast<uint32_t>(p.ppc - 1)) {
             p.chunk_cnt[fi] = 0u;
             const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
-            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, p.epoch);
+            if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, epoch);
             __threadfence();
-            st_release_gpu(p.chunk_flags + fi, p.epoch);
+            st_release_gpu(p.chunk_flags + fi, epoch);
             if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
           }
         }
@@ -1290,9 +1352,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
           if (release) {
             const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + ck);
-            if (prev >= p.epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, p.epoch);
+            if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, ck, prev, epoch);
             __threadfence();
-            st_release_gpu(p.chunk_flags + ck, p.epoch);
+            st_release_gpu(p.chunk_flags + ck, epoch);
             if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(ck));
           }
         }
@@ -1330,13 +1392,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         if (use_mma) ok = wait_mbar(p, tfull0 + 8 * acc, aph, abort_flag, 400 + acc);
         if (ok && read_s) {
           if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x20000u + it) & 4095u);
-          ok = wait_flag(p, p.chain_flags + (size_t)(w.c - 1) * p.T + w.tile, ROLE_CHAIN,
+          ok = wait_flag(p, epoch, p.chain_flags + (size_t)(w.c - 1) * p.T + w.tile, ROLE_CHAIN,
                          (w.c - 1) * p.T + w.tile, abort_flag, &chain_ns);
         }
         if (*abort_flag) ok = false;
         *decision = ok ? 1u : 0u;
         if (trace != nullptr && ok)
-          trace[4 + 4 * grid + 1 + p.trace_chunks + blockIdx.x * per_cta + local] =
+          trace[4 + kTraceStatWords * grid + 1 + p.trace_chunks + blockIdx.x * per_cta + local] =
               (static_cast<uint32_t>(w.c) << 24) | static_cast<uint32_t>(w.tile);
       }
       named_bar_sync(1, kEpiThreads);
@@ -1436,9 +1498,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
         if (chained && write_s) {
           __threadfence();
-          st_release_gpu(p.chain_flags + (size_t)w.c * p.T + w.tile, p.epoch);
+          st_release_gpu(p.chain_flags + (size_t)w.c * p.T + w.tile, epoch);
         }
-        if (slotted) {
+        if (slotted && p.coop_fold != 2) {
           // count this tile's stored partials; the element that completes the count folds them
           // (cooperative fold: every element waits for the count, then folds its share)
           if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x30000u + it) & 4095u);
@@ -1491,7 +1553,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
       }
-      if (slotted && p.coop_fold) {
+      if (slotted && p.coop_fold == 1) {
         // cooperative fold: this element folds float4 block [c*per, (c+1)*per) of the tile's slot
         // layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), all L
         // slots in order 0..L-1, and the element that completes the tile's done count resets both
@@ -1509,7 +1571,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
         }
-      } else if (slotted) {
+      } else if (slotted && p.coop_fold == 0) {
         named_bar_sync(1, kEpiThreads);
         if (*is_last) {
           // fixed-order fold of the L partial slots: ((P_0 + P_1) + P_2) + ..., two slots' loads in
@@ -1555,50 +1617,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
           }
 #pragma unroll 1
-          for (int ch = 0; ch < C::CHUNKS && !p.bf16_partials; ++ch) {
-            const int col0 = h * C::COLS_PER_WARP + ch * 32;
-            const size_t off = ((size_t)(col0 >> 5) * 8 * kBM + row_in_tile) * 4;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 s = ld_cg_f4_hint(p.sbuf + (size_t)w.tile * (kBM * BN) + off + j * kBM * 4, once);
-              v[4 * j + 0] = s.x;
-              v[4 * j + 1] = s.y;
-              v[4 * j + 2] = s.z;
-              v[4 * j + 3] = s.w;
-            }
-            int c = 1;
-#pragma unroll 1
-            for (; c + 1 < p.L; c += 2) {
-              const float* sp0 = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
-              const float* sp1 = sp0 + (size_t)p.T * (kBM * BN);
-              float4 s0[8], s1[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                s0[j] = ld_cg_f4_hint(sp0 + j * kBM * 4, once);
-                s1[j] = ld_cg_f4_hint(sp1 + j * kBM * 4, once);
-              }
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                v[4 * j + 0] = (v[4 * j + 0] + s0[j].x) + s1[j].x;
-                v[4 * j + 1] = (v[4 * j + 1] + s0[j].y) + s1[j].y;
-                v[4 * j + 2] = (v[4 * j + 2] + s0[j].z) + s1[j].z;
-                v[4 * j + 3] = (v[4 * j + 3] + s0[j].w) + s1[j].w;
-              }
-            }
-            if (c < p.L) {
-              const float* sp = p.sbuf + ((size_t)c * p.T + w.tile) * (kBM * BN) + off;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 s = ld_cg_f4_hint(sp + j * kBM * 4, once);
-                v[4 * j + 0] = v[4 * j + 0] + s.x;
-                v[4 * j + 1] = v[4 * j + 1] + s.y;
-                v[4 * j + 2] = v[4 * j + 2] + s.z;
-                v[4 * j + 3] = v[4 * j + 3] + s.w;
-              }
-            }
-            store_out_chunk<OP, FP8>(p, row, w.n0 + col0, v, once);
-          }
+          for (int ch = 0; ch < C::CHUNKS && !p.bf16_partials; ++ch)
+            fold_unit_fp32<OP, FP8, BN>(p, w.tile, h * C::COLS_PER_WARP + ch * 32, row_in_tile, once);
           if (TDX_DISCARD_DEAD) {
             // every slot of this tile is dead now: drop the lines from L2
             named_bar_sync(1, kEpiThreads);
@@ -1607,6 +1627,44 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             for (int c = 0; c < p.L; ++c)
               for (int l = et; l < (int)(sbytes / 128); l += kEpiThreads)
                 discard_l2_line(reinterpret_cast<uint8_t*>(p.sbuf) + ((size_t)c * p.T + w.tile) * sbytes + (size_t)l * 128);
+          }
+        }
+      }
+    }
+    if (chain && p.reduce_last && p.coop_fold == 2) {
+      // grid-wide fold: every CTA arrives once all its partials are stored (a grid barrier; every CTA
+      // of the cooperative launch is resident), then folds 1/grid of all tiles' (row, 32-column)
+      // units, each over the slots in order 0..L-1. The last CTA to leave resets both counters.
+      named_bar_sync(1, kEpiThreads);
+      if (elected) {
+        __threadfence();
+        atomicAdd(p.grid_bar, 1u);
+        bool ok = *abort_flag == 0;
+        if (ok) ok = wait_count(p, p.grid_bar, static_cast<uint32_t>(grid), abort_flag, 0xFFFFFFu);
+        if (ok) fence_acq_rel_gpu();
+        *decision = ok ? 1u : 0u;
+      }
+      named_bar_sync(1, kEpiThreads);
+      if (*decision != 0u) {
+        const int et = threadIdx.x - kEpiWarp0 * 32;
+        const int units = p.T * (BN / 32) * kBM;
+        const int per = (units + grid - 1) / grid;
+        const int u0 = blockIdx.x * per;
+        const int u1 = min(units, u0 + per);
+#pragma unroll 1
+        for (int u = u0 + et; u < u1; u += kEpiThreads) {
+          const int i = u % kBM;
+          const int rest = u / kBM;
+          const int cc = rest % (BN / 32);
+          fold_unit_fp32<OP, FP8, BN>(p, rest / (BN / 32), cc * 32, i, once);
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (elected) {
+          __threadfence();
+          if (atomicAdd(p.grid_bar + 1, 1u) == static_cast<uint32_t>(grid - 1)) {
+            p.grid_bar[0] = 0u;
+            p.grid_bar[1] = 0u;
+            __threadfence();
           }
         }
       }
@@ -1621,9 +1679,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       }
     }
     if (elected && trace != nullptr) {
-      uint32_t* st = trace + 4 + 4 * blockIdx.x;
+      uint32_t* st = trace + 4 + kTraceStatWords * blockIdx.x;
       st[2] = static_cast<uint32_t>(chain_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : chain_ns);
       st[3] = static_cast<uint32_t>(local);
+      st[7] = static_cast<uint32_t>(globaltimer_ns());
     }
   }
 
@@ -1655,6 +1714,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+  if (p.dev_epoch != nullptr && threadIdx.x == 0) {
+    // device-kept epochs: the last CTA to finish publishes this call's epoch for the next call
+    // (which, being stream-ordered after this kernel, reads it at its start) and resets the count
+    __threadfence();
+    if (atomicAdd(p.dev_epoch + 1, 1u) == gridDim.x - 1) {
+      p.dev_epoch[1] = 0u;
+      p.dev_epoch[0] = epoch;
+      __threadfence();
+    }
   }
 }
 

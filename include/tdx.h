@@ -54,6 +54,9 @@ typedef enum {
 
 typedef enum { TDX_BF16 = 0, TDX_FP8_E4M3 = 1, TDX_FP32 = 2 } tdx_dtype;
 
+/* tdx_opts.epoch value selecting epochs kept on the device (see tdx_opts). */
+#define TDX_EPOCH_DEVICE 0xFFFFFFFFu
+
 typedef enum {
   TDX_FUSED = 0,          /* producer and consumer overlapped in one persistent kernel (default) */
   TDX_GEMM_ONLY = 1,      /* AG: GEMM on an already gathered buffer, no flag waits, no copies.
@@ -84,7 +87,15 @@ typedef struct tdx_opts {
   tdx_producer producer;     /* default TDX_PRODUCER_SM */
   uint32_t epoch;            /* 0: the library clears the flags on `stream` and uses epoch 1.
                                 >0: flags are not cleared; the caller passes strictly increasing
-                                epochs on one workspace (after tdx_workspace_init) */
+                                epochs on one workspace (after tdx_workspace_init).
+                                TDX_EPOCH_DEVICE: the epochs are kept in the workspace itself: a
+                                call uses the epoch of the last completed call on that workspace
+                                plus one and stores it when its kernel finishes. Nothing is cleared
+                                and the host tracks nothing, so the same captured call replays
+                                correctly in a CUDA graph. Start from a workspace zeroed by
+                                tdx_workspace_init, and do not mix with caller epochs on one
+                                workspace without re-initialising it (a flag left at a higher
+                                epoch is reported as TDX_ERR_STALE_EPOCH). */
   uint64_t timeout_ns;       /* bound of every device-side wait (default 2e9 ns) */
   uint32_t perturb_seed;     /* test only: !=0 injects pseudo-random delays in producers/epilogues */
   void* trace;               /* optional device buffer of tdx_trace_size() bytes, or NULL */
@@ -94,8 +105,10 @@ typedef struct tdx_opts {
   int reduce_mode;           /* fixed-order reduction of RS ranks / AG K splits: 0 = library choice,
                                 1 = chained (element c adds its partial to the running sum of
                                 elements 0..c-1 and hands it on), 2 = slotted (each element stores its
-                                partial; the last to arrive folds them in order 0..L-1). Both give
-                                the same bits. */
+                                partial; the last to arrive folds them in order 0..L-1), 3 = slotted
+                                with a grid-wide fold (once every CTA has stored its partials, all
+                                CTAs fold 1/grid of every tile each, slots in order 0..L-1; single
+                                CTAs and fp32 partials only). All give the same bits. */
   int cluster;               /* how CTAs cooperate on the GEMM: 0 = library choice, 1 = single CTAs,
                                 3 = pairs running one 2-SM MMA stream on a 256 x 256 tile (each CTA
                                 stages its 128 rows of A and half of B in its own shared memory;
@@ -326,10 +339,11 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
  * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
  * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
- * 2 bf16 partials), [21] 1 if the slotted fold is cooperative (single CTAs, fp32 partials, every
- * work item in one wave of the persistent grid, which depends on the device's SM count and
- * opts.num_sms: each element of a tile waits for the tile's L partials and folds 1/L of it), 0 if
- * the last arriver folds the tile. */
+ * 2 bf16 partials), [21] how the slotted fold is shared (single CTAs, fp32 partials; depends on the
+ * device's SM count and opts.num_sms): 0 the last arriver folds the tile; 1 every work item is in
+ * one wave of the persistent grid, and each element of a tile waits for the tile's L partials and
+ * folds 1/L of it; 2 several waves but fewer tiles than CTAs (or reduce_mode 3): after a grid
+ * barrier every CTA folds 1/grid of all tiles. */
 tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtype dtype,
                          const tdx_opts* opts, int64_t* info);
 
@@ -337,8 +351,11 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
  * items and releasing `chunks` chunk flags (AllGather: W * chunks per rank; MoE dispatch: the 128-row
  * chunks of the dispatched rows; 0 otherwise). Layout, in 32-bit words:
  *  [0..3]  {grid, items, chain length, tiles};
- *  then per CTA 4 statistics words {ns spent waiting on chunk flags, number of flag waits, ns spent
- *          waiting on rank-chain flags, items taken};
+ *  then per CTA 8 statistics words {ns spent waiting on chunk flags, number of flag waits, ns spent
+ *          waiting on rank-chain flags, items taken, then four phase stamps: the low 32 bits of the
+ *          GPU's nanosecond global timer at kernel entry, at the first operand load issued, when
+ *          the CTA's last MMA completed (0 for the second CTA of a 2-SM pair) and when its epilogue
+ *          finished (reductions and folds included)};
  *  then the producer section: one count of released chunks, then `chunks` words: word k holds the
  *          flag index (AllGather: rank * chunks per rank + chunk) of the k-th chunk released by the
  *          call, whichever CTA released it. The count must be zero when the call starts (pass a

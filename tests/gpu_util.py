@@ -245,19 +245,31 @@ class CombineCase:
 
 
 # ------------------------------------------------------------------ trace decoding (tdx_trace_size)
+STAT_WORDS = 8   # statistics words per CTA
+
+
+def trace_phases(tr: np.ndarray, grid: int) -> np.ndarray:
+    """Per CTA (grid x 4, ns): first load issued, last MMA completed (0 if none) and epilogue done,
+    each relative to the earliest kernel entry of the grid; column 0 is the CTA's own entry."""
+    st = tr[4:4 + STAT_WORDS * grid].reshape(grid, STAT_WORDS).astype(np.int64)
+    t0 = st[:, 4].min()
+    rel = lambda col: (st[:, col] - t0) % (1 << 32)
+    out = np.stack([rel(4), rel(5), np.where(st[:, 6] == 0, 0, rel(6)), rel(7)], axis=1)
+    return out
+
 def trace_items(tr: np.ndarray, grid: int, chunks: int, cl: int = 1) -> dict:
     """Work items a traced call took: {(item index in the cluster-wide sequence, CTA rank in its
     pair): (chain element, tile id)}. CTA b of a grid of pairs (cl = 2) is CTA b % 2 of pair b // 2,
     and pair q takes items q, q + grid/2, ...; single CTAs (cl = 1) take b, b + grid, ..."""
     items = int(tr[1])
     per = (items + grid - 1) // grid
-    base = 4 + 4 * grid + 1 + chunks
+    base = 4 + STAT_WORDS * grid + 1 + chunks
     ncl = grid // cl
     out = {}
     for b in range(grid):
         cid, crank = divmod(b, cl)
         mine = list(range(cid, items // cl, ncl))
-        assert int(tr[4 + 4 * b + 3]) == len(mine), (b, int(tr[4 + 4 * b + 3]), len(mine))
+        assert int(tr[4 + STAT_WORDS * b + 3]) == len(mine), (b, int(tr[4 + STAT_WORDS * b + 3]), len(mine))
         for k, it in enumerate(mine):
             w = int(tr[base + b * per + k])
             out[(it, crank)] = (w >> 24, w & 0xFFFFFF)
@@ -266,7 +278,7 @@ def trace_items(tr: np.ndarray, grid: int, chunks: int, cl: int = 1) -> dict:
 
 def trace_releases(tr: np.ndarray, grid: int, chunks: int) -> list:
     """Flag indices of the chunks a traced call released, in release order."""
-    base = 4 + 4 * grid
+    base = 4 + STAT_WORDS * grid
     n = int(tr[base])
     assert n == chunks, (n, chunks)
     return [int(x) for x in tr[base + 1:base + 1 + n]]

@@ -219,7 +219,7 @@ PLANS = [
     ("small-M AG", "OP_AG", 8, 16, 8192, 1024, 16,
      dict(BN=128, L=16, cluster=1, reduce_mode=2, pull_a=1, coop_fold=1, T=8, n_chunks=1)),
     ("small-M RS", "OP_RS", 8, 128, 1024, 8192, 0,
-     dict(BN=256, L=8, cluster=1, reduce_mode=2, coop_fold=0, T=32)),
+     dict(BN=256, L=8, cluster=1, reduce_mode=2, coop_fold=2, T=32)),
     ("RS, 8 M-tiles", "OP_RS", 8, 1024, 1024, 8192, 0,
      dict(BN=128, L=8, cluster=1, reduce_mode=1, T=512)),
     ("AG, N=64, 2-row shards", "OP_AG", 8, 2, 8192, 64, 0,
@@ -234,7 +234,8 @@ def test_planner_choices_for_the_workloads(tdx, case):
     """Tile width, K splits, CTA cooperation and reduction chosen for the measured workloads and a
     few neighbours (a 152-SM device): 2-SM pairs with a chained running sum for the large RS,
     128-wide tiles over 16 K splits that read the shards in place and fold cooperatively for the
-    small-M AllGather, 256-wide tiles with a last-arriver fold for the small-M ReduceScatter."""
+    small-M AllGather, 256-wide tiles with a grid-wide fold for the small-M ReduceScatter (two waves
+    of work but only 32 tiles)."""
     _, op, W, M, K, N, cr, want = case
     p = tdx.tdx_plan_info(getattr(tdx, op), W, M, K, N, tdx.TDX_BF16, tdx.make_opts(chunk_rows=cr, num_sms=152))
     got = {k: p[k] for k in want}
@@ -242,10 +243,23 @@ def test_planner_choices_for_the_workloads(tdx, case):
     assert p["T"] == p["tiles_m"] * p["tiles_n"]
 
 
+def test_grid_fold_plan_and_limits(tdx):
+    o3 = tdx.make_opts(reduce_mode=3, num_sms=152)
+    p = tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, o3)
+    assert p["reduce_mode"] == 2 and p["coop_fold"] == 2
+    # a large problem that would take CTA pairs runs on single CTAs under reduce_mode 3
+    assert tdx.tdx_plan_info(tdx.OP_RS, 8, 8192, 3584, 8192, tdx.TDX_BF16, o3)["cluster"] == 1
+    for bad in (dict(reduce_mode=3, cluster=3, block_n=256), dict(reduce_mode=3, bf16_partials=1)):
+        with pytest.raises(tdx.TdxError):
+            tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, tdx.make_opts(**bad))
+    with pytest.raises(tdx.TdxError):
+        tdx.tdx_plan_info(tdx.OP_RS, 4, 512, 256, 512, tdx.TDX_BF16, tdx.make_opts(reduce_mode=4))
+
+
 def test_trace_size(tdx):
     # header, 4 statistics words per CTA, the producer's release count and sequence, items per CTA
-    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 16 + 1 + 4 * 3)
-    assert tdx.tdx_trace_size(4, 10, 64) == 4 * (4 + 16 + 1 + 64 + 4 * 3)
+    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 32 + 1 + 4 * 3)
+    assert tdx.tdx_trace_size(4, 10, 64) == 4 * (4 + 32 + 1 + 64 + 4 * 3)
     assert tdx.tdx_trace_size(0, 10) == 0
     assert tdx.tdx_trace_size(4, 10, -1) == 0
 

@@ -12,7 +12,8 @@ import comm_overlapped_gemm_gb300 as tdx
 from oracle import reference as R
 import workloads as wls
 from gpu_util import (AGCase, assert_bit_exact, assert_within_tol, check_ag_consumer_order,
-                      check_each_item_once, host_bits, sample_rows, trace_items, trace_releases)
+                      check_each_item_once, host_bits, sample_rows, trace_items, trace_phases,
+                      trace_releases)
 
 pytestmark = pytest.mark.gpu
 
@@ -155,6 +156,11 @@ def test_ag_trace_follows_the_oracle_orders(self_rank, grid):
     assert sorted(rel) == list(range(chunks))
     if grid == 1:
         assert rel == want
+    # phase stamps: entry <= first load <= epilogue done, all within the call
+    ph = trace_phases(tr, grid)
+    busy = tr[4 + 3:4 + 8 * grid:8] > 0
+    assert np.all(ph[busy, 0] <= ph[busy, 1]) and np.all(ph[busy, 1] <= ph[busy, 3])
+    assert np.all(ph[:, 3] < 10 ** 9)
 
 
 def test_ag_modes_and_epochs():
@@ -185,6 +191,40 @@ def test_ag_modes_and_epochs():
     assert torch.equal(gathered(case, plan), torch.cat(case.shards).view(torch.uint8).flatten())
     assert int(torch.count_nonzero(case.C)) == 0
     status_ok(case)
+
+
+def test_ag_device_epochs_eager_and_graph():
+    # epochs kept in the workspace: no flag clearing between calls, and a captured call replays
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=4, M=256, K=512, N=768, chunk_rows=64)
+    inp = wls.make_inputs(wl, integer=True)
+    o = opts(chunk_rows=64, epoch=tdx.TDX_EPOCH_DEVICE)
+    case = AGCase(inp, opts=o)
+    want = R.round_out(case.oracle(), "bf16")
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 4, 256, 512, 768, tdx.TDX_BF16, o)
+    n = 4 * plan["n_chunks"]
+    for call in range(1, 4):
+        case.C.fill_(float("nan"))
+        tdx.check(case.run())
+        assert np.array_equal(case.result_bits(), want)
+        status_ok(case)
+        assert int(case.ws[64:68].view(torch.int32).item()) == call          # header word 16
+        f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
+        assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, call))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(2):
+            tdx.check(tdx.tdx_ag_gemm(case.shards, case.B, case.C, case.ws, 4, 256, 512, 768, tdx.TDX_BF16, o,
+                                      stream=s))
+    torch.cuda.synchronize()
+    for rep in range(3):
+        case.C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(case.result_bits(), want)
+    status_ok(case)
+    assert int(case.ws[64:68].view(torch.int32).item()) == 3 + 2 * 3
 
 
 def test_ag_degenerate_sizes():
@@ -321,6 +361,27 @@ def test_ag_small_shards_pull_and_flag_paths_agree():
         n = wl.W * plan["n_chunks"]
         f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
         assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 4))
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_ag_split_k_grid_fold(integer):
+    # split-K items over several waves of a small grid, folded by every CTA after a grid barrier
+    wl = wls.with_shape(wls.WORKLOADS["ag_small"], W=8, M=16, K=4096, N=512)
+    inp = wls.make_inputs(wl, integer=integer)
+    o = opts(chunk_rows=16, split_k=8, reduce_mode=3, num_sms=6)
+    assert tdx.tdx_plan_info(tdx.OP_AG, 8, 16, 4096, 512, tdx.TDX_BF16, o)["coop_fold"] == 2
+    case = AGCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+    first = case.result_bits()
+    case.C.fill_(float("nan"))
+    tdx.check(case.run(opts(chunk_rows=16, split_k=8, reduce_mode=3, num_sms=6, epoch=5, perturb_seed=2)))
+    status_ok(case)
+    assert np.array_equal(case.result_bits(), first)
 
 
 @pytest.mark.parametrize("integer", [True, False])

@@ -110,6 +110,35 @@ def test_moe_modes_and_epochs():
         assert_bit_exact(case.result_bits(), want, "bf16")
 
 
+def test_moe_device_epochs_and_release_trace():
+    # epochs kept in the workspace across calls (modes included), and the dispatch's chunk
+    # releases recorded in the trace: every 128-row chunk of the receive buffer exactly once
+    wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=4, M=128, K=512, N=256, E=16, topk=4)
+    inp = wls.make_inputs(wl, integer=True)
+    want, _ = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E)
+    o = opts(epoch=tdx.TDX_EPOCH_DEVICE)
+    case = MoECase(inp, opts=o)
+    tdx.check(case.run(opts(mode=tdx.TDX_MOVE_ONLY, epoch=tdx.TDX_EPOCH_DEVICE)))
+    tdx.check(case.run(opts(mode=tdx.TDX_GEMM_ONLY, epoch=tdx.TDX_EPOCH_DEVICE)))
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), want, "bf16")
+    plan = case.plan()
+    grid = 24
+    chunks = plan["n_chunks"]
+    trace = torch.zeros(tdx.tdx_trace_size(grid, plan["max_tiles"] * plan["tiles_n"], chunks) // 4,
+                        dtype=torch.int32, device="cuda")
+    for call in range(2):
+        case.Y.fill_(float("nan"))
+        trace.zero_()
+        tdx.check(case.run(opts(epoch=tdx.TDX_EPOCH_DEVICE, num_sms=grid, trace=trace, perturb_seed=call + 1)))
+        status_ok(case)
+        assert_bit_exact(case.result_bits(), want, "bf16")
+        tr = trace.cpu().numpy().astype(np.uint32)
+        n = int(tr[4 + 8 * grid])
+        assert n == chunks and sorted(tr[4 + 8 * grid + 1:4 + 8 * grid + 1 + n].tolist()) == list(range(chunks))
+    assert int(case.ws[64:68].view(torch.int32).item()) == 4
+
+
 def test_moe_invalid_expert_id_is_reported_not_run():
     wl = wls.with_shape(wls.WORKLOADS["moe_w8"], W=2, M=16, K=64, N=64, E=4, topk=2)
     inp = wls.make_inputs(wl, integer=True)

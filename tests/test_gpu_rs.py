@@ -157,6 +157,69 @@ def test_rs_chained_and_slotted_give_identical_bits(shape):
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("shape,grid", [(dict(W=8, M=128, K=1024, N=8192), 0),     # the small-M shape
+                                        (dict(W=4, M=512, K=256, N=512), 7),       # several waves
+                                        (dict(W=3, M=384, K=200, N=136), 5),       # ragged K and N
+                                        (dict(W=16, M=256, K=64, N=64), 3)])
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_grid_fold(shape, grid, integer):
+    # every CTA stores its partials, meets the others at a grid barrier, then folds 1/grid of all
+    # tiles: the same bits as the chained running sum, bit-exact on integers
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=integer)
+    o = opts(reduce_mode=3, num_sms=grid, epoch=2)
+    plan = tdx.tdx_plan_info(tdx.OP_RS, wl.W, wl.M, wl.K, wl.N, tdx.TDX_BF16, o)
+    assert plan["coop_fold"] == 2
+    case = RSCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "bf16")
+    first = case.result_bits()
+    # counters reset: a second call (next epoch, injected delays) gives the same bits
+    for x in case.out:
+        x.fill_(float("nan"))
+    tdx.check(case.run(opts(reduce_mode=3, num_sms=grid, epoch=3, perturb_seed=11)))
+    status_ok(case)
+    assert np.array_equal(case.result_bits(), first)
+    n = 2
+    bar = case.ws[plan["off_tile_cnt"]:plan["off_tile_cnt"] + 4 * (2 * plan["T"] + n)].view(torch.int32).cpu().numpy()
+    assert not bar.any()
+    chained = RSCase(inp, opts=opts(reduce_mode=1))
+    tdx.check(chained.run())
+    status_ok(chained)
+    assert np.array_equal(chained.result_bits(), first)
+
+
+@pytest.mark.parametrize("rm", [1, 2, 3])
+def test_rs_device_epochs_in_a_graph(rm):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
+    inp = wls.make_inputs(wl, integer=True)
+    o = opts(reduce_mode=rm, epoch=tdx.TDX_EPOCH_DEVICE)
+    case = RSCase(inp, opts=o)
+    want = R.round_out(case.oracle(), "bf16")
+    tdx.check(case.run())
+    status_ok(case)
+    assert np.array_equal(case.result_bits(), want)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            tdx.check(tdx.tdx_gemm_rs(case.A, case.B, case.out, case.ws, 4, 512, 256, 512, tdx.TDX_BF16, o, stream=s))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for x in case.out:
+            x.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(case.result_bits(), want)
+    status_ok(case)
+    assert int(case.ws[64:68].view(torch.int32).item()) == 1 + 3 * 2
+
+
 def test_rs_slotted_bookkeeping():
     wl = wls.with_shape(wls.WORKLOADS["rs_w8"], W=4, M=512, K=256, N=512)
     inp = wls.make_inputs(wl, integer=True)
