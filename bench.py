@@ -751,7 +751,7 @@ def run_gpu(args):
     st.status()
     tr = trace.cpu().numpy().view(np.uint32)
     g_ag = int(tr[0])
-    per_cta = tr[4:4 + 8 * g_ag].reshape(g_ag, 8).astype(np.float64)
+    per_cta = tr[4:4 + 12 * g_ag].reshape(g_ag, 12).astype(np.float64)
     flag_wait = {"mean_us": float(per_cta[:, 0].mean() / 1e3), "max_us": float(per_cta[:, 0].max() / 1e3),
                  "tiles_that_waited_per_cta": float(per_cta[:, 1].mean())}
 
@@ -880,6 +880,23 @@ def run_gpu(args):
     return 0
 
 
+PHASES = ["entry", "setup", "first_load", "first_full", "mma_done", "items_done", "epilogue_done"]
+
+
+def trace_phase_summary(tr: np.ndarray) -> dict:
+    """Median and maximum over CTAs (us from the earliest kernel entry) of each phase stamp of a
+    traced call (12 statistics words per CTA; stamps a CTA did not record are left out)."""
+    g = int(tr[0])
+    stv = tr[4:4 + 12 * g].reshape(g, 12).astype(np.int64)
+    t0 = stv[:, 4].min()
+    out = {}
+    for k, name in enumerate(PHASES):
+        col = stv[:, 4 + k]
+        v = ((col[col != 0] - t0) % (1 << 32)) / 1e3
+        out[name] = [round(float(np.median(v)), 2), round(float(np.max(v)), 2)] if len(v) else None
+    return out
+
+
 def run_case(args):
     """One op on a given shape (profiling helper): --case ag|rs --shape W,M,K,N."""
     import torch
@@ -926,13 +943,7 @@ def run_case(args):
     st.status()
     tr = trace.cpu().numpy().view(np.uint32)
     g = int(tr[0])
-    stv = tr[4:4 + 8 * g].reshape(g, 8).astype(np.int64)
-    t0 = stv[:, 4].min()
-    rel = lambda col: ((stv[:, col] - t0) % (1 << 32)) / 1e3
-    phases = {}
-    for name, col in (("entry", 4), ("first_load", 5), ("mma_done", 6), ("epilogue_done", 7)):
-        v = rel(col) if col != 6 else rel(col)[stv[:, 6] != 0]
-        phases[name] = [round(float(np.median(v)), 2), round(float(np.max(v)), 2)] if len(v) else None
+    phases = trace_phase_summary(tr)
     print(json.dumps({"case": args.case, "shape": [W, M, K, N], "opts": extra, "ms": ms, "us_gpu_graph": gus,
                       "us_gpu_graph_clearing": gus_clear, "tflops": fl / (ms * 1e-3) / 1e12,
                       "phases_us_median_max": phases,

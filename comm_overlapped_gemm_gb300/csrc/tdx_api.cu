@@ -322,6 +322,10 @@ void fill_common(KParams& kp, const Plan& pl, const tdx_opts& o, uint8_t* ws) {
   kp.perturb = o.perturb_seed;
   kp.mode = o.mode;
   kp.row_bytes = static_cast<long long>(pl.K) * pl.elt;
+  // an A tile is re-read by the other N-tiles of its M-tile, a B tile by the other M-tiles (pairs of
+  // them with CTA pairs); with a single one of those the operand is read once and streamed
+  kp.a_streamed = pl.tiles_n <= 1 ? 1 : 0;
+  kp.b_streamed = pl.tiles_m / pl.CL <= 1 ? 1 : 0;
 }
 
 // Persistent grid: every CTA resident at once (one per SM; for pairs, the clusters that fit), capped

@@ -67,7 +67,7 @@ constexpr size_t kHeaderBytes = 4096;
 constexpr int kStatusWords = 8;
 constexpr int kDevEpochWord = 16;
 // Trace: statistics words per CTA (see tdx_trace_size in include/tdx.h).
-constexpr int kTraceStatWords = 8;
+constexpr int kTraceStatWords = 12;
 
 struct KParams {
   CUtensorMap tm_a[kMaxW];       // AG: [0] gathered buffer G, [1] self shard (pull mode: shard r). RS: A_r
@@ -105,6 +105,7 @@ struct KParams {
   int copy_active;               // producer warps copy chunks (AG, SM producer, fused/move)
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
   int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
+  int a_streamed, b_streamed;    // operand read by one tile only: loaded evict_first (else evict_last)
   int allreduce;                 // RS kernel as GEMM+AllReduce: out[r] are full M x N outputs
   int bf16_partials;             // slotted RS/AR: partials rounded to bf16 in their slots (else fp32)
   const int32_t* moe_src;        // MoE: source token of every dispatched row, s * moe_T + t

@@ -131,7 +131,7 @@ struct Cfg {
   static constexpr int STAGES_RAW = (RING_KB * 1024) / STAGE_BYTES;   // ring budget (216 KiB by default)
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;   // ring full/empty, accumulators full/empty, drain
   // flags/decisions (64 B), MoE producer row sources (kBM ints) and staging barriers (8)
   static constexpr int MISC_BYTES = 64 + kBM * 4 + 8 * 8;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
@@ -914,18 +914,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       tmem_relinquish();
     }
   }
-  if (threadIdx.x == kTmaWarp * 32) {
-    const int na = (OP == OP_MOE || OP == OP_MOE_COMBINE) ? 1 : (OP == OP_AG && !p.pull_a ? 2 : p.W);
-    const int nb = OP == OP_RS ? p.W : 1;
-    for (int i = 0; i < na; ++i) tma_prefetch_map(&p.tm_a[i]);
-    for (int i = 0; i < nb; ++i) tma_prefetch_map(&p.tm_b[i]);
-  }
   tc_fence_before();
   if constexpr (CL > 1)
     cluster_sync_all();   // the peer's barriers are initialised before its loads or commits target them
   else
     __syncthreads();
   tc_fence_after();
+  const uint64_t t_setup = globaltimer_ns();
   const uint32_t tmem_base = misc[0];
   const uint32_t epoch = misc[7];
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -966,7 +961,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      const uint64_t keep = policy_of(TDX_OPERAND_POLICY);   // operand tiles are re-read by other tiles
+      // operand tiles that other tiles re-read are kept in L2 (evict_last); an operand no other tile
+      // reads (B of a single M-tile, A of a single N-tile) is streamed (evict_first) so that it does
+      // not push out data that is reused, such as the partial slots folded at the end
+      const uint64_t keep_a = p.a_streamed ? policy_evict_first() : policy_of(TDX_OPERAND_POLICY);
+      const uint64_t keep_b = p.b_streamed ? policy_evict_first() : policy_of(TDX_OPERAND_POLICY);
       uint64_t flag_ns = 0;
       uint32_t n_waits = 0;
       uint64_t t_first = 0;
@@ -1048,11 +1047,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
               mbar_arrive_expect_tx(fb, a_bytes + C::B_BYTES);
               for (int q = 0; q < pull_nr; ++q)
                 tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES + q * p.M_local * 128), &p.tm_a[pull_r0 + q], fb,
-                                 kb * C::BK, 0, keep);
+                                 kb * C::BK, 0, keep_a);
 #pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep_b);
               goto issued_slice;
             }
           }
@@ -1060,29 +1059,29 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             // both CTAs' slices count on the leader's slot barrier, armed once for the pair
             if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
             const uint32_t fbl = mapa_shared(fb, 0);
-            tma_load_2d_pair_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fbl, kb * C::BK, arow, keep);
+            tma_load_2d_pair_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fbl, kb * C::BK, arow, keep_a);
 #pragma unroll
             for (int jj = 0; jj < C::B_BOXES_CTA; ++jj) {
               if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE)
                 tma_load_3d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
-                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, w.e, keep);
+                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, w.e, keep_b);
               else
                 tma_load_2d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
-                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep);
+                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep_b);
             }
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-            tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep);
+            tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fb, kb * C::BK, arow, keep_a);
             if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE) {
 #pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_3d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                 w.n0 + j * C::B_BOX_N, kb * C::BK, w.e, keep);
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, w.e, keep_b);
             } else {
 #pragma unroll
               for (int j = 0; j < C::B_BOXES; ++j)
                 tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep);
+                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep_b);
             }
           }
         issued_slice:
@@ -1100,7 +1099,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         st[0] = static_cast<uint32_t>(flag_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : flag_ns);
         st[1] = n_waits;
         st[4] = static_cast<uint32_t>(t_entry);
-        st[5] = static_cast<uint32_t>(t_first);
+        st[5] = static_cast<uint32_t>(t_setup);
+        st[6] = static_cast<uint32_t>(t_first);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -1110,6 +1110,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       uint32_t phase = 0;
       uint32_t consumed = 0;
       int local = 0;
+      uint64_t t_first_full = 0;
       bool stop = false;
       for (int it = cid; it < items && !stop; it += ncl, ++local) {
         const Item w = decode_item<OP, CL>(p, it, BN, crank);
@@ -1125,6 +1126,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             stop = true;
             break;
           }
+          if (consumed == 0) t_first_full = globaltimer_ns();
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
@@ -1167,7 +1169,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         tc_commit(drain_bar);
       wait_mbar_drain(p, drain_bar, 0);
       misc[3] = consumed;
-      if (trace != nullptr) trace[4 + kTraceStatWords * blockIdx.x + 6] = static_cast<uint32_t>(globaltimer_ns());
+      if (trace != nullptr) {
+        trace[4 + kTraceStatWords * blockIdx.x + 7] = static_cast<uint32_t>(t_first_full);
+        trace[4 + kTraceStatWords * blockIdx.x + 8] = static_cast<uint32_t>(globaltimer_ns());
+      }
     }
   } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
     // =============================================================== AllGather producer
@@ -1631,44 +1636,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         }
       }
     }
-    if (chain && p.reduce_last && p.coop_fold == 2) {
-      // grid-wide fold: every CTA arrives once all its partials are stored (a grid barrier; every CTA
-      // of the cooperative launch is resident), then folds 1/grid of all tiles' (row, 32-column)
-      // units, each over the slots in order 0..L-1. The last CTA to leave resets both counters.
-      named_bar_sync(1, kEpiThreads);
-      if (elected) {
-        __threadfence();
-        atomicAdd(p.grid_bar, 1u);
-        bool ok = *abort_flag == 0;
-        if (ok) ok = wait_count(p, p.grid_bar, static_cast<uint32_t>(grid), abort_flag, 0xFFFFFFu);
-        if (ok) fence_acq_rel_gpu();
-        *decision = ok ? 1u : 0u;
-      }
-      named_bar_sync(1, kEpiThreads);
-      if (*decision != 0u) {
-        const int et = threadIdx.x - kEpiWarp0 * 32;
-        const int units = p.T * (BN / 32) * kBM;
-        const int per = (units + grid - 1) / grid;
-        const int u0 = blockIdx.x * per;
-        const int u1 = min(units, u0 + per);
-#pragma unroll 1
-        for (int u = u0 + et; u < u1; u += kEpiThreads) {
-          const int i = u % kBM;
-          const int rest = u / kBM;
-          const int cc = rest % (BN / 32);
-          fold_unit_fp32<OP, FP8, BN>(p, rest / (BN / 32), cc * 32, i, once);
-        }
-        named_bar_sync(1, kEpiThreads);
-        if (elected) {
-          __threadfence();
-          if (atomicAdd(p.grid_bar + 1, 1u) == static_cast<uint32_t>(grid - 1)) {
-            p.grid_bar[0] = 0u;
-            p.grid_bar[1] = 0u;
-            __threadfence();
-          }
-        }
-      }
-    }
+    const uint64_t t_items_done = globaltimer_ns();
     if constexpr (OP == OP_MOE_COMBINE) {
       if (p.mode == MODE_MOVE_ONLY && !moe_bad) {
         // the combine alone (expert outputs already in place): one (token, N-tile) per warp task
@@ -1682,8 +1650,91 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       uint32_t* st = trace + 4 + kTraceStatWords * blockIdx.x;
       st[2] = static_cast<uint32_t>(chain_ns > 0xFFFFFFFFull ? 0xFFFFFFFFull : chain_ns);
       st[3] = static_cast<uint32_t>(local);
-      st[7] = static_cast<uint32_t>(globaltimer_ns());
+      st[9] = static_cast<uint32_t>(t_items_done);
+      st[10] = static_cast<uint32_t>(globaltimer_ns());
     }
+  }
+
+  // =============================================================== grid-wide fold
+  if (OP != OP_MOE && OP != OP_MOE_COMBINE && chain && p.reduce_last && p.coop_fold == 2) {
+    // Every CTA arrives once all its partials are stored (a grid barrier; every CTA of the
+    // cooperative launch is resident), then folds a contiguous 1/grid share of all tiles, cut into
+    // units of 128 rows x 8 columns (4 KiB of a slot, contiguous in the slot layout), slots in order
+    // 0..L-1. The last CTA to leave resets both counters.
+    __syncthreads();
+    volatile uint32_t* go = misc + 4;
+    const uint64_t pol = policy_evict_first();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(p.grid_bar, 1u);
+      bool ok = *abort_flag == 0;
+      if (ok) ok = wait_count(p, p.grid_bar, static_cast<uint32_t>(grid), abort_flag, 0xFFFFFFu);
+      if (ok) fence_acq_rel_gpu();
+      *go = ok ? 1u : 0u;
+    }
+    __syncthreads();
+    if (*go != 0u) {
+      // a task is one row of one unit (8 columns): the row's 8 columns of up to 8 slots are loaded at
+      // once (a warp's 32 lanes take 32 consecutive rows: 512 contiguous bytes per load), then added
+      // in slot order; all 12 warps take tasks
+      const int units = p.T * (BN / 8);
+      const int per = (units + grid - 1) / grid;
+      const int g0 = min(units, blockIdx.x * per);
+      const int g1 = min(units, g0 + per);
+      const size_t slot_f4 = (size_t)p.T * kBM * BN / 4;
+#pragma unroll 1
+      for (int task = threadIdx.x; task < (g1 - g0) * kBM; task += kNumThreads) {
+        const int gu = g0 + (task >> 7);
+        const int i = task & (kBM - 1);
+        const int tile = gu / (BN / 8);
+        const int r8 = gu - tile * (BN / 8);
+        const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)gu * (kBM * 2) + i;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < p.L; c0 += 8) {
+          float4 x0[8], x1[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c0 + c < p.L) {
+              x0[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4, pol);
+              x1[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4 + kBM, pol);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c0 + c < p.L) {
+              if (c0 + c == 0) {
+                a0 = x0[c];
+                a1 = x1[c];
+              } else {
+                a0.x = a0.x + x0[c].x;
+                a0.y = a0.y + x0[c].y;
+                a0.z = a0.z + x0[c].z;
+                a0.w = a0.w + x0[c].w;
+                a1.x = a1.x + x1[c].x;
+                a1.y = a1.y + x1[c].y;
+                a1.z = a1.z + x1[c].z;
+                a1.w = a1.w + x1[c].w;
+              }
+            }
+          }
+        }
+        const int row = (tile / p.tiles_n) * kBM + i;
+        const int col = (tile % p.tiles_n) * BN + r8 * 8;
+        store_out_4<OP, FP8>(p, row, col, a0);
+        store_out_4<OP, FP8>(p, row, col + 4, a1);
+      }
+      if (threadIdx.x == 0 && *go != 0u) {
+        __threadfence();
+        if (atomicAdd(p.grid_bar + 1, 1u) == static_cast<uint32_t>(grid - 1)) {
+          p.grid_bar[0] = 0u;
+          p.grid_bar[1] = 0u;
+          __threadfence();
+        }
+      }
+    }
+    if (trace != nullptr && threadIdx.x == 0)
+      trace[4 + kTraceStatWords * blockIdx.x + 10] = static_cast<uint32_t>(globaltimer_ns());
   }
 
   // =============================================================== teardown
@@ -1731,7 +1782,7 @@ template <int BN, bool FP8, int OP, int PM>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
   constexpr int CL = PM == 0 ? 1 : 2;
-  // MoE adds the dispatch staging ring (128-byte aligned) after the GEMM's shared memory
+  // the staging ring / fold region (128-byte aligned) follows the GEMM's shared memory
   constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
   static_assert(!uses_staging(OP) || (C::MOE_STG >= 4096 && kSmem <= 227 * 1024), "staging ring budget");
   // the dynamic shared-memory limit is raised once per device for each instantiation (setting it

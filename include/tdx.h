@@ -351,11 +351,13 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
  * items and releasing `chunks` chunk flags (AllGather: W * chunks per rank; MoE dispatch: the 128-row
  * chunks of the dispatched rows; 0 otherwise). Layout, in 32-bit words:
  *  [0..3]  {grid, items, chain length, tiles};
- *  then per CTA 8 statistics words {ns spent waiting on chunk flags, number of flag waits, ns spent
- *          waiting on rank-chain flags, items taken, then four phase stamps: the low 32 bits of the
- *          GPU's nanosecond global timer at kernel entry, at the first operand load issued, when
- *          the CTA's last MMA completed (0 for the second CTA of a 2-SM pair) and when its epilogue
- *          finished (reductions and folds included)};
+ *  then per CTA 12 statistics words {ns spent waiting on chunk flags, number of flag waits, ns
+ *          spent waiting on rank-chain flags, items taken, then seven phase stamps, each the low 32
+ *          bits of the GPU's nanosecond global timer: kernel entry, set-up done (barriers, Tensor
+ *          Memory, descriptors), first operand load issued, first ring slot full (seen by the MMA
+ *          issuer), last MMA completed, epilogue done with the CTA's own items, epilogue done
+ *          (shared folds included); the two MMA stamps are 0 for the second CTA of a 2-SM pair and
+ *          for a CTA without items; then one word 0};
  *  then the producer section: one count of released chunks, then `chunks` words: word k holds the
  *          flag index (AllGather: rank * chunks per rank + chunk) of the k-th chunk released by the
  *          call, whichever CTA released it. The count must be zero when the call starts (pass a

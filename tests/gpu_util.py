@@ -245,17 +245,17 @@ class CombineCase:
 
 
 # ------------------------------------------------------------------ trace decoding (tdx_trace_size)
-STAT_WORDS = 8   # statistics words per CTA
+STAT_WORDS = 12   # statistics words per CTA
+PHASES = ["entry", "setup", "first_load", "first_full", "mma_done", "items_done", "epilogue_done"]
 
 
 def trace_phases(tr: np.ndarray, grid: int) -> np.ndarray:
-    """Per CTA (grid x 4, ns): first load issued, last MMA completed (0 if none) and epilogue done,
-    each relative to the earliest kernel entry of the grid; column 0 is the CTA's own entry."""
+    """Per CTA (grid x 7, ns) the phase stamps of PHASES relative to the earliest kernel entry of
+    the grid; stamps a CTA did not record (0) stay 0."""
     st = tr[4:4 + STAT_WORDS * grid].reshape(grid, STAT_WORDS).astype(np.int64)
     t0 = st[:, 4].min()
-    rel = lambda col: (st[:, col] - t0) % (1 << 32)
-    out = np.stack([rel(4), rel(5), np.where(st[:, 6] == 0, 0, rel(6)), rel(7)], axis=1)
-    return out
+    cols = [np.where(st[:, c] == 0, 0, (st[:, c] - t0) % (1 << 32)) for c in range(4, 11)]
+    return np.stack(cols, axis=1)
 
 def trace_items(tr: np.ndarray, grid: int, chunks: int, cl: int = 1) -> dict:
     """Work items a traced call took: {(item index in the cluster-wide sequence, CTA rank in its

@@ -258,8 +258,8 @@ def test_grid_fold_plan_and_limits(tdx):
 
 def test_trace_size(tdx):
     # header, 4 statistics words per CTA, the producer's release count and sequence, items per CTA
-    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 32 + 1 + 4 * 3)
-    assert tdx.tdx_trace_size(4, 10, 64) == 4 * (4 + 32 + 1 + 64 + 4 * 3)
+    assert tdx.tdx_trace_size(4, 10) == 4 * (4 + 48 + 1 + 4 * 3)
+    assert tdx.tdx_trace_size(4, 10, 64) == 4 * (4 + 48 + 1 + 64 + 4 * 3)
     assert tdx.tdx_trace_size(0, 10) == 0
     assert tdx.tdx_trace_size(4, 10, -1) == 0
 

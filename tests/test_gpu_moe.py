@@ -134,8 +134,8 @@ def test_moe_device_epochs_and_release_trace():
         status_ok(case)
         assert_bit_exact(case.result_bits(), want, "bf16")
         tr = trace.cpu().numpy().astype(np.uint32)
-        n = int(tr[4 + 8 * grid])
-        assert n == chunks and sorted(tr[4 + 8 * grid + 1:4 + 8 * grid + 1 + n].tolist()) == list(range(chunks))
+        n = int(tr[4 + 12 * grid])
+        assert n == chunks and sorted(tr[4 + 12 * grid + 1:4 + 12 * grid + 1 + n].tolist()) == list(range(chunks))
     assert int(case.ws[64:68].view(torch.int32).item()) == 4
 
 
