@@ -880,7 +880,7 @@ def run_gpu(args):
     return 0
 
 
-PHASES = ["entry", "setup", "first_load", "first_full", "mma_done", "items_done", "epilogue_done"]
+PHASES = ["entry", "setup", "first_item_loaded", "first_item_mma", "mma_done", "items_done", "epilogue_done"]
 
 
 def trace_phase_summary(tr: np.ndarray) -> dict:
@@ -915,7 +915,9 @@ def run_case(args):
         extra[k] = int(v)
     st.extra = extra
     st.size_workspaces(extra)
-    fn = st.ag if args.case == "ag" else st.rs
+    mode = {"fused": tdx.TDX_FUSED, "gemm": tdx.TDX_GEMM_ONLY, "move": tdx.TDX_MOVE_ONLY}[args.mode]
+    base = st.ag if args.case == "ag" else st.rs
+    fn = lambda epoch=None: base(mode=mode, epoch=epoch)
     for _ in range(args.warmup + args.steps):
         tdx.check(fn())
     torch.cuda.synchronize()
@@ -944,7 +946,8 @@ def run_case(args):
     tr = trace.cpu().numpy().view(np.uint32)
     g = int(tr[0])
     phases = trace_phase_summary(tr)
-    print(json.dumps({"case": args.case, "shape": [W, M, K, N], "opts": extra, "ms": ms, "us_gpu_graph": gus,
+    print(json.dumps({"case": args.case, "shape": [W, M, K, N], "mode": args.mode, "opts": extra, "ms": ms,
+                      "us_gpu_graph": gus,
                       "us_gpu_graph_clearing": gus_clear, "tflops": fl / (ms * 1e-3) / 1e12,
                       "phases_us_median_max": phases,
                       "plan": {k: plan[k] for k in ("BN", "L", "T", "reduce_mode", "cluster", "coop_fold")}}))
@@ -982,7 +985,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra configurations")
     ap.add_argument("--case", choices=["ag", "rs", "moe", "moe_combine"], default=None)
-    ap.add_argument("--mode", choices=["fused", "gemm", "move"], default="fused", help="--case moe* only")
+    ap.add_argument("--mode", choices=["fused", "gemm", "move"], default="fused", help="--case only: which part runs")
     ap.add_argument("--shape", default="8,1024,8192,3584")
     ap.add_argument("--opts", default="", help="--case only: tdx_opts fields, e.g. block_n=256,split_k=4")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")

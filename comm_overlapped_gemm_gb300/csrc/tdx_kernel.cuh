@@ -1085,13 +1085,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             }
           }
         issued_slice:
-          if (issued == 0) t_first = globaltimer_ns();
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        if (t_first == 0) t_first = globaltimer_ns();   // once per item, never inside the K loop
       }
       misc[2] = issued;
       if (trace != nullptr) {
@@ -1126,7 +1126,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             stop = true;
             break;
           }
-          if (consumed == 0) t_first_full = globaltimer_ns();
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
@@ -1157,6 +1156,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           }
         }
         if (stop) break;
+        if (t_first_full == 0) t_first_full = globaltimer_ns();   // once per item, never inside the K loop
         if constexpr (PM == 2)
           tc_commit_pair_multicast(tfull0 + 8 * acc, static_cast<uint16_t>(0x3));   // both halves ready
         else

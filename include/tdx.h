@@ -354,10 +354,10 @@ tdx_status tdx_plan_info(int op, int W, int M_local_or_M, int K, int N, tdx_dtyp
  *  then per CTA 12 statistics words {ns spent waiting on chunk flags, number of flag waits, ns
  *          spent waiting on rank-chain flags, items taken, then seven phase stamps, each the low 32
  *          bits of the GPU's nanosecond global timer: kernel entry, set-up done (barriers, Tensor
- *          Memory, descriptors), first operand load issued, first ring slot full (seen by the MMA
- *          issuer), last MMA completed, epilogue done with the CTA's own items, epilogue done
- *          (shared folds included); the two MMA stamps are 0 for the second CTA of a 2-SM pair and
- *          for a CTA without items; then one word 0};
+ *          Memory), all operand loads of the CTA's first item issued, all MMAs of its first item
+ *          issued, last MMA completed, epilogue done with the CTA's own items, epilogue done (shared
+ *          folds included); the MMA stamps are 0 for the second CTA of a 2-SM pair, the load and
+ *          MMA stamps 0 for a CTA without items; then one word 0};
  *  then the producer section: one count of released chunks, then `chunks` words: word k holds the
  *          flag index (AllGather: rank * chunks per rank + chunk) of the k-th chunk released by the
  *          call, whichever CTA released it. The count must be zero when the call starts (pass a

@@ -246,7 +246,7 @@ class CombineCase:
 
 # ------------------------------------------------------------------ trace decoding (tdx_trace_size)
 STAT_WORDS = 12   # statistics words per CTA
-PHASES = ["entry", "setup", "first_load", "first_full", "mma_done", "items_done", "epilogue_done"]
+PHASES = ["entry", "setup", "first_item_loaded", "first_item_mma", "mma_done", "items_done", "epilogue_done"]
 
 
 def trace_phases(tr: np.ndarray, grid: int) -> np.ndarray:

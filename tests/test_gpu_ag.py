@@ -156,13 +156,14 @@ def test_ag_trace_follows_the_oracle_orders(self_rank, grid):
     assert sorted(rel) == list(range(chunks))
     if grid == 1:
         assert rel == want
-    # phase stamps in order: entry, set-up, first load, first full slot, last MMA, items done,
-    # epilogue done, all within the call
+    # phase stamps in order (entry, set-up, first item's loads issued, its MMAs issued, last MMA
+    # completed, items done, epilogue done; two roles that see the same completion may stamp a
+    # little apart, hence the 2 us allowance), all within the call
     ph = trace_phases(tr, grid)
     busy = tr[4 + 3:4 + 12 * grid:12] > 0
     assert busy.any()
     for a, b in zip(range(6), range(1, 7)):
-        assert np.all(ph[busy, a] <= ph[busy, b]), (a, ph[busy][:4])
+        assert np.all(ph[busy, a] <= ph[busy, b] + 2000), (a, ph[busy][:4])
     assert np.all(ph[:, 6] < 10 ** 9)
 
 
