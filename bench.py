@@ -279,15 +279,17 @@ class Step:
         self.size_workspaces({})
         self.epoch = 0
 
-    def size_workspaces(self, extra):
-        """(Re)allocate the two workspaces for the tiling options in `extra`."""
+    def size_workspaces(self, extra, ops=("ag", "rs")):
+        """(Re)allocate the two workspaces, those named in `ops` for the tiling options in `extra`."""
         tdx, t, wa, wr = self.tdx, self.torch, self.wa, self.wr
         dev = self.ws_ag.device
+        ea = extra if "ag" in ops else {}
+        er = extra if "rs" in ops else {}
         self.ws_ag = t.empty(tdx.tdx_workspace_size(tdx.OP_AG, wa.W, wa.M, wa.K, wa.N, tdx.TDX_BF16,
-                                                    tdx.make_opts(chunk_rows=wa.chunk_rows, **extra)),
+                                                    tdx.make_opts(chunk_rows=wa.chunk_rows, **ea)),
                              dtype=t.uint8, device=dev)
         self.ws_rs = t.empty(tdx.tdx_workspace_size(tdx.OP_RS, wr.W, wr.M, wr.K, wr.N, tdx.TDX_BF16,
-                                                    tdx.make_opts(**extra)), dtype=t.uint8, device=dev)
+                                                    tdx.make_opts(**er)), dtype=t.uint8, device=dev)
         tdx.check(tdx.tdx_workspace_init(self.ws_ag))
         tdx.check(tdx.tdx_workspace_init(self.ws_rs))
 
@@ -914,7 +916,7 @@ def run_case(args):
         k, v = kv.split("=")
         extra[k] = int(v)
     st.extra = extra
-    st.size_workspaces(extra)
+    st.size_workspaces(extra, ops=(args.case,))
     mode = {"fused": tdx.TDX_FUSED, "gemm": tdx.TDX_GEMM_ONLY, "move": tdx.TDX_MOVE_ONLY}[args.mode]
     base = st.ag if args.case == "ag" else st.rs
     fn = lambda epoch=None: base(mode=mode, epoch=epoch)

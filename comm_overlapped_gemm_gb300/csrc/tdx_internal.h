@@ -137,8 +137,8 @@ int fused_smem_bytes(int block_n, bool fp8);
 cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fused_fp8(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 // Largest grid whose CTAs are resident together (pairs: twice the 2-CTA clusters that fit).
-int fused_max_grid_bf16(int op, int pm, int sms);
-int fused_max_grid_fp8(int op, int pm, int sms);
+int fused_max_grid_bf16(int op, int pm, int sms, int block_n);
+int fused_max_grid_fp8(int op, int pm, int sms, int block_n);
 cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 
 // MoE: the fused dispatch + grouped GEMM kernel and the fused grouped GEMM + combine kernel

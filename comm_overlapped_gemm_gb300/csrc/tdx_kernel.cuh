@@ -126,11 +126,22 @@ struct Cfg {
   static constexpr int B_BOXES = BN / B_BOX_N;              // boxes across the tile width
   static constexpr int B_BOXES_CTA = PAIR_MMA ? B_BOXES / 2 : B_BOXES;   // boxes this CTA stages
   static constexpr int B_BOX_BYTES = BK * 128;
+  // A tile wider than one MMA (512 columns, 2-SM pairs only) takes N_PARTS MMAs of MMA_N columns per
+  // K step, part p on accumulator columns [p*MMA_N, (p+1)*MMA_N); this CTA's B boxes are stored part
+  // by part (each part: its half of the part's columns in a pair)
+  static constexpr int MMA_N = BN > 256 ? 256 : BN;
+  static constexpr int N_PARTS = BN / MMA_N;
+  static constexpr int BOXES_PART = MMA_N / B_BOX_N;
+  static constexpr int BOXES_PART_CTA = PAIR_MMA ? BOXES_PART / 2 : BOXES_PART;
+  static constexpr int B_PART_BYTES = BOXES_PART_CTA * B_BOX_BYTES;
   static constexpr int B_BYTES = B_BOXES_CTA * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (RING_KB * 1024) / STAGE_BYTES;   // ring budget (216 KiB by default)
   static constexpr int STAGES = STAGES_RAW > TDX_MAX_STAGES ? TDX_MAX_STAGES : STAGES_RAW;
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // 128 / 256 / 512
+  // two accumulators (the epilogue drains one while the MMA fills the other) up to 256 columns;
+  // a 512-column tile fills Tensor Memory with one accumulator
+  static constexpr int ACC_BUFS = 2 * BN <= 512 ? 2 : 1;
+  static constexpr int TMEM_COLS = (ACC_BUFS * BN < 32) ? 32 : ACC_BUFS * BN;   // 128 / 256 / 512
   static constexpr int NUM_BARS = 2 * STAGES + 5;   // ring full/empty, accumulators full/empty, drain
   // flags/decisions (64 B), MoE producer row sources (kBM ints) and staging barriers (8)
   static constexpr int MISC_BYTES = 64 + kBM * 4 + 8 * 8;
@@ -146,10 +157,12 @@ struct Cfg {
   // M >> 4 (bits 24-28).
   static constexpr int MMA_M = PAIR_MMA ? 2 * kBM : kBM;
   static constexpr uint32_t IDESC = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
-                                    (1u << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                    (1u << 16) | (static_cast<uint32_t>(MMA_N >> 3) << 17) |
                                     (static_cast<uint32_t>(MMA_M >> 4) << 24);
   static_assert(BN % B_BOX_N == 0 && B_BOXES >= 1, "tile width must cover whole 128-byte boxes");
   static_assert(!PAIR_MMA || B_BOXES % 2 == 0, "a 2-SM pair splits B into two halves");
+  static_assert(BN <= 256 || PAIR_MMA, "512-column tiles run on 2-SM pairs");
+  static_assert(BN <= 512 && BN % MMA_N == 0 && (!PAIR_MMA || BOXES_PART % 2 == 0), "tile parts");
   static_assert(CHUNKS >= 1, "at least one 32-column chunk per epilogue warp");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -856,7 +869,7 @@ template <int BN, bool FP8, int OP, int PM>
 __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_constant__ KParams p) {
   static_assert(PM == 0 || PM == 2, "pair modes: 0 single CTAs, 2 two-SM MMA pairs");
   constexpr int CL = PM == 0 ? 1 : 2;      // CTAs per cluster
-  static_assert(PM == 0 || Cfg<BN, FP8>::B_BOXES % 2 == 0, "pairs split B into two halves");
+  static_assert(PM == 0 || Cfg<BN, FP8, PM == 2>::B_BOXES % 2 == 0, "pairs split B into two halves");
   using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1062,12 +1075,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
             tma_load_2d_pair_hint(smem_u32(sA + stage * C::A_BYTES), map_a, fbl, kb * C::BK, arow, keep_a);
 #pragma unroll
             for (int jj = 0; jj < C::B_BOXES_CTA; ++jj) {
+              // smem box jj = box j of part `part`: this CTA's columns of that MMA's B operand
+              const int part = jj / C::BOXES_PART_CTA;
+              const int j = jj - part * C::BOXES_PART_CTA;
+              const int x = w.n0 + (part * C::BOXES_PART + crank * C::BOXES_PART_CTA + j) * C::B_BOX_N;
               if constexpr (OP == OP_MOE || OP == OP_MOE_COMBINE)
                 tma_load_3d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
-                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, w.e, keep_b);
+                                      x, kb * C::BK, w.e, keep_b);
               else
                 tma_load_2d_pair_hint(smem_u32(sB + stage * C::B_BYTES + jj * C::B_BOX_BYTES), map_b, fbl,
-                                      w.n0 + (crank * C::B_BOXES_CTA + jj) * C::B_BOX_N, kb * C::BK, keep_b);
+                                      x, kb * C::BK, keep_b);
             }
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
@@ -1114,8 +1131,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       bool stop = false;
       for (int it = cid; it < items && !stop; it += ncl, ++local) {
         const Item w = decode_item<OP, CL>(p, it, BN, crank);
-        const int acc = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+        const int acc = C::ACC_BUFS == 2 ? (local & 1) : 0;
+        const uint32_t aph = C::ACC_BUFS == 2 ? ((local >> 1) & 1) : (local & 1);
         if (!wait_mbar(p, tempty0 + 8 * acc, aph ^ 1u, abort_flag, 200 + acc)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -1132,17 +1149,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 #pragma unroll
           for (int k = 0; k < C::K_STEPS; ++k) {
             const uint64_t adesc = smem_desc(a_addr + k * 32, 16, C::A_SBO, C::A_LAYOUT);
-            const uint64_t bdesc = smem_desc(b_addr + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024, 2u);
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-            if constexpr (PM == 2) {
-              if constexpr (FP8)
-                umma_f8_pair(d, adesc, bdesc, C::IDESC, accum);
-              else
-                umma_bf16_pair(d, adesc, bdesc, C::IDESC, accum);
-            } else if constexpr (FP8) {
-              umma_f8(d, adesc, bdesc, C::IDESC, accum);
-            } else {
-              umma_bf16(d, adesc, bdesc, C::IDESC, accum);
+#pragma unroll
+            for (int part = 0; part < C::N_PARTS; ++part) {
+              const uint64_t bdesc =
+                  smem_desc(b_addr + part * C::B_PART_BYTES + k * C::UMMA_K * 128, C::B_BOX_BYTES, 1024, 2u);
+              const uint32_t dp = d + static_cast<uint32_t>(part * C::MMA_N);
+              if constexpr (PM == 2) {
+                if constexpr (FP8)
+                  umma_f8_pair(dp, adesc, bdesc, C::IDESC, accum);
+                else
+                  umma_bf16_pair(dp, adesc, bdesc, C::IDESC, accum);
+              } else if constexpr (FP8) {
+                umma_f8(dp, adesc, bdesc, C::IDESC, accum);
+              } else {
+                umma_bf16(dp, adesc, bdesc, C::IDESC, accum);
+              }
             }
           }
           if constexpr (PM == 0)
@@ -1385,8 +1407,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     int local = 0;
     for (int it = cid; it < items; it += ncl, ++local) {
       const Item w = decode_item<OP, CL>(p, it, BN, crank);
-      const int acc = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+      const int acc = C::ACC_BUFS == 2 ? (local & 1) : 0;
+      const uint32_t aph = C::ACC_BUFS == 2 ? ((local >> 1) & 1) : (local & 1);
       const bool read_s = chained && w.c > 0;
       const bool write_s = (chained && w.c < p.L - 1) || slotted;
       // ReduceScatter GEMM-only: every rank's partial is computed and read out of TMEM, but only the
@@ -1454,11 +1476,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
         if (read_s) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 s = ld_cg_f4_hint(sp + j * kBM * 4, once);
-            v[4 * j + 0] = s.x + v[4 * j + 0];
-            v[4 * j + 1] = s.y + v[4 * j + 1];
-            v[4 * j + 2] = s.z + v[4 * j + 2];
-            v[4 * j + 3] = s.w + v[4 * j + 3];
+            const float4 sv = ld_cg_f4_hint(sp + j * kBM * 4, once);
+            v[4 * j + 0] = sv.x + v[4 * j + 0];
+            v[4 * j + 1] = sv.y + v[4 * j + 1];
+            v[4 * j + 2] = sv.z + v[4 * j + 2];
+            v[4 * j + 3] = sv.w + v[4 * j + 3];
           }
         }
         if (write_s) {

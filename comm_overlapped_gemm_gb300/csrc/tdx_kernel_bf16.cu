@@ -5,7 +5,11 @@ namespace tdx {
 
 cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
   if (pm != 0) {
-    if (block_n != 256 || pm != 2) return cudaErrorInvalidValue;
+    if (pm != 2) return cudaErrorInvalidValue;
+    if (block_n == 512)
+      return op == OP_AG ? launch_fused_t<512, false, OP_AG, 2>(p, grid, stream)
+                         : launch_fused_t<512, false, OP_RS, 2>(p, grid, stream);
+    if (block_n != 256) return cudaErrorInvalidValue;
     return op == OP_AG ? launch_fused_t<256, false, OP_AG, 2>(p, grid, stream)
                        : launch_fused_t<256, false, OP_RS, 2>(p, grid, stream);
   }
@@ -25,9 +29,11 @@ cudaError_t launch_fused_bf16(int op, int block_n, int pm, const KParams& p, int
   }
 }
 
-int fused_max_grid_bf16(int op, int pm, int sms) {
+int fused_max_grid_bf16(int op, int pm, int sms, int block_n) {
   if (pm == 0) return sms;
   if (pm != 2) return 0;
+  if (block_n == 512)
+    return op == OP_AG ? max_grid_t<512, false, OP_AG, 2>(sms) : max_grid_t<512, false, OP_RS, 2>(sms);
   return op == OP_AG ? max_grid_t<256, false, OP_AG, 2>(sms) : max_grid_t<256, false, OP_RS, 2>(sms);
 }
 

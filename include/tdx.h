@@ -101,7 +101,9 @@ typedef struct tdx_opts {
   void* trace;               /* optional device buffer of tdx_trace_size() bytes, or NULL */
   int num_sms;               /* persistent grid size; 0 = every SM of the device */
   int split_k;               /* AG: K splits reduced in fixed order (0 = library choice, 1 = none) */
-  int block_n;               /* GEMM tile width 64/128/256 (0 = library choice) */
+  int block_n;               /* GEMM tile width 64/128/256, or 512 on 2-SM pairs (cluster 3; one
+                                512-column accumulator per CTA, two MMAs per K step; bf16 and e4m3
+                                AllGather / ReduceScatter / AllReduce). 0 = library choice */
   int reduce_mode;           /* fixed-order reduction of RS ranks / AG K splits: 0 = library choice,
                                 1 = chained (element c adds its partial to the running sum of
                                 elements 0..c-1 and hands it on), 2 = slotted (each element stores its

@@ -156,6 +156,8 @@ def test_ag_validation_codes(tdx):
     assert _ag(tdx, opts=tdx.make_opts(block_n=96)) == tdx.TDX_ERR_UNSUPPORTED
     assert _ag(tdx, opts=tdx.make_opts(cluster=4)) == tdx.TDX_ERR_INVALID_ARG
     assert _ag(tdx, opts=tdx.make_opts(cluster=3, block_n=128)) == tdx.TDX_ERR_UNSUPPORTED
+    # 512-wide tiles need 2-SM pairs
+    assert _ag(tdx, opts=tdx.make_opts(cluster=1, block_n=512)) == tdx.TDX_ERR_UNSUPPORTED
     # pairs sharing B through multicast loads are not offered
     assert _ag(tdx, M_local=256, opts=tdx.make_opts(cluster=2, block_n=256)) == tdx.TDX_ERR_UNSUPPORTED
     assert _ag(tdx, dtype=1, opts=tdx.make_opts(block_n=64)) == tdx.TDX_ERR_UNSUPPORTED
@@ -213,7 +215,7 @@ def test_bf16_partials_plan(tdx):
 PLANS = [
     # (name, op, W, M_local or M, K, N, chunk_rows, expected plan words)
     ("AG W=8", "OP_AG", 8, 1024, 8192, 3584, 0,
-     dict(BN=256, L=1, cluster=3, tiles_m=64, tiles_n=14, n_chunks=8, chunk_rows=128, pull_a=0)),
+     dict(BN=512, L=1, cluster=3, tiles_m=64, tiles_n=7, n_chunks=8, chunk_rows=128, pull_a=0)),
     ("RS W=8", "OP_RS", 8, 8192, 3584, 8192, 0,
      dict(BN=256, L=8, cluster=3, reduce_mode=1, group_n=16, tiles_m=64, tiles_n=32, coop_fold=0)),
     ("small-M AG", "OP_AG", 8, 16, 8192, 1024, 16,
@@ -232,7 +234,8 @@ PLANS = [
 @pytest.mark.parametrize("case", PLANS, ids=[c[0] for c in PLANS])
 def test_planner_choices_for_the_workloads(tdx, case):
     """Tile width, K splits, CTA cooperation and reduction chosen for the measured workloads and a
-    few neighbours (a 152-SM device): 2-SM pairs with a chained running sum for the large RS,
+    few neighbours (a 152-SM device): 512-wide 2-SM pair tiles for the large AllGather, 2-SM pairs
+    of 256-wide tiles with a chained running sum for the large RS,
     128-wide tiles over 16 K splits that read the shards in place and fold cooperatively for the
     small-M AllGather, 256-wide tiles with a grid-wide fold for the small-M ReduceScatter (two waves
     of work but only 32 tiles)."""

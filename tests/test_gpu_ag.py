@@ -410,3 +410,28 @@ def test_ag_split_k_cooperative_fold(integer):
     case.C.fill_(float("nan"))
     tdx.check(case.run(tdx.make_opts(timeout_ns=int(5e8), chunk_rows=16, split_k=8, epoch=2, perturb_seed=5)))
     assert np.array_equal(case.result_bits(), first)
+
+
+@pytest.mark.parametrize("name", ["ag_w8", "ag_fp8_w8"])
+@pytest.mark.parametrize("shape", [dict(W=4, M=256, K=1024, N=1024), dict(W=2, M=384, K=512, N=1344)])
+def test_ag_wide_tiles(name, shape):
+    # 512-column tiles on 2-SM pairs (two MMAs per K step into one 512-column accumulator): exact on
+    # integers, and the same bits as 256-column pairs on random inputs (ragged N included; one K
+    # split for both, since the library would split K differently for the two tile counts)
+    wl = wls.with_shape(wls.WORKLOADS[name], chunk_rows=128, **shape)
+    for integer in (True, False):
+        inp = wls.make_inputs(wl, integer=integer)
+        kw = dict(scale_a=inp.scale_a, scale_b=inp.scale_b[0]) if wl.dtype == "e4m3" else {}
+        bits = []
+        for bn in (512, 256):
+            o = opts(cluster=3, block_n=bn, split_k=1, **kw)
+            assert tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, 1 if wl.dtype == "e4m3" else 0, o)["BN"] == bn
+            case = AGCase(inp, opts=o)
+            tdx.check(case.run())
+            status_ok(case)
+            bits.append(case.result_bits())
+            if integer:
+                assert_bit_exact(bits[-1], case.oracle(), "bf16")
+            else:
+                assert_within_tol(case.result(), case.oracle(), wl.dtype)
+        assert np.array_equal(bits[0], bits[1])

@@ -419,3 +419,35 @@ def test_rs_e4m3_bf16_partials():
     tdx.check(case.run())
     status_ok(case)
     assert_bit_exact(case.result_bits(), case.oracle(partials="bf16"), "bf16")
+
+
+@pytest.mark.parametrize("variant", [dict(reduce_mode=1), dict(reduce_mode=2)])
+@pytest.mark.parametrize("shape", [dict(W=4, M=512, K=512, N=1024), dict(W=3, M=768, K=256, N=1344)])
+def test_rs_wide_tiles(variant, shape):
+    wl = wls.with_shape(wls.WORKLOADS["rs_w8"], **shape)
+    for integer in (True, False):
+        inp = wls.make_inputs(wl, integer=integer)
+        bits = []
+        for bn in (512, 256):
+            case = RSCase(inp, opts=opts(cluster=3, block_n=bn, perturb_seed=5, **variant))
+            tdx.check(case.run())
+            status_ok(case)
+            bits.append(case.result_bits())
+            if integer:
+                assert_bit_exact(bits[-1], case.oracle(), "bf16")
+            else:
+                assert_within_tol(case.result(), case.oracle(), "bf16")
+        assert np.array_equal(bits[0], bits[1])
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_rs_e4m3_wide_tiles(integer):
+    wl = wls.with_shape(wls.WORKLOADS["rs_fp8_w8"], W=4, M=512, K=1024, N=1024)
+    inp = wls.make_inputs(wl, integer=integer)
+    case = RSCase(inp, opts=opts(scale_a=inp.scale_a, scale_b=inp.scale_b, cluster=3, block_n=512))
+    tdx.check(case.run())
+    status_ok(case)
+    if integer:
+        assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    else:
+        assert_within_tol(case.result(), case.oracle(), "e4m3")
