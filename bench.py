@@ -405,19 +405,20 @@ def rs_case(tdx, torch, wl, dev, **kw):
     return call, status
 
 
-def moe_case(tdx, torch, wl, dev):
-    """Device buffers + a timed call for one MoE dispatch + grouped GEMM workload."""
+def moe_case(tdx, torch, wl, dev, **extra):
+    """Device buffers + a timed call for one MoE dispatch + grouped GEMM workload; ``extra`` are
+    tdx_opts fields (tiling)."""
     import workloads as wls
     inp = wls.make_inputs(wl)
     view = np.int16 if wl.dtype == "bf16" else np.uint8
     dt = tdx.TDX_BF16 if wl.dtype == "bf16" else tdx.TDX_FP8_E4M3
-    kw = {} if wl.dtype == "bf16" else dict(scale_a=inp.scale_a, scale_b=inp.scale_b)
+    kw = dict(extra) if wl.dtype == "bf16" else dict(extra, scale_a=inp.scale_a, scale_b=inp.scale_b)
     X = [torch.from_numpy(np.ascontiguousarray(a).view(view)).to(dev) for a in inp.a]
     route = [torch.from_numpy(np.ascontiguousarray(r)).to(dev) for r in inp.route]
     B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(view)).to(dev)
     Y = torch.empty((wl.M_total, wl.N), dtype=torch.bfloat16, device=dev)
     dest = torch.empty((wl.W, wl.M, wl.topk), dtype=torch.int32, device=dev)
-    ws = torch.empty(tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, dt),
+    ws = torch.empty(tdx.tdx_moe_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, dt, tdx.make_opts(**kw)),
                      dtype=torch.uint8, device=dev)
     tdx.check(tdx.tdx_workspace_init(ws))
     state = {"epoch": 0}
@@ -964,16 +965,23 @@ def run_moe_case(args):
     import workloads as wls
     W, T, K, N, E, k = (int(x) for x in args.shape.split(","))
     name = "moe_w8" if args.case == "moe" else "moe_combine_w8"
+    if args.case == "moe" and args.dtype == "e4m3":
+        name = "moe_fp8_w8"
     wl = wls.with_shape(wls.WORKLOADS[name], W=W, M=T, K=K, N=N, E=E, topk=k)
     dev = torch.device("cuda", 0)
-    call, status = (moe_case if args.case == "moe" else combine_case)(tdx, torch, wl, dev)
+    extra = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in filter(None, args.opts.split(","))}
+    if args.case == "moe":
+        call, status = moe_case(tdx, torch, wl, dev, **extra)
+    else:
+        call, status = combine_case(tdx, torch, wl, dev)
     mode = {"fused": 0, "gemm": 1, "move": 2}[args.mode]
     for _ in range(args.warmup + args.steps):
         call(mode=mode)
     torch.cuda.synchronize()
     status()
     ms = time_mode(torch, lambda: call(mode=mode), 5)
-    print(json.dumps({"case": args.case, "shape": [W, T, K, N, E, k], "mode": args.mode, "ms": ms,
+    print(json.dumps({"case": args.case, "shape": [W, T, K, N, E, k], "dtype": args.dtype, "opts": extra,
+                      "mode": args.mode, "ms": ms,
                       "tflops": wl.flops / (ms * 1e-3) / 1e12}))
     return 0
 
@@ -989,6 +997,7 @@ def main():
     ap.add_argument("--case", choices=["ag", "rs", "moe", "moe_combine"], default=None)
     ap.add_argument("--mode", choices=["fused", "gemm", "move"], default="fused", help="--case only: which part runs")
     ap.add_argument("--shape", default="8,1024,8192,3584")
+    ap.add_argument("--dtype", choices=["bf16", "e4m3"], default="bf16", help="--case moe only")
     ap.add_argument("--opts", default="", help="--case only: tdx_opts fields, e.g. block_n=256,split_k=4")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     args = ap.parse_args()

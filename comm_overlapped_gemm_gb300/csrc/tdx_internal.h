@@ -147,7 +147,7 @@ cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t stream);
 cudaError_t launch_fused_moe_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fused_moe_fp8(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream);
-int fused_max_grid_moe(bool combine, int pm, int sms, bool fp8 = false);
+int fused_max_grid_moe(bool combine, int pm, int sms, bool fp8, int block_n);
 
 // MoE routing layout: from every rank's top-k expert ids, the dispatched row of every (rank, token,
 // slot), the source of every dispatched row, the expert row offsets and the GEMM tile table.

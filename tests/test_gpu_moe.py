@@ -270,3 +270,28 @@ def test_moe_empty_and_skewed_experts(case_name, dtype):
         status_ok(case)
         check_layout(case, lay)
         assert_bit_exact(case.result_bits(), want, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_moe_wide_tiles_match_256(dtype):
+    # 512-column tiles on 2-SM pairs for the dispatch's grouped GEMM: the same bits as 256 columns
+    # (the K accumulation is the same), exact on integers; ragged F (1344 = 2.6 tiles of 512)
+    name = "moe_w8" if dtype == "bf16" else "moe_fp8_w8"
+    wl = wls.with_shape(wls.WORKLOADS[name], W=4, M=300, K=512, N=1344, E=8, topk=3)
+    for integer in (True, False):
+        inp = wls.make_inputs(wl, integer=integer)
+        kw = dict(scale_a=inp.scale_a, scale_b=inp.scale_b) if dtype == "e4m3" else {}
+        want, _ = MO.moe_dispatch_gemm(inp.a, inp.route, inp.b[0], wl.E, dtype=dtype,
+                                       scale_x=kw.get("scale_a"), scale_b=kw.get("scale_b"))
+        bits = []
+        for bn in (512, 256):
+            case = MoECase(inp, opts=opts(block_n=bn, cluster=3, **kw))
+            assert case.plan()["BN"] == bn and case.plan()["cluster"] == 3
+            tdx.check(case.run())
+            status_ok(case)
+            bits.append(case.result_bits())
+            if integer:
+                assert_bit_exact(bits[-1], want, "bf16")
+            else:
+                assert_within_tol(R.decode_bf16(bits[-1]), want, dtype)
+        assert np.array_equal(bits[0], bits[1])
