@@ -437,8 +437,9 @@ def moe_case(tdx, torch, wl, dev, **extra):
     return call, status
 
 
-def combine_case(tdx, torch, wl, dev):
-    """Device buffers + a timed call for one MoE grouped GEMM + combine workload."""
+def combine_case(tdx, torch, wl, dev, **extra):
+    """Device buffers + a timed call for one MoE grouped GEMM + combine workload; ``extra`` are
+    tdx_opts fields (tiling)."""
     import workloads as wls
     inp = wls.make_inputs(wl)
     Hd = torch.from_numpy(np.ascontiguousarray(inp.a[0]).view(np.int16)).to(dev)
@@ -446,14 +447,15 @@ def combine_case(tdx, torch, wl, dev):
     gates = [torch.from_numpy(np.ascontiguousarray(g)).to(dev) for g in inp.gates]
     B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(np.int16)).to(dev)
     out = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
-    ws = torch.empty(tdx.tdx_moe_combine_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16),
+    ws = torch.empty(tdx.tdx_moe_combine_workspace_size(wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk, tdx.TDX_BF16,
+                                                        tdx.make_opts(**extra)),
                      dtype=torch.uint8, device=dev)
     tdx.check(tdx.tdx_workspace_init(ws))
     state = {"epoch": 0}
 
     def call(mode=0, epoch=None):
         state["epoch"] += 1
-        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode)
+        o = tdx.make_opts(epoch=state["epoch"] if epoch is None else epoch, mode=mode, **extra)
         tdx.check(tdx.tdx_moe_gemm_combine(Hd, route, B, gates, out, ws, wl.W, wl.M, wl.K, wl.N, wl.E, wl.topk,
                                            tdx.TDX_BF16, o))
 
@@ -973,7 +975,7 @@ def run_moe_case(args):
     if args.case == "moe":
         call, status = moe_case(tdx, torch, wl, dev, **extra)
     else:
-        call, status = combine_case(tdx, torch, wl, dev)
+        call, status = combine_case(tdx, torch, wl, dev, **extra)
     mode = {"fused": 0, "gemm": 1, "move": 2}[args.mode]
     for _ in range(args.warmup + args.steps):
         call(mode=mode)

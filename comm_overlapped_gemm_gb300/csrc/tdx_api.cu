@@ -757,8 +757,8 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   int bn = o.block_n;
   if (bn != 0 && bn != 64 && bn != 128 && bn != 256 && bn != 512) return TDX_ERR_UNSUPPORTED;
   if (fp8 && bn == 64) return TDX_ERR_UNSUPPORTED;   // e4m3 B boxes are 128 columns wide
-  // 512-column tiles: the dispatch's grouped GEMM on 2-SM pairs (its epilogue only stores Y)
-  if (bn == 512 && (combine || o.cluster == 1)) return TDX_ERR_UNSUPPORTED;
+  // 512-column tiles run on 2-SM pairs
+  if (bn == 512 && o.cluster == 1) return TDX_ERR_UNSUPPORTED;
   if (bn == 0) bn = F > 128 ? 256 : ((F > 64 || fp8) ? 128 : 64);
   p.BN = bn;
   p.tiles_n = (F + bn - 1) / bn;

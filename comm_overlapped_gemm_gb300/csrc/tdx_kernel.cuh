@@ -772,89 +772,94 @@ static __device__ __forceinline__ void moe_combine_units(const KParams& p, const
     int nd = 0;
     float ng = 0.0f;
     if (q + 1 < npairs) meta(q + 1, nd, ng);
-    int tok[2], c[2];
-    bool live[2], full[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const long long u = 2 * q + h;
-      live[h] = u < count;
-      tok[h] = 0;
-      c[h] = 0;
-      if (live[h]) {
-        int c0;
-        moe_unit(p, tasks, first + u * stride, col0, BN, tok[h], c0);
-        c[h] = c0 + 8 * lane;
-        live[h] = 8 * lane < BN && c[h] < p.N;
-      }
-      full[h] = c[h] + 8 <= p.N;
-    }
-    float acc[2][8];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
-    // slots in groups of 8 per unit: a group's loads of both units are in flight together, the sum
-    // keeps slot order
+    // a warp covers 256 columns (8 per lane) at a time: tiles wider than that are walked in
+    // 256-column blocks
 #pragma unroll 1
-    for (int j0 = 0; j0 < k; j0 += 8) {
-      uint4 zr[2][8];
+    for (int cb = 0; cb < BN; cb += 256) {
+      int tok[2], c[2];
+      bool live[2], full[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        const long long u = 2 * q + h;
+        live[h] = u < count;
+        tok[h] = 0;
+        c[h] = 0;
+        if (live[h]) {
+          int c0;
+          moe_unit(p, tasks, first + u * stride, col0, BN, tok[h], c0);
+          c[h] = c0 + cb + 8 * lane;
+          live[h] = cb + 8 * lane < BN && c[h] < p.N;
+        }
+        full[h] = c[h] + 8 <= p.N;
+      }
+      float acc[2][8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj;
-          const int d = __shfl_sync(0xFFFFFFFFu, cd, 16 * h + (j & 15));
-          zr[h][jj] = make_uint4(0u, 0u, 0u, 0u);
-          if (j < k && live[h]) {
-            const uint8_t* zp = p.G + (size_t)d * p.N * 2 + (size_t)c[h] * 2;
-            if (full[h]) {
-              zr[h][jj] = ld_cg_v4_hint(zp, once);
-            } else {
-              uint16_t hv[8];
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-              for (int i = 0; i < 8; ++i) hv[i] = c[h] + i < p.N ? reinterpret_cast<const uint16_t*>(zp)[i] : 0;
-              zr[h][jj] = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16),
-                                     hv[4] | (uint32_t(hv[5]) << 16), hv[6] | (uint32_t(hv[7]) << 16));
+        for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
+      // slots in groups of 8 per unit: a group's loads of both units are in flight together, the sum
+      // keeps slot order
+#pragma unroll 1
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4 zr[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = j0 + jj;
+            const int d = __shfl_sync(0xFFFFFFFFu, cd, 16 * h + (j & 15));
+            zr[h][jj] = make_uint4(0u, 0u, 0u, 0u);
+            if (j < k && live[h]) {
+              const uint8_t* zp = p.G + (size_t)d * p.N * 2 + (size_t)c[h] * 2;
+              if (full[h]) {
+                zr[h][jj] = ld_cg_v4_hint(zp, once);
+              } else {
+                uint16_t hv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hv[i] = c[h] + i < p.N ? reinterpret_cast<const uint16_t*>(zp)[i] : 0;
+                zr[h][jj] = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16),
+                                       hv[4] | (uint32_t(hv[5]) << 16), hv[6] | (uint32_t(hv[7]) << 16));
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = j0 + jj;
+            const float g = __shfl_sync(0xFFFFFFFFu, cg, 16 * h + (j & 15));
+            if (j < k) {
+              float z[8];
+              unpack_bf16x8(zr[h][jj], z);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(g, z[i], acc[h][i]);
             }
           }
         }
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        if (!live[h]) continue;
+        const int s = tok[h] / p.moe_T;
+        const int t = tok[h] - s * p.moe_T;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[s] + (size_t)t * p.N * 2) + c[h];
+        if (full[h]) {
+          uint4 pk;
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[h][0], acc[h][1]);
+          __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[h][2], acc[h][3]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[h][4], acc[h][5]);
+          __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[h][6], acc[h][7]);
+          pk.x = *reinterpret_cast<uint32_t*>(&b0);
+          pk.y = *reinterpret_cast<uint32_t*>(&b1);
+          pk.z = *reinterpret_cast<uint32_t*>(&b2);
+          pk.w = *reinterpret_cast<uint32_t*>(&b3);
+          st_v4(o, pk);
+        } else {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj;
-          const float g = __shfl_sync(0xFFFFFFFFu, cg, 16 * h + (j & 15));
-          if (j < k) {
-            float z[8];
-            unpack_bf16x8(zr[h][jj], z);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(g, z[i], acc[h][i]);
-          }
+          for (int i = 0; i < 8; ++i)
+            if (c[h] + i < p.N) o[i] = __float2bfloat16_rn(acc[h][i]);
         }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (!live[h]) continue;
-      const int s = tok[h] / p.moe_T;
-      const int t = tok[h] - s * p.moe_T;
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out[s] + (size_t)t * p.N * 2) + c[h];
-      if (full[h]) {
-        uint4 pk;
-        __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[h][0], acc[h][1]);
-        __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[h][2], acc[h][3]);
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[h][4], acc[h][5]);
-        __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[h][6], acc[h][7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&b0);
-        pk.y = *reinterpret_cast<uint32_t*>(&b1);
-        pk.z = *reinterpret_cast<uint32_t*>(&b2);
-        pk.w = *reinterpret_cast<uint32_t*>(&b3);
-        st_v4(o, pk);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (c[h] + i < p.N) o[i] = __float2bfloat16_rn(acc[h][i]);
       }
     }
     cd = nd;

@@ -201,7 +201,9 @@ cudaError_t launch_fused_moe_bf16(int block_n, int pm, const KParams& p, int gri
 
 cudaError_t launch_fused_moe_combine_bf16(int block_n, int pm, const KParams& p, int grid, cudaStream_t stream) {
   if (pm == 2)
-    return block_n == 256 ? launch_fused_t<256, false, OP_MOE_COMBINE, 2>(p, grid, stream) : cudaErrorInvalidValue;
+    return block_n == 256   ? launch_fused_t<256, false, OP_MOE_COMBINE, 2>(p, grid, stream)
+           : block_n == 512 ? launch_fused_t<512, false, OP_MOE_COMBINE, 2>(p, grid, stream)
+                            : cudaErrorInvalidValue;
   switch (block_n) {
     case 64: return launch_fused_t<64, false, OP_MOE_COMBINE, 0>(p, grid, stream);
     case 128: return launch_fused_t<128, false, OP_MOE_COMBINE, 0>(p, grid, stream);
@@ -224,8 +226,9 @@ cudaError_t launch_fused_moe_fp8(int block_n, int pm, const KParams& p, int grid
 
 int fused_max_grid_moe(bool combine, int pm, int sms, bool fp8, int block_n) {
   if (pm != 2) return sms;
-  if (block_n == 512 && !combine)
-    return fp8 ? max_grid_t<512, true, OP_MOE, 2>(sms) : max_grid_t<512, false, OP_MOE, 2>(sms);
+  if (block_n == 512)
+    return combine ? max_grid_t<512, false, OP_MOE_COMBINE, 2>(sms)
+                   : (fp8 ? max_grid_t<512, true, OP_MOE, 2>(sms) : max_grid_t<512, false, OP_MOE, 2>(sms));
   if (fp8) return max_grid_t<256, true, OP_MOE, 2>(sms);
   return combine ? max_grid_t<256, false, OP_MOE_COMBINE, 2>(sms) : max_grid_t<256, false, OP_MOE, 2>(sms);
 }

@@ -367,10 +367,9 @@ def test_moe_plan(tdx):
     assert tdx.tdx_moe_plan_info(8, 4096, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(block_n=256))["BN"] == 256
     with pytest.raises(tdx.TdxError):
         tdx.tdx_moe_plan_info(8, 4096, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(block_n=512, cluster=1))
-    # the combine keeps 256-column tiles and takes no 512
+    # the combine keeps 256-column tiles unless asked for 512 (pairs)
     assert tdx.tdx_moe_combine_plan_info(8, 4096, 2048, 7168, 64, 8, tdx.TDX_BF16)["BN"] == 256
-    with pytest.raises(tdx.TdxError):
-        tdx.tdx_moe_combine_plan_info(8, 4096, 2048, 7168, 64, 8, tdx.TDX_BF16, tdx.make_opts(block_n=512))
+    assert tdx.tdx_moe_combine_plan_info(8, 4096, 2048, 7168, 64, 8, tdx.TDX_BF16, tdx.make_opts(block_n=512))["BN"] == 512
     assert p["total"] - p["off_R"] == 262144 * 7168 * 2
 
 

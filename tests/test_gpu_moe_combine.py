@@ -156,3 +156,22 @@ def test_combine_alone_matches_fused(topk):
         tdx.check(case.run(opts(block_n=bn, mode=tdx.TDX_MOVE_ONLY, epoch=3)))
         status_ok(case)
         assert np.array_equal(case.result_bits(), fused), f"topk={topk} bn={bn}"
+
+
+def test_combine_wide_tiles_match_256():
+    # 512-column pair tiles for the combine's grouped GEMM: the same expert outputs and combined
+    # tokens as 256 columns; exact on integers; ragged H (1344)
+    wl = wls.with_shape(wls.WORKLOADS["moe_combine_w8"], W=4, M=300, K=512, N=1344, E=8, topk=3)
+    for integer in (True, False):
+        inp = wls.make_inputs(wl, integer=integer)
+        bits = []
+        for bn in (512, 256):
+            case = CombineCase(inp, opts=opts(block_n=bn, cluster=3))
+            assert case.plan()["BN"] == bn
+            tdx.check(case.run())
+            status_ok(case)
+            bits.append(case.result_bits())
+        want = np.stack(MO.moe_gemm_combine(inp.a[0], inp.route, inp.b[0], inp.gates, wl.E, z_dtype="bf16"))
+        if integer:
+            assert_bit_exact(bits[0], want, "bf16")
+        assert np.array_equal(bits[0], bits[1])
