@@ -62,7 +62,8 @@ enum FailRole { ROLE_FLAG = 1, ROLE_PIPE = 2, ROLE_CHAIN = 3, ROLE_PRODUCER = 4,
 enum DevStatus { DEV_OK = 0, DEV_BAD_INPUT = 1, DEV_TIMEOUT = 6, DEV_STALE = 7 };
 
 // Word offsets in the workspace header (first 4 KiB): the status word and its details, then the
-// device-kept epoch (the last completed call's epoch) and the count of CTAs that finished this call.
+// device-kept epoch (the last completed call's epoch) and the count of this call's CTAs that have
+// read it (reset by the CTA that completes the count).
 constexpr size_t kHeaderBytes = 4096;
 constexpr int kStatusWords = 8;
 constexpr int kDevEpochWord = 16;
@@ -119,7 +120,7 @@ struct KParams {
   uint32_t* moe_cnt;             // MoE combine: arrivals per (token, N-tile), reset by the last
   float moe_bscale[kMoeMaxExperts];   // MoE e4m3: per-expert weight scale (row_scale: per source rank)
   uint32_t epoch;                // this call's epoch (unused when dev_epoch is set)
-  uint32_t* dev_epoch;           // device-kept epochs: [0] last completed call's epoch, [1] CTAs done
+  uint32_t* dev_epoch;           // device-kept epochs: [0] last completed call's epoch, [1] CTAs that read it
   uint64_t timeout_ns;
   uint32_t perturb;
   int piece_bytes;               // producer copy unit (multiple of kCopyRoundBytes)

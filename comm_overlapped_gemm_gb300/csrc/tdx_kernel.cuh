@@ -633,6 +633,12 @@ __device__ __forceinline__ void store_out_4(const KParams& p, int row, int col, 
   }
 }
 
+// Slots whose loads a cooperative-fold thread keeps in flight at once.
+#ifndef TDX_FOLD_GROUP
+#define TDX_FOLD_GROUP 8
+#endif
+constexpr int kFoldGroup = TDX_FOLD_GROUP;
+
 // Fold part `part` of `nparts` of tile `tile`: float4 blocks [part*per, (part+1)*per) of the slot
 // layout (float4 f holds row f % 128, columns 32*(f/1024) + 4*((f/128) % 8) .. +3), every one of
 // the L slots added in order 0..L-1, rounded once and stored. Called by all epilogue threads.
@@ -646,17 +652,18 @@ __device__ __forceinline__ void fold_part(const KParams& p, int tile, int part, 
   const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)tile * N4;
   const int m0 = (tile / p.tiles_n) * kBM;
   const int n0 = (tile % p.tiles_n) * BN;
+#pragma unroll 1
   for (int f = f0 + et; f < f1; f += kEpiThreads) {
-    // slots in groups of 8: a group's loads are all in flight before the in-order adds
+    // slots in groups of kFoldGroup: a group's loads are all in flight before the in-order adds
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 1
-    for (int c0 = 0; c0 < p.L; c0 += 8) {
-      float4 sv[8];
+    for (int c0 = 0; c0 < p.L; c0 += kFoldGroup) {
+      float4 sv[kFoldGroup];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
+      for (int c = 0; c < kFoldGroup; ++c)
         if (c0 + c < p.L) sv[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4 + f, pol);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < kFoldGroup; ++c) {
         if (c0 + c < p.L) {
           if (c0 + c == 0) {
             acc = sv[c];
@@ -901,9 +908,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   const int lane = threadIdx.x & 31;
   const uint64_t t_entry = globaltimer_ns();
 
+  // Device-kept epochs: every CTA reads the last completed call's epoch at its start and, once it
+  // is in shared memory, counts itself in; the CTA whose count completes the grid knows that every
+  // CTA has read it, and publishes this call's epoch at its end (the next call, stream-ordered after
+  // this kernel, reads it at its start). An epilogue thread, idle until the first accumulator,
+  // takes the count, so its round trip is off the kernel's critical path and its tail.
+  uint32_t publish_old = 0u;
   if (threadIdx.x == 0) {
-    // device-kept epochs: the workspace holds the last completed call's epoch (every CTA reads it
-    // before any CTA of this call can have finished, so all agree)
     misc[7] = p.dev_epoch != nullptr ? ld_relaxed_gpu(p.dev_epoch) + 1u : p.epoch;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -941,6 +952,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   const uint64_t t_setup = globaltimer_ns();
   const uint32_t tmem_base = misc[0];
   const uint32_t epoch = misc[7];
+  if (p.dev_epoch != nullptr && threadIdx.x == kEpiWarp0 * 32) publish_old = atomicAdd(p.dev_epoch + 1, 1u);
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const bool leader = crank == 0;           // PM 2: the CTA that issues the pair's MMAs
   const int cid = blockIdx.x / CL;          // cluster index
@@ -1793,15 +1805,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (p.dev_epoch != nullptr && threadIdx.x == 0) {
-    // device-kept epochs: the last CTA to finish publishes this call's epoch for the next call
-    // (which, being stream-ordered after this kernel, reads it at its start) and resets the count
-    __threadfence();
-    if (atomicAdd(p.dev_epoch + 1, 1u) == gridDim.x - 1) {
-      p.dev_epoch[1] = 0u;
-      p.dev_epoch[0] = epoch;
-      __threadfence();
-    }
+  if (p.dev_epoch != nullptr && threadIdx.x == kEpiWarp0 * 32 && publish_old == gridDim.x - 1) {
+    // the CTA that completed the start count publishes this call's epoch and resets the count
+    p.dev_epoch[1] = 0u;
+    p.dev_epoch[0] = epoch;
   }
 }
 
