@@ -106,11 +106,20 @@ namespace tdx {
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
 #endif
+// AllGather: GEMM ring budget and largest bulk-copy staging ring (KiB). 168 / 80 (three 2-SM pair
+// stages of a 512-column tile, a 2.5x staging ring) copied faster alone (0.108 -> 0.089 ms) but
+// slowed the GEMM, e4m3 most (fused 0.683 -> 0.731 ms).
+#ifndef TDX_AG_RING_KB
+#define TDX_AG_RING_KB 216
+#endif
+#ifndef TDX_AG_STG_MAX_KB
+#define TDX_AG_STG_MAX_KB 32
+#endif
 
 // PAIR_MMA: the CTA is one half of a 2-SM MMA pair (tcgen05 cta_group::2). The pair computes a
 // 256 x BN tile with one instruction stream issued by the leader; each CTA stages its own 128 rows
 // of A and its half (BN/2 columns) of the B slice, and holds its 128 x BN accumulator in TMEM.
-template <int BN, bool FP8, bool PAIR_MMA = false, int RING_KB = 216>
+template <int BN, bool FP8, bool PAIR_MMA = false, int RING_KB = 216, int STG_MAX_KB = TDX_MOE_STG_MAX_KB>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
   // K bytes per ring slot (k_slice_bytes): A rows in a slot are KB bytes long; B keeps 128-byte MN
@@ -146,10 +155,10 @@ struct Cfg {
   // flags/decisions (64 B), MoE producer row sources (kBM ints) and staging barriers (8)
   static constexpr int MISC_BYTES = 64 + kBM * 4 + 8 * 8;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
-  // MoE dispatch staging ring for bulk row copies: what the GEMM ring leaves of the 227 KiB, at
-  // most 32 KiB, in whole KiB (at least 4 KiB)
+  // staging ring for bulk copies (MoE dispatch, AllGather producer): what the GEMM ring leaves of
+  // the 227 KiB, at most STG_MAX_KB, in whole KiB (at least 4 KiB)
   static constexpr int MOE_STG_RAW = 227 * 1024 - SMEM_BYTES - 128;
-  static constexpr int MOE_STG = (MOE_STG_RAW > TDX_MOE_STG_MAX_KB * 1024 ? TDX_MOE_STG_MAX_KB * 1024 : MOE_STG_RAW) / 1024 * 1024;
+  static constexpr int MOE_STG = (MOE_STG_RAW > STG_MAX_KB * 1024 ? STG_MAX_KB * 1024 : MOE_STG_RAW) / 1024 * 1024;
   static constexpr int COLS_PER_WARP = BN / 2;    // 8 epilogue warps = 4 lane quarters x 2 halves
   static constexpr int CHUNKS = COLS_PER_WARP / 32;
   // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B type (bits 7-9, 10-12: bf16 = 1,
@@ -171,7 +180,8 @@ struct Cfg {
 #ifndef TDX_MOE_RING_KB
 #define TDX_MOE_RING_KB 216
 #endif
-constexpr int ring_kb(int op) { return op == OP_MOE ? TDX_MOE_RING_KB : 216; }
+constexpr int ring_kb(int op) { return op == OP_MOE ? TDX_MOE_RING_KB : op == OP_AG ? TDX_AG_RING_KB : 216; }
+constexpr int stg_kb(int op) { return op == OP_AG ? TDX_AG_STG_MAX_KB : TDX_MOE_STG_MAX_KB; }
 // Ops whose producer moves data with bulk copies through a shared-memory staging ring.
 constexpr bool uses_staging(int op) { return op == OP_MOE || (op == OP_AG && TDX_AG_BULK != 0); }
 
@@ -882,7 +892,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   static_assert(PM == 0 || PM == 2, "pair modes: 0 single CTAs, 2 two-SM MMA pairs");
   constexpr int CL = PM == 0 ? 1 : 2;      // CTAs per cluster
   static_assert(PM == 0 || Cfg<BN, FP8, PM == 2>::B_BOXES % 2 == 0, "pairs split B into two halves");
-  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
+  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP), stg_kb(OP)>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1814,7 +1824,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
 
 template <int BN, bool FP8, int OP, int PM>
 cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
+  using C = Cfg<BN, FP8, PM == 2, ring_kb(OP), stg_kb(OP)>;
   constexpr int CL = PM == 0 ? 1 : 2;
   // the staging ring / fold region (128-byte aligned) follows the GEMM's shared memory
   constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
@@ -1861,7 +1871,7 @@ int max_grid_t(int sms) {
   if constexpr (CL == 1) {
     return sms;
   } else {
-    using C = Cfg<BN, FP8, PM == 2, ring_kb(OP)>;
+    using C = Cfg<BN, FP8, PM == 2, ring_kb(OP), stg_kb(OP)>;
     constexpr int kSmem = C::SMEM_BYTES + (uses_staging(OP) ? 128 + C::MOE_STG : 0);
     static std::atomic<int> cache[64];
     int dev = 0;
