@@ -212,6 +212,7 @@ def test_ag_device_epochs_eager_and_graph():
         assert np.array_equal(case.result_bits(), want)
         status_ok(case)
         assert int(case.ws[64:68].view(torch.int32).item()) == call          # header word 16
+        assert int(case.ws[68:72].view(torch.int32).item()) == 0             # start count, reset
         f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
         assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, call))
     s = torch.cuda.Stream()
@@ -229,6 +230,27 @@ def test_ag_device_epochs_eager_and_graph():
         assert np.array_equal(case.result_bits(), want)
     status_ok(case)
     assert int(case.ws[64:68].view(torch.int32).item()) == 3 + 2 * 3
+
+
+@pytest.mark.parametrize("shape", [dict(W=8, M=16, K=2048, N=512, chunk_rows=16),      # pull tiles, K splits
+                                   dict(W=4, M=256, K=512, N=1024, chunk_rows=128)])  # 2-SM pairs
+def test_ag_device_epochs_across_modes(shape):
+    # every call advances the kept epoch by one whatever its mode (movement alone, GEMM alone on the
+    # gathered buffer it left, fused), and the count of CTAs that read the epoch is back to zero
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], **shape)
+    inp = wls.make_inputs(wl, integer=True)
+    case = AGCase(inp, opts=opts(chunk_rows=wl.chunk_rows))
+    want = R.round_out(case.oracle(), "bf16")
+    modes = [tdx.TDX_MOVE_ONLY, tdx.TDX_GEMM_ONLY, tdx.TDX_FUSED, tdx.TDX_FUSED, tdx.TDX_MOVE_ONLY, tdx.TDX_FUSED]
+    for call, mode in enumerate(modes, start=1):
+        case.C.fill_(float("nan"))
+        tdx.check(case.run(opts(chunk_rows=wl.chunk_rows, epoch=tdx.TDX_EPOCH_DEVICE, mode=mode)))
+        torch.cuda.synchronize()
+        status_ok(case)
+        assert int(case.ws[64:68].view(torch.int32).item()) == call
+        assert int(case.ws[68:72].view(torch.int32).item()) == 0
+        if mode != tdx.TDX_MOVE_ONLY:
+            assert np.array_equal(case.result_bits(), want), f"call {call}"
 
 
 def test_ag_degenerate_sizes():
