@@ -355,6 +355,14 @@ int grid_for(const tdx_opts& o, const Plan& pl, bool fp8, int items_or_zero) {
   if (g <= 0) return 0;
   if (o.num_sms > 0 && o.num_sms < g) g = o.num_sms;
   if (items_or_zero > 0 && items_or_zero < g) g = items_or_zero;
+  // grid-wide fold (several waves, fewer tiles than CTAs): as many CTAs as give every CTA the same
+  // number of work items, so that the last wave leaves no CTA idle before the grid barrier. Small-M
+  // ReduceScatter (W=8, 256 items): 128 CTAs instead of 152, 36.5 -> 35.6 us.
+  if (pl.coop == 2) {
+    const long long items = static_cast<long long>(pl.L) * pl.T;
+    const long long waves = (items + g - 1) / g;
+    if (waves > 1) g = static_cast<int>((items + waves - 1) / waves);
+  }
   g -= g % pl.CL;
   return g;
 }
