@@ -118,7 +118,11 @@ tdx_status make_plan(int op, int W, int Mx, int K, int N, tdx_dtype dtype, const
     if (o.split_k > 0) {
       L = o.split_k;
     } else if (small && tiles > 0) {
-      L = static_cast<int>(kRefSMs / tiles);
+      // one wave of split-K items over the device's SMs (the CTAs of the persistent grid)
+      int sms = device_sms();
+      if (o.num_sms > 0 && (sms <= 0 || o.num_sms < sms)) sms = o.num_sms;
+      if (sms <= 0) sms = kRefSMs;
+      L = static_cast<int>(sms / tiles);
     }
     const int kb_bn = (int)((static_cast<long long>(K) * p.elt + k_slice_bytes(bn) - 1) / k_slice_bytes(bn));
     if (L > kMaxSplitK) L = kMaxSplitK;

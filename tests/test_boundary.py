@@ -219,13 +219,13 @@ PLANS = [
     ("RS W=8", "OP_RS", 8, 8192, 3584, 8192, 0,
      dict(BN=256, L=8, cluster=3, reduce_mode=1, group_n=16, tiles_m=64, tiles_n=32, coop_fold=0)),
     ("small-M AG", "OP_AG", 8, 16, 8192, 1024, 16,
-     dict(BN=128, L=16, cluster=1, reduce_mode=2, pull_a=1, coop_fold=1, T=8, n_chunks=1)),
+     dict(BN=128, L=19, cluster=1, reduce_mode=2, pull_a=1, coop_fold=1, T=8, n_chunks=1)),
     ("small-M RS", "OP_RS", 8, 128, 1024, 8192, 0,
      dict(BN=256, L=8, cluster=1, reduce_mode=2, coop_fold=2, T=32)),
     ("RS, 8 M-tiles", "OP_RS", 8, 1024, 1024, 8192, 0,
      dict(BN=128, L=8, cluster=1, reduce_mode=1, T=512)),
     ("AG, N=64, 2-row shards", "OP_AG", 8, 2, 8192, 64, 0,
-     dict(BN=64, L=16, cluster=1, reduce_mode=2, pull_a=0)),
+     dict(BN=64, L=19, cluster=1, reduce_mode=2, pull_a=0)),
     ("tiny AG", "OP_AG", 2, 64, 128, 256, 32,
      dict(BN=128, L=2, cluster=1, reduce_mode=2, pull_a=1, n_chunks=2)),
 ]
@@ -236,9 +236,9 @@ def test_planner_choices_for_the_workloads(tdx, case):
     """Tile width, K splits, CTA cooperation and reduction chosen for the measured workloads and a
     few neighbours (a 152-SM device): 512-wide 2-SM pair tiles for the large AllGather, 2-SM pairs
     of 256-wide tiles with a chained running sum for the large RS,
-    128-wide tiles over 16 K splits that read the shards in place and fold cooperatively for the
-    small-M AllGather, 256-wide tiles with a grid-wide fold for the small-M ReduceScatter (two waves
-    of work but only 32 tiles)."""
+    128-wide tiles over 19 K splits (one wave on 152 SMs) that read the shards in place and fold
+    cooperatively for the small-M AllGather, 256-wide tiles with a grid-wide fold for the small-M
+    ReduceScatter (two waves of work but only 32 tiles)."""
     _, op, W, M, K, N, cr, want = case
     p = tdx.tdx_plan_info(getattr(tdx, op), W, M, K, N, tdx.TDX_BF16, tdx.make_opts(chunk_rows=cr, num_sms=152))
     got = {k: p[k] for k in want}
