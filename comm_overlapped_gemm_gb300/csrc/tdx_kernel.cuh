@@ -106,6 +106,10 @@ namespace tdx {
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
 #endif
+// Programmatic dependent launch of the fused kernels (1 = on).
+#ifndef TDX_PDL
+#define TDX_PDL 1
+#endif
 // AllGather: GEMM ring budget and largest bulk-copy staging ring (KiB). 168 / 80 (three 2-SM pair
 // stages of a 512-column tile, a 2.5x staging ring) copied faster alone (0.108 -> 0.089 ms) but
 // slowed the GEMM, e4m3 most (fused 0.683 -> 0.731 ms).
@@ -925,7 +929,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   // takes the count, so its round trip is off the kernel's critical path and its tail.
   uint32_t publish_old = 0u;
   if (threadIdx.x == 0) {
-    misc[7] = p.dev_epoch != nullptr ? ld_relaxed_gpu(p.dev_epoch) + 1u : p.epoch;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -954,6 +957,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   }
   tc_fence_before();
+  // Set-up above touches only this CTA's shared and Tensor Memory, so it may overlap the previous
+  // kernel on the stream (programmatic dependent launch); everything below may read what that
+  // kernel wrote.
+  griddep_wait();
+  if (threadIdx.x == 0) misc[7] = p.dev_epoch != nullptr ? ld_relaxed_gpu(p.dev_epoch) + 1u : p.epoch;
   if constexpr (CL > 1)
     cluster_sync_all();   // the peer's barriers are initialised before its loads or commits target them
   else
@@ -1787,6 +1795,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   }
 
   // =============================================================== teardown
+  // the next kernel on the stream may start its set-up on SMs this grid frees from here on
+  griddep_launch_dependents();
   __syncthreads();
   if (PM == 2 && !leader && threadIdx.x == kTmaWarp * 32 && use_mma &&
       (*abort_flag || ld_relaxed_gpu(p.status) != 0u)) {
@@ -1846,7 +1856,7 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kNumThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if constexpr (CL == 1) {
     // CTAs wait on flags other CTAs release: all of them must be resident at once
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -1858,8 +1868,12 @@ cudaError_t launch_fused_t(const KParams& p, int grid, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
   }
+  // programmatic dependent launch: the set-up may overlap the previous kernel's tail (the kernel
+  // waits for that kernel's completion before reading any global memory)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = TDX_PDL;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tdx_fused_kernel<BN, FP8, OP, PM>, p);
 }
 
