@@ -777,8 +777,13 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   p.num_kb = static_cast<int>((static_cast<long long>(H) * p.elt + 127) / 128);
   p.n_chunks = static_cast<int>((p.total + kBM - 1) / kBM);
   // 2-SM pairs (M = 256 per MMA, two tiles of one expert) when the experts average at least 8 tiles:
-  // the tile table then pads every expert to an even tile count (at most one empty tile each)
-  if (o.cluster == 3 || bn == 512 || (o.cluster == 0 && bn == 256 && p.total >= 8LL * kBM * E)) {
+  // the tile table then pads every expert to an even tile count (at most one empty tile each). The
+  // bf16 dispatch takes pairs from one tile per expert on: at 128 tokens per rank (W=8, top-8 of 64
+  // experts, 7168 -> 2048) pairs of 256-wide tiles ran in 417 us against 434 us on single CTAs,
+  // while e4m3 ran slower on pairs (230 against 220 us).
+  const bool many_tiles = p.total >= 8LL * kBM * E;
+  const bool bf16_dispatch_pairs = !fp8 && !combine && p.total >= static_cast<long long>(kBM) * E;
+  if (o.cluster == 3 || bn == 512 || (o.cluster == 0 && bn == 256 && (many_tiles || bf16_dispatch_pairs))) {
     if (bn != 256 && bn != 512) return TDX_ERR_UNSUPPORTED;
     p.PM = 2;
   }
@@ -787,7 +792,7 @@ tdx_status make_moe_plan(int W, int T, int H, int F, int E, int k, tdx_dtype dty
   // 262144 rows x 7168 -> 2048): fused 5.44 -> 5.02 ms, GEMM alone 4.35 -> 3.96 ms; e4m3 fused
   // 3.04 -> 2.84 ms. The combine keeps 256 (its token folds run in the epilogue, which one
   // accumulator would leave exposed).
-  if (o.block_n == 0 && !combine && p.PM == 2 && F >= 1024) {
+  if (o.block_n == 0 && !combine && p.PM == 2 && F >= 1024 && many_tiles) {
     bn = 512;
     p.BN = bn;
     p.tiles_n = (F + bn - 1) / bn;

@@ -356,10 +356,14 @@ def test_moe_plan(tdx):
     p = tdx.tdx_moe_plan_info(8, 4096, 7168, 2048, 64, 8, tdx.TDX_BF16)
     assert p["total_rows"] == 262144 and p["n_chunks"] == 2048 and p["max_tiles"] == 2048 + 128
     assert p["cluster"] == 3
-    # 128 tokens per rank: 128 rows per expert on average, single CTAs
+    # 128 tokens per rank: 128 rows per expert on average; bf16 on pairs of 256-wide tiles (a partial
+    # and a padding tile per expert), e4m3 on single CTAs
     q = tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16)
-    assert q["cluster"] == 1 and q["max_tiles"] == 64 + 64
-    assert tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(cluster=3))["cluster"] == 3
+    assert q["cluster"] == 3 and q["BN"] == 256 and q["max_tiles"] == 64 + 2 * 64
+    q8 = tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_FP8_E4M3)
+    assert q8["cluster"] == 1 and q8["BN"] == 256 and q8["max_tiles"] == 64 + 64
+    assert tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(cluster=1))["cluster"] == 1
+    assert tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_FP8_E4M3, tdx.make_opts(cluster=3))["cluster"] == 3
     with pytest.raises(tdx.TdxError):
         tdx.tdx_moe_plan_info(8, 128, 7168, 2048, 64, 8, tdx.TDX_BF16, tdx.make_opts(cluster=3, block_n=128))
     # 512-column pair tiles for the dispatch's grouped GEMM (library choice on pairs)
