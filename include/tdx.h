@@ -99,7 +99,9 @@ typedef struct tdx_opts {
   uint64_t timeout_ns;       /* bound of every device-side wait (default 2e9 ns) */
   uint32_t perturb_seed;     /* test only: !=0 injects pseudo-random delays in producers/epilogues */
   void* trace;               /* optional device buffer of tdx_trace_size() bytes, or NULL */
-  int num_sms;               /* persistent grid size; 0 = every SM of the device */
+  int num_sms;               /* largest persistent grid; 0 = every SM of the device (a plan with a
+                                grid-wide fold takes as many CTAs as give each the same number of
+                                work items; small AllGathers split K to fill this many CTAs) */
   int split_k;               /* AG: K splits reduced in fixed order (0 = library choice, 1 = none) */
   int block_n;               /* GEMM tile width 64/128/256, or 512 on 2-SM pairs (cluster 3; one
                                 512-column accumulator per CTA, two MMAs per K step; bf16 and e4m3
