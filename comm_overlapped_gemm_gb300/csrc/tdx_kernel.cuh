@@ -106,6 +106,11 @@ namespace tdx {
 #ifndef TDX_MOE_STG_MAX_KB
 #define TDX_MOE_STG_MAX_KB 32
 #endif
+// Grid-wide fold: float4 per slot a task loads (2: 8 columns; 4: 16 columns, which spilled
+// registers and measured slower on the small-M ReduceScatter, 34.9 -> 36.3 us).
+#ifndef TDX_GRID_FOLD_F4
+#define TDX_GRID_FOLD_F4 2
+#endif
 // Programmatic dependent launch of the fused kernels (1 = on).
 #ifndef TDX_PDL
 #define TDX_PDL 1
@@ -1713,7 +1718,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   }
 
   // =============================================================== grid-wide fold
-  if (OP != OP_MOE && OP != OP_MOE_COMBINE && chain && p.reduce_last && p.coop_fold == 2) {
+  if (PM == 0 && OP != OP_MOE && OP != OP_MOE_COMBINE && chain && p.reduce_last && p.coop_fold == 2) {   // single CTAs only
     // Every CTA arrives once all its partials are stored (a grid barrier; every CTA of the
     // cooperative launch is resident), then folds a contiguous 1/grid share of all tiles, cut into
     // units of 128 rows x 8 columns (4 KiB of a slot, contiguous in the slot layout), slots in order
@@ -1731,10 +1736,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
     __syncthreads();
     if (*go != 0u) {
-      // a task is one row of one unit (8 columns): the row's 8 columns of up to 8 slots are loaded at
-      // once (a warp's 32 lanes take 32 consecutive rows: 512 contiguous bytes per load), then added
-      // in slot order; all 12 warps take tasks
-      const int units = p.T * (BN / 8);
+      // a task is one row of one unit (kCols columns): the row's columns of up to 8 slots are loaded
+      // at once (a warp's 32 lanes take 32 consecutive rows: 512 contiguous bytes per load), then
+      // added in slot order; all 12 warps take tasks
+      constexpr int kV = TDX_GRID_FOLD_F4;   // float4 of a slot per task
+      constexpr int kCols = 4 * kV;
+      const int units = p.T * (BN / kCols);
       const int per = (units + grid - 1) / grid;
       const int g0 = min(units, blockIdx.x * per);
       const int g1 = min(units, g0 + per);
@@ -1743,43 +1750,41 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       for (int task = threadIdx.x; task < (g1 - g0) * kBM; task += kNumThreads) {
         const int gu = g0 + (task >> 7);
         const int i = task & (kBM - 1);
-        const int tile = gu / (BN / 8);
-        const int r8 = gu - tile * (BN / 8);
-        const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)gu * (kBM * 2) + i;
-        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        const int tile = gu / (BN / kCols);
+        const int ru = gu - tile * (BN / kCols);
+        const float4* base = reinterpret_cast<const float4*>(p.sbuf) + (size_t)gu * (kBM * kV) + i;
+        float4 a[kV];
 #pragma unroll 1
         for (int c0 = 0; c0 < p.L; c0 += 8) {
-          float4 x0[8], x1[8];
+          float4 x[8][kV];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             if (c0 + c < p.L) {
-              x0[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4, pol);
-              x1[c] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4 + kBM, pol);
+#pragma unroll
+              for (int v = 0; v < kV; ++v) x[c][v] = ld_cg_f4_hint(base + (size_t)(c0 + c) * slot_f4 + v * kBM, pol);
             }
           }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             if (c0 + c < p.L) {
-              if (c0 + c == 0) {
-                a0 = x0[c];
-                a1 = x1[c];
-              } else {
-                a0.x = a0.x + x0[c].x;
-                a0.y = a0.y + x0[c].y;
-                a0.z = a0.z + x0[c].z;
-                a0.w = a0.w + x0[c].w;
-                a1.x = a1.x + x1[c].x;
-                a1.y = a1.y + x1[c].y;
-                a1.z = a1.z + x1[c].z;
-                a1.w = a1.w + x1[c].w;
+#pragma unroll
+              for (int v = 0; v < kV; ++v) {
+                if (c0 + c == 0) {
+                  a[v] = x[c][v];
+                } else {
+                  a[v].x = a[v].x + x[c][v].x;
+                  a[v].y = a[v].y + x[c][v].y;
+                  a[v].z = a[v].z + x[c][v].z;
+                  a[v].w = a[v].w + x[c][v].w;
+                }
               }
             }
           }
         }
         const int row = (tile / p.tiles_n) * kBM + i;
-        const int col = (tile % p.tiles_n) * BN + r8 * 8;
-        store_out_4<OP, FP8>(p, row, col, a0);
-        store_out_4<OP, FP8>(p, row, col + 4, a1);
+        const int col = (tile % p.tiles_n) * BN + ru * kCols;
+#pragma unroll
+        for (int v = 0; v < kV; ++v) store_out_4<OP, FP8>(p, row, col + 4 * v, a[v]);
       }
       if (threadIdx.x == 0 && *go != 0u) {
         __threadfence();
