@@ -11,7 +11,7 @@ import torch
 import comm_overlapped_gemm_gb300 as tdx
 from oracle import reference as R
 import workloads as wls
-from gpu_util import (AGCase, assert_bit_exact, assert_within_tol, check_ag_consumer_order,
+from gpu_util import (AGCase, assert_bit_exact, dev_bits, assert_within_tol, check_ag_consumer_order,
                       check_each_item_once, host_bits, sample_rows, trace_items, trace_phases,
                       trace_releases)
 
@@ -251,6 +251,37 @@ def test_ag_device_epochs_across_modes(shape):
         assert int(case.ws[68:72].view(torch.int32).item()) == 0
         if mode != tdx.TDX_MOVE_ONLY:
             assert np.array_equal(case.result_bits(), want), f"call {call}"
+
+
+@pytest.mark.parametrize("shape2", [dict(M=64, N=128), dict(M=16, N=512)])
+def test_ag_chained_calls_read_the_previous_output(shape2):
+    # two calls queued back to back on one stream, the second gathering the first one's output rows
+    # as its shards: the second kernel may start its set-up while the first still runs (programmatic
+    # dependent launch) and must read the first's finished output (bit-exact on integers; every
+    # value stays exact in bf16 and in the fp32 accumulation)
+    wl1 = wls.with_shape(wls.WORKLOADS["ag_w8"], W=2, M=64, K=128, N=256, chunk_rows=64)
+    inp1 = wls.make_inputs(wl1, integer=True)
+    first = AGCase(inp1, opts=opts(chunk_rows=64))
+    W2, M2, N2 = 128 // shape2["M"], shape2["M"], shape2["N"]
+    wl2 = wls.with_shape(wls.WORKLOADS["ag_w8"], W=W2, M=M2, K=256, N=N2, chunk_rows=M2)
+    b2 = wls.make_inputs(wl2, integer=True).b[0]
+    B2 = dev_bits(b2)
+    C2 = torch.full((128, N2), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws2 = torch.zeros(tdx.tdx_workspace_size(tdx.OP_AG, W2, M2, 256, N2, tdx.TDX_BF16, opts(chunk_rows=M2)),
+                      dtype=torch.uint8, device="cuda")
+    shards2 = [first.C[r * M2:(r + 1) * M2] for r in range(W2)]   # views into the first call's output
+    for rep in range(3):
+        first.C.fill_(float("nan"))
+        C2.fill_(float("nan"))
+        tdx.check(first.run(opts(chunk_rows=64, epoch=rep + 1)))
+        tdx.check(tdx.tdx_ag_gemm(shards2, B2, C2, ws2, W2, M2, 256, N2, tdx.TDX_BF16,
+                                  opts(chunk_rows=M2, epoch=rep + 1)))
+        torch.cuda.synchronize()
+        status_ok(first)
+        c1 = R.round_out(first.oracle(), "bf16")
+        assert np.array_equal(first.result_bits(), c1)
+        want = R.round_out(R.ag_gemm([c1[r * M2:(r + 1) * M2] for r in range(W2)], b2, "bf16"), "bf16")
+        assert np.array_equal(host_bits(C2), want), f"rep {rep}"
 
 
 def test_ag_degenerate_sizes():
