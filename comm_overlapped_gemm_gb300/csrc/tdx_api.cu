@@ -2,6 +2,7 @@
 // carving (status word, chunk flags, gathered buffer, running-sum / partial-slot buffer, MoE layout
 // tables and receive buffer), TMA tensor maps and the launches of the persistent fused kernel and
 // of the MoE routing-layout kernel. No arithmetic of the operations happens here.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -371,6 +372,47 @@ int grid_for(const tdx_opts& o, const Plan& pl, bool fp8, int items_or_zero) {
   return g;
 }
 
+// AllGather producer order. The first wave of the persistent grid takes the self rank's tiles (no
+// wait) and then tiles of ranks self+1, self+2, ..., which wait for their chunks. The CTAs holding
+// those tiles (kp.copy_lo on: the first wave's self tiles come first) copy the chunks those tiles
+// wait for (release-order chunks 0..kp.copy_q1-1) themselves, through their operand ring, which is
+// idle until then. Otherwise copy_q1 = 0 and every chunk goes round-robin in pieces.
+void first_wave_chunks(KParams& kp, const Plan& pl, int grid, int self_rank, bool on) {
+  kp.copy_lo = grid;
+  kp.copy_q1 = 0;
+  if (!on || pl.L != 1 || pl.M_local <= 0 || pl.n_chunks <= 0) return;
+  const int CL = pl.CL;
+  const int ncl = grid / CL;
+  const int tiles_g = pl.tiles_m / CL;
+  int start = (self_rank * pl.M_local + CL * kBM - 1) / (CL * kBM);
+  if (start >= tiles_g) start = 0;
+  const long long self_lo = static_cast<long long>(self_rank) * pl.M_local;
+  const long long self_hi = self_lo + pl.M_local;
+  int first_wait = -1;
+  int q1 = 0;
+  for (int pos = 0; pos < ncl && pos < tiles_g * pl.tiles_n; ++pos) {
+    int mg = start + pos / pl.tiles_n;
+    if (mg >= tiles_g) mg -= tiles_g;
+    const long long r0 = static_cast<long long>(mg) * CL * kBM;
+    const long long r1 = std::min(r0 + CL * kBM, static_cast<long long>(pl.M));
+    if (r0 >= self_lo && r1 <= self_hi) {
+      if (first_wait >= 0) return;   // a self tile after a waiting one: keep the round-robin order
+      continue;
+    }
+    if (first_wait < 0) first_wait = pos;
+    for (long long r = r0; r < r1; r += pl.chunk_rows) {
+      const int j = static_cast<int>(r / pl.M_local);
+      const int ck = static_cast<int>((r - static_cast<long long>(j) * pl.M_local) / pl.chunk_rows);
+      const int rr = (j - self_rank - 1 + pl.W) % pl.W;   // release order of rank j's chunks
+      q1 = std::max(q1, rr * pl.n_chunks + ck + 1);
+    }
+  }
+  if (first_wait > 0 && q1 > 0 && q1 < pl.W * pl.n_chunks) {
+    kp.copy_lo = first_wait * CL;
+    kp.copy_q1 = q1;
+  }
+}
+
 // Every host-side check of an AllGather+GEMM call that does not involve the workspace (arguments,
 // options, tiling, alignment); fills the plan. Launches nothing.
 tdx_status ag_check(const void* const* shards, const void* B, const void* C, int W, int M_local, int K, int N,
@@ -440,6 +482,8 @@ tdx_status ag_run(const void* const* shards, const void* B, void* C, uint8_t* ws
   kp.copy_active = moving ? 1 : 0;
   kp.pull_a = pl.pull_a;
   kp.wait_flags = (!pl.pull_a && (o.mode == TDX_FUSED || o.mode == TDX_CONSUMER_ONLY)) ? 1 : 0;
+  first_wave_chunks(kp, pl, grid, o.self_rank, o.mode == TDX_FUSED && kp.wait_flags);
+  kp.total_pieces = (W * pl.n_chunks - kp.copy_q1) * kp.ppc;
   // A: K slices of k_slice_bytes(BN) bytes, 128 rows; B: 128-byte N rows, one K slice deep
   const int ks = k_slice_bytes(pl.BN);
   const int a_box = ks / pl.elt, b_box_n = 128 / pl.elt, b_box_k = ks / pl.elt;

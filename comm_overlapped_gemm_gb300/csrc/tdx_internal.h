@@ -128,7 +128,9 @@ struct KParams {
   uint32_t perturb;
   int piece_bytes;               // producer copy unit (multiple of kCopyRoundBytes)
   int ppc;                       // pieces per chunk
-  int total_pieces;
+  int total_pieces;              // AG: phase-2 pieces (chunks copy_q1.. in release order)
+  int copy_lo, copy_q1;          // AG: chunks 0..copy_q1-1 (release order) are copied first by CTAs
+                                 // copy_lo.. through their operand ring (copy_q1 = 0: none)
   long long row_bytes;           // K * element size
   long long chunk_bytes;
 };

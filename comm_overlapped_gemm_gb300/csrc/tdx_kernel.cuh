@@ -9,11 +9,11 @@
 //   warp 1  lane 0  MMA issuer: tcgen05.mma (bf16: kind::f16, e4m3: kind::f8f6f4) into one of two
 //                   TMEM accumulators of 128 x BN fp32; tcgen05.commit frees ring slots and
 //                   hands finished accumulators to the epilogue. Warp 1 allocates TMEM.
-//   warps 2-3       producer: one thread moves pieces of shard chunks (AllGather) or gathered
-//                   token rows (MoE dispatch) into the gathered / receive buffer with TMA bulk
-//                   copies through a shared-memory staging ring; the piece that completes a chunk
-//                   releases the chunk's flag (= epoch). (Build switch TDX_AG_BULK=0: the two
-//                   warps copy AllGather pieces in register rounds.)
+//   warps 2-3       producer: one thread moves shard chunks (AllGather) or gathered token rows
+//                   (MoE dispatch) into the gathered / receive buffer with TMA bulk copies through
+//                   a shared-memory staging ring (AllGather, first wave's chunks: through the
+//                   operand ring of a CTA waiting for them); the copy that completes a chunk
+//                   releases the chunk's flag (= epoch).
 //   warps 4-11      epilogue: TMEM -> registers; either the output tile (rounded once) or, along
 //                   a chain (RS ranks or AG K-splits) of L elements, the fixed-order fp32 sum
 //                   ((P_0 + P_1) + P_2) + ... of the elements' partial tiles, in one of two ways:
@@ -92,11 +92,6 @@ namespace tdx {
 // MoE combine: L2 policy of the expert-output stores (read back by the combine): as above.
 #ifndef TDX_COMBINE_Z_POLICY
 #define TDX_COMBINE_Z_POLICY 1
-#endif
-// AllGather producer: 1 = TMA bulk copies through the staging ring (one thread per CTA), 0 =
-// register rounds of the two producer warps.
-#ifndef TDX_AG_BULK
-#define TDX_AG_BULK 1
 #endif
 // AllGather bulk producer: L2 policy of the gathered-buffer stores (as TDX_OPERAND_POLICY).
 #ifndef TDX_AG_STORE_POLICY
@@ -192,7 +187,7 @@ struct Cfg {
 constexpr int ring_kb(int op) { return op == OP_MOE ? TDX_MOE_RING_KB : op == OP_AG ? TDX_AG_RING_KB : 216; }
 constexpr int stg_kb(int op) { return op == OP_AG ? TDX_AG_STG_MAX_KB : TDX_MOE_STG_MAX_KB; }
 // Ops whose producer moves data with bulk copies through a shared-memory staging ring.
-constexpr bool uses_staging(int op) { return op == OP_MOE || (op == OP_AG && TDX_AG_BULK != 0); }
+constexpr bool uses_staging(int op) { return op == OP_MOE || op == OP_AG; }
 
 
 
@@ -363,14 +358,31 @@ static __device__ __noinline__ bool wait_mbar_drain(const KParams& p, uint32_t b
   }
 }
 
+// Count `units` 16-byte units of AllGather chunk fi as copied (their stores completed and ordered
+// before this); the copy that completes the chunk resets the count and releases the chunk's flag.
+__device__ __forceinline__ void ag_chunk_done(const KParams& p, int fi, uint32_t units, uint32_t epoch, int grid) {
+  __threadfence();
+  const uint32_t total = static_cast<uint32_t>(p.chunk_bytes / 16);
+  const uint32_t old = atomicAdd(p.chunk_cnt + fi, units);
+  if (old + units == total) {
+    p.chunk_cnt[fi] = 0u;
+    const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
+    if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, epoch);
+    __threadfence();
+    st_release_gpu(p.chunk_flags + fi, epoch);
+    if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
+  }
+}
+
 // Copy `n` bytes (16-byte aligned addresses, n a multiple of 16) from src to dst with bulk copies
-// through the staging ring: segments of `seg` bytes in `nb` ring buffers, nb - 1 loads in flight,
-// each segment stored back as soon as it lands; returns once every store has completed and is
-// ordered before later generic accesses. `g` counts the CTA's segments (ring barrier phases). One
-// thread.
+// through a staging ring: segments of `seg` bytes in `nb` (<= 8) ring buffers, nb - 1 loads in
+// flight, each segment stored back as soon as it lands; returns once every store has completed and
+// is ordered before later generic accesses. `g` rotates the buffers; bit b of `par` is the phase
+// parity the next wait on barrier b expects (so that rings of different shapes may share the
+// barriers). One thread.
 static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* stg, uint64_t* bars, uint32_t seg, int nb,
-                                                     uint32_t& g, const uint8_t* src, uint8_t* dst, uint32_t n,
-                                                     uint64_t lpol, uint64_t spol) {
+                                                     uint32_t& g, uint32_t& par, const uint8_t* src, uint8_t* dst,
+                                                     uint32_t n, uint64_t lpol, uint64_t spol) {
   const int nseg = static_cast<int>((n + seg - 1) / seg);
   auto issue = [&](int i) {
     const uint32_t off = static_cast<uint32_t>(i) * seg;
@@ -389,7 +401,8 @@ static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* 
     }
     const uint32_t gi = g + static_cast<uint32_t>(i);
     const uint32_t b = gi % static_cast<uint32_t>(nb);
-    wait_mbar_drain(p, smem_u32(bars + b), (gi / static_cast<uint32_t>(nb)) & 1u);
+    wait_mbar_drain(p, smem_u32(bars + b), (par >> b) & 1u);
+    par ^= 1u << b;
     const uint32_t off = static_cast<uint32_t>(i) * seg;
     const uint32_t m = n - off < seg ? n - off : seg;
     bulk_store_s2g_hint(dst + off, smem_u32(stg + b * seg), m, spol);
@@ -398,6 +411,28 @@ static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* 
   g += static_cast<uint32_t>(nseg);
   bulk_wait_all();
   fence_proxy_async_global();
+}
+
+// Bounded wait until a shared-memory word set by another warp of the CTA is nonzero. Gives up
+// (false) when the CTA abort flag is raised or after 2 * p.timeout_ns (recorded as DEV_TIMEOUT /
+// ROLE_PIPE with index idx).
+static __device__ __noinline__ bool wait_smem_flag(const KParams& p, const uint32_t* flag, volatile int* abort_flag,
+                                                   uint32_t idx) {
+  const volatile uint32_t* f = flag;
+  if (*f != 0u) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (*f != 0u) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > 2 * p.timeout_ns) {
+        report_error(p, DEV_TIMEOUT, ROLE_PIPE, idx, 0, 1);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
 }
 
 // Bounded acquire-wait until *flag == epoch. A value above the epoch is a stale flag. Also gives
@@ -911,7 +946,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] TMA k-blocks issued, misc[3] MMA k-blocks
   // consumed, misc[4] epilogue go/stop decision, misc[5] epilogue "last arriver" decision, misc[6]
-  // MoE combine task count, misc[7] this call's epoch
+  // MoE combine task count, misc[7] this call's epoch, misc[9] AllGather producer done with the
+  // operand ring
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   // MoE dispatch: staging barriers after the row-source table, staging ring 128-byte aligned after them
   uint64_t* stg_bars = reinterpret_cast<uint64_t*>(misc + 16 + kBM);
@@ -950,6 +986,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     misc[3] = 0;
     misc[4] = 0;
     misc[5] = 0;
+    misc[9] = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -1023,6 +1060,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
       uint32_t n_waits = 0;
       uint64_t t_first = 0;
       bool stop = false;
+      if (ag && p.copy_active && p.copy_q1 > 0 && static_cast<int>(blockIdx.x) >= p.copy_lo) {
+        // this CTA's producer copies the first chunks through the operand ring: wait until it is done
+        stop = !wait_smem_flag(p, misc + 9, abort_flag, 500);
+        fence_proxy_async_shared();
+      }
       for (int it = cid; it < items && !stop; it += ncl) {
         if (*abort_flag) break;
         const Item w = decode_item<OP, CL>(p, it, BN, crank);
@@ -1238,90 +1280,61 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
     }
   } else if (warp >= kCopyWarp0 && warp < kCopyWarp0 + kNumCopyWarps) {
     // =============================================================== AllGather producer
-    if (ag && p.copy_active && uses_staging(OP)) {
-      // One thread moves the CTA's pieces with bulk copies through the staging ring; the piece that
-      // completes a chunk's count releases the chunk's flag.
+    if (ag && p.copy_active) {
+      // One thread moves chunk bytes with bulk copies and counts them; the copy that completes a
+      // chunk releases the chunk's flag. Chunks are numbered in release order (ranks self+1, ...,
+      // self). Phase 1 (fused calls): the chunks the first wave's peer tiles wait for are split
+      // evenly over the CTAs holding those tiles (copy_lo..), which copy their share through their
+      // own operand ring (idle until those chunks arrive; seven 1/8-ring segments in flight) and
+      // then hand the ring to the TMA warp. Phase 2: the other chunks, in pieces taken round-robin
+      // by every CTA, through the staging ring after the operand ring.
       const int ct = threadIdx.x - kCopyWarp0 * 32;
       if (ct == 0) {
-        constexpr uint32_t kStg = static_cast<uint32_t>(C::MOE_STG);
-        const uint32_t seg = (kStg / 4) / 16 * 16;
-        const int nb = min(8, static_cast<int>(kStg / seg));
         const uint64_t lpol = policy_evict_first();   // each shard byte is read once
         const uint64_t spol = policy_of(TDX_AG_STORE_POLICY);   // the GEMM reads the gathered rows next
-        uint32_t gseg = 0;
-        for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
-          const int q = piece / p.ppc;
-          const int pc = piece - q * p.ppc;
+        uint32_t par = 0;   // staging barrier parities, shared by both rings
+        auto copy_chunk_part = [&](int q, long long off, uint32_t n, uint8_t* ring, uint32_t seg, int nb, uint32_t& g) {
           const int rr = q / p.n_chunks;
           const int rank = (p.self_rank + 1 + rr) % p.W;
           const int ck = q - rr * p.n_chunks;
-          const long long off = (long long)pc * p.piece_bytes;
-          const long long rem = p.chunk_bytes - off;
-          const int n = rem < p.piece_bytes ? static_cast<int>(rem) : p.piece_bytes;
-          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
           if (n > 0)
-            bulk_copy_contig(p, stg, stg_bars, seg, nb, gseg, p.shard[rank] + (long long)ck * p.chunk_bytes + off,
-                             p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off,
-                             static_cast<uint32_t>(n), lpol, spol);
-          const int fi = rank * p.n_chunks + ck;
-          __threadfence();
-          const uint32_t old = atomicAdd(p.chunk_cnt + fi, 1u);
-          if (old == static_cast<uint32_t>(p.ppc - 1)) {
-            p.chunk_cnt[fi] = 0u;
-            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
-            if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, epoch);
-            __threadfence();
-            st_release_gpu(p.chunk_flags + fi, epoch);
-            if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
+            bulk_copy_contig(p, ring, stg_bars, seg, nb, g, par, p.shard[rank] + (long long)ck * p.chunk_bytes + off,
+                             p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off, n,
+                             lpol, spol);
+          ag_chunk_done(p, rank * p.n_chunks + ck, n / 16u, epoch, grid);
+        };
+        if (p.copy_q1 > 0 && static_cast<int>(blockIdx.x) >= p.copy_lo) {
+          constexpr uint32_t kRing = static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);
+          constexpr uint32_t kSeg1 = (kRing / 8) / 16 * 16;
+          uint32_t g1 = 0;
+          const long long region = (long long)p.copy_q1 * p.chunk_bytes;
+          const int nw = grid - p.copy_lo;
+          const int b = static_cast<int>(blockIdx.x) - p.copy_lo;
+          const long long lo = (region * b / nw) & ~15LL;
+          const long long hi = b == nw - 1 ? region : ((region * (b + 1) / nw) & ~15LL);
+          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x18000u + blockIdx.x) & 4095u);
+          for (long long o = lo; o < hi;) {
+            const int q = static_cast<int>(o / p.chunk_bytes);
+            const long long off = o - (long long)q * p.chunk_bytes;
+            const long long end = min(hi, (long long)(q + 1) * p.chunk_bytes);
+            copy_chunk_part(q, off, static_cast<uint32_t>(end - o), smem, kSeg1, 8, g1);
+            o = end;
           }
+          // the operand ring is free: every bulk copy through it has completed
+          __threadfence_block();
+          *reinterpret_cast<volatile uint32_t*>(misc + 9) = 1u;
         }
-      }
-    } else if (ag && p.copy_active) {
-      // A piece (p.piece_bytes, a multiple of 16 KiB) is copied in rounds of 16 KiB: each of the
-      // 64 producer threads keeps 16 vector loads in flight, stores them, and the next round
-      // starts at once; the synchronisation that releases a chunk (barrier, fence, counter
-      // atomic) is paid once per piece.
-      const int ct = threadIdx.x - kCopyWarp0 * 32;
-      const uint64_t stream_pol = policy_evict_first();   // each shard byte is read once
-      constexpr int kVec = kCopyRoundBytes / (16 * kCopyThreads);   // 16 vectors per thread
-      for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
-        const int q = piece / p.ppc;            // chunk position in release order
-        const int pc = piece - q * p.ppc;
-        const int rr = q / p.n_chunks;
-        const int rank = (p.self_rank + 1 + rr) % p.W;   // peers in ring order, self last
-        const int ck = q - rr * p.n_chunks;
-        const long long off = (long long)pc * p.piece_bytes;
-        const long long rem = p.chunk_bytes - off;
-        const int n = rem < p.piece_bytes ? static_cast<int>(rem) : p.piece_bytes;
-        const uint8_t* src = p.shard[rank] + (long long)ck * p.chunk_bytes + off;
-        uint8_t* dst = p.G + ((long long)rank * p.M_local + (long long)ck * p.chunk_rows) * p.row_bytes + off;
-        if (p.perturb && ct == 0) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
-        for (int r0 = 0; r0 < n; r0 += kCopyRoundBytes) {
-          uint4 v[kVec];
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) {
-            const int b = r0 + (j * kCopyThreads + ct) * 16;
-            if (b < n) v[j] = ld_nc_v4_hint(src + b, stream_pol);
-          }
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) {
-            const int b = r0 + (j * kCopyThreads + ct) * 16;
-            if (b < n) st_v4(dst + b, v[j]);
-          }
-        }
-        named_bar_sync(2, kCopyThreads);
-        if (ct == 0) {
-          const int fi = rank * p.n_chunks + ck;
-          __threadfence();
-          const uint32_t old = atomicAdd(p.chunk_cnt + fi, 1u);
-          if (old == static_cast<uint32_t>(p.ppc - 1)) {
-            p.chunk_cnt[fi] = 0u;
-            const uint32_t prev = ld_relaxed_gpu(p.chunk_flags + fi);
-            if (prev >= epoch) report_error(p, DEV_STALE, ROLE_PRODUCER, fi, prev, epoch);
-            __threadfence();
-            st_release_gpu(p.chunk_flags + fi, epoch);
-            if (p.trace != nullptr) trace_release(p, grid, static_cast<uint32_t>(fi));
-          }
+        constexpr uint32_t kStg = static_cast<uint32_t>(C::MOE_STG);
+        const uint32_t seg = (kStg / 4) / 16 * 16;
+        const int nb = min(8, static_cast<int>(kStg / seg));
+        uint32_t g2 = 0;
+        for (int piece = blockIdx.x; piece < p.total_pieces; piece += grid) {
+          const int q = p.copy_q1 + piece / p.ppc;
+          const long long off = (long long)(piece % p.ppc) * p.piece_bytes;
+          const long long rem = p.chunk_bytes - off;
+          const uint32_t n = static_cast<uint32_t>(rem < p.piece_bytes ? rem : p.piece_bytes);
+          if (p.perturb) __nanosleep(perturb_hash(p.perturb, 0x10000u + piece) & 4095u);
+          copy_chunk_part(q, off, n, stg, seg, nb, g2);
         }
       }
     } else if (OP == OP_MOE && p.copy_active && !moe_bad) {

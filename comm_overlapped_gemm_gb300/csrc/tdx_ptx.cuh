@@ -196,6 +196,9 @@ __device__ __forceinline__ void cluster_sync_all() {
 // ------------------------------------------------------------------------------- proxies, flags
 // Order this thread's generic-proxy global accesses (e.g. an acquired flag) before its later
 // async-proxy accesses (TMA reads of the data the flag guards).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
