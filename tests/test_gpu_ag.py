@@ -284,6 +284,38 @@ def test_ag_chained_calls_read_the_previous_output(shape2):
         assert np.array_equal(host_bits(C2), want), f"rep {rep}"
 
 
+@pytest.mark.parametrize("self_rank", [0, 5])
+@pytest.mark.parametrize("perturb", [0, 9])
+def test_ag_first_wave_chunks_through_the_operand_ring(self_rank, perturb):
+    # 16 CTAs: the first wave holds the self rank's 8 tiles and 8 tiles of the next rank, whose CTAs
+    # copy that rank's chunks through their operand ring before loading operands into it (delays
+    # injected into both copy phases with perturb); exact result, every chunk released once
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], W=8, M=256, K=512, N=1024, chunk_rows=64)
+    inp = wls.make_inputs(wl, integer=True)
+    o = opts(self_rank=self_rank, num_sms=16, chunk_rows=64, block_n=256, cluster=1)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, 8, 256, 512, 1024, tdx.TDX_BF16, o)
+    assert plan["cluster"] == 1 and plan["BN"] == 256 and plan["L"] == 1 and plan["T"] == 64
+    items, chunks = plan["T"], 8 * plan["n_chunks"]
+    trace = torch.zeros(tdx.tdx_trace_size(16, items, chunks) // 4, dtype=torch.int32, device="cuda")
+    case = AGCase(inp, opts=o)
+    want = R.round_out(case.oracle(), "bf16")
+    for call in range(2):
+        trace.zero_()
+        case.C.fill_(float("nan"))
+        tdx.check(case.run(opts(self_rank=self_rank, num_sms=16, chunk_rows=64, block_n=256, cluster=1,
+                                epoch=call + 1, perturb_seed=perturb + call if perturb else 0, trace=trace)))
+        status_ok(case)
+        assert np.array_equal(case.result_bits(), want)
+        tr = trace.cpu().numpy().astype(np.uint32)
+        assert sorted(trace_releases(tr, 16, chunks)) == list(range(chunks))
+        check_each_item_once(trace_items(tr, 16, chunks), 1, plan["T"])
+        n = chunks
+        f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
+        assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, call + 1))
+        cnt = case.ws[plan["off_chunk_cnt"]:plan["off_chunk_cnt"] + 4 * n].view(torch.int32).cpu().numpy()
+        assert not cnt.any()   # the completing copy reset every chunk's count
+
+
 def test_ag_degenerate_sizes():
     # K == 0: C = 0 (empty sums); M_local == 0 and N == 0: nothing to do
     B = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
