@@ -501,18 +501,18 @@ def graph_time_us(torch, fn, reps: int = 50, reset=None):
 
 
 def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
-    """The other configurations, timed alone (median of CUDA-event times, warm): e4m3 AllGather
-    and ReduceScatter, GEMM+AllReduce, bf16 partials, the MoE dispatch and combine, and the small-M
-    latency cases."""
+    """The other configurations, timed alone (median of CUDA-event times, warm; the fused / GEMM
+    alone / movement alone modes of one configuration interleaved call by call, so that all three
+    run under the same clock and power state): e4m3 AllGather and ReduceScatter, GEMM+AllReduce,
+    bf16 partials, the MoE dispatch and combine, and the small-M latency cases."""
     import workloads as wls
     W = wls.WORKLOADS
     res = {}
     call, status = ag_case(tdx, torch, W["ag_fp8_w8"], dev)
     for _ in range(3):
         call()
-    f = time_mode(torch, call, reps)
-    g = time_mode(torch, lambda: call(mode=1), reps)
-    m = time_mode(torch, lambda: call(mode=2), reps)
+    t = time_interleaved(torch, {"f": call, "g": lambda: call(mode=1), "m": lambda: call(mode=2)}, reps)
+    f, g, m = t["f"], t["g"], t["m"]
     status()
     tf = W["ag_fp8_w8"].flops / (f * 1e-3) / 1e12
     res["ag_fp8_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
@@ -579,9 +579,8 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     call, status = moe_case(tdx, torch, wl, dev)
     for _ in range(3):
         call()
-    f = time_mode(torch, call, reps)
-    m = time_mode(torch, lambda: call(mode=2), reps)
-    g = time_mode(torch, lambda: call(mode=1), reps)
+    t = time_interleaved(torch, {"f": call, "g": lambda: call(mode=1), "m": lambda: call(mode=2)}, reps)
+    f, g, m = t["f"], t["g"], t["m"]
     status()
     tf = wl.flops / (f * 1e-3) / 1e12
     moved = 2 * wl.M_total * wl.K * 2                       # dispatched rows read + written
@@ -594,9 +593,8 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     call, status = moe_case(tdx, torch, wl, dev)
     for _ in range(3):
         call()
-    f = time_mode(torch, call, reps)
-    m = time_mode(torch, lambda: call(mode=2), reps)
-    g = time_mode(torch, lambda: call(mode=1), reps)
+    t = time_interleaved(torch, {"f": call, "g": lambda: call(mode=1), "m": lambda: call(mode=2)}, reps)
+    f, g, m = t["f"], t["g"], t["m"]
     status()
     tf = wl.flops / (f * 1e-3) / 1e12
     res["moe_fp8_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m, "overlap_efficiency": max(g, m) / f,
@@ -620,9 +618,8 @@ def extra_configs(tdx, torch, dev, peak_bf16, hbm_gbs, reps=20):
     call, status = combine_case(tdx, torch, wl, dev)
     for _ in range(3):
         call()
-    f = time_mode(torch, call, reps)
-    g = time_mode(torch, lambda: call(mode=1), reps)
-    m = time_mode(torch, lambda: call(mode=2), reps)
+    t = time_interleaved(torch, {"f": call, "g": lambda: call(mode=1), "m": lambda: call(mode=2)}, reps)
+    f, g, m = t["f"], t["g"], t["m"]
     status()
     tf = wl.flops / (f * 1e-3) / 1e12
     res["moe_combine_w8"] = {"ms_fused": f, "ms_gemm_only": g, "ms_move_only": m,
