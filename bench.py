@@ -355,7 +355,9 @@ def ag_case(tdx, torch, wl, dev, integer=False):
     import workloads as wls
     inp = wls.make_inputs(wl, integer=integer)
     view = np.int16 if wl.dtype == "bf16" else np.uint8
-    shards = [torch.from_numpy(np.ascontiguousarray(a).view(view)).to(dev) for a in inp.a]
+    # the ranks' shards at one stride in one buffer, as a symmetric heap places them
+    stacked = torch.from_numpy(np.ascontiguousarray(np.stack(inp.a)).view(view)).to(dev)
+    shards = [stacked[r] for r in range(wl.W)]
     B = torch.from_numpy(np.ascontiguousarray(inp.b[0]).view(view)).to(dev)
     C = torch.empty((wl.W * wl.M, wl.N), dtype=torch.bfloat16, device=dev)
     dt = tdx.TDX_BF16 if wl.dtype == "bf16" else tdx.TDX_FP8_E4M3

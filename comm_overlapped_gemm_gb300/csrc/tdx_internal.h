@@ -109,6 +109,11 @@ struct KParams {
   int copy_active;               // producer warps copy chunks (AG, SM producer, fused/move)
   int wait_flags;                // consumers wait on chunk flags (AG fused / consumer-only)
   int pull_a;                    // AG small shards: tiles read A from the shards (tm_a[r]), no waits
+  int pull_3d;                   // pull_a with shards at one stride: tm_a[0] is a 3D map (K, row, rank)
+                                 // and a tile's shards are one box
+  int b_groups;                  // AG single CTAs, N whole 128-byte groups: tm_b[0] is a 3D map
+                                 // (128-byte column, K, column group) and a K slice of B is one box
+                                 // across the tile width
   int a_streamed, b_streamed;    // operand read by one tile only: loaded evict_first (else evict_last)
   int allreduce;                 // RS kernel as GEMM+AllReduce: out[r] are full M x N outputs
   int bf16_partials;             // slotted RS/AR: partials rounded to bf16 in their slots (else fp32)

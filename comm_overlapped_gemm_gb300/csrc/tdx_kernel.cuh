@@ -413,6 +413,21 @@ static __device__ __noinline__ void bulk_copy_contig(const KParams& p, uint8_t* 
   fence_proxy_async_global();
 }
 
+// One K slice of B for a single CTA's tile at column n0: the tile's 128-byte column boxes land one
+// after another in shared memory. With `groups`, the map is 3D (128-byte column, K row, column
+// group of 128 bytes) and one box covers every column group of the tile; else one 2D box per group.
+template <class C>
+static __device__ __forceinline__ void load_b_slice(uint8_t* dst, const CUtensorMap* map, uint32_t bar, int n0,
+                                                    int kb, int groups, uint64_t pol) {
+  if (groups) {
+    tma_load_3d_hint(smem_u32(dst), map, bar, 0, kb * C::BK, n0 / C::B_BOX_N, pol);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < C::B_BOXES; ++j)
+    tma_load_2d_hint(smem_u32(dst + j * C::B_BOX_BYTES), map, bar, n0 + j * C::B_BOX_N, kb * C::BK, pol);
+}
+
 // Bounded wait until a shared-memory word set by another warp of the CTA is nonzero. Gives up
 // (false) when the CTA abort flag is raised or after 2 * p.timeout_ns (recorded as DEV_TIMEOUT /
 // ROLE_PIPE with index idx).
@@ -1080,7 +1095,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           map_b = &p.tm_b[0];
           pull_r0 = w.m0 / p.M_local;
           pull_nr = min(kBM / p.M_local, p.W - pull_r0);
-          a_bytes = pull_nr * p.M_local * 128;
+          // one 3D box counts its whole extent (ranks past W are zero-filled); per-shard boxes count
+          // only the shards that exist
+          a_bytes = p.pull_3d ? C::A_BYTES : pull_nr * p.M_local * 128;
         } else if (ag) {
           map_b = &p.tm_b[0];
           const int self_lo = p.self_rank * p.M_local;
@@ -1140,13 +1157,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
           if constexpr (PM == 0) {
             if (ag && p.pull_a) {
               mbar_arrive_expect_tx(fb, a_bytes + C::B_BYTES);
-              for (int q = 0; q < pull_nr; ++q)
-                tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES + q * p.M_local * 128), &p.tm_a[pull_r0 + q], fb,
-                                 kb * C::BK, 0, keep_a);
-#pragma unroll
-              for (int j = 0; j < C::B_BOXES; ++j)
-                tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep_b);
+              if (p.pull_3d) {
+                tma_load_3d_hint(smem_u32(sA + stage * C::A_BYTES), &p.tm_a[0], fb, kb * C::BK, 0, pull_r0, keep_a);
+              } else {
+                for (int q = 0; q < pull_nr; ++q)
+                  tma_load_2d_hint(smem_u32(sA + stage * C::A_BYTES + q * p.M_local * 128), &p.tm_a[pull_r0 + q],
+                                   fb, kb * C::BK, 0, keep_a);
+              }
+              load_b_slice<C>(sB + stage * C::B_BYTES, map_b, fb, w.n0, kb, p.b_groups, keep_b);
               goto issued_slice;
             }
           }
@@ -1177,10 +1195,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) tdx_fused_kernel(const __grid_
                 tma_load_3d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
                                  w.n0 + j * C::B_BOX_N, kb * C::BK, w.e, keep_b);
             } else {
-#pragma unroll
-              for (int j = 0; j < C::B_BOXES; ++j)
-                tma_load_2d_hint(smem_u32(sB + stage * C::B_BYTES + j * C::B_BOX_BYTES), map_b, fb,
-                                 w.n0 + j * C::B_BOX_N, kb * C::BK, keep_b);
+              load_b_slice<C>(sB + stage * C::B_BYTES, map_b, fb, w.n0, kb, p.b_groups, keep_b);
             }
           }
         issued_slice:

@@ -31,6 +31,34 @@ def workspace(op, W, Mx, K, N, dtype, opts=None) -> torch.Tensor:
     return ws
 
 
+def shard_layout(shards, layout: str):
+    """Place the shards in device memory: "separate" (one allocation each), "stacked" (one buffer,
+    rank r at r times the shard size: one stride), "scattered" (one buffer, uneven gaps between
+    shards) or "reversed" (one buffer, rank r at (W-1-r) times the shard size)."""
+    if layout == "separate" or not shards:
+        return shards
+    W = len(shards)
+    nb = shards[0].numel() * shards[0].element_size()
+    if layout == "stacked":
+        offs = [r * nb for r in range(W)]
+    elif layout == "reversed":
+        offs = [(W - 1 - r) * nb for r in range(W)]
+    elif layout == "scattered":
+        offs, o = [], 0
+        for r in range(W):
+            offs.append(o)
+            o += nb + 256 * (1 + r % 3)
+    else:
+        raise ValueError(layout)
+    buf = torch.zeros(max(offs) + nb, dtype=torch.uint8, device="cuda")
+    out = []
+    for r, t in enumerate(shards):
+        v = buf[offs[r]:offs[r] + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        out.append(v)
+    return out
+
+
 def dtype_code(name: str) -> int:
     return tdx.TDX_BF16 if name == "bf16" else tdx.TDX_FP8_E4M3
 
@@ -38,12 +66,12 @@ def dtype_code(name: str) -> int:
 class AGCase:
     """Device buffers of one AllGather+GEMM problem."""
 
-    def __init__(self, inp, out_dtype="bf16", opts=None):
+    def __init__(self, inp, out_dtype="bf16", opts=None, layout="separate"):
         wl = inp.wl
         self.inp, self.wl = inp, wl
         self.W, self.M_local, self.K, self.N = wl.W, wl.M, wl.K, wl.N
         self.dt = dtype_code(wl.dtype)
-        self.shards = [dev_bits(a) for a in inp.a]
+        self.shards = shard_layout([dev_bits(a) for a in inp.a], layout)
         self.B = dev_bits(inp.b[0])
         tdt = torch.float32 if out_dtype == "fp32" else torch.bfloat16
         self.C = torch.full((wl.W * wl.M, wl.N), float("nan"), dtype=tdt, device="cuda")

@@ -11,7 +11,7 @@ import torch
 import comm_overlapped_gemm_gb300 as tdx
 from oracle import reference as R
 import workloads as wls
-from gpu_util import (AGCase, assert_bit_exact, dev_bits, assert_within_tol, check_ag_consumer_order,
+from gpu_util import (AGCase, assert_bit_exact, dev_bits, dtype_code, assert_within_tol, check_ag_consumer_order,
                       check_each_item_once, host_bits, sample_rows, trace_items, trace_phases,
                       trace_releases)
 
@@ -450,6 +450,30 @@ def test_ag_small_shards_pull_and_flag_paths_agree():
         n = wl.W * plan["n_chunks"]
         f = case.ws[plan["off_chunk_flags"]:plan["off_chunk_flags"] + 4 * n].view(torch.int32).cpu().numpy()
         assert np.array_equal(f.astype(np.uint32), R.expected_flags(n, 4))
+
+
+@pytest.mark.parametrize("layout", ["stacked", "scattered", "reversed"])
+@pytest.mark.parametrize("shape", [
+    dict(W=8, M=16, K=2048, N=512, dtype="bf16"),     # 8 shards per tile; B in one box per K slice
+    dict(W=4, M=16, K=1024, N=200, dtype="bf16"),     # 4 of 8 shard rows exist; ragged N: 2D B boxes
+    dict(W=16, M=8, K=512, N=256, dtype="bf16"),      # 16 shards per tile
+    dict(W=2, M=32, K=704, N=384, dtype="e4m3"),      # e4m3, ragged K, 2 of 4 shard rows
+])
+def test_ag_pull_tiles_over_shard_layouts(shape, layout):
+    # pull tiles read a tile's shards as one 3D box when the shards sit at one stride (stacked) and
+    # shard by shard otherwise (uneven gaps, or descending addresses); both match the oracle bit for
+    # bit, and so does the gathered copy
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], chunk_rows=shape["M"], **shape)
+    inp = wls.make_inputs(wl, integer=True)
+    kw = dict(scale_a=inp.scale_a, scale_b=inp.scale_b[0]) if wl.dtype == "e4m3" else {}
+    o = opts(chunk_rows=wl.M, **kw)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, dtype_code(wl.dtype), o)
+    assert plan["pull_a"] == 1
+    case = AGCase(inp, opts=o, layout=layout)
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+    assert torch.equal(gathered(case, plan), torch.cat([s.view(torch.uint8).flatten() for s in case.shards]))
 
 
 @pytest.mark.parametrize("integer", [True, False])
