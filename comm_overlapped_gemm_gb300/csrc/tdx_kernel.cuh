@@ -702,9 +702,11 @@ __device__ __forceinline__ void store_out_4(const KParams& p, int row, int col, 
   }
 }
 
-// Slots whose loads a cooperative-fold thread keeps in flight at once.
+// Slots whose loads a cooperative-fold thread keeps in flight at once: 10 folds the 19 K splits of
+// the small-M AllGather in two rounds of loads (12.96 -> 12.74 us per call against 8, three
+// rounds); 20 spills registers.
 #ifndef TDX_FOLD_GROUP
-#define TDX_FOLD_GROUP 8
+#define TDX_FOLD_GROUP 10
 #endif
 constexpr int kFoldGroup = TDX_FOLD_GROUP;
 

@@ -160,7 +160,9 @@ def test_rs_chained_and_slotted_give_identical_bits(shape):
 @pytest.mark.parametrize("shape,grid", [(dict(W=8, M=128, K=1024, N=8192), 0),     # the small-M shape
                                         (dict(W=4, M=512, K=256, N=512), 7),       # several waves
                                         (dict(W=3, M=384, K=200, N=136), 5),       # ragged K and N
-                                        (dict(W=16, M=256, K=64, N=64), 3)])
+                                        (dict(W=16, M=256, K=64, N=64), 3),
+                                        (dict(W=4, M=128, K=320, N=2048), 8),      # one M-tile, four waves
+                                        (dict(W=3, M=126, K=200, N=1000), 6)])     # ragged M, K, N
 @pytest.mark.parametrize("integer", [True, False])
 def test_rs_grid_fold(shape, grid, integer):
     # every CTA stores its partials, meets the others at a grid barrier, then folds 1/grid of all
