@@ -146,6 +146,9 @@ tdx_status tdx_workspace_init(void* workspace, size_t bytes, void* stream);
  * (Triton-distributed article, section "The first move was to expose the overlap": the AllGather
  * moves shards into place, split into chunks, and the GEMM consumes each chunk once it has arrived.)
  *  shards     host array of W device pointers; shards[r] is M_local x K of `dtype`, row-major.
+ *             Any addresses; shards at one stride (shards[r] = shards[0] + r * pitch, as in a
+ *             symmetric heap) let tiles of small shards read them with fewer, larger loads (a
+ *             performance difference only).
  *  B          device, K x N of `dtype`, row-major.
  *  C          device, (W*M_local) x N, row-major, of opts->out_dtype (bf16 or fp32). Row
  *             r*M_local + i of C is row i of shards[r] times B, whatever the arrival order.
@@ -341,8 +344,8 @@ tdx_status tdx_read_device_status(const void* workspace, void* stream, tdx_statu
  * that many positions of a rank's tile order are processed for ranks 0..W-1 before the next block
  * (positions count tiles, or tile pairs when [16] >= 2), [19] 1 if AllGather tiles read A straight
  * from the shards (shards smaller than a 128-row tile: a tile covers 128/M_local whole shards, each
- * loaded from its own buffer, so no tile waits on the gathered copy, which still completes G and
- * its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
+ * loaded from its own buffer, or all in one load when the shards sit at one stride, so no tile waits
+ * on the gathered copy, which still completes G and its flags), else 0, [20] bytes per element of the running-sum / partial-slot buffer (4 fp32,
  * 2 bf16 partials), [21] how the slotted fold is shared (single CTAs, fp32 partials; depends on the
  * device's SM count and opts.num_sms): 0 the last arriver folds the tile; 1 every work item is in
  * one wave of the persistent grid, and each element of a tile waits for the tile's L partials and
