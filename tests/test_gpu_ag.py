@@ -458,6 +458,8 @@ def test_ag_small_shards_pull_and_flag_paths_agree():
     dict(W=4, M=16, K=1024, N=200, dtype="bf16"),     # 4 of 8 shard rows exist; ragged N: 2D B boxes
     dict(W=16, M=8, K=512, N=256, dtype="bf16"),      # 16 shards per tile
     dict(W=2, M=32, K=704, N=384, dtype="e4m3"),      # e4m3, ragged K, 2 of 4 shard rows
+    dict(W=8, M=16, K=200, N=320, dtype="bf16"),      # ragged K; the last tile's second column
+                                                      # group lies past N (zero-filled)
 ])
 def test_ag_pull_tiles_over_shard_layouts(shape, layout):
     # pull tiles read a tile's shards as one 3D box when the shards sit at one stride (stacked) and
