@@ -478,6 +478,27 @@ def test_ag_pull_tiles_over_shard_layouts(shape, layout):
     assert torch.equal(gathered(case, plan), torch.cat([s.view(torch.uint8).flatten() for s in case.shards]))
 
 
+@pytest.mark.parametrize("shape,extra", [
+    (dict(W=3, M=256, K=320, N=384, dtype="bf16"), {}),                # B: one box per K slice
+    (dict(W=3, M=256, K=320, N=392, dtype="bf16"), {}),                # ragged N: 2D B boxes
+    (dict(W=4, M=256, K=512, N=640, dtype="bf16"), {"block_n": 256}),  # 4 groups; last tile half past N
+    (dict(W=2, M=128, K=1024, N=1024, dtype="e4m3"), {}),              # e4m3: 128-column groups
+])
+def test_ag_single_cta_b_column_groups(shape, extra):
+    # single-CTA tiles that wait on chunk flags load a K slice of B across the tile width as one 3D
+    # box when N is whole 128-byte column groups (2D boxes otherwise); bit-exact on integers
+    wl = wls.with_shape(wls.WORKLOADS["ag_w8"], chunk_rows=128, **shape)
+    inp = wls.make_inputs(wl, integer=True)
+    kw = dict(scale_a=inp.scale_a, scale_b=inp.scale_b[0]) if wl.dtype == "e4m3" else {}
+    o = opts(chunk_rows=128, **kw, **extra)
+    plan = tdx.tdx_plan_info(tdx.OP_AG, wl.W, wl.M, wl.K, wl.N, dtype_code(wl.dtype), o)
+    assert plan["cluster"] == 1 and plan["pull_a"] == 0
+    case = AGCase(inp, opts=o)
+    tdx.check(case.run())
+    status_ok(case)
+    assert_bit_exact(case.result_bits(), case.oracle(), "bf16")
+
+
 @pytest.mark.parametrize("integer", [True, False])
 def test_ag_split_k_grid_fold(integer):
     # split-K items over several waves of a small grid, folded by every CTA after a grid barrier
